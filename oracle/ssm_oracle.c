@@ -1,0 +1,298 @@
+/*
+ * ssm_oracle.c -- plain, slow, fp64 CPU oracle for the selective state space
+ * (S6) scan and its single-step state update.
+ *
+ * THIS IS TEST INFRASTRUCTURE, NOT PART OF THE PRODUCT PATH.  Only the test
+ * suite, the smoke check and the CPU-baseline leg of the benchmark may load
+ * it.  It shares no code, header, table or helper with the CUDA library.
+ *
+ * What it computes (Mamba paper, arXiv 2312.00752, as restated on the pages):
+ *   - per channel (b,d) the SSM runs independently over a diagonal A
+ *     ("Mamba / gitcode.csdn.net", section 2 "Structure and dimensions");
+ *   - Delta = softplus(delta + delta_bias[d]) ("gitcode", section 3.2 for the
+ *     softplus tau_Delta, section 3.6 for the bias; "docs.ifdog.com", section
+ *     "Mamba: selective state space model", softplus(z) = log(1 + exp(z)));
+ *   - Abar = exp(Delta * A) ("docs.ifdog.com", section "Discretisation", ZOH
+ *     diagonal form);
+ *   - Bbar * x = Delta * B * u (Euler form used by the same page's numpy
+ *     selective-SSM listing); the exact ZOH form
+ *     Bbar = (Delta A)^-1 (exp(Delta A) - 1) Delta B is a second mode;
+ *   - h_t = Abar_t h_{t-1} + Bbar_t x_t, y_t = C_t . h_t + D x_t
+ *     ("docs.ifdog.com", sections "Continuous state space model" and
+ *     "Discretisation"; "gitcode", section 2, recurrent mode);
+ *   - optional gate y_t *= silu(z_t) = z_t * sigmoid(z_t) ("docs.ifdog.com",
+ *     section "Mamba architecture", steps 4-5).
+ * The hardware-aware scan of "gitcode" section 3.3.2 is an exact reordering
+ * of this recurrence, so the oracle is the sequential definition itself.  A
+ * second evaluation order (work-efficient tree scan of the associative
+ * combine (a2*a1, a2*b1 + b2), "docs.ifdog.com", section "Hardware-aware
+ * parallel scan"; Blelloch 1990) exists only so that tests can check the
+ * two orders against each other.
+ *
+ * Readings where the pages are silent (each also listed in the design notes):
+ *   - the gate multiplies the whole output C.h + D.u;
+ *   - y_t uses the state after the update at step t;
+ *   - the initial state is zero unless h0 is given;
+ *   - softplus is exact: max(s,0) + log1p(exp(-|s|)), no linear threshold.
+ *
+ * Layout: every array is dense row-major.
+ *   u, delta, z, y : (B, D, L)      Bm, Cm : (B, N, L)
+ *   A : (D, N)    Dskip, delta_bias : (D)    h0, h_last, state : (B, D, N)
+ * Nullable: z, Dskip, delta_bias, h0, h_last.
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#include <unistd.h>
+
+#define ORACLE_DISC_EULER 0
+#define ORACLE_DISC_ZOH 1
+#define ORACLE_ORDER_SEQUENTIAL 0
+#define ORACLE_ORDER_TREE 1
+
+/* softplus(s) = log(1 + exp(s)), written in the overflow-free form. */
+static double softplus(double s) {
+    return (s > 0.0 ? s : 0.0) + log1p(exp(-fabs(s)));
+}
+
+static double sigmoid(double v) { return 1.0 / (1.0 + exp(-v)); }
+
+/* Delta for one (b,d,t): softplus(delta + bias) or, if disabled, the sum. */
+static double discretisation_step(double delta, double bias, int use_softplus) {
+    double s = delta + bias;
+    return use_softplus ? softplus(s) : s;
+}
+
+/* Input coefficient Bbar * x for one state component. */
+static double input_term(double dt, double a_cont, double b, double x, int disc) {
+    if (disc == ORACLE_DISC_ZOH) {
+        /* (Delta A)^-1 (exp(Delta A) - 1) Delta B = (exp(Delta A) - 1) / A * B */
+        if (a_cont == 0.0) return dt * b * x;
+        return expm1(dt * a_cont) / a_cont * b * x;
+    }
+    return dt * b * x; /* Euler: Bbar = Delta B */
+}
+
+typedef struct {
+    int64_t B, D, L, N;
+    const double *u, *delta, *z, *Bm, *Cm, *A, *Dskip, *delta_bias, *h0;
+    int delta_softplus, disc, order;
+    double *y, *h_last;
+    int64_t first, last; /* channel range [first, last) over b*D + d */
+    int status;
+} scan_job_t;
+
+/* Identity-padded work-efficient (Blelloch) scan over pairs (a, b), where
+ * a pair stands for the affine map h -> a h + b and pairs are composed in
+ * time order: combine(first, second) = (a2 a1, a2 b1 + b2).  On return
+ * (ea[t], eb[t]) is the composition of pairs 0..t (inclusive prefix). */
+static void tree_scan(int64_t L, const double *a, const double *b,
+                      double *ea, double *eb, double *xa, double *xb, int64_t P) {
+    for (int64_t i = 0; i < P; ++i) {
+        xa[i] = i < L ? a[i] : 1.0;
+        xb[i] = i < L ? b[i] : 0.0;
+    }
+    /* up-sweep: node (i + 2s - 1) := combine(left child, right child) */
+    for (int64_t s = 1; s < P; s *= 2) {
+        for (int64_t i = 0; i < P; i += 2 * s) {
+            int64_t l = i + s - 1, r = i + 2 * s - 1;
+            double na = xa[r] * xa[l];
+            double nb = xa[r] * xb[l] + xb[r];
+            xa[r] = na;
+            xb[r] = nb;
+        }
+    }
+    /* down-sweep with the identity at the root: exclusive prefixes */
+    xa[P - 1] = 1.0;
+    xb[P - 1] = 0.0;
+    for (int64_t s = P / 2; s >= 1; s /= 2) {
+        for (int64_t i = 0; i < P; i += 2 * s) {
+            int64_t l = i + s - 1, r = i + 2 * s - 1;
+            double la = xa[l], lb = xb[l];   /* total of the left subtree  */
+            double pa = xa[r], pb = xb[r];   /* prefix before this subtree */
+            xa[l] = pa;
+            xb[l] = pb;
+            xa[r] = la * pa;                 /* combine(prefix, left)      */
+            xb[r] = la * pb + lb;
+        }
+    }
+    /* inclusive prefix: combine(exclusive prefix, own pair) */
+    for (int64_t t = 0; t < L; ++t) {
+        ea[t] = a[t] * xa[t];
+        eb[t] = a[t] * xb[t] + b[t];
+    }
+}
+
+static void *scan_worker(void *arg) {
+    scan_job_t *j = (scan_job_t *)arg;
+    const int64_t L = j->L, N = j->N, D = j->D;
+    double *h = (double *)malloc(sizeof(double) * (size_t)(N > 0 ? N : 1));
+    double *dts = (double *)malloc(sizeof(double) * (size_t)(L > 0 ? L : 1));
+    double *hs = NULL, *ta = NULL, *tb = NULL, *ea = NULL, *eb = NULL, *xa = NULL, *xb = NULL;
+    int64_t P = 1;
+    if (j->order == ORACLE_ORDER_TREE) {
+        while (P < L) P *= 2;
+        hs = (double *)malloc(sizeof(double) * (size_t)(L * N + 1));
+        ta = (double *)malloc(sizeof(double) * (size_t)(L + 1));
+        tb = (double *)malloc(sizeof(double) * (size_t)(L + 1));
+        ea = (double *)malloc(sizeof(double) * (size_t)(L + 1));
+        eb = (double *)malloc(sizeof(double) * (size_t)(L + 1));
+        xa = (double *)malloc(sizeof(double) * (size_t)P);
+        xb = (double *)malloc(sizeof(double) * (size_t)P);
+        if (!hs || !ta || !tb || !ea || !eb || !xa || !xb) { j->status = -1; goto done; }
+    }
+    if (!h || !dts) { j->status = -1; goto done; }
+
+    for (int64_t c = j->first; c < j->last; ++c) {
+        const int64_t b = c / D, d = c % D;
+        const double *u = j->u + c * L;
+        const double *dl = j->delta + c * L;
+        const double *z = j->z ? j->z + c * L : NULL;
+        const double *Bb = j->Bm + b * N * L;
+        const double *Cb = j->Cm + b * N * L;
+        const double *Ad = j->A + d * N;
+        const double bias = j->delta_bias ? j->delta_bias[d] : 0.0;
+        const double Dd = j->Dskip ? j->Dskip[d] : 0.0;
+        double *y = j->y + c * L;
+
+        for (int64_t t = 0; t < L; ++t)
+            dts[t] = discretisation_step(dl[t], bias, j->delta_softplus);
+        for (int64_t n = 0; n < N; ++n)
+            h[n] = j->h0 ? j->h0[c * N + n] : 0.0;
+
+        if (j->order == ORACLE_ORDER_SEQUENTIAL) {
+            for (int64_t t = 0; t < L; ++t) {
+                double acc = 0.0;
+                for (int64_t n = 0; n < N; ++n) {
+                    double abar = exp(dts[t] * Ad[n]);
+                    double bx = input_term(dts[t], Ad[n], Bb[n * L + t], u[t], j->disc);
+                    h[n] = abar * h[n] + bx;
+                    acc += Cb[n * L + t] * h[n];
+                }
+                y[t] = acc;
+            }
+        } else {
+            for (int64_t n = 0; n < N; ++n) {
+                for (int64_t t = 0; t < L; ++t) {
+                    ta[t] = exp(dts[t] * Ad[n]);
+                    tb[t] = input_term(dts[t], Ad[n], Bb[n * L + t], u[t], j->disc);
+                }
+                tree_scan(L, ta, tb, ea, eb, xa, xb, P);
+                for (int64_t t = 0; t < L; ++t) hs[t * N + n] = ea[t] * h[n] + eb[t];
+                if (L > 0) h[n] = hs[(L - 1) * N + n];
+            }
+            for (int64_t t = 0; t < L; ++t) {
+                double acc = 0.0;
+                for (int64_t n = 0; n < N; ++n) acc += Cb[n * L + t] * hs[t * N + n];
+                y[t] = acc;
+            }
+        }
+        for (int64_t t = 0; t < L; ++t) {
+            double v = y[t] + Dd * u[t];
+            if (z) v *= z[t] * sigmoid(z[t]);
+            y[t] = v;
+        }
+        if (j->h_last)
+            for (int64_t n = 0; n < N; ++n) j->h_last[c * N + n] = h[n];
+    }
+done:
+    free(h); free(dts); free(hs); free(ta); free(tb); free(ea); free(eb); free(xa); free(xb);
+    return NULL;
+}
+
+static int default_threads(void) {
+    long n = sysconf(_SC_NPROCESSORS_ONLN);
+    return n > 0 ? (int)n : 1;
+}
+
+/* Returns the number of threads the host offers the oracle by default. */
+int oracle_default_threads(void) { return default_threads(); }
+
+/*
+ * Selective scan over all channels.  Returns 0 on success, -1 on a bad
+ * argument or an allocation failure.  nthreads <= 0 picks one per online
+ * core; channels are split into contiguous blocks, one per thread.
+ */
+int oracle_selective_scan(int64_t B, int64_t D, int64_t L, int64_t N,
+                          const double *u, const double *delta, const double *z,
+                          const double *Bm, const double *Cm, const double *A,
+                          const double *Dskip, const double *delta_bias,
+                          const double *h0, int delta_softplus, int disc, int order,
+                          double *y, double *h_last, int nthreads) {
+    if (B < 0 || D < 0 || L < 0 || N < 0) return -1;
+    if (!u || !delta || !Bm || !Cm || !A || !y) return -1;
+    if (disc != ORACLE_DISC_EULER && disc != ORACLE_DISC_ZOH) return -1;
+    if (order != ORACLE_ORDER_SEQUENTIAL && order != ORACLE_ORDER_TREE) return -1;
+    const int64_t channels = B * D;
+    if (channels == 0) return 0;
+    if (nthreads <= 0) nthreads = default_threads();
+    if (nthreads > channels) nthreads = (int)channels;
+
+    scan_job_t *jobs = (scan_job_t *)calloc((size_t)nthreads, sizeof(scan_job_t));
+    pthread_t *tids = (pthread_t *)calloc((size_t)nthreads, sizeof(pthread_t));
+    if (!jobs || !tids) { free(jobs); free(tids); return -1; }
+    for (int i = 0; i < nthreads; ++i) {
+        scan_job_t *j = &jobs[i];
+        j->B = B; j->D = D; j->L = L; j->N = N;
+        j->u = u; j->delta = delta; j->z = z; j->Bm = Bm; j->Cm = Cm; j->A = A;
+        j->Dskip = Dskip; j->delta_bias = delta_bias; j->h0 = h0;
+        j->delta_softplus = delta_softplus; j->disc = disc; j->order = order;
+        j->y = y; j->h_last = h_last;
+        j->first = channels * i / nthreads;
+        j->last = channels * (i + 1) / nthreads;
+    }
+    int rc = 0;
+    if (nthreads == 1) {
+        scan_worker(&jobs[0]);
+    } else {
+        int started = 0;
+        for (int i = 0; i < nthreads; ++i) {
+            if (pthread_create(&tids[i], NULL, scan_worker, &jobs[i]) != 0) break;
+            ++started;
+        }
+        for (int i = 0; i < started; ++i) pthread_join(tids[i], NULL);
+        for (int i = started; i < nthreads; ++i) scan_worker(&jobs[i]);
+    }
+    for (int i = 0; i < nthreads; ++i) if (jobs[i].status) rc = -1;
+    free(jobs);
+    free(tids);
+    return rc;
+}
+
+/*
+ * One recurrent (decode) step for every channel, the loop body of the scan
+ * applied once ("gitcode", section 1: constant time per step; section 2: the
+ * recurrent mode used for autoregressive inference).
+ *   state : (B, D, N), read and overwritten in place
+ *   u, delta, z, y : (B, D)      Bm, Cm : (B, N)
+ */
+int oracle_state_update(int64_t B, int64_t D, int64_t N, double *state,
+                        const double *u, const double *delta, const double *z,
+                        const double *Bm, const double *Cm, const double *A,
+                        const double *Dskip, const double *delta_bias,
+                        int delta_softplus, int disc, double *y) {
+    if (B < 0 || D < 0 || N < 0) return -1;
+    if (!state || !u || !delta || !Bm || !Cm || !A || !y) return -1;
+    if (disc != ORACLE_DISC_EULER && disc != ORACLE_DISC_ZOH) return -1;
+    for (int64_t b = 0; b < B; ++b) {
+        for (int64_t d = 0; d < D; ++d) {
+            const int64_t c = b * D + d;
+            const double bias = delta_bias ? delta_bias[d] : 0.0;
+            const double dt = discretisation_step(delta[c], bias, delta_softplus);
+            double acc = 0.0;
+            for (int64_t n = 0; n < N; ++n) {
+                double abar = exp(dt * A[d * N + n]);
+                double bx = input_term(dt, A[d * N + n], Bm[b * N + n], u[c], disc);
+                double hn = abar * state[c * N + n] + bx;
+                state[c * N + n] = hn;
+                acc += Cm[b * N + n] * hn;
+            }
+            double v = acc + (Dskip ? Dskip[d] : 0.0) * u[c];
+            if (z) v *= z[c] * sigmoid(z[c]);
+            y[c] = v;
+        }
+    }
+    return 0;
+}

@@ -1,0 +1,198 @@
+"""Seeded synthetic inputs for the selective scan and the decode step.
+
+This module holds the input recipe only -- none of the scan's arithmetic --
+so that the CUDA path and the fp64 oracle can consume identical values.
+
+Recipe (the distributions of the Mamba layer workloads):
+  * u, delta, z, B, C, D ~ N(0, 1) drawn as float32;
+  * Delta0[d] log-uniform in [dt_min, dt_max] per channel, and
+    delta_bias = softplus^-1(Delta0) (the Delta-bias initialisation of the
+    Mamba paper, "gitcode.csdn.net", section 3.6 "Parameterization of Delta");
+  * A[d, n] = -(n + 1) (S4D-Real initialisation, same page, section 3.6
+    "Initialization");
+  * tensors whose I/O dtype is bf16 are rounded once, round-to-nearest-even,
+    and both sides consume exactly those values.
+
+Every row of every tensor has its own PCG64 stream, keyed by
+(seed, tensor id, batch index, row index[, step]).  Any channel can therefore
+be regenerated alone, which is how the oracle checks sampled channels of
+workloads too large to hold on the host.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass, replace
+
+import numpy as np
+
+# tensor ids of the per-row streams
+T_U, T_DELTA, T_Z, T_B, T_C, T_D, T_DT0, T_STATE = range(8)
+
+
+@dataclass(frozen=True)
+class ScanConfig:
+    name: str
+    batch: int
+    dim: int
+    seqlen: int
+    dstate: int
+    io_dtype: str            # "f32" or "bf16"
+    dt_min: float = 1e-3
+    dt_max: float = 1e-1
+    gate: bool = True
+    dskip: bool = True
+    time_invariant: bool = False   # delta, B, C constant over t
+    shared_bc: bool = False        # B, C shared across the batch (batch stride 0)
+
+    @property
+    def updates(self) -> int:
+        return self.batch * self.dim * self.seqlen * self.dstate
+
+
+@dataclass(frozen=True)
+class DecodeConfig:
+    name: str
+    batch: int
+    dim: int
+    dstate: int
+    steps: int
+    io_dtype: str = "bf16"
+    dt_min: float = 1e-3
+    dt_max: float = 1e-1
+    gate: bool = True
+    dskip: bool = True
+
+    @property
+    def updates_per_step(self) -> int:
+        return self.batch * self.dim * self.dstate
+
+
+# The five workloads: a tiny fp32 case, two Mamba layer shapes, a long
+# sequence, and the decode step.
+TINY = ScanConfig("tiny_fp32_b1_d16_l256_n16", 1, 16, 256, 16, "f32")
+M130 = ScanConfig("mamba130m_bf16_b8_d1536_l2048_n16", 8, 1536, 2048, 16, "bf16")
+M2P8 = ScanConfig("mamba2.8b_bf16_b4_d5120_l2048_n16", 4, 5120, 2048, 16, "bf16")
+M2P8_TI = ScanConfig("mamba2.8b_ti_bf16_b1_d5120_l2048_n16", 1, 5120, 2048, 16, "bf16",
+                     time_invariant=True, shared_bc=True)
+LONG = ScanConfig("long_bf16_b1_d1536_l1048576_n16", 1, 1536, 1 << 20, 16, "bf16",
+                  dt_min=1e-4, dt_max=1e-2)
+DECODE = DecodeConfig("decode_bf16_b256_d5120_n16_x1000", 256, 5120, 16, 1000)
+
+SCAN_CONFIGS = {c.name: c for c in (TINY, M130, M2P8, M2P8_TI, LONG)}
+
+
+def with_shape(cfg: ScanConfig, **kw) -> ScanConfig:
+    """A copy of ``cfg`` with some fields replaced (same distributions)."""
+    return replace(cfg, **kw)
+
+
+def _rng(seed: int, *key: int) -> np.random.Generator:
+    return np.random.Generator(np.random.PCG64(np.random.SeedSequence([seed, *key])))
+
+
+def round_to_bf16_bits(x: np.ndarray) -> np.ndarray:
+    """float32 -> bf16 bit patterns (uint16), round-to-nearest-even."""
+    bits = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32)
+    lsb = (bits >> 16) & np.uint32(1)
+    return ((bits + np.uint32(0x7FFF) + lsb) >> 16).astype(np.uint16)
+
+
+def bf16_bits_to_f32(bits: np.ndarray) -> np.ndarray:
+    return (np.asarray(bits, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32)
+
+
+def round_io(x: np.ndarray, io_dtype: str) -> np.ndarray:
+    """Round float32 values to the I/O dtype and return them as exact float32."""
+    x = np.asarray(x, dtype=np.float32)
+    if io_dtype == "bf16":
+        return bf16_bits_to_f32(round_to_bf16_bits(x))
+    if io_dtype == "f32":
+        return x
+    raise ValueError(io_dtype)
+
+
+def _normal_row(seed: int, tensor: int, b: int, row: int, n: int) -> np.ndarray:
+    return _rng(seed, tensor, b, row).standard_normal(n, dtype=np.float32)
+
+
+def channel_rows(cfg: ScanConfig, tensor: int, b: int, d0: int, d1: int, seed: int = 0) -> np.ndarray:
+    """Rows d0..d1-1 of u / delta / z for batch b: float32 (d1-d0, L), rounded to the I/O dtype."""
+    L = cfg.seqlen
+    out = np.empty((d1 - d0, L), dtype=np.float32)
+    for i, d in enumerate(range(d0, d1)):
+        if tensor == T_DELTA and cfg.time_invariant:
+            out[i, :] = _normal_row(seed, tensor, b, d, 1)[0]
+        else:
+            out[i, :] = _normal_row(seed, tensor, b, d, L)
+    return round_io(out, cfg.io_dtype)
+
+
+def bc_rows(cfg: ScanConfig, tensor: int, b: int, seed: int = 0) -> np.ndarray:
+    """B or C for batch b: float32 (N, L), rounded to the I/O dtype."""
+    N, L = cfg.dstate, cfg.seqlen
+    bb = 0 if cfg.shared_bc else b
+    out = np.empty((N, L), dtype=np.float32)
+    for n in range(N):
+        if cfg.time_invariant:
+            out[n, :] = _normal_row(seed, tensor, bb, n, 1)[0]
+        else:
+            out[n, :] = _normal_row(seed, tensor, bb, n, L)
+    return round_io(out, cfg.io_dtype)
+
+
+def softplus_inverse(x: np.ndarray) -> np.ndarray:
+    """softplus^-1(x) = log(exp(x) - 1) = x + log(-expm1(-x)), stable for small x."""
+    x = np.asarray(x, dtype=np.float64)
+    return x + np.log(-np.expm1(-x))
+
+
+def layer_params(dim: int, dstate: int, dt_min: float, dt_max: float, seed: int = 0):
+    """A (D, N), Dskip (D,), delta_bias (D,) as float32."""
+    A = -np.tile(np.arange(1, dstate + 1, dtype=np.float32), (dim, 1))
+    Dskip = _rng(seed, T_D).standard_normal(dim, dtype=np.float32)
+    lo, hi = np.log(dt_min), np.log(dt_max)
+    dt0 = np.exp(_rng(seed, T_DT0).uniform(lo, hi, dim))
+    delta_bias = softplus_inverse(dt0).astype(np.float32)
+    return A, Dskip, delta_bias
+
+
+def scan_inputs(cfg: ScanConfig, seed: int = 0, batches=None) -> dict:
+    """All scan inputs of ``cfg`` as float32 arrays (values exact in the I/O dtype).
+
+    Keys: u, delta, z (B, D, L); Bm, Cm (B or 1, N, L); A (D, N); Dskip,
+    delta_bias (D,).  ``batches`` restricts the batch indices generated.
+    """
+    bs = list(range(cfg.batch)) if batches is None else list(batches)
+    D = cfg.dim
+    u = np.stack([channel_rows(cfg, T_U, b, 0, D, seed) for b in bs])
+    delta = np.stack([channel_rows(cfg, T_DELTA, b, 0, D, seed) for b in bs])
+    z = np.stack([channel_rows(cfg, T_Z, b, 0, D, seed) for b in bs]) if cfg.gate else None
+    bc_b = [0] if cfg.shared_bc else bs
+    Bm = np.stack([bc_rows(cfg, T_B, b, seed) for b in bc_b])
+    Cm = np.stack([bc_rows(cfg, T_C, b, seed) for b in bc_b])
+    A, Dskip, delta_bias = layer_params(D, cfg.dstate, cfg.dt_min, cfg.dt_max, seed)
+    return dict(u=u, delta=delta, z=z, Bm=Bm, Cm=Cm, A=A,
+                Dskip=Dskip if cfg.dskip else None, delta_bias=delta_bias)
+
+
+def decode_params(cfg: DecodeConfig, seed: int = 0):
+    return layer_params(cfg.dim, cfg.dstate, cfg.dt_min, cfg.dt_max, seed)
+
+
+def decode_state(cfg: DecodeConfig, seed: int = 0, batches=None) -> np.ndarray:
+    """Initial persistent state h ~ N(0,1), float32 (B, D, N)."""
+    bs = list(range(cfg.batch)) if batches is None else list(batches)
+    return np.stack([_rng(seed, T_STATE, b).standard_normal((cfg.dim, cfg.dstate), dtype=np.float32)
+                     for b in bs])
+
+
+def decode_step_inputs(cfg: DecodeConfig, step: int, seed: int = 0) -> dict:
+    """One token per sequence: u, delta, z (B, D) and Bm, Cm (B, N), rounded to the I/O dtype."""
+    B, D, N = cfg.batch, cfg.dim, cfg.dstate
+
+    def draw(tensor, shape):
+        return round_io(_rng(seed, tensor, 1_000_000 + step).standard_normal(shape, dtype=np.float32),
+                        cfg.io_dtype)
+
+    return dict(u=draw(T_U, (B, D)), delta=draw(T_DELTA, (B, D)),
+                z=draw(T_Z, (B, D)) if cfg.gate else None,
+                Bm=draw(T_B, (B, N)), Cm=draw(T_C, (B, N)))

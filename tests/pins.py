@@ -1,0 +1,315 @@
+"""Pins that tie the fp64 oracle to facts fixed by the pages and by mathematics.
+
+Each pin takes an oracle library handle (``oracle.load()`` or a deliberately
+broken build of it) and raises AssertionError when the oracle disagrees.  None
+of them re-types the oracle's own loop: each checks against a different
+formula, a hand-worked value, a limit, or an invariant.
+
+Sources (pages on the Mamba selective SSM):
+  * "Mamba and state space models" (docs.ifdog.com): sections "Discretisation"
+    (Abar = exp(Delta A), ZOH Bbar), "S4" (expanded outputs y[0] = CBx[0],
+    y[1] = CAbarBx[0] + CBx[1], ..., i.e. the kernel K = [CB, CAbarB, ...]),
+    "Hardware-aware parallel scan" (associative combine), "Mamba
+    architecture" (silu gate);
+  * "Mamba paper translation" (gitcode.csdn.net): section 2 (recurrent and
+    convolution modes, LTI), section 3.5 (Theorem 1, gating; Delta -> inf
+    resets, Delta -> 0 ignores);
+  * "Mamba close reading" (alishangtian.com), section on the core innovation
+    (Theorem 1 stated: N=1, A=-1 gives h_t = (1-g_t) h_{t-1} + g_t x_t).
+"""
+from __future__ import annotations
+
+import math
+import os
+
+import numpy as np
+
+import oracle
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+def _read_golden(name):
+    vals = {}
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            k, v = (s.strip() for s in line.split("=", 1))
+            vals[k] = np.array([float(x) for x in v.split()], dtype=np.float64)
+    return vals
+
+
+def _sigmoid(v):
+    return 1.0 / (1.0 + np.exp(-v))
+
+
+def _softplus(s):
+    return np.logaddexp(0.0, s)
+
+
+def _close(a, b, rtol=1e-12, atol=1e-13, what=""):
+    a = np.asarray(a, dtype=np.float64)
+    b = np.asarray(b, dtype=np.float64)
+    assert a.shape == b.shape, (what, a.shape, b.shape)
+    err = np.max(np.abs(a - b) - rtol * np.abs(b)) if a.size else -1.0
+    assert err <= atol, f"{what}: max excess error {err:.3e}"
+
+
+def _rand_inputs(rng, Bsz, D, L, N, gate=True, dskip=True, h0=False):
+    return dict(
+        u=rng.standard_normal((Bsz, D, L)),
+        delta=rng.standard_normal((Bsz, D, L)),
+        z=rng.standard_normal((Bsz, D, L)) if gate else None,
+        Bm=rng.standard_normal((Bsz, N, L)),
+        Cm=rng.standard_normal((Bsz, N, L)),
+        A=-rng.uniform(0.2, 3.0, (D, N)),
+        Dskip=rng.standard_normal(D) if dskip else None,
+        delta_bias=rng.uniform(-4.0, -1.0, D),
+        h0=rng.standard_normal((Bsz, D, N)) if h0 else None,
+    )
+
+
+# --------------------------------------------------------------------------
+# hand-worked examples (tests/golden)
+# --------------------------------------------------------------------------
+
+def pin_golden_recurrence(lib):
+    g = _read_golden("hand_recurrence_n2_l4.txt")
+    A = (g["A_over_ln2"] * math.log(2.0)).reshape(1, 2)
+    Bm = np.stack([g["B0"], g["B1"]])[None]
+    Cm = np.stack([g["C0"], g["C1"]])[None]
+    for order in (oracle.ORDER_SEQUENTIAL, oracle.ORDER_TREE):
+        y, hl = oracle.selective_scan(g["u"][None, None], g["delta"][None, None], A, Bm, Cm,
+                                      Dskip=g["Dskip"], delta_softplus=False, order=order,
+                                      return_last_state=True, lib=lib)
+        _close(y[0, 0], g["y"], what="golden recurrence y")
+        _close(hl[0, 0], g["h_last"], what="golden recurrence h_last")
+
+
+def pin_golden_gated(lib):
+    g = _read_golden("hand_gated_l1.txt")
+    z = np.full((1, 1, 1), math.log(3.0))
+    y, hl = oracle.selective_scan(g["u"].reshape(1, 1, 1), g["delta"].reshape(1, 1, 1),
+                                  g["A"].reshape(1, 3), g["B"].reshape(1, 3, 1),
+                                  g["C"].reshape(1, 3, 1), Dskip=g["Dskip"], z=z,
+                                  delta_bias=g["bias"], delta_softplus=True,
+                                  return_last_state=True, lib=lib)
+    _close(y.ravel(), g["y"], what="golden gated y")
+    _close(hl.ravel(), g["h_last_over_ln2"] * math.log(2.0), what="golden gated h_last")
+
+
+# --------------------------------------------------------------------------
+# closed forms and other formulas
+# --------------------------------------------------------------------------
+
+def pin_lti_equals_convolution(lib, disc=oracle.DISC_EULER):
+    """Time-invariant case: the recurrence equals y = K * x with
+    K_k = sum_n C[n] Abar[n]^k Bbar[n] (powers, not a recurrence), plus D x, gated."""
+    rng = np.random.default_rng(11)
+    Bsz, D, L, N = 2, 3, 40, 4
+    delta_c = rng.standard_normal((Bsz, D, 1))
+    Bc = rng.standard_normal((Bsz, N, 1))
+    Cc = rng.standard_normal((Bsz, N, 1))
+    A = -rng.uniform(0.1, 2.0, (D, N))
+    bias = rng.uniform(-3.0, 0.0, D)
+    Dskip = rng.standard_normal(D)
+    u = rng.standard_normal((Bsz, D, L))
+    z = rng.standard_normal((Bsz, D, L))
+    y = oracle.selective_scan(u, np.repeat(delta_c, L, 2), A, np.repeat(Bc, L, 2),
+                              np.repeat(Cc, L, 2), Dskip=Dskip, z=z, delta_bias=bias,
+                              disc=disc, lib=lib)
+    ks = np.arange(L)
+    for b in range(Bsz):
+        for d in range(D):
+            dt = _softplus(delta_c[b, d, 0] + bias[d])
+            abar = np.exp(dt * A[d])                               # (N,)
+            if disc == oracle.DISC_ZOH:
+                bbar = np.expm1(dt * A[d]) / A[d] * Bc[b, :, 0]
+            else:
+                bbar = dt * Bc[b, :, 0]
+            K = (Cc[b, :, 0][None, :] * np.power(abar[None, :], ks[:, None]) * bbar[None, :]).sum(1)
+            conv = np.array([np.dot(K[:t + 1][::-1], u[b, d, :t + 1]) for t in range(L)])
+            ref = (conv + Dskip[d] * u[b, d]) * z[b, d] * _sigmoid(z[b, d])
+            _close(y[b, d], ref, rtol=1e-11, atol=1e-12, what=f"LTI conv b{b} d{d}")
+
+
+def pin_theorem1_gated_rnn(lib):
+    """N=1, A=-1, B=1, C=1 under ZOH: h_t = (1-g_t) h_{t-1} + g_t x_t, g_t = sigmoid(s_t);
+    under Euler the same holds when B_t = g_t / Delta_t."""
+    rng = np.random.default_rng(5)
+    L = 64
+    s = rng.standard_normal(L) * 2.5
+    x = rng.standard_normal(L)
+    g = _sigmoid(s)
+    h = np.empty(L)
+    prev = 0.0
+    for t in range(L):
+        prev = (1.0 - g[t]) * prev + g[t] * x[t]
+        h[t] = prev
+    A = np.array([[-1.0]])
+    ones = np.ones((1, 1, L))
+    y_zoh = oracle.selective_scan(x[None, None], s[None, None], A, ones, ones,
+                                  disc=oracle.DISC_ZOH, lib=lib)
+    _close(y_zoh[0, 0], h, rtol=1e-12, atol=1e-13, what="theorem 1 (ZOH)")
+    dt = _softplus(s)
+    y_eul = oracle.selective_scan(x[None, None], s[None, None], A, (g / dt)[None, None], ones,
+                                  disc=oracle.DISC_EULER, lib=lib)
+    _close(y_eul[0, 0], h, rtol=1e-12, atol=1e-13, what="theorem 1 (Euler, B = g/Delta)")
+
+
+def pin_unrolled_sum(lib):
+    """Brute force on tiny inputs: h_t = (prod_{r<=t} a_r) h0 + sum_{s<=t} (prod_{s<r<=t} a_r) b_s."""
+    rng = np.random.default_rng(3)
+    Bsz, D, L, N = 2, 2, 9, 3
+    for disc in (oracle.DISC_EULER, oracle.DISC_ZOH):
+        p = _rand_inputs(rng, Bsz, D, L, N, h0=True)
+        y, hl = oracle.selective_scan(**p, disc=disc, return_last_state=True, lib=lib)
+        for b in range(Bsz):
+            for d in range(D):
+                dt = _softplus(p["delta"][b, d] + p["delta_bias"][d])          # (L,)
+                a = np.exp(dt[:, None] * p["A"][d][None, :])                   # (L, N)
+                if disc == oracle.DISC_ZOH:
+                    bb = np.expm1(dt[:, None] * p["A"][d][None, :]) / p["A"][d][None, :] \
+                        * p["Bm"][b].T * p["u"][b, d][:, None]
+                else:
+                    bb = dt[:, None] * p["Bm"][b].T * p["u"][b, d][:, None]
+                hs = np.zeros((L, N))
+                for t in range(L):
+                    acc = np.prod(a[:t + 1], axis=0) * p["h0"][b, d]
+                    for s_ in range(t + 1):
+                        acc = acc + np.prod(a[s_ + 1:t + 1], axis=0) * bb[s_]
+                    hs[t] = acc
+                ref = (p["Cm"][b].T * hs).sum(1) + p["Dskip"][d] * p["u"][b, d]
+                ref = ref * p["z"][b, d] * _sigmoid(p["z"][b, d])
+                _close(y[b, d], ref, rtol=1e-11, atol=1e-12, what="unrolled sum y")
+                _close(hl[b, d], hs[-1], rtol=1e-11, atol=1e-12, what="unrolled sum h_last")
+
+
+def pin_single_step_closed_form(lib):
+    """L = 1, h0 = 0: y = (Delta u sum_n C_n B_n + D u) * silu(z)."""
+    rng = np.random.default_rng(8)
+    p = _rand_inputs(rng, 3, 4, 1, 5)
+    y = oracle.selective_scan(**p, lib=lib)
+    dt = _softplus(p["delta"][..., 0] + p["delta_bias"][None, :])
+    cb = (p["Cm"][..., 0] * p["Bm"][..., 0]).sum(1)                            # (B,)
+    u0, z0 = p["u"][..., 0], p["z"][..., 0]
+    ref = (dt * u0 * cb[:, None] + p["Dskip"][None, :] * u0) * z0 * _sigmoid(z0)
+    _close(y[..., 0], ref, what="single step")
+
+
+# --------------------------------------------------------------------------
+# invariants and limits
+# --------------------------------------------------------------------------
+
+def pin_tree_order_matches_sequential(lib):
+    rng = np.random.default_rng(17)
+    for L in (1, 2, 3, 17, 64):
+        p = _rand_inputs(rng, 2, 3, L, 4, h0=True)
+        y1, h1 = oracle.selective_scan(**p, order=oracle.ORDER_SEQUENTIAL, return_last_state=True,
+                                       lib=lib)
+        y2, h2 = oracle.selective_scan(**p, order=oracle.ORDER_TREE, return_last_state=True, lib=lib)
+        _close(y2, y1, rtol=1e-12, atol=1e-12, what=f"tree vs sequential y L={L}")
+        _close(h2, h1, rtol=1e-12, atol=1e-12, what=f"tree vs sequential h L={L}")
+
+
+def pin_boundary_reset(lib):
+    """Delta -> inf at t*: outputs from t* on forget everything before t*."""
+    rng = np.random.default_rng(23)
+    Bsz, D, L, N, ts = 1, 3, 48, 4, 20
+    p = _rand_inputs(rng, Bsz, D, L, N, h0=True)
+    p["A"] = -np.tile(np.arange(1.0, N + 1), (D, 1))
+    p["delta"][..., ts] = 60.0
+    y1 = oracle.selective_scan(**p, lib=lib)
+    q = dict(p)
+    q["u"] = p["u"].copy()
+    q["u"][..., :ts] = rng.standard_normal((Bsz, D, ts))
+    q["delta"] = p["delta"].copy()
+    q["delta"][..., :ts] = rng.standard_normal((Bsz, D, ts))
+    q["h0"] = rng.standard_normal((Bsz, D, N))
+    y2 = oracle.selective_scan(**q, lib=lib)
+    _close(y2[..., ts:], y1[..., ts:], rtol=1e-12, atol=1e-12, what="reset")
+    assert np.max(np.abs(y2[..., :ts] - y1[..., :ts])) > 1e-3, "prefix should differ"
+
+
+def pin_ignore_window(lib):
+    """Delta -> 0 over a window: the state is held and the inputs are ignored."""
+    rng = np.random.default_rng(29)
+    Bsz, D, L, N, t0, t1 = 2, 3, 40, 4, 10, 30
+    p = _rand_inputs(rng, Bsz, D, L, N)
+    p["delta"][..., t0:t1] = -60.0
+    _, h_start = oracle.selective_scan(**{k: (v[..., :t0] if k in ("u", "delta", "z", "Bm", "Cm")
+                                              else v) for k, v in p.items()},
+                                       return_last_state=True, lib=lib)
+    _, h_end = oracle.selective_scan(**{k: (v[..., :t1] if k in ("u", "delta", "z", "Bm", "Cm")
+                                            else v) for k, v in p.items()},
+                                     return_last_state=True, lib=lib)
+    _close(h_end, h_start, rtol=1e-12, atol=1e-14, what="ignore: state held")
+    y = oracle.selective_scan(**p, lib=lib)
+    for t in range(t0, t1):
+        ref = np.einsum("bn,bdn->bd", p["Cm"][..., t], h_start) + p["Dskip"][None] * p["u"][..., t]
+        ref = ref * p["z"][..., t] * _sigmoid(p["z"][..., t])
+        _close(y[..., t], ref, rtol=1e-12, atol=1e-13, what="ignore: readout of held state")
+
+
+def pin_chunk_invariance(lib):
+    """scan(L) == scan(L1) -> h_last -> scan(L - L1, h0 = h_last)."""
+    rng = np.random.default_rng(31)
+    p = _rand_inputs(rng, 2, 3, 50, 4, h0=True)
+    y, hl = oracle.selective_scan(**p, return_last_state=True, lib=lib)
+    for L1 in (1, 23, 49):
+        head = {k: (v[..., :L1] if k in ("u", "delta", "z", "Bm", "Cm") else v) for k, v in p.items()}
+        y1, h1 = oracle.selective_scan(**head, return_last_state=True, lib=lib)
+        tail = {k: (v[..., L1:] if k in ("u", "delta", "z", "Bm", "Cm") else v) for k, v in p.items()}
+        tail["h0"] = h1
+        y2, h2 = oracle.selective_scan(**tail, return_last_state=True, lib=lib)
+        _close(np.concatenate([y1, y2], -1), y, rtol=1e-13, atol=1e-14, what=f"chunk y L1={L1}")
+        _close(h2, hl, rtol=1e-13, atol=1e-14, what=f"chunk h L1={L1}")
+
+
+def pin_step_matches_scan(lib):
+    """T decode steps from h0 equal a T-step scan from h0 (final state and every y)."""
+    rng = np.random.default_rng(37)
+    p = _rand_inputs(rng, 2, 3, 12, 4, h0=True)
+    y, hl = oracle.selective_scan(**p, return_last_state=True, lib=lib)
+    st = p["h0"]
+    for t in range(12):
+        st, yt = oracle.state_update(st, p["u"][..., t], p["delta"][..., t], p["A"],
+                                     p["Bm"][..., t], p["Cm"][..., t], Dskip=p["Dskip"],
+                                     z=p["z"][..., t], delta_bias=p["delta_bias"], lib=lib)
+        _close(yt, y[..., t], rtol=1e-13, atol=1e-14, what=f"step y t={t}")
+    _close(st, hl, rtol=1e-13, atol=1e-14, what="step final state")
+
+
+def pin_linearity(lib):
+    """Gate off: y is linear in (u, h0) for fixed delta, B, C."""
+    rng = np.random.default_rng(41)
+    p = _rand_inputs(rng, 2, 3, 20, 4, gate=False, h0=True)
+    u2 = rng.standard_normal(p["u"].shape)
+    h2 = rng.standard_normal(p["h0"].shape)
+    al, be = 0.7, -1.3
+    y1 = oracle.selective_scan(**p, lib=lib)
+    q = dict(p, u=u2, h0=h2)
+    y2 = oracle.selective_scan(**q, lib=lib)
+    r = dict(p, u=al * p["u"] + be * u2, h0=al * p["h0"] + be * h2)
+    y3 = oracle.selective_scan(**r, lib=lib)
+    _close(y3, al * y1 + be * y2, rtol=1e-11, atol=1e-12, what="linearity")
+
+
+def pin_zoh_to_euler_small_delta(lib):
+    """As Delta -> 0 the exact ZOH input term tends to the Euler one, (expm1(dA)/A)/Delta -> 1."""
+    rng = np.random.default_rng(43)
+    p = _rand_inputs(rng, 1, 2, 10, 3, h0=True)
+    p["delta"] = np.full_like(p["delta"], -30.0)      # Delta ~ e^{-30-|bias|}
+    ye = oracle.selective_scan(**p, disc=oracle.DISC_EULER, lib=lib)
+    yz = oracle.selective_scan(**p, disc=oracle.DISC_ZOH, lib=lib)
+    _close(yz, ye, rtol=1e-10, atol=1e-14, what="zoh -> euler")
+
+
+ALL_PINS = [
+    pin_golden_recurrence, pin_golden_gated, pin_lti_equals_convolution, pin_theorem1_gated_rnn,
+    pin_unrolled_sum, pin_single_step_closed_form, pin_tree_order_matches_sequential,
+    pin_boundary_reset, pin_ignore_window, pin_chunk_invariance, pin_step_matches_scan,
+    pin_linearity, pin_zoh_to_euler_small_delta,
+]
