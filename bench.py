@@ -1,0 +1,395 @@
+#!/usr/bin/env python3
+"""Benchmark of the selective-scan hot path on B300.
+
+Default workload: the Mamba-2.8B-shaped layer scan, bf16 I/O with fp32 state,
+batch 4, D = 5120, L = 2048, N = 16 (671,088,640 state updates per step).  A
+step is one full ``ssm_scan_fwd`` over that batch: softplus discretisation,
+exp(Delta A), the recurrence, the C contraction, the D skip and the silu gate,
+in one kernel launch.
+
+Metric: state-updates/s = B*D*L*N / time, and the achieved HBM GB/s of the
+scan kernel against the measured B300 copy bandwidth.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--workload NAME] [--small] [--no-e2e] [--no-cpu-baseline]
+
+Under torchrun (N > 1) every rank runs an independent replica of the
+workload on its own GPU (channels are independent: no data-path collective);
+the step time is the max over ranks and the value counts all ranks' updates.
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "selective-scan state-updates/s (B·D·L·N/s); achieved HBM GB/s vs B300 peak"
+UNIT = "state-updates/s"
+SCAN_SOURCES = ["selective_state_space_126_b300/csrc/scan_tiled.cu",
+                "selective_state_space_126_b300/csrc/device_math.cuh"]
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "scan_tiled_traffic.json")
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="mamba2.8b_bf16_b4_d5120_l2048_n16")
+    ap.add_argument("--small", action="store_true", help="batch 2 of the workload (profiling captures)")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    return ap.parse_args()
+
+
+def dist_info():
+    return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
+
+
+def workload(args):
+    from selective_state_space_126_b300 import synthetic as syn
+    cfg = syn.SCAN_CONFIGS[args.workload]
+    if args.small:
+        cfg = syn.with_shape(cfg, batch=2, name=cfg.name + "_batch2")
+    return cfg
+
+
+def algorithmic_bytes(cfg) -> int:
+    """Bytes the scan must move once: read u, delta, z; write y (B*D*L each); read B, C
+    (B*N*L each, once per batch row); read A (D*N) and D, delta_bias (D) in fp32."""
+    es = 4 if cfg.io_dtype == "f32" else 2
+    bd_l = cfg.batch * cfg.dim * cfg.seqlen
+    seq = (3 if cfg.gate else 2) * bd_l + bd_l
+    bc = 2 * (1 if cfg.shared_bc else cfg.batch) * cfg.dstate * cfg.seqlen
+    params = cfg.dim * cfg.dstate * 4 + 2 * cfg.dim * 4
+    return (seq + bc) * es + params
+
+
+def source_sha() -> str:
+    h = hashlib.sha256()
+    for f in SCAN_SOURCES:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6400.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling during the timed region."""
+    Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.samples = []
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "20"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (FileNotFoundError, OSError):
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+        time.sleep(0.15)
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.samples.append((time.time(), line.strip()))
+
+    def stop(self):
+        if self.proc is None:
+            return
+        time.sleep(0.05)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+
+    def summary(self, t0, t1):
+        rows = [s for t, s in self.samples if t0 - 0.03 <= t <= t1 + 0.03] or [s for _, s in self.samples]
+        window = "timed" if any(t0 - 0.03 <= t <= t1 + 0.03 for t, _ in self.samples) else "around-timed"
+        mhz, maxes, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            f = [x.strip() for x in r.split(",")]
+            if len(f) < 7:
+                continue
+            try:
+                mhz.append(float(f[0]))
+                maxes.append(float(f[1]))
+            except ValueError:
+                continue
+            for name, v in zip(names, f[3:7]):
+                if v.lower() == "active":
+                    reasons.add(name)
+        if not mhz:
+            return None
+        return {"sm_mhz": float(np.median(mhz)), "sm_max_mhz": max(maxes), "reasons": sorted(reasons),
+                "samples": len(mhz), "window": window}
+
+
+def cpu_baseline(cfg, target_s=12.0):
+    """The fp64 oracle, as it stands, on a bounded sample of the workload (whole rows of channels)."""
+    import oracle
+    from selective_state_space_126_b300 import synthetic as syn
+    threads = oracle.default_threads()
+    try:
+        cores = len(os.sched_getaffinity(0))
+    except AttributeError:
+        cores = os.cpu_count() or 1
+    L, N = cfg.seqlen, cfg.dstate
+    A, Dskip, bias = syn.layer_params(cfg.dim, N, cfg.dt_min, cfg.dt_max)
+    chans = 64
+    elapsed, done = 0.0, 0
+    while True:
+        d1 = min(cfg.dim, chans)
+        u = syn.channel_rows(cfg, syn.T_U, 0, 0, d1)[None]
+        dl = syn.channel_rows(cfg, syn.T_DELTA, 0, 0, d1)[None]
+        z = syn.channel_rows(cfg, syn.T_Z, 0, 0, d1)[None] if cfg.gate else None
+        Bm = syn.bc_rows(cfg, syn.T_B, 0)[None]
+        Cm = syn.bc_rows(cfg, syn.T_C, 0)[None]
+        t0 = time.perf_counter()
+        oracle.selective_scan(u, dl, A[:d1], Bm, Cm, Dskip=Dskip[:d1] if cfg.dskip else None, z=z,
+                              delta_bias=bias[:d1], nthreads=threads)
+        elapsed = time.perf_counter() - t0
+        done = d1
+        if elapsed >= target_s / 4 or d1 == cfg.dim:
+            break
+        chans = min(cfg.dim, int(chans * max(2.0, min(8.0, target_s / 4 / max(elapsed, 1e-3)))))
+    updates = done * L * N
+    return {"value": updates / elapsed, "unit": UNIT, "cores": threads, "host_cores_visible": cores,
+            "kind": "oracle",
+            "sample": f"batch row 0, channels 0..{done - 1} of {cfg.dim}, full L={L}, N={N} "
+                      f"({updates} state updates, {elapsed:.2f} s)"}
+
+
+def run_reference(args, rank, world):
+    """--impl reference: the fp64 oracle timed on the host cores (rank 0 only)."""
+    if rank != 0:
+        return
+    import oracle
+    from selective_state_space_126_b300 import synthetic as syn
+    cfg = workload(args)
+    L, N = cfg.seqlen, cfg.dstate
+    A, Dskip, bias = syn.layer_params(cfg.dim, N, cfg.dt_min, cfg.dt_max)
+    threads = oracle.default_threads()
+    chans = max(threads, 16)          # one bounded sample per step: `chans` full rows
+    u = syn.channel_rows(cfg, syn.T_U, 0, 0, chans)[None]
+    dl = syn.channel_rows(cfg, syn.T_DELTA, 0, 0, chans)[None]
+    z = syn.channel_rows(cfg, syn.T_Z, 0, 0, chans)[None] if cfg.gate else None
+    Bm = syn.bc_rows(cfg, syn.T_B, 0)[None]
+    Cm = syn.bc_rows(cfg, syn.T_C, 0)[None]
+
+    def step():
+        oracle.selective_scan(u, dl, A[:chans], Bm, Cm, Dskip=Dskip[:chans] if cfg.dskip else None, z=z,
+                              delta_bias=bias[:chans], nthreads=threads)
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    dt = time.perf_counter() - t0
+    updates = chans * L * N * args.steps
+    value = updates / dt
+    sample = f"each step: batch row 0, channels 0..{chans - 1} of {cfg.dim}, full L={L}, N={N}"
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": cfg.name, "batch": cfg.batch, "dim": cfg.dim, "seqlen": cfg.seqlen,
+                   "dstate": cfg.dstate, "io_dtype": cfg.io_dtype},
+        "cpu_baseline": {"kind": "oracle", "cores": threads, "sample": sample, "value": value, "unit": UNIT},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def main():
+    args = parse()
+    rank, world, local = dist_info()
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+
+    import torch
+    import selective_state_space_126_b300 as ssm
+    from selective_state_space_126_b300 import build
+    from selective_state_space_126_b300.synthetic import device_inputs
+
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        torch.cuda.set_device(0)
+    if build.is_stale():
+        if rank == 0:
+            build.build_library(quiet=True)
+        if world > 1:
+            torch.distributed.barrier()
+    lib = ssm.load_library()
+    cfg = workload(args)
+    dev = torch.device("cuda", torch.cuda.current_device())
+
+    # ---- inputs resident in HBM (each rank its own replica, seeded by rank) ----
+    inp = device_inputs(cfg, seed=rank)
+    y = torch.empty_like(inp["u"])
+    a = ssm.make_scan_args(inp["u"], inp["delta"], inp["A"], inp["Bm"], inp["Cm"], y, inp["Dskip"], inp["z"],
+                           inp["delta_bias"])
+    path = ssm.ssm_scan_plan_path(a)
+    ws_bytes = ssm.ssm_scan_workspace_size(a)
+    ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
+    a.workspace, a.workspace_bytes = ws.data_ptr(), ws_bytes
+    launches_per_step = {"tiled": 1, "chunked": 3, "generic": 1}[path]
+    stream = torch.cuda.current_stream()
+    sh = ctypes.c_void_p(stream.cuda_stream)
+    argp = ctypes.byref(a)
+
+    def step():
+        rc = lib.ssm_scan_fwd(argp, sh)
+        if rc != 0:
+            raise RuntimeError(ssm.status_name(rc) + " " + lib.ssm_last_error_detail().decode())
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+
+    sampler = ClockSampler(int(os.environ.get("CUDA_VISIBLE_DEVICES", "0").split(",")[0])
+                           if os.environ.get("CUDA_VISIBLE_DEVICES", "").isdigit() else local)
+    sampler.start()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    w0 = time.time()
+    start.record(stream)
+    for i in range(args.steps):
+        ev[i][0].record(stream)
+        step()
+        ev[i][1].record(stream)
+    stop.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    w1 = time.time()
+    sampler.stop()
+    total_ms = start.elapsed_time(stop)
+    launch_ms = float(np.mean([s.elapsed_time(e) for s, e in ev]))
+    if world > 1:
+        t = torch.tensor([total_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    updates_per_step = cfg.updates * world
+    value = updates_per_step / (ms_per_step * 1e-3)
+
+    # ---- end to end through the C ABI from pinned host buffers ----
+    e2e = None
+    if not args.no_e2e:
+        names = ["u", "delta", "z", "Bm", "Cm", "A", "Dskip", "delta_bias"]
+        hbuf = {k: inp[k].cpu().pin_memory() for k in names if inp[k] is not None}
+        hy = torch.empty(y.shape, dtype=y.dtype).pin_memory()
+        h2d = sum(t.numel() * t.element_size() for t in hbuf.values())
+        d2h = hy.numel() * hy.element_size()
+
+        def e2e_step():
+            for k, t in hbuf.items():
+                inp[k].copy_(t, non_blocking=True)
+            step()
+            hy.copy_(y, non_blocking=True)
+
+        for _ in range(3):
+            e2e_step()
+        torch.cuda.synchronize()
+        s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s0.record(stream)
+        for _ in range(args.e2e_steps):
+            e2e_step()
+        s1.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = s0.elapsed_time(s1) / args.e2e_steps
+        if world > 1:
+            t = torch.tensor([e2e_ms], device=dev)
+            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+            e2e_ms = float(t.item())
+        e2e = {"value": updates_per_step / (e2e_ms * 1e-3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms, "steps": args.e2e_steps,
+               "host_memory": "pinned"}
+
+    if rank != 0:
+        if world > 1:
+            torch.distributed.destroy_process_group()
+        return
+
+    # ---- roofline of the scan kernel ----
+    peak, peak_kind = measured_peaks()
+    algo = algorithmic_bytes(cfg)
+    kernel_ms = launch_ms / launches_per_step if path != "tiled" else launch_ms
+    achieved = algo / (launch_ms * 1e-3) / 1e9
+    traffic = None
+    if os.path.exists(TRAFFIC_FILE):
+        with open(TRAFFIC_FILE) as f:
+            tr = json.load(f)
+        if tr.get("kernel_source_sha") == source_sha() and tr.get("workload") == cfg.name:
+            traffic = tr.get("dram_bytes_per_launch")
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    clocks = sampler.summary(w0, w1)
+    mhz = (clocks or {}).get("sm_mhz") or 1900.0
+    ex2_rate = cfg.updates / (launch_ms * 1e-3)                 # one SFU ex2 per state update
+    ex2_peak = 32 * sms * mhz * 1e6                             # 32 ex2 / clk / SM on B300
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": max(3, args.warmup), "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": cfg.name, "batch": cfg.batch, "dim": cfg.dim, "seqlen": cfg.seqlen,
+                   "dstate": cfg.dstate, "io_dtype": cfg.io_dtype, "path": path,
+                   "l2": f"inputs larger than L2 ({algo / 1e6:.0f} MB moved per step vs 126 MB L2)",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                     "traffic": traffic, "peak_kind": peak_kind, "algorithmic_bytes_per_launch": algo,
+                     "kernel_ms": kernel_ms},
+        "sfu_roofline": {"bound": "alu", "achieved": ex2_rate / 1e12, "peak": ex2_peak / 1e12,
+                         "unit": "Tex2/s", "frac": ex2_rate / ex2_peak,
+                         "peak_basis": f"32 ex2/clk/SM x {sms} SMs x median {mhz:.0f} MHz"},
+        "gpu_launches": args.steps * launches_per_step,
+        "clocks": clocks,
+        "e2e": e2e,
+    }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(cfg)
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,167 @@
+/*
+ * ssm.h -- C ABI of the B300 selective state space (S6) library (libssm.so).
+ *
+ * Two operations, both defined by the Mamba paper (arXiv 2312.00752) as
+ * restated on the pages this library follows:
+ *
+ *   ssm_scan_fwd      the selective-scan forward pass.  For every batch b,
+ *                     channel d and state n:
+ *                       Delta_t   = softplus(delta[b,d,t] + delta_bias[d])
+ *                       Abar_t[n] = exp(Delta_t * A[d,n])
+ *                       h_t[n]    = Abar_t[n] h_{t-1}[n] + Delta_t B[b,n,t] u[b,d,t]
+ *                       y[b,d,t]  = (sum_n C[b,n,t] h_t[n] + Dskip[d] u[b,d,t]) * silu(z[b,d,t])
+ *                     ("Mamba paper translation", gitcode.csdn.net: section 2
+ *                     "State Space Models" for the recurrence and the
+ *                     per-channel diagonal A, section 3.2 for the selection
+ *                     of Delta, B, C and softplus, section 3.3.2 for the
+ *                     fused scan that never writes h to HBM, section 3.6 for
+ *                     the Delta bias; "Mamba and state space models",
+ *                     docs.ifdog.com: section "Discretisation" for
+ *                     Abar = exp(Delta A), the numpy selective-SSM listing for
+ *                     the Euler input term Delta B u, section "Mamba
+ *                     architecture" for the silu gate.)
+ *   ssm_state_update  one recurrent (decode) step of the same recurrence
+ *                     against a persistent fp32 state ("gitcode", section 1
+ *                     and section 2: constant time per generated token).
+ *
+ * Conventions for every entry point
+ *   - All tensor pointers are DEVICE pointers unless stated otherwise; the
+ *     caller owns every buffer, including the optional workspace.  The
+ *     library never allocates, frees or synchronises, and keeps no state
+ *     between calls other than the device status word (below).
+ *   - Strides are in ELEMENTS.  The time (last) stride of every sequence
+ *     tensor must be 1.  Other strides must be >= 0; a batch stride of 0
+ *     broadcasts a tensor across the batch.  Output tensors (y, h_last,
+ *     state) must not overlap each other or any input.
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  Calls
+ *     are asynchronous: SSM_OK means "validated and enqueued".  Errors in a
+ *     kernel that has already been enqueued surface at the caller's next
+ *     synchronisation, or through ssm_get_device_status().
+ *   - Argument errors are detected on the host before anything is enqueued;
+ *     nothing is written in that case.  No C++ exception crosses the ABI.
+ *   - Calls on different streams may run concurrently; the library is
+ *     re-entrant.
+ */
+#ifndef SSM_B300_H
+#define SSM_B300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    SSM_OK = 0,
+    SSM_ERR_INVALID_ARG = 1,   /* null pointer, bad size or stride, overlapping outputs */
+    SSM_ERR_UNSUPPORTED = 2,   /* well-formed but outside what the kernels implement */
+    SSM_ERR_CUDA = 3,          /* a CUDA call failed while enqueueing (error is cleared) */
+    SSM_ERR_TIMEOUT = 4,       /* a bounded device-side wait gave up (device status only) */
+    SSM_ERR_WORKSPACE = 5      /* workspace missing or smaller than ssm_scan_workspace_size() */
+} ssm_status_t;
+
+typedef enum {
+    SSM_F32 = 0,               /* IEEE binary32 */
+    SSM_BF16 = 1               /* bfloat16; the state and all arithmetic stay fp32 */
+} ssm_dtype_t;
+
+/* flags for ssm_scan_args_t.flags (testing and tuning; 0 = automatic) */
+#define SSM_SCAN_FORCE_GENERIC 0x1   /* use the stride-general kernel */
+#define SSM_SCAN_FORCE_TILED   0x2   /* use the tiled single-pass kernel (error if impossible) */
+#define SSM_SCAN_FORCE_CHUNKED 0x4   /* use the three-pass chunked kernel (error if impossible) */
+
+/*
+ * Arguments of ssm_scan_fwd.  Shapes (with strides in elements, time stride 1):
+ *   u, delta, z, y : (batch, dim, seqlen)     io_dtype
+ *   Bm, Cm         : (batch, dstate, seqlen)  io_dtype  (batch stride may be 0)
+ *   A              : (dim, dstate)            fp32, real (normally negative)
+ *   Dskip          : (dim,)                   fp32, contiguous, nullable (no skip term)
+ *   delta_bias     : (dim,)                   fp32, contiguous, nullable (bias 0)
+ *   h0, h_last     : (batch, dim, dstate)     fp32, nullable (zero initial state /
+ *                                             final state not returned)
+ *   z              : nullable (no gate)
+ * Limits: 1 <= dstate <= 64; batch, dim, seqlen >= 0 (an empty problem is a no-op).
+ */
+typedef struct ssm_scan_args {
+    int64_t batch, dim, seqlen, dstate;        /* B, D, L, N */
+    ssm_dtype_t io_dtype;
+    int32_t delta_softplus;                    /* 1: Delta = softplus(delta + bias); 0: delta + bias */
+    const void *u, *delta, *z, *Bm, *Cm;
+    const float *A, *Dskip, *delta_bias;
+    const float *h0;
+    float *h_last;
+    void *y;
+    int64_t stride_u[3], stride_delta[3], stride_z[3], stride_y[3];   /* (b, d, t) */
+    int64_t stride_B[3], stride_C[3];                                 /* (b, n, t) */
+    int64_t stride_A[2];                                              /* (d, n)    */
+    int64_t stride_h0[3], stride_h_last[3];                           /* (b, d, n) */
+    int32_t flags;                             /* SSM_SCAN_FORCE_*; 0 = automatic */
+    int32_t reserved0;
+    int64_t chunk_len;                         /* chunked path: timesteps per chunk; 0 = automatic */
+    void *workspace;                           /* device scratch, caller-owned, nullable if 0 bytes needed */
+    size_t workspace_bytes;
+} ssm_scan_args_t;
+
+/*
+ * Arguments of ssm_state_update (one decode step, the state updated in place).
+ *   state          : (batch, dim, dstate)  fp32, read then overwritten
+ *   u, delta, z, y : (batch, dim)          io_dtype; z nullable
+ *   Bm, Cm         : (batch, dstate)       io_dtype (batch stride may be 0)
+ *   A              : (dim, dstate) fp32;  Dskip, delta_bias : (dim,) fp32 contiguous, nullable
+ * Limits: 1 <= dstate <= 64.
+ */
+typedef struct ssm_step_args {
+    int64_t batch, dim, dstate;
+    ssm_dtype_t io_dtype;
+    int32_t delta_softplus;
+    float *state;
+    const void *u, *delta, *z, *Bm, *Cm;
+    const float *A, *Dskip, *delta_bias;
+    void *y;
+    int64_t stride_state[3];                   /* (b, d, n) */
+    int64_t stride_u[2], stride_delta[2], stride_z[2], stride_y[2];   /* (b, d) */
+    int64_t stride_B[2], stride_C[2];          /* (b, n) */
+    int64_t stride_A[2];                       /* (d, n) */
+} ssm_step_args_t;
+
+/* Bytes of device workspace ssm_scan_fwd needs for these arguments (0 for
+ * the single-pass paths).  Host-only; validates the arguments first.  The
+ * plan it reflects depends on the current device's SM count. */
+ssm_status_t ssm_scan_workspace_size(const ssm_scan_args_t *args, size_t *bytes);
+
+/* The selective-scan forward pass (see the header comment). */
+ssm_status_t ssm_scan_fwd(const ssm_scan_args_t *args, void *stream);
+
+/* One decode step against a persistent fp32 state. */
+ssm_status_t ssm_state_update(const ssm_step_args_t *args, void *stream);
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char *ssm_status_string(ssm_status_t status);
+
+/* Details of the last host-side error on the calling thread (static
+ * thread-local buffer, empty string if none). */
+const char *ssm_last_error_detail(void);
+
+/* Reads (and, if clear != 0, resets) the current device's status word, which
+ * kernels set when a bounded wait gives up (SSM_ERR_TIMEOUT).  Synchronises
+ * `stream`.  *code receives SSM_OK or the first error recorded. */
+ssm_status_t ssm_get_device_status(void *stream, int clear, int *code);
+
+/* Kernel path ssm_scan_fwd would take for these arguments:
+ * 0 = generic, 1 = tiled single pass, 2 = chunked three-pass; -1 on error. */
+int ssm_scan_plan_path(const ssm_scan_args_t *args);
+
+/* Library ABI version: (major << 16) | minor. */
+int ssm_version(void);
+
+/* sizeof of the argument structs as compiled into the library, so that a
+ * binding can check its mirror of them: which = 0 -> ssm_scan_args_t,
+ * 1 -> ssm_step_args_t; 0 for any other value. */
+size_t ssm_abi_sizeof(int which);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SSM_B300_H */

@@ -1,0 +1,296 @@
+"""B300-native selective state space (S6) scan and decode step.
+
+A thin ctypes binding over ``libssm.so`` (C ABI in ``include/ssm.h``).  The
+functions here only marshal torch tensors into the C argument structs; every
+step of the scan and of the decode update runs in the library's CUDA
+kernels.  There is no CPU fallback: if ``libssm.so`` is missing or no CUDA
+device is present, the calls raise.
+
+Public API (same names as the C entry points):
+  ssm_scan_fwd(u, delta, A, Bm, Cm, Dskip=None, z=None, delta_bias=None, h0=None, ...)
+  ssm_state_update(state, u, delta, A, Bm, Cm, Dskip=None, z=None, delta_bias=None, ...)
+  ssm_scan_workspace_size(...), ssm_status_string(code), ssm_version()
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libssm.so")
+
+SSM_OK, SSM_ERR_INVALID_ARG, SSM_ERR_UNSUPPORTED, SSM_ERR_CUDA, SSM_ERR_TIMEOUT, SSM_ERR_WORKSPACE = range(6)
+SSM_F32, SSM_BF16 = 0, 1
+SSM_SCAN_FORCE_GENERIC, SSM_SCAN_FORCE_TILED, SSM_SCAN_FORCE_CHUNKED = 0x1, 0x2, 0x4
+PATH_NAMES = {0: "generic", 1: "tiled", 2: "chunked"}
+
+# every symbol include/ssm.h declares
+EXPORTED_SYMBOLS = ["ssm_scan_workspace_size", "ssm_scan_fwd", "ssm_state_update", "ssm_status_string",
+                    "ssm_last_error_detail", "ssm_get_device_status", "ssm_scan_plan_path", "ssm_version",
+                    "ssm_abi_sizeof"]
+
+_i64 = ctypes.c_int64
+_vp = ctypes.c_void_p
+
+
+class ScanArgs(ctypes.Structure):
+    """Mirror of ssm_scan_args_t."""
+    _fields_ = [
+        ("batch", _i64), ("dim", _i64), ("seqlen", _i64), ("dstate", _i64),
+        ("io_dtype", ctypes.c_int), ("delta_softplus", ctypes.c_int32),
+        ("u", _vp), ("delta", _vp), ("z", _vp), ("Bm", _vp), ("Cm", _vp),
+        ("A", _vp), ("Dskip", _vp), ("delta_bias", _vp), ("h0", _vp), ("h_last", _vp), ("y", _vp),
+        ("stride_u", _i64 * 3), ("stride_delta", _i64 * 3), ("stride_z", _i64 * 3), ("stride_y", _i64 * 3),
+        ("stride_B", _i64 * 3), ("stride_C", _i64 * 3), ("stride_A", _i64 * 2),
+        ("stride_h0", _i64 * 3), ("stride_h_last", _i64 * 3),
+        ("flags", ctypes.c_int32), ("reserved0", ctypes.c_int32), ("chunk_len", _i64),
+        ("workspace", _vp), ("workspace_bytes", ctypes.c_size_t),
+    ]
+
+
+class StepArgs(ctypes.Structure):
+    """Mirror of ssm_step_args_t."""
+    _fields_ = [
+        ("batch", _i64), ("dim", _i64), ("dstate", _i64),
+        ("io_dtype", ctypes.c_int), ("delta_softplus", ctypes.c_int32),
+        ("state", _vp), ("u", _vp), ("delta", _vp), ("z", _vp), ("Bm", _vp), ("Cm", _vp),
+        ("A", _vp), ("Dskip", _vp), ("delta_bias", _vp), ("y", _vp),
+        ("stride_state", _i64 * 3), ("stride_u", _i64 * 2), ("stride_delta", _i64 * 2),
+        ("stride_z", _i64 * 2), ("stride_y", _i64 * 2), ("stride_B", _i64 * 2), ("stride_C", _i64 * 2),
+        ("stride_A", _i64 * 2),
+    ]
+
+
+class SsmError(RuntimeError):
+    def __init__(self, code, detail=""):
+        self.code = code
+        super().__init__(f"{status_name(code)}: {detail}" if detail else status_name(code))
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def load_library(path: str = LIB_PATH):
+    """Load libssm.so (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is not None and path == LIB_PATH:
+            return _lib
+        if not os.path.exists(path):
+            raise ImportError(f"{path} is missing: build it with `python -m selective_state_space_126_b300.build`")
+        lib = ctypes.CDLL(path)
+        lib.ssm_scan_workspace_size.argtypes = [ctypes.POINTER(ScanArgs), ctypes.POINTER(ctypes.c_size_t)]
+        lib.ssm_scan_workspace_size.restype = ctypes.c_int
+        lib.ssm_scan_fwd.argtypes = [ctypes.POINTER(ScanArgs), _vp]
+        lib.ssm_scan_fwd.restype = ctypes.c_int
+        lib.ssm_state_update.argtypes = [ctypes.POINTER(StepArgs), _vp]
+        lib.ssm_state_update.restype = ctypes.c_int
+        lib.ssm_status_string.argtypes = [ctypes.c_int]
+        lib.ssm_status_string.restype = ctypes.c_char_p
+        lib.ssm_last_error_detail.argtypes = []
+        lib.ssm_last_error_detail.restype = ctypes.c_char_p
+        lib.ssm_get_device_status.argtypes = [_vp, ctypes.c_int, ctypes.POINTER(ctypes.c_int)]
+        lib.ssm_get_device_status.restype = ctypes.c_int
+        lib.ssm_scan_plan_path.argtypes = [ctypes.POINTER(ScanArgs)]
+        lib.ssm_scan_plan_path.restype = ctypes.c_int
+        lib.ssm_version.argtypes = []
+        lib.ssm_version.restype = ctypes.c_int
+        lib.ssm_abi_sizeof.argtypes = [ctypes.c_int]
+        lib.ssm_abi_sizeof.restype = ctypes.c_size_t
+        if lib.ssm_abi_sizeof(0) != ctypes.sizeof(ScanArgs) or lib.ssm_abi_sizeof(1) != ctypes.sizeof(StepArgs):
+            raise ImportError("libssm.so argument structs do not match this binding")
+        if path == LIB_PATH:
+            _lib = lib
+        return lib
+
+
+def status_name(code: int) -> str:
+    try:
+        return load_library().ssm_status_string(int(code)).decode()
+    except ImportError:
+        return f"status {code}"
+
+
+def ssm_status_string(code: int) -> str:
+    return status_name(code)
+
+
+def ssm_version() -> int:
+    return int(load_library().ssm_version())
+
+
+def _check(code: int):
+    if code != SSM_OK:
+        raise SsmError(code, load_library().ssm_last_error_detail().decode())
+
+
+# ---------------------------------------------------------------------------
+# torch marshalling
+# ---------------------------------------------------------------------------
+
+def _torch():
+    import torch
+    return torch
+
+
+def _io_dtype(t):
+    torch = _torch()
+    if t.dtype == torch.float32:
+        return SSM_F32
+    if t.dtype == torch.bfloat16:
+        return SSM_BF16
+    raise TypeError(f"unsupported I/O dtype {t.dtype} (float32 or bfloat16)")
+
+
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+def _strides(t, rank, dims=None):
+    if t is None:
+        return [0] * rank
+    s = list(t.stride())
+    if dims is not None and t.dim() == rank - 1:   # broadcast over a missing batch dimension
+        s = [0] + s
+    if len(s) != rank:
+        raise ValueError(f"expected a {rank}-d tensor, got shape {tuple(t.shape)}")
+    return s
+
+
+def _stream_handle(stream):
+    torch = _torch()
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _f32(t, name):
+    torch = _torch()
+    if t is None:
+        return None
+    if t.dtype != torch.float32:
+        raise TypeError(f"{name} must be float32")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    return t
+
+
+def make_scan_args(u, delta, A, Bm, Cm, y, Dskip=None, z=None, delta_bias=None, h0=None, h_last=None,
+                   delta_softplus=True, flags=0, chunk_len=0, workspace=None) -> ScanArgs:
+    """Fill an ssm_scan_args_t from torch tensors (no copies, strides passed through)."""
+    Bsz, D, L = u.shape
+    N = A.shape[1]
+    a = ScanArgs()
+    a.batch, a.dim, a.seqlen, a.dstate = Bsz, D, L, N
+    a.io_dtype = _io_dtype(u)
+    a.delta_softplus = 1 if delta_softplus else 0
+    a.u, a.delta, a.z, a.Bm, a.Cm = _ptr(u), _ptr(delta), _ptr(z), _ptr(Bm), _ptr(Cm)
+    a.A, a.Dskip, a.delta_bias = _ptr(A), _ptr(Dskip), _ptr(delta_bias)
+    a.h0, a.h_last, a.y = _ptr(h0), _ptr(h_last), _ptr(y)
+    a.stride_u[:] = _strides(u, 3)
+    a.stride_delta[:] = _strides(delta, 3)
+    a.stride_z[:] = _strides(z, 3)
+    a.stride_y[:] = _strides(y, 3)
+    a.stride_B[:] = _strides(Bm, 3, dims="b")
+    a.stride_C[:] = _strides(Cm, 3, dims="b")
+    a.stride_A[:] = _strides(A, 2)
+    a.stride_h0[:] = _strides(h0, 3)
+    a.stride_h_last[:] = _strides(h_last, 3)
+    a.flags = int(flags)
+    a.chunk_len = int(chunk_len)
+    if workspace is not None:
+        a.workspace = workspace.data_ptr()
+        a.workspace_bytes = workspace.numel() * workspace.element_size()
+    return a
+
+
+def ssm_scan_workspace_size(args: ScanArgs) -> int:
+    n = ctypes.c_size_t(0)
+    _check(load_library().ssm_scan_workspace_size(ctypes.byref(args), ctypes.byref(n)))
+    return int(n.value)
+
+
+def ssm_scan_plan_path(args: ScanArgs) -> str:
+    return PATH_NAMES.get(int(load_library().ssm_scan_plan_path(ctypes.byref(args))), "invalid")
+
+
+def ssm_scan_fwd(u, delta, A, Bm, Cm, Dskip=None, z=None, delta_bias=None, h0=None, delta_softplus=True,
+                 y=None, return_last_state=False, h_last=None, workspace=None, flags=0, chunk_len=0,
+                 stream=None):
+    """Selective-scan forward pass on the GPU.
+
+    u, delta, z: (B, D, L); Bm, Cm: (B, N, L) or (N, L) (shared across the batch);
+    A: (D, N) fp32; Dskip, delta_bias: (D,) fp32; h0: (B, D, N) fp32.
+    I/O tensors are float32 or bfloat16 (all the same dtype), on one CUDA device.
+    Returns y (B, D, L) in the I/O dtype, and h_last (B, D, N) fp32 if requested.
+    """
+    torch = _torch()
+    lib = load_library()
+    for name, t in (("u", u), ("delta", delta), ("Bm", Bm), ("Cm", Cm), ("z", z)):
+        if t is not None and not t.is_cuda:
+            raise ValueError(f"{name} must be a CUDA tensor")
+    _f32(A, "A"); _f32(Dskip, "Dskip"); _f32(delta_bias, "delta_bias"); _f32(h0, "h0")
+    if Dskip is not None:
+        Dskip = Dskip.contiguous()
+    if delta_bias is not None:
+        delta_bias = delta_bias.contiguous()
+    if y is None:
+        y = torch.empty(u.shape, dtype=u.dtype, device=u.device)
+    if return_last_state and h_last is None:
+        h_last = torch.empty((u.shape[0], u.shape[1], A.shape[1]), dtype=torch.float32, device=u.device)
+    args = make_scan_args(u, delta, A, Bm, Cm, y, Dskip, z, delta_bias, h0, h_last, delta_softplus, flags,
+                          chunk_len, None)
+    need = ssm_scan_workspace_size(args)
+    if need > 0:
+        if workspace is None or workspace.numel() * workspace.element_size() < need:
+            workspace = torch.empty(need, dtype=torch.uint8, device=u.device)
+        args.workspace = workspace.data_ptr()
+        args.workspace_bytes = workspace.numel() * workspace.element_size()
+    _check(lib.ssm_scan_fwd(ctypes.byref(args), _vp(_stream_handle(stream))))
+    return (y, h_last) if return_last_state else y
+
+
+def make_step_args(state, u, delta, A, Bm, Cm, y, Dskip=None, z=None, delta_bias=None,
+                   delta_softplus=True) -> StepArgs:
+    Bsz, D, N = state.shape
+    a = StepArgs()
+    a.batch, a.dim, a.dstate = Bsz, D, N
+    a.io_dtype = _io_dtype(u)
+    a.delta_softplus = 1 if delta_softplus else 0
+    a.state, a.u, a.delta, a.z, a.Bm, a.Cm = _ptr(state), _ptr(u), _ptr(delta), _ptr(z), _ptr(Bm), _ptr(Cm)
+    a.A, a.Dskip, a.delta_bias, a.y = _ptr(A), _ptr(Dskip), _ptr(delta_bias), _ptr(y)
+    a.stride_state[:] = _strides(state, 3)
+    a.stride_u[:] = _strides(u, 2)
+    a.stride_delta[:] = _strides(delta, 2)
+    a.stride_z[:] = _strides(z, 2)
+    a.stride_y[:] = _strides(y, 2)
+    a.stride_B[:] = _strides(Bm, 2)
+    a.stride_C[:] = _strides(Cm, 2)
+    a.stride_A[:] = _strides(A, 2)
+    return a
+
+
+def ssm_state_update(state, u, delta, A, Bm, Cm, Dskip=None, z=None, delta_bias=None, delta_softplus=True,
+                     y=None, stream=None):
+    """One decode step: ``state`` (B, D, N) fp32 is updated in place; returns y (B, D)."""
+    torch = _torch()
+    lib = load_library()
+    _f32(state, "state"); _f32(A, "A"); _f32(Dskip, "Dskip"); _f32(delta_bias, "delta_bias")
+    if Dskip is not None:
+        Dskip = Dskip.contiguous()
+    if delta_bias is not None:
+        delta_bias = delta_bias.contiguous()
+    if y is None:
+        y = torch.empty(u.shape, dtype=u.dtype, device=u.device)
+    args = make_step_args(state, u, delta, A, Bm, Cm, y, Dskip, z, delta_bias, delta_softplus)
+    _check(lib.ssm_state_update(ctypes.byref(args), _vp(_stream_handle(stream))))
+    return y
+
+
+def ssm_get_device_status(clear=True, stream=None) -> int:
+    code = ctypes.c_int(0)
+    _check(load_library().ssm_get_device_status(_vp(_stream_handle(stream)), int(bool(clear)),
+                                                 ctypes.byref(code)))
+    return int(code.value)

@@ -1,0 +1,145 @@
+// device_math.cuh -- small device helpers shared by the scan and decode kernels.
+//
+// Precision policy:
+//  * the state recurrence, the C contraction and every intermediate are fp32;
+//  * exp(Delta * A) uses the SFU base-2 exponential (ex2.approx.ftz) on
+//    Delta * A * log2(e), relative error a few ulp;
+//  * softplus has two forms.  For bf16 I/O the SFU form
+//    max(s,0) + ln2 * lg2(1 + 2^(-|s| log2 e)) is used (absolute error
+//    ~1e-7, far inside bf16 rounding).  For fp32 I/O the accurate library
+//    log1pf/expf form is used, because lg2.approx has an absolute (not
+//    relative) error bound near 1 and Delta can be as small as ~1e-5;
+//  * silu(z) = z / (1 + 2^(-z log2 e)) with the SFU reciprocal.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cstdint>
+
+namespace ssm {
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ float lg2_approx(float x) {
+  float y;
+  asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ float rcp_approx(float x) {
+  float y;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// softplus(s) = log(1 + e^s) = max(s, 0) + log1p(e^{-|s|})
+template <bool PRECISE>
+__device__ __forceinline__ float softplus(float s) {
+  if (PRECISE) {
+    return fmaxf(s, 0.f) + log1pf(expf(-fabsf(s)));
+  } else {
+    const float e = ex2_approx(-fabsf(s) * kLog2e);
+    return fmaf(lg2_approx(1.f + e), kLn2, fmaxf(s, 0.f));
+  }
+}
+
+template <bool PRECISE>
+__device__ __forceinline__ float silu(float z) {
+  if (PRECISE) {
+    return z / (1.f + expf(-z));
+  } else {
+    return z * rcp_approx(1.f + ex2_approx(-z * kLog2e));
+  }
+}
+
+// Delta for one element: softplus(delta + bias) or the plain sum.
+template <bool PRECISE>
+__device__ __forceinline__ float delta_of(float delta, float bias, bool use_softplus) {
+  const float s = delta + bias;
+  return use_softplus ? softplus<PRECISE>(s) : s;
+}
+
+// ---------------------------------------------------------------------------
+// I/O element types
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float to_f32(float v) { return v; }
+__device__ __forceinline__ float to_f32(__nv_bfloat16 v) { return __bfloat162float(v); }
+
+template <typename T>
+__device__ __forceinline__ T from_f32(float v);
+template <>
+__device__ __forceinline__ float from_f32<float>(float v) { return v; }
+template <>
+__device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float v) { return __float2bfloat16_rn(v); }
+
+// 16-byte vectors: 8 bf16 or 4 fp32 values.
+template <typename T>
+struct Vec16;
+template <>
+struct Vec16<float> {
+  static constexpr int kN = 4;
+};
+template <>
+struct Vec16<__nv_bfloat16> {
+  static constexpr int kN = 8;
+};
+
+__device__ __forceinline__ void unpack16(const uint4& q, float (&f)[4]) {
+  f[0] = __uint_as_float(q.x);
+  f[1] = __uint_as_float(q.y);
+  f[2] = __uint_as_float(q.z);
+  f[3] = __uint_as_float(q.w);
+}
+
+__device__ __forceinline__ void unpack16(const uint4& q, float (&f)[8]) {
+  f[0] = __uint_as_float(q.x << 16);
+  f[1] = __uint_as_float(q.x & 0xffff0000u);
+  f[2] = __uint_as_float(q.y << 16);
+  f[3] = __uint_as_float(q.y & 0xffff0000u);
+  f[4] = __uint_as_float(q.z << 16);
+  f[5] = __uint_as_float(q.z & 0xffff0000u);
+  f[6] = __uint_as_float(q.w << 16);
+  f[7] = __uint_as_float(q.w & 0xffff0000u);
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+__device__ __forceinline__ uint4 pack16(const float (&f)[4]) {
+  return make_uint4(__float_as_uint(f[0]), __float_as_uint(f[1]), __float_as_uint(f[2]), __float_as_uint(f[3]));
+}
+
+__device__ __forceinline__ uint4 pack16(const float (&f)[8]) {
+  return make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]), pack_bf16x2(f[4], f[5]),
+                    pack_bf16x2(f[6], f[7]));
+}
+
+__device__ __forceinline__ uint4 ldg_nc_v4(const void* p) {
+  uint4 r;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "l"(p));
+  return r;
+}
+
+__device__ __forceinline__ void stg_v4(void* p, const uint4& v) {
+  asm volatile("st.global.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+               : "memory");
+}
+
+// ---------------------------------------------------------------------------
+// device status word (bounded waits record SSM_ERR_TIMEOUT here)
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void record_status(int* status, int code) {
+  if (status) atomicCAS(status, 0, code);
+}
+
+}  // namespace ssm

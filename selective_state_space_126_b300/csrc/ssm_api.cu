@@ -1,0 +1,452 @@
+// ssm_api.cu -- the C ABI: argument validation, path planning, dispatch.
+//
+// Every check here runs on the host before anything is enqueued, so a bad
+// argument never reaches a kernel.  The library allocates nothing: the
+// chunked path's records live in the caller's workspace.
+#include <algorithm>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "ssm_internal.h"
+
+namespace ssm {
+
+size_t tiled_smem_bytes(ssm_dtype_t io, int K, int NS);
+
+namespace {
+
+thread_local char g_detail[256] = {0};
+
+ssm_status_t fail(ssm_status_t st, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_detail, sizeof(g_detail), fmt, ap);
+  va_end(ap);
+  return st;
+}
+
+ssm_status_t ok() {
+  g_detail[0] = 0;
+  return SSM_OK;
+}
+
+int elem_size(ssm_dtype_t t) { return t == SSM_F32 ? 4 : 2; }
+
+// Address range [lo, hi) touched by a strided tensor (bytes), extents all > 0.
+void tensor_range(const void* base, int rank, const int64_t* ext, const int64_t* str, int es, uintptr_t* lo,
+                  uintptr_t* hi) {
+  int64_t last = 0;
+  for (int i = 0; i < rank; ++i) last += (ext[i] - 1) * str[i];
+  *lo = reinterpret_cast<uintptr_t>(base);
+  *hi = *lo + (uintptr_t)(last + 1) * es;
+}
+
+// Sufficient condition for a strided mapping to be one-to-one: sorted by
+// stride, each stride is at least the span of the dimensions below it.
+bool injective(int rank, const int64_t* ext, const int64_t* str) {
+  int idx[4];
+  int m = 0;
+  for (int i = 0; i < rank; ++i)
+    if (ext[i] > 1) idx[m++] = i;
+  for (int i = 1; i < m; ++i)   // insertion sort by stride (m <= 3)
+    for (int j = i; j > 0 && str[idx[j]] < str[idx[j - 1]]; --j) {
+      const int tmp = idx[j];
+      idx[j] = idx[j - 1];
+      idx[j - 1] = tmp;
+    }
+  int64_t span = 1;
+  for (int k = 0; k < m; ++k) {
+    if (str[idx[k]] < span) return false;
+    span = str[idx[k]] * ext[idx[k]];
+  }
+  return true;
+}
+
+bool overlaps(uintptr_t a0, uintptr_t a1, uintptr_t b0, uintptr_t b1) { return a0 < b1 && b0 < a1; }
+
+bool aligned(const void* p, int bytes) { return reinterpret_cast<uintptr_t>(p) % bytes == 0; }
+
+int device_sm_count() {
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0) return 148;
+  return sms;
+}
+
+ssm_status_t validate_scan(const ssm_scan_args_t* a, ScanProblem* p) {
+  if (!a) return fail(SSM_ERR_INVALID_ARG, "args is NULL");
+  if (a->io_dtype != SSM_F32 && a->io_dtype != SSM_BF16) return fail(SSM_ERR_INVALID_ARG, "io_dtype %d", (int)a->io_dtype);
+  if (a->batch < 0 || a->dim < 0 || a->seqlen < 0) return fail(SSM_ERR_INVALID_ARG, "negative size");
+  if (a->dstate < 1 || a->dstate > 64) return fail(SSM_ERR_UNSUPPORTED, "dstate %lld outside [1, 64]", (long long)a->dstate);
+  if (a->batch > 65535) return fail(SSM_ERR_UNSUPPORTED, "batch %lld > 65535", (long long)a->batch);
+  std::memset(p, 0, sizeof(*p));
+  p->B = a->batch; p->D = a->dim; p->L = a->seqlen; p->N = a->dstate;
+  p->io = a->io_dtype;
+  p->softplus = a->delta_softplus != 0;
+  p->u = a->u; p->delta = a->delta; p->z = a->z; p->Bm = a->Bm; p->Cm = a->Cm;
+  p->A = a->A; p->Dskip = a->Dskip; p->bias = a->delta_bias; p->h0 = a->h0; p->h_last = a->h_last; p->y = a->y;
+  std::memcpy(p->su, a->stride_u, sizeof(p->su));
+  std::memcpy(p->sd, a->stride_delta, sizeof(p->sd));
+  std::memcpy(p->sz, a->stride_z, sizeof(p->sz));
+  std::memcpy(p->sy, a->stride_y, sizeof(p->sy));
+  std::memcpy(p->sB, a->stride_B, sizeof(p->sB));
+  std::memcpy(p->sC, a->stride_C, sizeof(p->sC));
+  std::memcpy(p->sA, a->stride_A, sizeof(p->sA));
+  std::memcpy(p->sh0, a->stride_h0, sizeof(p->sh0));
+  std::memcpy(p->shl, a->stride_h_last, sizeof(p->shl));
+  if (p->B == 0 || p->D == 0) return ok();   // nothing to compute or write
+
+  if (!p->A) return fail(SSM_ERR_INVALID_ARG, "A is NULL");
+  if (p->sA[0] < 0 || p->sA[1] < 0) return fail(SSM_ERR_INVALID_ARG, "negative A stride");
+  const int es = elem_size(p->io);
+  struct Seq {
+    const char* name;
+    const void* ptr;
+    const int64_t* s;
+    int64_t ext1;
+    bool required;
+  } seqs[] = {{"u", p->u, p->su, p->D, true},         {"delta", p->delta, p->sd, p->D, true},
+              {"z", p->z, p->sz, p->D, false},        {"y", p->y, p->sy, p->D, true},
+              {"Bm", p->Bm, p->sB, p->N, true},       {"Cm", p->Cm, p->sC, p->N, true}};
+  for (const Seq& q : seqs) {
+    if (!q.ptr) {
+      // an empty sequence reads and writes none of these tensors
+      if (q.required && p->L > 0) return fail(SSM_ERR_INVALID_ARG, "%s is NULL", q.name);
+      continue;
+    }
+    if (q.s[0] < 0 || q.s[1] < 0) return fail(SSM_ERR_INVALID_ARG, "%s has a negative stride", q.name);
+    if (q.s[2] != 1 && p->L > 1) return fail(SSM_ERR_UNSUPPORTED, "%s time stride must be 1", q.name);
+    if (!aligned(q.ptr, es)) return fail(SSM_ERR_INVALID_ARG, "%s is not %d-byte aligned", q.name, es);
+  }
+  if (!aligned(p->A, 4)) return fail(SSM_ERR_INVALID_ARG, "A misaligned");
+  for (int i = 0; i < 3; ++i)
+    if ((p->h0 && p->sh0[i] < 0) || (p->h_last && p->shl[i] < 0))
+      return fail(SSM_ERR_INVALID_ARG, "negative state stride");
+
+  // outputs: one-to-one and disjoint from every input and from each other
+  int64_t ey[3] = {p->B, p->D, p->L};
+  int64_t sy[3] = {p->sy[0], p->sy[1], 1};
+  int64_t eh[3] = {p->B, p->D, p->N};
+  if (p->L > 0 && !injective(3, ey, sy)) return fail(SSM_ERR_INVALID_ARG, "y strides overlap");
+  if (p->h_last && !injective(3, eh, p->shl)) return fail(SSM_ERR_INVALID_ARG, "h_last strides overlap");
+  uintptr_t y0 = 0, y1 = 0, hl0 = 0, hl1 = 0;
+  if (p->L > 0) tensor_range(p->y, 3, ey, sy, es, &y0, &y1);
+  if (p->h_last) tensor_range(p->h_last, 3, eh, p->shl, 4, &hl0, &hl1);
+  struct In {
+    const void* ptr;
+    int rank;
+    int64_t ext[3];
+    int64_t str[3];
+    int es;
+  } ins[] = {
+      {p->u, 3, {p->B, p->D, p->L}, {p->su[0], p->su[1], 1}, es},
+      {p->delta, 3, {p->B, p->D, p->L}, {p->sd[0], p->sd[1], 1}, es},
+      {p->z, 3, {p->B, p->D, p->L}, {p->sz[0], p->sz[1], 1}, es},
+      {p->Bm, 3, {p->B, p->N, p->L}, {p->sB[0], p->sB[1], 1}, es},
+      {p->Cm, 3, {p->B, p->N, p->L}, {p->sC[0], p->sC[1], 1}, es},
+      {p->A, 2, {p->D, p->N, 1}, {p->sA[0], p->sA[1], 0}, 4},
+      {p->Dskip, 1, {p->D, 1, 1}, {1, 0, 0}, 4},
+      {p->bias, 1, {p->D, 1, 1}, {1, 0, 0}, 4},
+      {p->h0, 3, {p->B, p->D, p->N}, {p->sh0[0], p->sh0[1], p->sh0[2]}, 4},
+  };
+  for (const In& in : ins) {
+    if (!in.ptr) continue;
+    if (in.ext[2] == 0) continue;   // empty sequence: nothing is read
+    uintptr_t i0, i1;
+    tensor_range(in.ptr, in.rank, in.ext, in.str, in.es, &i0, &i1);
+    if (p->L > 0 && overlaps(y0, y1, i0, i1)) return fail(SSM_ERR_INVALID_ARG, "y overlaps an input");
+    if (p->h_last && overlaps(hl0, hl1, i0, i1)) return fail(SSM_ERR_INVALID_ARG, "h_last overlaps an input");
+  }
+  if (p->L > 0 && p->h_last && overlaps(y0, y1, hl0, hl1)) return fail(SSM_ERR_INVALID_ARG, "y overlaps h_last");
+  return ok();
+}
+
+// Tiled path eligibility: 16-byte vectors along t and TMA-compatible B/C.
+bool tiled_eligible(const ScanProblem& p) {
+  const int es = elem_size(p.io);
+  const int vec = 16 / es;
+  if (p.L <= 0 || p.L % vec != 0) return false;
+  if (p.L > (int64_t)INT32_MAX - 64) return false;
+  auto vrow = [&](const void* ptr, const int64_t* s) {
+    return aligned(ptr, 16) && s[0] % vec == 0 && s[1] % vec == 0;
+  };
+  if (!vrow(p.u, p.su) || !vrow(p.delta, p.sd) || !vrow(p.y, p.sy)) return false;
+  if (p.z && !vrow(p.z, p.sz)) return false;
+  auto bc = [&](const void* ptr, const int64_t* s) {
+    return aligned(ptr, 16) && s[1] > 0 && (s[1] * es) % 16 == 0 && (s[0] * es) % 16 == 0;
+  };
+  if (!bc(p.Bm, p.sB) || !bc(p.Cm, p.sC)) return false;
+  // both B and C must be batched, or both shared across the batch
+  const bool rb = p.sB[0] != 0 && p.B > 1, rc = p.sC[0] != 0 && p.B > 1;
+  return rb == rc;
+}
+
+TiledShape pick_shape(const ScanProblem& p) {
+  if (p.N > 32) return TiledShape{4, 16, 32};
+  if (p.N > 16) return TiledShape{4, 8, 32};
+  // N <= 16: the warp count per SM sets the load balance; the fewer threads
+  // share a channel the less shared-memory traffic per state update.
+  const int sms = device_sm_count();
+  const int64_t chan = p.B * p.D;
+  const char* env = getenv("SSM_TILED_K");
+  if (env) {
+    const int k = atoi(env);
+    if (k == 1) return TiledShape{1, 16, 128};
+    if (k == 4) return TiledShape{4, 4, 32};
+    if (k == 2) return TiledShape{2, 8, 64};
+  }
+  // threads per SM of work for K = 2; below ~4 warps per SM prefer K = 4
+  const double warps_per_sm_k2 = (double)chan * 2 / 32 / sms;
+  if (warps_per_sm_k2 < 8.0) return TiledShape{4, 4, 32};
+  return TiledShape{2, 8, 64};
+}
+
+ssm_status_t plan_scan(const ssm_scan_args_t* a, const ScanProblem& p, ScanPlan* plan) {
+  std::memset(plan, 0, sizeof(*plan));
+  plan->nchunks = 1;
+  plan->chunk_len = p.L;
+  const bool eligible = tiled_eligible(p);
+  const int flags = a->flags;
+  if (flags & SSM_SCAN_FORCE_GENERIC) {
+    plan->path = kPathGeneric;
+    return ok();
+  }
+  if (!eligible) {
+    if (flags & (SSM_SCAN_FORCE_TILED | SSM_SCAN_FORCE_CHUNKED))
+      return fail(SSM_ERR_UNSUPPORTED, "layout not eligible for the tiled kernels (alignment / strides / seqlen)");
+    plan->path = kPathGeneric;
+    return ok();
+  }
+  plan->shape = pick_shape(p);
+  const int CH = plan->shape.CH;
+  const int NP = plan->shape.K * plan->shape.NS;
+  const int sms = device_sm_count();
+  const int64_t ctas = p.B * ((p.D + CH - 1) / CH);
+  bool chunked = false;
+  int64_t chunk_len = 0;
+  if (flags & SSM_SCAN_FORCE_CHUNKED) {
+    chunked = true;
+  } else if (!(flags & SSM_SCAN_FORCE_TILED)) {
+    chunked = ctas < 2 * sms && p.L >= 8 * 1024;
+  }
+  if (chunked) {
+    if (a->chunk_len > 0) {
+      chunk_len = (a->chunk_len + kTileT - 1) / kTileT * kTileT;
+    } else {
+      // enough chunks for ~8 CTAs per SM, chunks of at least 1024 steps
+      int64_t want = (8 * (int64_t)sms + ctas - 1) / ctas;
+      want = std::max<int64_t>(2, std::min<int64_t>(want, p.L / 1024));
+      chunk_len = (p.L + want - 1) / want;
+      chunk_len = (chunk_len + kTileT - 1) / kTileT * kTileT;
+    }
+    const int64_t nchunks = (p.L + chunk_len - 1) / chunk_len;
+    if (nchunks > 65535) return fail(SSM_ERR_UNSUPPORTED, "too many chunks (%lld)", (long long)nchunks);
+    if (nchunks >= 2) {
+      plan->path = kPathChunked;
+      plan->nchunks = nchunks;
+      plan->chunk_len = chunk_len;
+      plan->workspace_bytes = (size_t)(p.B * p.D * nchunks * (NP + 1)) * sizeof(float);
+      return ok();
+    }
+  }
+  plan->path = kPathTiled;
+  return ok();
+}
+
+ssm_status_t cuda_fail(cudaError_t e) {
+  cudaGetLastError();   // clear the sticky-free error state
+  return fail(SSM_ERR_CUDA, "%s", cudaGetErrorString(e));
+}
+
+std::mutex g_enc_mu;
+EncodeTiledFn g_enc = nullptr;
+
+}  // namespace
+
+EncodeTiledFn get_encode_tiled() {
+  std::lock_guard<std::mutex> lk(g_enc_mu);
+  if (!g_enc) {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_enc = reinterpret_cast<EncodeTiledFn>(fn);
+  }
+  return g_enc;
+}
+
+// Device status words, one per device (set only by bounded waits that gave up).
+__device__ int g_device_status;
+
+int* device_status_ptr() {
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_device_status) != cudaSuccess) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  return static_cast<int*>(p);
+}
+
+}  // namespace ssm
+
+using namespace ssm;
+
+extern "C" {
+
+int ssm_version(void) { return (1 << 16) | 0; }
+
+size_t ssm_abi_sizeof(int which) {
+  if (which == 0) return sizeof(ssm_scan_args_t);
+  if (which == 1) return sizeof(ssm_step_args_t);
+  return 0;
+}
+
+const char* ssm_status_string(ssm_status_t s) {
+  switch (s) {
+    case SSM_OK: return "SSM_OK";
+    case SSM_ERR_INVALID_ARG: return "SSM_ERR_INVALID_ARG";
+    case SSM_ERR_UNSUPPORTED: return "SSM_ERR_UNSUPPORTED";
+    case SSM_ERR_CUDA: return "SSM_ERR_CUDA";
+    case SSM_ERR_TIMEOUT: return "SSM_ERR_TIMEOUT";
+    case SSM_ERR_WORKSPACE: return "SSM_ERR_WORKSPACE";
+  }
+  return "SSM_ERR_UNKNOWN";
+}
+
+const char* ssm_last_error_detail(void) { return g_detail; }
+
+ssm_status_t ssm_scan_workspace_size(const ssm_scan_args_t* args, size_t* bytes) {
+  if (!bytes) return fail(SSM_ERR_INVALID_ARG, "bytes is NULL");
+  *bytes = 0;
+  ScanProblem p;
+  ssm_status_t st = validate_scan(args, &p);
+  if (st != SSM_OK) return st;
+  if (p.B == 0 || p.D == 0) return ok();
+  ScanPlan plan;
+  st = plan_scan(args, p, &plan);
+  if (st != SSM_OK) return st;
+  *bytes = plan.workspace_bytes;
+  return ok();
+}
+
+int ssm_scan_plan_path(const ssm_scan_args_t* args) {
+  ScanProblem p;
+  if (validate_scan(args, &p) != SSM_OK) return -1;
+  if (p.B == 0 || p.D == 0) return 0;
+  ScanPlan plan;
+  if (plan_scan(args, p, &plan) != SSM_OK) return -1;
+  return (int)plan.path;
+}
+
+ssm_status_t ssm_scan_fwd(const ssm_scan_args_t* args, void* stream) {
+  ScanProblem p;
+  ssm_status_t st = validate_scan(args, &p);
+  if (st != SSM_OK) return st;
+  if (p.B == 0 || p.D == 0) return ok();
+  ScanPlan plan;
+  st = plan_scan(args, p, &plan);
+  if (st != SSM_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  if (plan.path == kPathGeneric) {
+    e = launch_scan_generic(p, s);
+  } else {
+    if (plan.workspace_bytes > 0) {
+      if (!args->workspace) return fail(SSM_ERR_WORKSPACE, "workspace of %zu bytes required", plan.workspace_bytes);
+      if (args->workspace_bytes < plan.workspace_bytes)
+        return fail(SSM_ERR_WORKSPACE, "workspace %zu < %zu bytes", args->workspace_bytes, plan.workspace_bytes);
+      if (!aligned(args->workspace, 16)) return fail(SSM_ERR_WORKSPACE, "workspace not 16-byte aligned");
+    }
+    e = launch_scan_tiled(p, plan, args->workspace, s);
+  }
+  if (e != cudaSuccess) return cuda_fail(e);
+  return ok();
+}
+
+ssm_status_t ssm_state_update(const ssm_step_args_t* a, void* stream) {
+  if (!a) return fail(SSM_ERR_INVALID_ARG, "args is NULL");
+  if (a->io_dtype != SSM_F32 && a->io_dtype != SSM_BF16) return fail(SSM_ERR_INVALID_ARG, "io_dtype");
+  if (a->batch < 0 || a->dim < 0) return fail(SSM_ERR_INVALID_ARG, "negative size");
+  if (a->dstate < 1 || a->dstate > 64) return fail(SSM_ERR_UNSUPPORTED, "dstate outside [1, 64]");
+  StepProblem p;
+  std::memset(&p, 0, sizeof(p));
+  p.B = a->batch; p.D = a->dim; p.N = a->dstate; p.io = a->io_dtype; p.softplus = a->delta_softplus != 0;
+  p.state = a->state; p.u = a->u; p.delta = a->delta; p.z = a->z; p.Bm = a->Bm; p.Cm = a->Cm;
+  p.A = a->A; p.Dskip = a->Dskip; p.bias = a->delta_bias; p.y = a->y;
+  std::memcpy(p.sst, a->stride_state, sizeof(p.sst));
+  std::memcpy(p.su, a->stride_u, sizeof(p.su));
+  std::memcpy(p.sd, a->stride_delta, sizeof(p.sd));
+  std::memcpy(p.sz, a->stride_z, sizeof(p.sz));
+  std::memcpy(p.sy, a->stride_y, sizeof(p.sy));
+  std::memcpy(p.sB, a->stride_B, sizeof(p.sB));
+  std::memcpy(p.sC, a->stride_C, sizeof(p.sC));
+  std::memcpy(p.sA, a->stride_A, sizeof(p.sA));
+  if (p.B == 0 || p.D == 0) return ok();
+  if (!p.state || !p.u || !p.delta || !p.Bm || !p.Cm || !p.A || !p.y)
+    return fail(SSM_ERR_INVALID_ARG, "required pointer is NULL");
+  const int es = elem_size(p.io);
+  const int64_t* strides[] = {p.su, p.sd, p.sz, p.sy, p.sB, p.sC, p.sA};
+  for (const int64_t* s : strides)
+    if (s[0] < 0 || s[1] < 0) return fail(SSM_ERR_INVALID_ARG, "negative stride");
+  for (int i = 0; i < 3; ++i)
+    if (p.sst[i] < 0) return fail(SSM_ERR_INVALID_ARG, "negative state stride");
+  const void* eptrs[] = {p.u, p.delta, p.z, p.Bm, p.Cm, p.y};
+  for (const void* q : eptrs)
+    if (q && !aligned(q, es)) return fail(SSM_ERR_INVALID_ARG, "misaligned pointer");
+  if (!aligned(p.state, 4) || !aligned(p.A, 4)) return fail(SSM_ERR_INVALID_ARG, "misaligned fp32 pointer");
+  int64_t est[3] = {p.B, p.D, p.N};
+  int64_t ey[2] = {p.B, p.D};
+  if (!injective(3, est, p.sst)) return fail(SSM_ERR_INVALID_ARG, "state strides overlap");
+  if (!injective(2, ey, p.sy)) return fail(SSM_ERR_INVALID_ARG, "y strides overlap");
+  uintptr_t s0, s1, y0, y1;
+  tensor_range(p.state, 3, est, p.sst, 4, &s0, &s1);
+  tensor_range(p.y, 2, ey, p.sy, es, &y0, &y1);
+  if (overlaps(s0, s1, y0, y1)) return fail(SSM_ERR_INVALID_ARG, "y overlaps state");
+  struct In {
+    const void* ptr;
+    int rank;
+    int64_t ext[2];
+    const int64_t* str;
+    int es;
+  } ins[] = {{p.u, 2, {p.B, p.D}, p.su, es},  {p.delta, 2, {p.B, p.D}, p.sd, es}, {p.z, 2, {p.B, p.D}, p.sz, es},
+             {p.Bm, 2, {p.B, p.N}, p.sB, es}, {p.Cm, 2, {p.B, p.N}, p.sC, es},    {p.A, 2, {p.D, p.N}, p.sA, 4}};
+  for (const In& in : ins) {
+    if (!in.ptr) continue;
+    uintptr_t i0, i1;
+    tensor_range(in.ptr, in.rank, in.ext, in.str, in.es, &i0, &i1);
+    if (overlaps(s0, s1, i0, i1) || overlaps(y0, y1, i0, i1))
+      return fail(SSM_ERR_INVALID_ARG, "an output overlaps an input");
+  }
+  const void* vecs[] = {p.Dskip, p.bias};
+  for (const void* v : vecs) {
+    if (!v) continue;
+    uintptr_t i0 = reinterpret_cast<uintptr_t>(v), i1 = i0 + (uintptr_t)p.D * 4;
+    if (overlaps(s0, s1, i0, i1) || overlaps(y0, y1, i0, i1))
+      return fail(SSM_ERR_INVALID_ARG, "an output overlaps an input");
+  }
+  cudaError_t e = launch_state_update(p, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e);
+  return ok();
+}
+
+ssm_status_t ssm_get_device_status(void* stream, int clear, int* code) {
+  if (!code) return fail(SSM_ERR_INVALID_ARG, "code is NULL");
+  *code = SSM_OK;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int host = 0;
+  cudaError_t e = cudaMemcpyFromSymbolAsync(&host, g_device_status, sizeof(int), 0, cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e == cudaSuccess && clear && host != 0) {
+    const int zero = 0;
+    e = cudaMemcpyToSymbolAsync(g_device_status, &zero, sizeof(int), 0, cudaMemcpyHostToDevice, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  }
+  if (e != cudaSuccess) return cuda_fail(e);
+  *code = host;
+  return ok();
+}
+
+}  // extern "C"

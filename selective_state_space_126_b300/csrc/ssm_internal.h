@@ -1,0 +1,70 @@
+// ssm_internal.h -- host-side structures shared by the library's translation units.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cstddef>
+#include <cstdint>
+
+#include "../../include/ssm.h"
+
+namespace ssm {
+
+// Validated scan problem, strides in elements.
+struct ScanProblem {
+  int64_t B, D, L, N;
+  ssm_dtype_t io;
+  bool softplus;
+  const void *u, *delta, *z, *Bm, *Cm;
+  const float *A, *Dskip, *bias, *h0;
+  float* h_last;
+  void* y;
+  int64_t su[3], sd[3], sz[3], sy[3], sB[3], sC[3], sA[2], sh0[3], shl[3];
+};
+
+struct StepProblem {
+  int64_t B, D, N;
+  ssm_dtype_t io;
+  bool softplus;
+  float* state;
+  const void *u, *delta, *z, *Bm, *Cm;
+  const float *A, *Dskip, *bias;
+  void* y;
+  int64_t sst[3], su[2], sd[2], sz[2], sy[2], sB[2], sC[2], sA[2];
+};
+
+enum ScanPath { kPathGeneric = 0, kPathTiled = 1, kPathChunked = 2 };
+
+// Tiled-kernel shape: K threads share one channel's states, NS states per thread.
+struct TiledShape {
+  int K;        // threads per channel (1, 2 or 4)
+  int NS;       // states per thread
+  int CH;       // channels per CTA (= 128 / K)
+};
+
+struct ScanPlan {
+  ScanPath path;
+  TiledShape shape;
+  int64_t chunk_len;      // chunked path: timesteps per chunk (multiple of the tile)
+  int64_t nchunks;
+  size_t workspace_bytes;
+};
+
+// device status word of the current device (bounded-wait timeouts)
+int* device_status_ptr();
+
+// launchers (return a cudaError_t from the launch)
+cudaError_t launch_scan_generic(const ScanProblem& p, cudaStream_t s);
+cudaError_t launch_scan_tiled(const ScanProblem& p, const ScanPlan& plan, void* workspace, cudaStream_t s);
+cudaError_t launch_state_update(const StepProblem& p, cudaStream_t s);
+
+// tile length of the tiled kernel (timesteps)
+constexpr int kTileT = 32;
+
+// tensor-map encoder from the driver (resolved once through the runtime)
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn get_encode_tiled();
+
+}  // namespace ssm

@@ -196,3 +196,37 @@ def decode_step_inputs(cfg: DecodeConfig, step: int, seed: int = 0) -> dict:
     return dict(u=draw(T_U, (B, D)), delta=draw(T_DELTA, (B, D)),
                 z=draw(T_Z, (B, D)) if cfg.gate else None,
                 Bm=draw(T_B, (B, N)), Cm=draw(T_C, (B, N)))
+
+
+def device_inputs(cfg: ScanConfig, seed=0, block=128, workers=8, device="cuda"):
+    """All inputs of ``cfg`` on the GPU (torch tensors), generated block by block on the host."""
+    import concurrent.futures as cf
+
+    import torch
+    B, D, L, N = cfg.batch, cfg.dim, cfg.seqlen, cfg.dstate
+    dt = torch.float32 if cfg.io_dtype == "f32" else torch.bfloat16
+    out = {}
+    tensors = [("u", T_U), ("delta", T_DELTA)] + ([("z", T_Z)] if cfg.gate else [])
+    for name, _ in tensors:
+        out[name] = torch.empty((B, D, L), dtype=dt, device=device)
+    jobs = [(name, tid, b, d0, min(D, d0 + block)) for name, tid in tensors for b in range(B)
+            for d0 in range(0, D, block)]
+
+    def gen(job):
+        name, tid, b, d0, d1 = job
+        return job, channel_rows(cfg, tid, b, d0, d1, seed)
+
+    with cf.ThreadPoolExecutor(max_workers=workers) as ex:
+        for (name, tid, b, d0, d1), rows in ex.map(gen, jobs):
+            out[name][b, d0:d1].copy_(torch.from_numpy(rows).to(dt))
+    if not cfg.gate:
+        out["z"] = None
+    bb = [0] if cfg.shared_bc else list(range(B))
+    up = lambda x, t=torch.float32: torch.from_numpy(np.ascontiguousarray(x)).to(t).to(device)
+    out["Bm"] = up(np.stack([bc_rows(cfg, T_B, b, seed) for b in bb]), dt)
+    out["Cm"] = up(np.stack([bc_rows(cfg, T_C, b, seed) for b in bb]), dt)
+    A, Dskip, bias = layer_params(D, N, cfg.dt_min, cfg.dt_max, seed)
+    out["A"] = up(A)
+    out["Dskip"] = up(Dskip) if cfg.dskip else None
+    out["delta_bias"] = up(bias)
+    return out

@@ -1,0 +1,197 @@
+"""C-ABI checks that need no GPU: the library loads, exports every symbol that
+include/ssm.h declares, its structs match the binding, host-side validation
+rejects bad arguments with the documented codes, and path planning picks the
+kernels it should.  No call here reaches a kernel: every argument set is
+either invalid (rejected before any CUDA call) or goes to host-only entry
+points (workspace size, plan)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import selective_state_space_126_b300 as ssm
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "ssm.h")
+
+# fake, distinct, 1 KiB-aligned device addresses; never dereferenced by these tests
+FAKE = {k: 0x10_0000_0000 + i * 0x1_0000_0000 for i, k in enumerate(
+    ["u", "delta", "z", "Bm", "Cm", "A", "Dskip", "bias", "h0", "h_last", "y", "state", "ws"])}
+
+
+def header_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(ssm_[a-z_]+)\s*\(", text)))
+
+
+def scan_args(B=2, D=64, L=256, N=16, io=ssm.SSM_BF16, **over):
+    a = ssm.ScanArgs()
+    a.batch, a.dim, a.seqlen, a.dstate = B, D, L, N
+    a.io_dtype = io
+    a.delta_softplus = 1
+    a.u, a.delta, a.z, a.Bm, a.Cm = FAKE["u"], FAKE["delta"], FAKE["z"], FAKE["Bm"], FAKE["Cm"]
+    a.A, a.Dskip, a.delta_bias, a.y = FAKE["A"], FAKE["Dskip"], FAKE["bias"], FAKE["y"]
+    for f in ("stride_u", "stride_delta", "stride_z", "stride_y"):
+        getattr(a, f)[:] = [D * L, L, 1]
+    a.stride_B[:] = [N * L, L, 1]
+    a.stride_C[:] = [N * L, L, 1]
+    a.stride_A[:] = [N, 1]
+    for k, v in over.items():
+        if isinstance(v, list):
+            getattr(a, k)[:] = v
+        else:
+            setattr(a, k, v)
+    return a
+
+
+def call_scan(a):
+    lib = ssm.load_library()
+    return lib.ssm_scan_fwd(ctypes.byref(a), None)
+
+
+@pytest.fixture(scope="module")
+def lib(ssm_lib):
+    return ssm.load_library()
+
+
+def test_every_header_symbol_is_exported(lib):
+    names = header_functions()
+    assert names, "no declarations parsed"
+    assert sorted(ssm.EXPORTED_SYMBOLS) == names
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_struct_sizes_match(lib):
+    assert lib.ssm_abi_sizeof(0) == ctypes.sizeof(ssm.ScanArgs)
+    assert lib.ssm_abi_sizeof(1) == ctypes.sizeof(ssm.StepArgs)
+    assert lib.ssm_abi_sizeof(7) == 0
+    assert ssm.ssm_version() >> 16 == 1
+
+
+def test_status_strings(lib):
+    for code, name in enumerate(["SSM_OK", "SSM_ERR_INVALID_ARG", "SSM_ERR_UNSUPPORTED", "SSM_ERR_CUDA",
+                                 "SSM_ERR_TIMEOUT", "SSM_ERR_WORKSPACE"]):
+        assert ssm.ssm_status_string(code) == name
+    assert ssm.ssm_status_string(99) == "SSM_ERR_UNKNOWN"
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(dstate=0), ssm.SSM_ERR_UNSUPPORTED),
+    (dict(dstate=65), ssm.SSM_ERR_UNSUPPORTED),
+    (dict(batch=-1), ssm.SSM_ERR_INVALID_ARG),
+    (dict(seqlen=-5), ssm.SSM_ERR_INVALID_ARG),
+    (dict(io_dtype=7), ssm.SSM_ERR_INVALID_ARG),
+    (dict(u=None), ssm.SSM_ERR_INVALID_ARG),
+    (dict(delta=None), ssm.SSM_ERR_INVALID_ARG),
+    (dict(Bm=None), ssm.SSM_ERR_INVALID_ARG),
+    (dict(Cm=None), ssm.SSM_ERR_INVALID_ARG),
+    (dict(A=None), ssm.SSM_ERR_INVALID_ARG),
+    (dict(y=None), ssm.SSM_ERR_INVALID_ARG),
+    (dict(stride_u=[64 * 256, 256, 2]), ssm.SSM_ERR_UNSUPPORTED),      # time stride must be 1
+    (dict(stride_B=[16 * 256, -256, 1]), ssm.SSM_ERR_INVALID_ARG),     # negative stride
+    (dict(y=FAKE["u"] + 1024), ssm.SSM_ERR_INVALID_ARG),               # y overlaps u
+    (dict(stride_y=[256, 256, 1]), ssm.SSM_ERR_INVALID_ARG),           # y maps two (b,d,t) to one address
+    (dict(u=FAKE["u"] + 1), ssm.SSM_ERR_INVALID_ARG),                  # misaligned bf16 pointer
+    (dict(h_last=FAKE["Bm"]), ssm.SSM_ERR_INVALID_ARG),                # h_last overlaps B
+])
+def test_scan_validation(lib, over, code):
+    rc = call_scan(scan_args(**over))
+    assert rc == code, (rc, ssm.ssm_status_string(rc), lib.ssm_last_error_detail())
+    assert lib.ssm_last_error_detail()
+
+
+def test_null_args(lib):
+    assert lib.ssm_scan_fwd(None, None) == ssm.SSM_ERR_INVALID_ARG
+    assert lib.ssm_state_update(None, None) == ssm.SSM_ERR_INVALID_ARG
+    n = ctypes.c_size_t(5)
+    assert lib.ssm_scan_workspace_size(None, ctypes.byref(n)) == ssm.SSM_ERR_INVALID_ARG
+    assert lib.ssm_scan_workspace_size(ctypes.byref(scan_args()), None) == ssm.SSM_ERR_INVALID_ARG
+
+
+def test_empty_problem_is_a_noop(lib):
+    # batch 0 or dim 0: nothing to read or write, no CUDA call
+    assert call_scan(scan_args(batch=0)) == ssm.SSM_OK
+    assert call_scan(scan_args(dim=0, u=None, y=None)) == ssm.SSM_OK
+
+
+def step_args(B=4, D=32, N=16, **over):
+    a = ssm.StepArgs()
+    a.batch, a.dim, a.dstate = B, D, N
+    a.io_dtype = ssm.SSM_BF16
+    a.delta_softplus = 1
+    a.state, a.u, a.delta, a.z = FAKE["state"], FAKE["u"], FAKE["delta"], FAKE["z"]
+    a.Bm, a.Cm, a.A, a.y = FAKE["Bm"], FAKE["Cm"], FAKE["A"], FAKE["y"]
+    a.stride_state[:] = [D * N, N, 1]
+    for f in ("stride_u", "stride_delta", "stride_z", "stride_y"):
+        getattr(a, f)[:] = [D, 1]
+    a.stride_B[:] = [N, 1]
+    a.stride_C[:] = [N, 1]
+    a.stride_A[:] = [N, 1]
+    for k, v in over.items():
+        if isinstance(v, list):
+            getattr(a, k)[:] = v
+        else:
+            setattr(a, k, v)
+    return a
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(dstate=0), ssm.SSM_ERR_UNSUPPORTED),
+    (dict(state=None), ssm.SSM_ERR_INVALID_ARG),
+    (dict(y=FAKE["state"]), ssm.SSM_ERR_INVALID_ARG),          # y overlaps the state
+    (dict(stride_state=[16, 16, 1]), ssm.SSM_ERR_INVALID_ARG),  # state rows alias
+    (dict(u=FAKE["state"] + 64), ssm.SSM_ERR_INVALID_ARG),      # input inside the state
+    (dict(stride_u=[-1, 1]), ssm.SSM_ERR_INVALID_ARG),
+])
+def test_step_validation(lib, over, code):
+    rc = lib.ssm_state_update(ctypes.byref(step_args(**over)), None)
+    assert rc == code, (rc, lib.ssm_last_error_detail())
+
+
+def test_step_empty_is_noop(lib):
+    assert lib.ssm_state_update(ctypes.byref(step_args(batch=0)), None) == ssm.SSM_OK
+
+
+@pytest.mark.parametrize("kw,path", [
+    (dict(L=255), "generic"),                       # ragged rows: not 16-byte vectors
+    (dict(L=256), "tiled"),
+    (dict(L=260, io=ssm.SSM_F32), "tiled"),          # fp32 rows of 4-element vectors
+    (dict(L=258, io=ssm.SSM_F32), "generic"),
+    (dict(L=256, flags=ssm.SSM_SCAN_FORCE_GENERIC), "generic"),
+    (dict(L=4096, flags=ssm.SSM_SCAN_FORCE_CHUNKED, chunk_len=1024), "chunked"),
+    (dict(B=1, D=1536, L=1 << 20), "chunked"),       # long sequence, few channels
+    (dict(B=4, D=5120, L=2048), "tiled"),
+])
+def test_plan(lib, kw, path):
+    kw = dict(kw)
+    flags = kw.pop("flags", 0)
+    chunk_len = kw.pop("chunk_len", 0)
+    B, D, L = kw.get("B", 2), kw.get("D", 64), kw["L"]
+    a = scan_args(B=B, D=D, L=L, io=kw.get("io", ssm.SSM_BF16), flags=flags, chunk_len=chunk_len)
+    assert ssm.ssm_scan_plan_path(a) == path
+    ws = ssm.ssm_scan_workspace_size(a)
+    assert (ws > 0) == (path == "chunked")
+
+
+def test_force_tiled_on_ragged_is_unsupported(lib):
+    a = scan_args(L=255, flags=ssm.SSM_SCAN_FORCE_TILED)
+    assert call_scan(a) == ssm.SSM_ERR_UNSUPPORTED
+
+
+def test_chunked_without_workspace_is_rejected(lib):
+    a = scan_args(L=4096, flags=ssm.SSM_SCAN_FORCE_CHUNKED, chunk_len=1024)
+    assert call_scan(a) == ssm.SSM_ERR_WORKSPACE
+    a.workspace = FAKE["ws"]
+    a.workspace_bytes = 16
+    assert call_scan(a) == ssm.SSM_ERR_WORKSPACE
+
+
+def test_workspace_size_formula(lib):
+    # records: (N padded + 1) floats per (batch, channel, chunk)
+    a = scan_args(B=2, D=64, L=4096, flags=ssm.SSM_SCAN_FORCE_CHUNKED, chunk_len=1000)
+    ws = ssm.ssm_scan_workspace_size(a)
+    chunk = 1024                       # rounded up to the 32-step tile
+    nchunks = -(-4096 // chunk)
+    assert ws == 2 * 64 * nchunks * (16 + 1) * 4

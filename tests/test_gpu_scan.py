@@ -1,0 +1,237 @@
+"""GPU parity of ssm_scan_fwd against the fp64 oracle, through the C ABI.
+
+Every kernel path (generic, tiled single pass, chunked three-pass) is
+compared element by element with the oracle on small and ragged shapes, and
+on the five workloads at full size through sampled channels (the launch
+configuration the benchmark times).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import selective_state_space_126_b300 as ssm
+from selective_state_space_126_b300 import synthetic as syn
+from gpu_util import (assert_close, device_inputs, host, oracle_channels, rel_l2, sample_channels, to_dev)
+
+pytestmark = pytest.mark.gpu
+
+FLAGS = {"auto": 0, "generic": ssm.SSM_SCAN_FORCE_GENERIC, "tiled": ssm.SSM_SCAN_FORCE_TILED,
+         "chunked": ssm.SSM_SCAN_FORCE_CHUNKED}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _setup(ssm_lib, cuda_ok):
+    torch.manual_seed(0)
+    yield
+    assert ssm.ssm_get_device_status(clear=True) == ssm.SSM_OK
+
+
+def rand_case(B, D, L, N, io, seed=0, gate=True, dskip=True, bias=True, h0=False, shared_bc=False):
+    """Inputs drawn with the workload distributions, at an arbitrary shape."""
+    rng = np.random.default_rng(seed)
+    r = lambda *s: syn.round_io(rng.standard_normal(s, dtype=np.float32), io)
+    A, Dv, bv = syn.layer_params(D, N, 1e-3, 1e-1, seed)
+    A = A * rng.uniform(0.5, 1.5, A.shape).astype(np.float32)     # general (not S4D-structured) A
+    return dict(u=r(B, D, L), delta=r(B, D, L), z=r(B, D, L) if gate else None,
+                Bm=r(1 if shared_bc else B, N, L), Cm=r(1 if shared_bc else B, N, L), A=A,
+                Dskip=Dv if dskip else None, delta_bias=bv if bias else None,
+                h0=rng.standard_normal((B, D, N)).astype(np.float32) if h0 else None)
+
+
+def gpu_scan(case, io, path="auto", chunk_len=0, softplus=True):
+    dev = {k: (to_dev(v, io) if k in ("u", "delta", "z", "Bm", "Cm") else to_dev(v)) for k, v in case.items()}
+    Bm, Cm = dev["Bm"], dev["Cm"]
+    if Bm.shape[0] == 1 and dev["u"].shape[0] > 1:
+        Bm, Cm = Bm[0], Cm[0]                  # (N, L): batch stride 0
+    y, hl = ssm.ssm_scan_fwd(dev["u"], dev["delta"], dev["A"], Bm, Cm, Dskip=dev["Dskip"], z=dev["z"],
+                             delta_bias=dev["delta_bias"], h0=dev["h0"], delta_softplus=softplus,
+                             return_last_state=True, flags=FLAGS[path], chunk_len=chunk_len)
+    torch.cuda.synchronize()
+    return host(y), host(hl)
+
+
+def oracle_case(case, softplus=True):
+    return oracle.selective_scan(case["u"], case["delta"], case["A"], case["Bm"], case["Cm"],
+                                 Dskip=case["Dskip"], z=case["z"], delta_bias=case["delta_bias"],
+                                 h0=case["h0"], delta_softplus=softplus, return_last_state=True)
+
+
+# ---------------------------------------------------------------------------
+# the tiny fp32 workload through every path
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("path,chunk", [("auto", 0), ("generic", 0), ("tiled", 0), ("chunked", 64),
+                                        ("chunked", 32)])
+def test_tiny_fp32_every_path(path, chunk):
+    cfg = syn.TINY
+    inp = syn.scan_inputs(cfg)
+    case = dict(inp, h0=None)
+    y, hl = gpu_scan(case, "f32", path, chunk)
+    yr, hr = oracle_case(case)
+    assert_close("f32", y, yr, f"y {path}")
+    assert_close("f32", hl, hr, f"h_last {path}")
+
+
+# ---------------------------------------------------------------------------
+# ragged, odd and edge shapes, both dtypes, every option
+# ---------------------------------------------------------------------------
+
+SHAPES = [
+    # B, D, L, N
+    (1, 1, 1, 16), (1, 3, 7, 4), (2, 5, 31, 16), (1, 37, 255, 16), (2, 33, 256, 16), (1, 100, 1000, 13),
+    (2, 65, 296, 16), (1, 17, 4097, 16), (2, 40, 512, 1), (1, 129, 64, 32), (1, 20, 128, 64), (3, 7, 40, 5),
+]
+
+
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+@pytest.mark.parametrize("shape", SHAPES, ids=lambda s: "x".join(map(str, s)))
+def test_shapes(io, shape):
+    B, D, L, N = shape
+    case = rand_case(B, D, L, N, io, seed=B * 1000 + D + L + N, h0=True)
+    yr, hr = oracle_case(case)
+    paths = ["auto", "generic"]
+    vec = 4 if io == "f32" else 8
+    if L % vec == 0:
+        paths += ["tiled"]
+        if L >= 64:
+            paths += ["chunked"]
+    for path in paths:
+        y, hl = gpu_scan(case, io, path, chunk_len=64 if path == "chunked" else 0)
+        assert_close(io, y, yr, f"y {path} {shape}")
+        assert_close(io, hl, hr, f"h_last {path} {shape}")
+
+
+@pytest.mark.parametrize("opt", ["no_gate", "no_dskip", "no_bias", "no_h0", "shared_bc", "softplus_off", "bare"])
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+def test_options(io, opt):
+    kw = dict(gate=opt not in ("no_gate", "bare"), dskip=opt not in ("no_dskip", "bare"),
+              bias=opt not in ("no_bias", "bare"), h0=opt not in ("no_h0", "bare"), shared_bc=opt == "shared_bc")
+    case = rand_case(3, 70, 320, 16, io, seed=7, **kw)
+    softplus = opt != "softplus_off"
+    if not softplus:   # keep Delta positive and O(0.01..0.1) without the softplus
+        case["delta"] = syn.round_io(np.abs(case["delta"]) * 0.05, io)
+        case["delta_bias"] = None
+    yr, hr = oracle_case(case, softplus)
+    for path in ("auto", "generic", "chunked"):
+        y, hl = gpu_scan(case, io, path, chunk_len=96 if path == "chunked" else 0, softplus=softplus)
+        assert_close(io, y, yr, f"y {opt} {path}")
+        assert_close(io, hl, hr, f"h_last {opt} {path}")
+
+
+def test_padded_row_strides():
+    """Rows stored with padding (row stride 104 for L = 100), seen through strides."""
+    case = rand_case(2, 24, 100, 16, "f32", seed=3)
+    dev = {}
+    for k in ("u", "delta", "z"):
+        buf = torch.zeros((2, 24, 104), dtype=torch.float32, device="cuda")   # padded rows: stride 104
+        buf[..., :100] = to_dev(case[k])
+        dev[k] = buf[..., :100]
+    y = ssm.ssm_scan_fwd(dev["u"], dev["delta"], to_dev(case["A"]), to_dev(case["Bm"]), to_dev(case["Cm"]),
+                         Dskip=to_dev(case["Dskip"]), z=dev["z"], delta_bias=to_dev(case["delta_bias"]))
+    yr, _ = oracle_case(case)
+    assert_close("f32", host(y), yr, "strided")
+
+
+def test_chunked_equals_single_pass_medium():
+    case = rand_case(2, 96, 4096, 16, "bf16", seed=11, h0=True)
+    yr, hr = oracle_case(case)
+    y1, h1 = gpu_scan(case, "bf16", "tiled")
+    for chunk in (512, 1000, 2048):
+        y2, h2 = gpu_scan(case, "bf16", "chunked", chunk_len=chunk)
+        assert_close("bf16", y2, yr, f"chunked {chunk}")
+        assert_close("bf16", h2, hr, f"chunked h {chunk}")
+        assert rel_l2(y2, y1) < 2e-3
+
+
+def test_deterministic():
+    case = rand_case(2, 64, 512, 16, "bf16", seed=5)
+    a, _ = gpu_scan(case, "bf16", "auto")
+    b, _ = gpu_scan(case, "bf16", "auto")
+    assert np.array_equal(a, b)
+    c, _ = gpu_scan(case, "bf16", "chunked", chunk_len=128)
+    d, _ = gpu_scan(case, "bf16", "chunked", chunk_len=128)
+    assert np.array_equal(c, d)
+
+
+def test_empty_and_zero_length():
+    u = torch.zeros((2, 3, 0), dtype=torch.float32, device="cuda")
+    A = -torch.ones((3, 4), device="cuda")
+    h0 = torch.randn((2, 3, 4), device="cuda")
+    y, hl = ssm.ssm_scan_fwd(u, u, A, torch.zeros((2, 4, 0), device="cuda"), torch.zeros((2, 4, 0), device="cuda"),
+                             h0=h0, return_last_state=True)
+    torch.cuda.synchronize()
+    assert y.shape == (2, 3, 0)
+    assert torch.equal(hl, h0)          # an empty sequence returns the initial state
+    e = torch.zeros((0, 3, 8), dtype=torch.bfloat16, device="cuda")
+    y = ssm.ssm_scan_fwd(e, e, A, torch.zeros((0, 4, 8), dtype=torch.bfloat16, device="cuda"),
+                         torch.zeros((0, 4, 8), dtype=torch.bfloat16, device="cuda"))
+    assert y.shape == (0, 3, 8)
+
+
+# ---------------------------------------------------------------------------
+# the workloads at full size (sampled channels against the oracle)
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("cfg", [syn.M130, syn.M2P8], ids=lambda c: c.name)
+def test_workload_full_size(cfg):
+    inp = device_inputs(cfg)
+    y, hl = ssm.ssm_scan_fwd(inp["u"], inp["delta"], inp["A"], inp["Bm"], inp["Cm"], Dskip=inp["Dskip"],
+                             z=inp["z"], delta_bias=inp["delta_bias"], return_last_state=True)
+    torch.cuda.synchronize()
+    chans = sample_channels(cfg, k=64)
+    yr, hr = oracle_channels(cfg, chans)
+    got = np.stack([host(y[b, d]) for b, d in chans])
+    goth = np.stack([host(hl[b, d]) for b, d in chans])
+    assert_close(cfg.io_dtype, got, yr, cfg.name)
+    assert_close(cfg.io_dtype, goth, hr, cfg.name + " h_last")
+    assert torch.isfinite(y.float()).all()
+
+
+def test_time_invariant_equals_convolution():
+    """Delta, B, C constant in t (B/C shared across the batch): y = K * u + D u, gated, with
+    K_k = sum_n C[n] Abar[n]^k Delta B[n] -- the convolution form of the LTI SSM."""
+    cfg = syn.M2P8_TI
+    inp = device_inputs(cfg)
+    Bm, Cm = inp["Bm"][0], inp["Cm"][0]             # (N, L), batch stride 0
+    y = ssm.ssm_scan_fwd(inp["u"], inp["delta"], inp["A"], Bm, Cm, Dskip=inp["Dskip"], z=inp["z"],
+                         delta_bias=inp["delta_bias"])
+    torch.cuda.synchronize()
+    A, Dskip, bias = syn.layer_params(cfg.dim, cfg.dstate, cfg.dt_min, cfg.dt_max)
+    Bv = syn.bc_rows(cfg, syn.T_B, 0)[:, 0].astype(np.float64)
+    Cv = syn.bc_rows(cfg, syn.T_C, 0)[:, 0].astype(np.float64)
+    L = cfg.seqlen
+    ks = np.arange(L)
+    chans = sample_channels(cfg, k=24)
+    got, ref = [], []
+    for _, d in chans:
+        u = syn.channel_rows(cfg, syn.T_U, 0, d, d + 1)[0].astype(np.float64)
+        z = syn.channel_rows(cfg, syn.T_Z, 0, d, d + 1)[0].astype(np.float64)
+        s = float(syn.channel_rows(cfg, syn.T_DELTA, 0, d, d + 1)[0, 0]) + float(bias[d])
+        dt = np.logaddexp(0.0, s)
+        abar = np.exp(dt * A[d].astype(np.float64))
+        K = (Cv[None, :] * np.power(abar[None, :], ks[:, None]) * (dt * Bv)[None, :]).sum(1)
+        conv = np.convolve(u, K)[:L]
+        ref.append((conv + Dskip[d] * u) * z / (1.0 + np.exp(-z)))
+        got.append(host(y[0, d]))
+    assert_close("bf16", np.stack(got), np.stack(ref), "TI convolution")
+
+
+@pytest.mark.slow
+def test_long_sequence_chunked():
+    cfg = syn.LONG
+    inp = device_inputs(cfg, block=64)
+    args = ssm.make_scan_args(inp["u"], inp["delta"], inp["A"], inp["Bm"], inp["Cm"], inp["u"], inp["Dskip"],
+                              inp["z"], inp["delta_bias"])
+    assert ssm.ssm_scan_plan_path(args) == "chunked"
+    y, hl = ssm.ssm_scan_fwd(inp["u"], inp["delta"], inp["A"], inp["Bm"], inp["Cm"], Dskip=inp["Dskip"],
+                             z=inp["z"], delta_bias=inp["delta_bias"], return_last_state=True)
+    torch.cuda.synchronize()
+    chans = sample_channels(cfg, k=8)
+    yr, hr = oracle_channels(cfg, chans)
+    got = np.stack([host(y[b, d]) for b, d in chans])
+    goth = np.stack([host(hl[b, d]) for b, d in chans])
+    assert_close("bf16", got, yr, "long y")
+    assert_close("bf16", goth, hr, "long h_last")
+    # the late part of the sequence (after ~10^6 carried steps) on its own
+    assert_close("bf16", got[:, -4096:], yr[:, -4096:], "long y tail")
