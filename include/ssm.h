@@ -148,6 +148,37 @@ const char *ssm_last_error_detail(void);
  * `stream`.  *code receives SSM_OK or the first error recorded. */
 ssm_status_t ssm_get_device_status(void *stream, int clear, int *code);
 
+/*
+ * ssm_scan_fwd_noalloc -- the chunked (three-pass) scan for callers that
+ * cannot allocate device memory.  No counterpart in the paper: it is a
+ * packaging of ssm_scan_fwd's chunked path for a deployment constraint.
+ *
+ * Some callers have no way to hand the library a workspace: a plugin inside
+ * an engine that owns every byte of device memory, a host that only holds
+ * the raw input and output pointers, or code that must not take the implicit
+ * device synchronisation of cudaMalloc/cudaFree.  This entry point takes the
+ * same arguments as ssm_scan_fwd (args->workspace and args->workspace_bytes
+ * are ignored) and keeps the chunk records in a scratch array that the
+ * library reserves statically on every GPU it is loaded on, for the life of
+ * the process: SSM_NOALLOC_SCRATCH_BYTES bytes.  It calls no allocator.
+ *
+ *   - The problem must fit: ssm_scan_workspace_size() with
+ *     flags = SSM_SCAN_FORCE_CHUNKED must report at most
+ *     SSM_NOALLOC_SCRATCH_BYTES, else SSM_ERR_WORKSPACE is returned and
+ *     nothing is enqueued.  Layouts the chunked path cannot take return
+ *     SSM_ERR_UNSUPPORTED.
+ *   - The first call on each device resolves the scratch array's device
+ *     address (cudaGetSymbolAddress) with that device current; make that
+ *     first call before any stream capture on the device.
+ *   - Every call on a device shares the one scratch array and leaves its
+ *     records there.  No record needs to start at zero (each call writes
+ *     every record before reading it), but calls whose kernels overlap on
+ *     the GPU (different streams, no ordering between them) race on the
+ *     array and corrupt each other's results: order them on one stream.
+ */
+#define SSM_NOALLOC_SCRATCH_BYTES ((size_t)8 << 20)
+ssm_status_t ssm_scan_fwd_noalloc(const ssm_scan_args_t *args, void *stream);
+
 /* Kernel path ssm_scan_fwd would take for these arguments:
  * 0 = generic, 1 = tiled single pass, 2 = chunked three-pass; -1 on error. */
 int ssm_scan_plan_path(const ssm_scan_args_t *args);

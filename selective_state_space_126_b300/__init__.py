@@ -28,7 +28,7 @@ PATH_NAMES = {0: "generic", 1: "tiled", 2: "chunked"}
 # every symbol include/ssm.h declares
 EXPORTED_SYMBOLS = ["ssm_scan_workspace_size", "ssm_scan_fwd", "ssm_state_update", "ssm_status_string",
                     "ssm_last_error_detail", "ssm_get_device_status", "ssm_scan_plan_path", "ssm_version",
-                    "ssm_abi_sizeof"]
+                    "ssm_abi_sizeof", "ssm_scan_fwd_noalloc"]
 
 _i64 = ctypes.c_int64
 _vp = ctypes.c_void_p
@@ -97,6 +97,8 @@ def load_library(path: str = LIB_PATH):
         lib.ssm_scan_plan_path.restype = ctypes.c_int
         lib.ssm_version.argtypes = []
         lib.ssm_version.restype = ctypes.c_int
+        lib.ssm_scan_fwd_noalloc.argtypes = [ctypes.POINTER(ScanArgs), _vp]
+        lib.ssm_scan_fwd_noalloc.restype = ctypes.c_int
         lib.ssm_abi_sizeof.argtypes = [ctypes.c_int]
         lib.ssm_abi_sizeof.restype = ctypes.c_size_t
         if lib.ssm_abi_sizeof(0) != ctypes.sizeof(ScanArgs) or lib.ssm_abi_sizeof(1) != ctypes.sizeof(StepArgs):
@@ -294,3 +296,23 @@ def ssm_get_device_status(clear=True, stream=None) -> int:
     _check(load_library().ssm_get_device_status(_vp(_stream_handle(stream)), int(bool(clear)),
                                                  ctypes.byref(code)))
     return int(code.value)
+
+
+# Bytes of the static scratch array ssm_scan_fwd_noalloc keeps its chunk records in.
+SSM_NOALLOC_SCRATCH_BYTES = 8 << 20
+
+
+def ssm_scan_fwd_noalloc(u, delta, A, Bm, Cm, y, Dskip=None, z=None, delta_bias=None, h0=None, h_last=None,
+                         delta_softplus=True, chunk_len=0, stream=None):
+    """The chunked scan without a caller workspace, for callers that cannot allocate.
+
+    The caller passes every input and the outputs (``y`` and optionally
+    ``h_last``); the chunk records live in a scratch array the library holds
+    statically on each GPU (SSM_NOALLOC_SCRATCH_BYTES).  Nothing is allocated
+    here or in the library.  Calls on one device share that array: do not let
+    two of them overlap on the GPU.
+    """
+    args = make_scan_args(u, delta, A, Bm, Cm, y, Dskip, z, delta_bias, h0, h_last, delta_softplus,
+                          SSM_SCAN_FORCE_CHUNKED, chunk_len, None)
+    _check(load_library().ssm_scan_fwd_noalloc(ctypes.byref(args), _vp(_stream_handle(stream))))
+    return y

@@ -432,6 +432,72 @@ ssm_status_t ssm_state_update(const ssm_step_args_t* a, void* stream) {
   return ok();
 }
 
+// ---------------------------------------------------------------------------
+// ssm_scan_fwd_noalloc: the chunked scan with its records in a static device
+// array instead of a caller workspace (for callers that cannot allocate).
+// ---------------------------------------------------------------------------
+}  // extern "C"
+
+namespace ssm {
+namespace {
+
+// One per device that loads the library, held until the process exits.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[SSM_NOALLOC_SCRATCH_BYTES];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_noalloc_mu;
+void* g_noalloc_ptr[kMaxDevices] = {nullptr};
+
+// Device address of the scratch array on the current device, resolved once per
+// device.  Returns nullptr (and fills *err) if the lookup fails.
+void* noalloc_scratch(cudaError_t* err) {
+  int dev = 0;
+  *err = cudaGetDevice(&dev);
+  if (*err != cudaSuccess) return nullptr;
+  if (dev < 0 || dev >= kMaxDevices) {
+    *err = cudaErrorInvalidDevice;
+    return nullptr;
+  }
+  std::lock_guard<std::mutex> lk(g_noalloc_mu);
+  if (!g_noalloc_ptr[dev]) {
+    void* p = nullptr;
+    *err = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (*err != cudaSuccess) return nullptr;
+    g_noalloc_ptr[dev] = p;
+  }
+  return g_noalloc_ptr[dev];
+}
+
+}  // namespace
+}  // namespace ssm
+
+extern "C" {
+
+ssm_status_t ssm_scan_fwd_noalloc(const ssm_scan_args_t* args, void* stream) {
+  ScanProblem p;
+  ssm_status_t st = validate_scan(args, &p);
+  if (st != SSM_OK) return st;
+  if (p.B == 0 || p.D == 0) return ok();
+  ssm_scan_args_t a = *args;
+  a.flags = SSM_SCAN_FORCE_CHUNKED;
+  a.workspace = nullptr;
+  a.workspace_bytes = 0;
+  ScanPlan plan;
+  st = plan_scan(&a, p, &plan);
+  if (st != SSM_OK) return st;
+  if (plan.path != kPathChunked)
+    return fail(SSM_ERR_UNSUPPORTED, "sequence too short for the chunked path (%lld steps)", (long long)p.L);
+  if (plan.workspace_bytes > SSM_NOALLOC_SCRATCH_BYTES)
+    return fail(SSM_ERR_WORKSPACE, "needs %zu bytes of chunk records; the static scratch holds %zu",
+                plan.workspace_bytes, (size_t)SSM_NOALLOC_SCRATCH_BYTES);
+  cudaError_t e = cudaSuccess;
+  void* scratch = noalloc_scratch(&e);
+  if (!scratch) return cuda_fail(e);
+  e = launch_scan_tiled(p, plan, scratch, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e);
+  return ok();
+}
+
 ssm_status_t ssm_get_device_status(void* stream, int clear, int* code) {
   if (!code) return fail(SSM_ERR_INVALID_ARG, "code is NULL");
   *code = SSM_OK;
