@@ -221,11 +221,12 @@ def test_time_invariant_equals_convolution():
 def test_long_sequence_chunked():
     cfg = syn.LONG
     inp = device_inputs(cfg, block=64)
-    args = ssm.make_scan_args(inp["u"], inp["delta"], inp["A"], inp["Bm"], inp["Cm"], inp["u"], inp["Dskip"],
+    y = torch.empty_like(inp["u"])
+    args = ssm.make_scan_args(inp["u"], inp["delta"], inp["A"], inp["Bm"], inp["Cm"], y, inp["Dskip"],
                               inp["z"], inp["delta_bias"])
     assert ssm.ssm_scan_plan_path(args) == "chunked"
     y, hl = ssm.ssm_scan_fwd(inp["u"], inp["delta"], inp["A"], inp["Bm"], inp["Cm"], Dskip=inp["Dskip"],
-                             z=inp["z"], delta_bias=inp["delta_bias"], return_last_state=True)
+                             z=inp["z"], delta_bias=inp["delta_bias"], return_last_state=True, y=y)
     torch.cuda.synchronize()
     chans = sample_channels(cfg, k=8)
     yr, hr = oracle_channels(cfg, chans)
