@@ -10,10 +10,12 @@
 // state never reaches HBM; this kernel keeps that property with a design of
 // its own for this GPU:
 //
-//   * one CTA = 128 threads = one batch row and CH = 128/K channels; K threads
-//     share a channel, each owning NS = NP/K states in registers.  A warp is
-//     32 channels with the same state group, so every read of B_t / C_t from
-//     shared memory is a warp-uniform broadcast;
+//   * one CTA = 32*K threads = one batch row and CH = 32 channels; K threads
+//     share a channel, each owning NS = NP/K states in registers.  Warp g holds
+//     state group g of all 32 channels, so every read of B_t / C_t from shared
+//     memory is a warp-uniform broadcast.  Small CTAs keep the work per SM even
+//     (640 CTAs for 4 x 5120 channels on 148 SMs) and let the load, scan and
+//     store phases of neighbouring CTAs overlap;
 //   * the time axis is walked in tiles of T = 32 steps.  Per tile:
 //       A. u / delta (and z) arrive through coalesced 16-byte loads issued one
 //          tile ahead; Delta = softplus(delta + bias) and Delta*u are computed
@@ -43,7 +45,12 @@
 namespace ssm {
 namespace {
 
-constexpr int kThreads = 128;
+constexpr int CH = 32;   // channels per CTA, one per lane
+
+// Minimum resident CTAs of 128 threads per SM the register allocation is sized for.
+#ifndef SSM_TILED_MIN_BLOCKS
+#define SSM_TILED_MIN_BLOCKS 3
+#endif
 constexpr int T = kTileT;
 constexpr int MODE_OUTPUT = 0;
 constexpr int MODE_RECORD = 1;
@@ -120,7 +127,6 @@ __device__ __forceinline__ void tma_load(uint32_t dst, const CUtensorMap* map, i
 // Shared-memory layout of one CTA (byte offsets from a 1024-aligned base).
 template <typename IO, int K, int NS>
 struct Smem {
-  static constexpr int CH = kThreads / K;
   static constexpr int NP = K * NS;
   static constexpr int kRawStage = 2 * NP * T * (int)sizeof(IO);   // B and C tiles, N <= NP rows
   static constexpr int kRaw = 0;
@@ -135,11 +141,11 @@ struct Smem {
 };
 
 template <typename IO, int K, int NS, int MODE, bool PRECISE>
-__global__ void __launch_bounds__(kThreads, 3)
+__global__ void __launch_bounds__(32 * K, SSM_TILED_MIN_BLOCKS * 4 / K)
     scan_tiled_kernel(const __grid_constant__ TiledParams p, const __grid_constant__ CUtensorMap tmB,
                       const __grid_constant__ CUtensorMap tmC) {
   using S = Smem<IO, K, NS>;
-  constexpr int CH = S::CH;
+  constexpr int kThreads = 32 * K;
   constexpr int NP = S::NP;
   constexpr int VEC = Vec16<IO>::kN;     // elements per 16-byte vector
   constexpr int VPR = T / VEC;           // vectors per channel row per tile
@@ -158,8 +164,8 @@ __global__ void __launch_bounds__(kThreads, 3)
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
-  const int g = warp % K;                        // state group of this warp
-  const int c = (warp / K) * 32 + lane;          // channel within the CTA
+  const int g = warp;                            // state group of this warp
+  const int c = lane;                            // channel within the CTA
   const int64_t b = blockIdx.z;
   const int chunk = blockIdx.y;
   const int64_t d0 = (int64_t)blockIdx.x * CH;
@@ -325,7 +331,7 @@ __global__ void __launch_bounds__(kThreads, 3)
             const float* Bt = bc_s + (t + j + s) * 2 * NP + g * NS;
             const float2 dt2 = make_float2(dt, dt);
             const float2 du2 = make_float2(du, du);
-            float2 acc = make_float2(0.f, 0.f);
+            float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
 #pragma unroll
             for (int q = 0; q < NS; q += 4) {
               const float4 bq = *reinterpret_cast<const float4*>(Bt + q);
@@ -337,11 +343,11 @@ __global__ void __launch_bounds__(kThreads, 3)
               h[q / 2 + 1] = __ffma2_rn(a1, h[q / 2 + 1], __fmul2_rn(du2, make_float2(bq.z, bq.w)));
               if (MODE == MODE_OUTPUT) {
                 const float4 cq = *reinterpret_cast<const float4*>(Bt + NP + q);
-                acc = __ffma2_rn(make_float2(cq.x, cq.y), h[q / 2], acc);
-                acc = __ffma2_rn(make_float2(cq.z, cq.w), h[q / 2 + 1], acc);
+                acc0 = __ffma2_rn(make_float2(cq.x, cq.y), h[q / 2], acc0);
+                acc1 = __ffma2_rn(make_float2(cq.z, cq.w), h[q / 2 + 1], acc1);
               }
             }
-            yv[j + s] = acc.x + acc.y;
+            yv[j + s] = (acc0.x + acc1.x) + (acc0.y + acc1.y);
             if (MODE == MODE_RECORD) dsum += dt;
           }
         }
@@ -434,14 +440,13 @@ cudaError_t launch_one(const TiledParams& tp, const CUtensorMap& mB, const CUten
     if (e != cudaSuccess) return e;
     __atomic_fetch_or(&attr_set, bit, __ATOMIC_RELEASE);
   }
-  kern<<<grid, kThreads, S::kAlloc, s>>>(tp, mB, mC);
+  kern<<<grid, 32 * K, S::kAlloc, s>>>(tp, mB, mC);
   return cudaGetLastError();
 }
 
 template <typename IO, int K, int NS, bool PRECISE>
 cudaError_t launch_shape(const ScanProblem& p, const ScanPlan& plan, TiledParams& tp, const CUtensorMap& mB,
                          const CUtensorMap& mC, cudaStream_t s) {
-  constexpr int CH = kThreads / K;
   constexpr int NP = K * NS;
   const dim3 grid((unsigned)((p.D + CH - 1) / CH), (unsigned)plan.nchunks, (unsigned)p.B);
   cudaError_t e;

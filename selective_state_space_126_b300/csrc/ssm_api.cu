@@ -186,21 +186,17 @@ bool tiled_eligible(const ScanProblem& p) {
 TiledShape pick_shape(const ScanProblem& p) {
   if (p.N > 32) return TiledShape{4, 16, 32};
   if (p.N > 16) return TiledShape{4, 8, 32};
-  // N <= 16: the warp count per SM sets the load balance; the fewer threads
-  // share a channel the less shared-memory traffic per state update.
-  const int sms = device_sm_count();
-  const int64_t chan = p.B * p.D;
   const char* env = getenv("SSM_TILED_K");
   if (env) {
     const int k = atoi(env);
-    if (k == 1) return TiledShape{1, 16, 128};
+    if (k == 1) return TiledShape{1, 16, 32};
     if (k == 4) return TiledShape{4, 4, 32};
-    if (k == 2) return TiledShape{2, 8, 64};
+    if (k == 2) return TiledShape{2, 8, 32};
   }
-  // threads per SM of work for K = 2; below ~4 warps per SM prefer K = 4
-  const double warps_per_sm_k2 = (double)chan * 2 / 32 / sms;
-  if (warps_per_sm_k2 < 8.0) return TiledShape{4, 4, 32};
-  return TiledShape{2, 8, 64};
+  // N <= 16: two threads per channel, 8 states each, balance per-thread
+  // instruction-level parallelism against the per-step work that the states
+  // of one thread share.
+  return TiledShape{2, 8, 32};
 }
 
 ssm_status_t plan_scan(const ssm_scan_args_t* a, const ScanProblem& p, ScanPlan* plan) {

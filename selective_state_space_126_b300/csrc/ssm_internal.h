@@ -39,7 +39,7 @@ enum ScanPath { kPathGeneric = 0, kPathTiled = 1, kPathChunked = 2 };
 struct TiledShape {
   int K;        // threads per channel (1, 2 or 4)
   int NS;       // states per thread
-  int CH;       // channels per CTA (= 128 / K)
+  int CH;       // channels per CTA (32)
 };
 
 struct ScanPlan {
