@@ -163,24 +163,31 @@ ssm_status_t validate_scan(const ssm_scan_args_t* a, ScanProblem* p) {
   return ok();
 }
 
-// Tiled path eligibility: 16-byte vectors along t and TMA-compatible B/C.
+// Tiled path eligibility: every sequence tensor is read through TMA boxes of
+// 32 steps (16-byte aligned base and row strides), y is written with 16-byte
+// stores, and the batch dimension of each tensor is either nested outside its
+// rows or broadcast (stride 0).
 bool tiled_eligible(const ScanProblem& p) {
   const int es = elem_size(p.io);
   const int vec = 16 / es;
   if (p.L <= 0 || p.L % vec != 0) return false;
-  if (p.L > (int64_t)INT32_MAX - 64) return false;
-  auto vrow = [&](const void* ptr, const int64_t* s) {
-    return aligned(ptr, 16) && s[0] % vec == 0 && s[1] % vec == 0;
+  if (p.L > (int64_t)INT32_MAX - 64 || p.D > (int64_t)INT32_MAX - 64) return false;
+  // rows: D for u / delta / z, N for B / C
+  auto tma_ok = [&](const void* ptr, const int64_t* s, int64_t rows) {
+    if (!aligned(ptr, 16) || s[0] % vec != 0 || s[1] % vec != 0) return false;
+    if (rows > 1 && s[1] < p.L) return false;                       // rows may not overlap
+    if (p.B > 1 && s[0] != 0 && rows > 1 && s[0] < s[1] * rows) return false;
+    if (p.B > 1 && s[0] != 0 && rows == 1 && s[0] < p.L) return false;
+    return true;
   };
-  if (!vrow(p.u, p.su) || !vrow(p.delta, p.sd) || !vrow(p.y, p.sy)) return false;
-  if (p.z && !vrow(p.z, p.sz)) return false;
-  auto bc = [&](const void* ptr, const int64_t* s) {
-    return aligned(ptr, 16) && s[1] > 0 && (s[1] * es) % 16 == 0 && (s[0] * es) % 16 == 0;
-  };
-  if (!bc(p.Bm, p.sB) || !bc(p.Cm, p.sC)) return false;
-  // both B and C must be batched, or both shared across the batch
-  const bool rb = p.sB[0] != 0 && p.B > 1, rc = p.sC[0] != 0 && p.B > 1;
-  return rb == rc;
+  if (!tma_ok(p.u, p.su, p.D) || !tma_ok(p.delta, p.sd, p.D)) return false;
+  if (p.z && !tma_ok(p.z, p.sz, p.D)) return false;
+  if (!aligned(p.y, 16) || p.sy[0] % vec != 0 || p.sy[1] % vec != 0) return false;
+  if (!tma_ok(p.Bm, p.sB, p.N) || !tma_ok(p.Cm, p.sC, p.N)) return false;
+  // u, delta, z share one batch layout kind (batched or broadcast); so do B and C
+  auto batched = [&](const int64_t* s) { return s[0] != 0 && p.B > 1; };
+  if (batched(p.sd) != batched(p.su) || (p.z && batched(p.sz) != batched(p.su))) return false;
+  return batched(p.sB) == batched(p.sC);
 }
 
 TiledShape pick_shape(const ScanProblem& p) {
