@@ -58,11 +58,42 @@ __device__ __forceinline__ float silu(float z) {
   }
 }
 
+// Two-lane forms of the SFU softplus and silu above, with the FMA-pipe work
+// on packed f32x2 instructions (same arithmetic, half the issue slots).
+__device__ __forceinline__ float2 softplus2_fast(float2 s) {
+  const float2 x = __fmul2_rn(make_float2(fabsf(s.x), fabsf(s.y)), make_float2(-kLog2e, -kLog2e));
+  const float2 ope = __fadd2_rn(make_float2(ex2_approx(x.x), ex2_approx(x.y)), make_float2(1.f, 1.f));
+  return __ffma2_rn(make_float2(lg2_approx(ope.x), lg2_approx(ope.y)), make_float2(kLn2, kLn2),
+                    make_float2(fmaxf(s.x, 0.f), fmaxf(s.y, 0.f)));
+}
+
+__device__ __forceinline__ float2 silu2_fast(float2 z) {
+  const float2 x = __fmul2_rn(z, make_float2(-kLog2e, -kLog2e));
+  const float2 den = __fadd2_rn(make_float2(ex2_approx(x.x), ex2_approx(x.y)), make_float2(1.f, 1.f));
+  return __fmul2_rn(z, make_float2(rcp_approx(den.x), rcp_approx(den.y)));
+}
+
 // Delta for one element: softplus(delta + bias) or the plain sum.
 template <bool PRECISE>
 __device__ __forceinline__ float delta_of(float delta, float bias, bool use_softplus) {
   const float s = delta + bias;
   return use_softplus ? softplus<PRECISE>(s) : s;
+}
+
+// Delta for two elements of one channel.
+template <bool PRECISE>
+__device__ __forceinline__ float2 delta_of2(float2 delta, float bias, bool use_softplus) {
+  const float2 s = __fadd2_rn(delta, make_float2(bias, bias));
+  if (!use_softplus) return s;
+  if (PRECISE) return make_float2(softplus<true>(s.x), softplus<true>(s.y));
+  return softplus2_fast(s);
+}
+
+// silu of two elements.
+template <bool PRECISE>
+__device__ __forceinline__ float2 silu2(float2 z) {
+  if (PRECISE) return make_float2(silu<true>(z.x), silu<true>(z.y));
+  return silu2_fast(z);
 }
 
 // ---------------------------------------------------------------------------

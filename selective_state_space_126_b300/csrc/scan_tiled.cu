@@ -43,6 +43,7 @@
 #include <cstdio>
 #include <cstring>
 
+#include "async_copy.cuh"
 #include "device_math.cuh"
 #include "ssm_internal.h"
 
@@ -61,7 +62,9 @@ constexpr int T = kTileT;
 constexpr int kStages = 2;
 constexpr int MODE_OUTPUT = 0;
 constexpr int MODE_RECORD = 1;
-constexpr uint32_t kWaitLimit = 1u << 22;
+#ifndef SSM_EXP_AHEAD
+#define SSM_EXP_AHEAD 0
+#endif
 
 struct TiledParams {
   int64_t B, D, L;
@@ -91,50 +94,7 @@ struct TensorMaps {
   CUtensorMap u, delta, z, B, C;
 };
 
-__device__ __forceinline__ uint32_t smem_u32(const void* p) {
-  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
-}
-
-__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
-}
-
-// Bounded wait on an mbarrier phase: false if the limit ran out.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t phase) {
-  for (uint32_t i = 0; i < kWaitLimit; ++i) {
-    uint32_t done;
-    asm volatile(
-        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
-        : "=r"(done)
-        : "r"(bar), "r"(phase)
-        : "memory");
-    if (done) return true;
-  }
-  return false;
-}
-
-__device__ __forceinline__ void tma_load(uint32_t dst, const CUtensorMap* map, int x, int y, int z, bool rank3,
-                                         uint32_t bar) {
-  if (rank3) {
-    asm volatile(
-        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(
-            dst),
-        "l"(map), "r"(x), "r"(y), "r"(z), "r"(bar)
-        : "memory");
-  } else {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
-            dst),
-        "l"(map), "r"(x), "r"(y), "r"(bar)
-        : "memory");
-  }
-}
-
-// Shared-memory layout of one CTA (byte offsets from a 1024-aligned base).
+// Shared-memory layout of one CTA (byte offsets from a 128-aligned base).
 template <typename IO, int K, int NS>
 struct Smem {
   static constexpr int NP = K * NS;
@@ -151,7 +111,7 @@ struct Smem {
   static constexpr int kPartRow = T + 4;
   static constexpr int kBar = kPart + K * CH * kPartRow * 4;         // kStages x uint64
   static constexpr int kBytes = kBar + 8 * kStages;
-  static constexpr int kAlloc = kBytes + 1024;                       // slack for the 1024-byte alignment
+  static constexpr int kAlloc = kBytes + 128;                        // slack for the 128-byte alignment
 };
 
 template <typename IO, int K, int NS, int MODE, bool PRECISE>
@@ -162,14 +122,16 @@ __global__ void __launch_bounds__(32 * K, min_blocks(K, NS))
   constexpr int NP = S::NP;
   constexpr int VEC = Vec16<IO>::kN;     // elements per 16-byte vector
   constexpr int VPR = T / VEC;           // vectors per channel row per tile
-  constexpr int NV = CH * VPR / kThreads;
-  static_assert(CH * VPR % kThreads == 0, "vector mapping");
+  constexpr int NVEC = CH * VPR;                            // 16-byte vectors per (32 ch x T) tile
+  constexpr int NV = (NVEC + kThreads - 1) / kThreads;      // per thread
+  static_assert(NVEC % kThreads == 0 || NVEC < kThreads, "vector mapping");
   static_assert(NS % 4 == 0, "states per thread");
 
-  // Align the dynamic shared memory to 1024 bytes by an offset from the
-  // array itself, so that the compiler keeps shared-space addressing.
+  // Align the dynamic shared memory to 128 bytes (TMA destinations) by an
+  // offset from the array itself, so that the compiler keeps shared-space
+  // addressing.
   extern __shared__ __align__(128) unsigned char smem_raw[];
-  unsigned char* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  unsigned char* smem = smem_raw + ((128u - (smem_u32(smem_raw) & 127u)) & 127u);
   float* bc_s = reinterpret_cast<float*>(smem + S::kBC);
   float2* dt_s = reinterpret_cast<float2*>(smem + S::kDT);
   float* part_s = reinterpret_cast<float*>(smem + S::kPart);
@@ -216,7 +178,7 @@ __global__ void __launch_bounds__(32 * K, min_blocks(K, NS))
   if (tid == 0) {
 #pragma unroll
     for (int s = 0; s < kStages; ++s) mbar_init(bar_base + 8 * s, 1);
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    mbar_init_fence();
   }
   __syncthreads();
 
@@ -242,9 +204,10 @@ __global__ void __launch_bounds__(32 * K, min_blocks(K, NS))
   // ---- per-vector constants of the load / store stages ----
   int vc[NV], vt[NV];
   float vbias[NV], vD[NV];
+  const bool vec_thread = NVEC >= kThreads || tid < NVEC;   // threads past the vectors idle in stages A and C
 #pragma unroll
   for (int i = 0; i < NV; ++i) {
-    const int v = tid + i * kThreads;
+    const int v = vec_thread ? tid + i * kThreads : 0;
     vc[i] = v / VPR;
     vt[i] = (v % VPR) * VEC;
     const int64_t dv = d0 + vc[i];
@@ -265,20 +228,22 @@ __global__ void __launch_bounds__(32 * K, min_blocks(K, NS))
     if (ok) {
 #pragma unroll
       for (int i = 0; i < NV; ++i) {
+        if (!vec_thread) break;
         float uv[VEC], dv[VEC];
         unpack16(*reinterpret_cast<const uint4*>(ring + S::kU + (vc[i] * T + vt[i]) * (int)sizeof(IO)), uv);
         unpack16(*reinterpret_cast<const uint4*>(ring + S::kDelta + (vc[i] * T + vt[i]) * (int)sizeof(IO)), dv);
-        float2 out[VEC];
-#pragma unroll
-        for (int j = 0; j < VEC; ++j) {
-          const bool in = t0 + vt[i] + j < t_end;
-          const float dt = in ? delta_of<PRECISE>(dv[j], vbias[i], p.softplus) : 0.f;
-          out[j] = make_float2(dt, dt * uv[j]);
-        }
+        const bool full = t0 + vt[i] + VEC <= t_end;      // else a ragged chunk end: mask per step
         float4* dst = reinterpret_cast<float4*>(dt_s + vc[i] * S::kDTRow + vt[i]);
 #pragma unroll
-        for (int j = 0; j < VEC / 2; ++j)
-          dst[j] = make_float4(out[2 * j].x, out[2 * j].y, out[2 * j + 1].x, out[2 * j + 1].y);
+        for (int j = 0; j < VEC; j += 2) {
+          float2 dt = delta_of2<PRECISE>(make_float2(dv[j], dv[j + 1]), vbias[i], p.softplus);
+          if (!full) {
+            if (t0 + vt[i] + j >= t_end) dt.x = 0.f;
+            if (t0 + vt[i] + j + 1 >= t_end) dt.y = 0.f;
+          }
+          const float2 du = __fmul2_rn(dt, make_float2(uv[j], uv[j + 1]));
+          dst[j / 2] = make_float4(dt.x, du.x, dt.y, du.y);
+        }
       }
       const int per_tensor = N * VPR;                      // 16-byte vectors per B or C tile
       const int nvec = (MODE == MODE_OUTPUT ? 2 : 1) * per_tensor;
@@ -307,6 +272,19 @@ __global__ void __launch_bounds__(32 * K, min_blocks(K, NS))
       const float* bcg = bc_s + g * NS;
       float* prow = part_s + (g * CH + c) * S::kPartRow;
       float yv[4];
+#if SSM_EXP_AHEAD
+      // Abar of the next step is computed one step ahead, so that its SFU
+      // latency overlaps the dependent FMAs of the current step.
+      float2 an[NS / 2];
+      {
+        const float dt0 = dt4[0].x;
+#pragma unroll
+        for (int q = 0; q < NS / 2; ++q) {
+          const float2 x = __fmul2_rn(make_float2(dt0, dt0), A2[q]);
+          an[q] = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+        }
+      }
+#endif
 #pragma unroll
       for (int t = 0; t < T; t += 2) {
         const float4 dd = dt4[t / 2];
@@ -315,18 +293,32 @@ __global__ void __launch_bounds__(32 * K, min_blocks(K, NS))
           const float dt = s ? dd.z : dd.x;
           const float du = s ? dd.w : dd.y;
           const float* Bt = bcg + (t + s) * 2 * NP;
-          const float2 dt2 = make_float2(dt, dt);
           const float2 du2 = make_float2(du, du);
+          float2 a[NS / 2];
+#if SSM_EXP_AHEAD
+#pragma unroll
+          for (int q = 0; q < NS / 2; ++q) a[q] = an[q];
+          if (t + s + 1 < T) {
+            const float dtn = s ? dt4[t / 2 + 1].x : dd.z;
+#pragma unroll
+            for (int q = 0; q < NS / 2; ++q) {
+              const float2 x = __fmul2_rn(make_float2(dtn, dtn), A2[q]);
+              an[q] = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+            }
+          }
+#else
+#pragma unroll
+          for (int q = 0; q < NS / 2; ++q) {
+            const float2 x = __fmul2_rn(make_float2(dt, dt), A2[q]);
+            a[q] = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+          }
+#endif
           float2 acc = make_float2(0.f, 0.f);
 #pragma unroll
           for (int q = 0; q < NS; q += 4) {
             const float4 bq = *reinterpret_cast<const float4*>(Bt + q);
-            const float2 x0 = __fmul2_rn(dt2, A2[q / 2]);
-            const float2 x1 = __fmul2_rn(dt2, A2[q / 2 + 1]);
-            const float2 a0 = make_float2(ex2_approx(x0.x), ex2_approx(x0.y));
-            const float2 a1 = make_float2(ex2_approx(x1.x), ex2_approx(x1.y));
-            h[q / 2] = __ffma2_rn(a0, h[q / 2], __fmul2_rn(du2, make_float2(bq.x, bq.y)));
-            h[q / 2 + 1] = __ffma2_rn(a1, h[q / 2 + 1], __fmul2_rn(du2, make_float2(bq.z, bq.w)));
+            h[q / 2] = __ffma2_rn(a[q / 2], h[q / 2], __fmul2_rn(du2, make_float2(bq.x, bq.y)));
+            h[q / 2 + 1] = __ffma2_rn(a[q / 2 + 1], h[q / 2 + 1], __fmul2_rn(du2, make_float2(bq.z, bq.w)));
             if (MODE == MODE_OUTPUT) {
               const float4 cq = *reinterpret_cast<const float4*>(Bt + NP + q);
               acc = __ffma2_rn(make_float2(cq.x, cq.y), h[q / 2], acc);
@@ -347,26 +339,30 @@ __global__ void __launch_bounds__(32 * K, min_blocks(K, NS))
 #pragma unroll
       for (int i = 0; i < NV; ++i) {
         const int64_t dv = d0 + vc[i];
-        if (!(dv < p.D && t0 + vt[i] < t_end)) continue;
+        if (!(vec_thread && dv < p.D && t0 + vt[i] < t_end)) continue;
         float yo[VEC], uv[VEC], zv[VEC];
 #pragma unroll
         for (int j = 0; j < VEC; j += 4) {
           float4 s4 = *reinterpret_cast<const float4*>(part_s + vc[i] * S::kPartRow + vt[i] + j);
+          float2 lo = make_float2(s4.x, s4.y), hi = make_float2(s4.z, s4.w);
 #pragma unroll
           for (int gg = 1; gg < K; ++gg) {
             const float4 o = *reinterpret_cast<const float4*>(part_s + (gg * CH + vc[i]) * S::kPartRow + vt[i] + j);
-            s4.x += o.x; s4.y += o.y; s4.z += o.z; s4.w += o.w;
+            lo = __fadd2_rn(lo, make_float2(o.x, o.y));
+            hi = __fadd2_rn(hi, make_float2(o.z, o.w));
           }
-          yo[j] = s4.x; yo[j + 1] = s4.y; yo[j + 2] = s4.z; yo[j + 3] = s4.w;
+          yo[j] = lo.x; yo[j + 1] = lo.y; yo[j + 2] = hi.x; yo[j + 3] = hi.y;
         }
         unpack16(*reinterpret_cast<const uint4*>(ring + S::kU + (vc[i] * T + vt[i]) * (int)sizeof(IO)), uv);
         if (p.has_z)
           unpack16(*reinterpret_cast<const uint4*>(ring + S::kZ + (vc[i] * T + vt[i]) * (int)sizeof(IO)), zv);
+        const float2 D2 = make_float2(vD[i], vD[i]);
 #pragma unroll
-        for (int j = 0; j < VEC; ++j) {
-          float o = fmaf(vD[i], uv[j], yo[j]);
-          if (p.has_z) o *= silu<PRECISE>(zv[j]);
-          yo[j] = o;
+        for (int j = 0; j < VEC; j += 2) {
+          float2 o = __ffma2_rn(D2, make_float2(uv[j], uv[j + 1]), make_float2(yo[j], yo[j + 1]));
+          if (p.has_z) o = __fmul2_rn(o, silu2<PRECISE>(make_float2(zv[j], zv[j + 1])));
+          yo[j] = o.x;
+          yo[j + 1] = o.y;
         }
         IO* yp = static_cast<IO*>(p.y) + b * p.sy0 + dv * p.sy1 + t0 + vt[i];
         stg_v4(yp, pack16(yo));

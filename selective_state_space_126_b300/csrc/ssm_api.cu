@@ -180,9 +180,8 @@ bool tiled_eligible(const ScanProblem& p) {
     if (p.B > 1 && s[0] != 0 && rows == 1 && s[0] < p.L) return false;
     return true;
   };
-  if (!tma_ok(p.u, p.su, p.D) || !tma_ok(p.delta, p.sd, p.D)) return false;
+  if (!tma_ok(p.u, p.su, p.D) || !tma_ok(p.delta, p.sd, p.D) || !tma_ok(p.y, p.sy, p.D)) return false;
   if (p.z && !tma_ok(p.z, p.sz, p.D)) return false;
-  if (!aligned(p.y, 16) || p.sy[0] % vec != 0 || p.sy[1] % vec != 0) return false;
   if (!tma_ok(p.Bm, p.sB, p.N) || !tma_ok(p.Cm, p.sC, p.N)) return false;
   // u, delta, z share one batch layout kind (batched or broadcast); so do B and C
   auto batched = [&](const int64_t* s) { return s[0] != 0 && p.B > 1; };
@@ -190,19 +189,27 @@ bool tiled_eligible(const ScanProblem& p) {
   return batched(p.sB) == batched(p.sC);
 }
 
-TiledShape pick_shape(const ScanProblem& p) {
+// Tiled kernel shape.  N > 16 needs 4 threads per channel.  For N <= 16 two
+// threads per channel (8 states each) is the better balance of per-thread
+// parallelism against shared-memory traffic, except when the whole grid fits
+// on the GPU at 4 CTAs of 128 threads per SM: then 4 threads per channel give
+// twice the warps.  SSM_SCAN_KERNEL (k1, k2, k4, lane) overrides the choice
+// for tuning.
+TiledShape pick_shape(const ScanProblem& p, int64_t ctas, int sms, bool* lane) {
+  *lane = false;
   if (p.N > 32) return TiledShape{4, 16, 32};
   if (p.N > 16) return TiledShape{4, 8, 32};
-  const char* env = getenv("SSM_TILED_K");
+  const char* env = getenv("SSM_SCAN_KERNEL");
   if (env) {
-    const int k = atoi(env);
-    if (k == 1) return TiledShape{1, 16, 32};
-    if (k == 4) return TiledShape{4, 4, 32};
-    if (k == 2) return TiledShape{2, 8, 32};
+    if (!strcmp(env, "k1")) return TiledShape{1, 16, 32};
+    if (!strcmp(env, "k2")) return TiledShape{2, 8, 32};
+    if (!strcmp(env, "k4")) return TiledShape{4, 4, 32};
+    if (!strcmp(env, "lane")) {
+      *lane = true;
+      return TiledShape{1, 16, 32};
+    }
   }
-  // N <= 16: two threads per channel, 8 states each, balance per-thread
-  // instruction-level parallelism against the per-step work that the states
-  // of one thread share.
+  if (ctas <= 4 * (int64_t)sms) return TiledShape{4, 4, 32};
   return TiledShape{2, 8, 32};
 }
 
@@ -222,19 +229,16 @@ ssm_status_t plan_scan(const ssm_scan_args_t* a, const ScanProblem& p, ScanPlan*
     plan->path = kPathGeneric;
     return ok();
   }
-  plan->shape = pick_shape(p);
-  const int CH = plan->shape.CH;
-  const int NP = plan->shape.K * plan->shape.NS;
   const int sms = device_sm_count();
-  const int64_t ctas = p.B * ((p.D + CH - 1) / CH);
-  bool chunked = false;
+  const int64_t ctas = p.B * ((p.D + 31) / 32);
+  bool chunk_wanted = false;
+  if (flags & SSM_SCAN_FORCE_CHUNKED) chunk_wanted = true;
+  else if (!(flags & SSM_SCAN_FORCE_TILED)) chunk_wanted = ctas < 2 * sms && p.L >= 8 * 1024;
+  // the chunked path launches many more CTAs than the single pass
+  plan->shape = pick_shape(p, chunk_wanted ? 8 * (int64_t)sms : ctas, sms, &plan->lane);
+  const int NP = plan->shape.K * plan->shape.NS;
   int64_t chunk_len = 0;
-  if (flags & SSM_SCAN_FORCE_CHUNKED) {
-    chunked = true;
-  } else if (!(flags & SSM_SCAN_FORCE_TILED)) {
-    chunked = ctas < 2 * sms && p.L >= 8 * 1024;
-  }
-  if (chunked) {
+  if (chunk_wanted) {
     if (a->chunk_len > 0) {
       chunk_len = (a->chunk_len + kTileT - 1) / kTileT * kTileT;
     } else {
@@ -363,7 +367,7 @@ ssm_status_t ssm_scan_fwd(const ssm_scan_args_t* args, void* stream) {
         return fail(SSM_ERR_WORKSPACE, "workspace %zu < %zu bytes", args->workspace_bytes, plan.workspace_bytes);
       if (!aligned(args->workspace, 16)) return fail(SSM_ERR_WORKSPACE, "workspace not 16-byte aligned");
     }
-    e = launch_scan_tiled(p, plan, args->workspace, s);
+    e = plan.lane ? launch_scan_lane(p, plan, args->workspace, s) : launch_scan_tiled(p, plan, args->workspace, s);
   }
   if (e != cudaSuccess) return cuda_fail(e);
   return ok();
@@ -496,7 +500,8 @@ ssm_status_t ssm_scan_fwd_noalloc(const ssm_scan_args_t* args, void* stream) {
   cudaError_t e = cudaSuccess;
   void* scratch = noalloc_scratch(&e);
   if (!scratch) return cuda_fail(e);
-  e = launch_scan_tiled(p, plan, scratch, static_cast<cudaStream_t>(stream));
+  e = plan.lane ? launch_scan_lane(p, plan, scratch, static_cast<cudaStream_t>(stream))
+                : launch_scan_tiled(p, plan, scratch, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e);
   return ok();
 }

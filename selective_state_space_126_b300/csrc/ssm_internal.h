@@ -44,6 +44,7 @@ struct TiledShape {
 
 struct ScanPlan {
   ScanPath path;
+  bool lane;              // tiled / chunked paths: the one-warp lane kernel (N <= 16)
   TiledShape shape;
   int64_t chunk_len;      // chunked path: timesteps per chunk (multiple of the tile)
   int64_t nchunks;
@@ -56,10 +57,14 @@ int* device_status_ptr();
 // launchers (return a cudaError_t from the launch)
 cudaError_t launch_scan_generic(const ScanProblem& p, cudaStream_t s);
 cudaError_t launch_scan_tiled(const ScanProblem& p, const ScanPlan& plan, void* workspace, cudaStream_t s);
+cudaError_t launch_scan_lane(const ScanProblem& p, const ScanPlan& plan, void* workspace, cudaStream_t s);
 cudaError_t launch_state_update(const StepProblem& p, cudaStream_t s);
 
 // tile length of the tiled kernel (timesteps)
-constexpr int kTileT = 32;
+#ifndef SSM_TILE_T
+#define SSM_TILE_T 32
+#endif
+constexpr int kTileT = SSM_TILE_T;
 
 // tensor-map encoder from the driver (resolved once through the runtime)
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
