@@ -20,16 +20,20 @@
 //     of a time tile -- u, delta, z as (32 steps x 32 channels) boxes and B, C
 //     as (32 steps x N) boxes -- arrive by TMA (cp.async.bulk.tensor) into a
 //     two-slot ring, one tile ahead of the tile being computed, completing
-//     on one mbarrier per slot.  Per tile:
+//     on one mbarrier per slot.  The boxes use the 64-byte (bf16) or 128-byte
+//     (fp32) swizzle, so that reading 16-byte pieces of 8 consecutive rows
+//     touches 8 different bank groups.  Per tile:
 //       A. Delta = softplus(delta + bias) and Delta*u, once per (channel, t),
-//          into shared memory; B and C widened to fp32 in a [t][B|C][n]
-//          layout;
+//          into shared memory (a quarter-warp covers 8 channels at the same
+//          steps, so these accesses are free of bank conflicts); B and C
+//          widened to fp32 in a [t][B|C][n] layout;
 //       B. the recurrence, fully unrolled over the tile so that the SFU ex2
 //          of later steps overlaps the dependent FMAs of earlier ones: per
 //          step one ex2 per state, Abar*h + (Delta u) B on packed f32x2 FMAs
 //          and the C contraction into a partial y;
-//       C. the K partial outputs are summed, D*u added, multiplied by silu(z)
-//          and written back with coalesced 16-byte stores.
+//       C. the K partial outputs are summed, D*u added and multiplied by
+//          silu(z) into a swizzled staging box, which a TMA store writes back
+//          (issued after the next tile's first barrier; two boxes alternate).
 //   * h stays in registers across tiles (never written to HBM, except the
 //     optional final state and the chunk records below).
 //
@@ -71,8 +75,6 @@ struct TiledParams {
   int N;
   int nchunks;
   int64_t chunk_len;
-  void* y;
-  int64_t sy0, sy1;
   const float* A;
   int64_t sA0, sA1;
   const float* Dskip;
@@ -87,32 +89,46 @@ struct TiledParams {
   int has_z;
   int seq_rank3;    // u / delta / z tensor maps carry a batch dimension (else shared across the batch)
   int bc_rank3;     // B / C tensor maps carry a batch dimension
+  int y_rank3;      // the y tensor map carries a batch dimension
   int* status;
 };
 
 struct TensorMaps {
-  CUtensorMap u, delta, z, B, C;
+  CUtensorMap u, delta, z, B, C, y;
 };
 
-// Shared-memory layout of one CTA (byte offsets from a 128-aligned base).
+// Shared-memory layout of one CTA (byte offsets from a 1024-aligned base;
+// every TMA box starts on a 1024-byte boundary, as the swizzled layouts need).
 template <typename IO, int K, int NS>
 struct Smem {
   static constexpr int NP = K * NS;
-  static constexpr int kSeqTile = CH * T * (int)sizeof(IO);          // one (32 ch x 32 t) box
-  static constexpr int kBCTile = NP * T * (int)sizeof(IO);           // one (N x 32 t) box, N <= NP rows
+  static constexpr int ROWB = T * (int)sizeof(IO);                   // bytes per box row
+  static constexpr int kSeqTile = CH * ROWB;                         // one (32 ch x 32 t) box
+  static constexpr int kBCTile = NP * ROWB;                          // one (N x 32 t) box, N <= NP rows
   static constexpr int kU = 0, kDelta = kSeqTile, kZ = 2 * kSeqTile, kB = 3 * kSeqTile;
   static constexpr int kC = kB + kBCTile;
-  static constexpr int kStage = ((kC + kBCTile) + 127) / 128 * 128;  // bytes per ring slot
+  static constexpr int kStage = (kC + kBCTile + 1023) / 1024 * 1024; // bytes per ring slot
   static constexpr int kRing = 0;
-  static constexpr int kBC = kRing + kStages * kStage;               // float [T][2][NP]
+  static constexpr int kY = kRing + kStages * kStage;                // two y staging boxes
+  static constexpr int kBC = kY + 2 * kSeqTile;                      // float [T][2][NP]
   static constexpr int kDT = kBC + T * 2 * NP * 4;                   // float2 [CH][T+2]
   static constexpr int kDTRow = T + 2;
   static constexpr int kPart = kDT + CH * kDTRow * 8;                // float [K][CH][T+4]
   static constexpr int kPartRow = T + 4;
   static constexpr int kBar = kPart + K * CH * kPartRow * 4;         // kStages x uint64
   static constexpr int kBytes = kBar + 8 * kStages;
-  static constexpr int kAlloc = kBytes + 128;                        // slack for the 128-byte alignment
+  static constexpr int kAlloc = kBytes + 1024;                       // slack for the 1024-byte alignment
+  static_assert(kSeqTile % 1024 == 0 && kBCTile % 1024 == 0, "box alignment");
 };
+
+// Byte offset of 16-byte piece `chunk` of row `row` in a box that TMA wrote
+// with the 64-byte (rows of 64 bytes) or 128-byte (rows of 128 bytes)
+// swizzle: the piece index is XOR-ed with address bits 7.. of the row.
+template <int ROWB>
+__device__ __forceinline__ int swz(int row, int chunk) {
+  if (ROWB == 64) return row * 64 + ((chunk ^ ((row >> 1) & 3)) << 4);
+  return row * 128 + ((chunk ^ (row & 7)) << 4);
+}
 
 template <typename IO, int K, int NS, int MODE, bool PRECISE>
 __global__ void __launch_bounds__(32 * K, min_blocks(K, NS))
@@ -122,16 +138,17 @@ __global__ void __launch_bounds__(32 * K, min_blocks(K, NS))
   constexpr int NP = S::NP;
   constexpr int VEC = Vec16<IO>::kN;     // elements per 16-byte vector
   constexpr int VPR = T / VEC;           // vectors per channel row per tile
+  constexpr int ROWB = S::ROWB;
   constexpr int NVEC = CH * VPR;                            // 16-byte vectors per (32 ch x T) tile
   constexpr int NV = (NVEC + kThreads - 1) / kThreads;      // per thread
   static_assert(NVEC % kThreads == 0 || NVEC < kThreads, "vector mapping");
   static_assert(NS % 4 == 0, "states per thread");
 
-  // Align the dynamic shared memory to 128 bytes (TMA destinations) by an
+  // Align the dynamic shared memory to 1024 bytes (swizzled TMA boxes) by an
   // offset from the array itself, so that the compiler keeps shared-space
   // addressing.
-  extern __shared__ __align__(128) unsigned char smem_raw[];
-  unsigned char* smem = smem_raw + ((128u - (smem_u32(smem_raw) & 127u)) & 127u);
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  unsigned char* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   float* bc_s = reinterpret_cast<float*>(smem + S::kBC);
   float2* dt_s = reinterpret_cast<float2*>(smem + S::kDT);
   float* part_s = reinterpret_cast<float*>(smem + S::kPart);
@@ -199,6 +216,12 @@ __global__ void __launch_bounds__(32 * K, min_blocks(K, NS))
     tma_load(dst + S::kB, &tm.B, x, 0, bc_z, p.bc_rank3, bar);
     if (MODE == MODE_OUTPUT) tma_load(dst + S::kC, &tm.C, x, 0, bc_z, p.bc_rank3, bar);
   };
+  const int y_z = p.y_rank3 ? (int)b : 0;
+  auto store_y = [&](int tile) {
+    tma_store(&tm.y, smem_u32(smem + S::kY + (tile & 1) * S::kSeqTile), (int)(t_begin + (int64_t)tile * T),
+              (int)d0, y_z, p.y_rank3);
+    bulk_commit();
+  };
   if (tid == 0 && ntiles > 0) issue(0);
 
   // ---- per-vector constants of the load / store stages ----
@@ -208,8 +231,8 @@ __global__ void __launch_bounds__(32 * K, min_blocks(K, NS))
 #pragma unroll
   for (int i = 0; i < NV; ++i) {
     const int v = vec_thread ? tid + i * kThreads : 0;
-    vc[i] = v / VPR;
-    vt[i] = (v % VPR) * VEC;
+    vc[i] = v % CH;                 // a warp covers the 32 channels at one 16-byte piece of steps
+    vt[i] = (v / CH) * VEC;
     const int64_t dv = d0 + vc[i];
     const int64_t dvc = dv < p.D ? dv : 0;
     vbias[i] = p.bias ? p.bias[dvc] : 0.f;
@@ -230,8 +253,9 @@ __global__ void __launch_bounds__(32 * K, min_blocks(K, NS))
       for (int i = 0; i < NV; ++i) {
         if (!vec_thread) break;
         float uv[VEC], dv[VEC];
-        unpack16(*reinterpret_cast<const uint4*>(ring + S::kU + (vc[i] * T + vt[i]) * (int)sizeof(IO)), uv);
-        unpack16(*reinterpret_cast<const uint4*>(ring + S::kDelta + (vc[i] * T + vt[i]) * (int)sizeof(IO)), dv);
+        const int off = swz<ROWB>(vc[i], vt[i] / VEC);
+        unpack16(*reinterpret_cast<const uint4*>(ring + S::kU + off), uv);
+        unpack16(*reinterpret_cast<const uint4*>(ring + S::kDelta + off), dv);
         const bool full = t0 + vt[i] + VEC <= t_end;      // else a ragged chunk end: mask per step
         float4* dst = reinterpret_cast<float4*>(dt_s + vc[i] * S::kDTRow + vt[i]);
 #pragma unroll
@@ -245,26 +269,38 @@ __global__ void __launch_bounds__(32 * K, min_blocks(K, NS))
           dst[j / 2] = make_float4(dt.x, du.x, dt.y, du.y);
         }
       }
-      const int per_tensor = N * VPR;                      // 16-byte vectors per B or C tile
-      const int nvec = (MODE == MODE_OUTPUT ? 2 : 1) * per_tensor;
-      for (int v = tid; v < nvec; v += kThreads) {
-        const int tensor = v >= per_tensor ? 1 : 0;         // 0: B, 1: C (C starts at row NP)
-        const int rem = v - tensor * per_tensor;
-        const int n = rem / VPR;
-        const int tv = (rem % VPR) * VEC;
+      // B and C rows -> fp32 [t][B|C][n]: thread v takes row v % ACT (B rows
+      // first, then C rows; the record pass needs only B) and piece v / ACT
+      // of it, so that a warp writes consecutive floats per step
+      constexpr int ROWS = 2 * NP;
+      constexpr int ACT = MODE == MODE_OUTPUT ? ROWS : NP;
+      for (int v = tid; v < ACT * VPR; v += kThreads) {
+        const int row = v % ACT, piece = v / ACT;
+        const int tensor = row / NP, n = row % NP;
+        if (n >= N) continue;
         float f[VEC];
-        unpack16(*reinterpret_cast<const uint4*>(ring + S::kB + tensor * S::kBCTile + rem * 16), f);
+        unpack16(*reinterpret_cast<const uint4*>(ring + S::kB + tensor * S::kBCTile + swz<ROWB>(n, piece)), f);
 #pragma unroll
-        for (int j = 0; j < VEC; ++j) bc_s[(tv + j) * 2 * NP + tensor * NP + n] = f[j];
+        for (int e = 0; e < VEC; ++e) bc_s[(piece * VEC + e) * ROWS + row] = f[e];
       }
     } else {
       record_status(p.status, SSM_ERR_TIMEOUT);
     }
-    if (__syncthreads_or(!ok)) return;   // a TMA copy never completed (the next tile is not issued yet)
+    // the y store of tile k-2 (issued at tile k-1) must be done reading its
+    // staging box before stage C of this tile rewrites it
+    if (MODE == MODE_OUTPUT && tid == 0 && k >= 2) bulk_wait_read<0>();
+    if (__syncthreads_or(!ok)) {   // a TMA copy never completed (the next tile is not issued yet)
+      if (MODE == MODE_OUTPUT && tid == 0) bulk_wait<0>();
+      return;
+    }
 
     // Every thread is past stage C of tile k-1 and stage A of tile k: the
-    // other ring slot is free, so the next tile's copies go out now.
-    if (tid == 0 && k + 1 < ntiles) issue(k + 1);
+    // other ring slot is free, so the next tile's copies go out now; the
+    // staging box of tile k-1 is complete, so its store goes out too.
+    if (tid == 0) {
+      if (k + 1 < ntiles) issue(k + 1);
+      if (MODE == MODE_OUTPUT && k >= 1) store_y(k - 1);
+    }
 
     // ---- stage B: the recurrence over the T steps of the tile ----
     {
@@ -353,9 +389,9 @@ __global__ void __launch_bounds__(32 * K, min_blocks(K, NS))
           }
           yo[j] = lo.x; yo[j + 1] = lo.y; yo[j + 2] = hi.x; yo[j + 3] = hi.y;
         }
-        unpack16(*reinterpret_cast<const uint4*>(ring + S::kU + (vc[i] * T + vt[i]) * (int)sizeof(IO)), uv);
-        if (p.has_z)
-          unpack16(*reinterpret_cast<const uint4*>(ring + S::kZ + (vc[i] * T + vt[i]) * (int)sizeof(IO)), zv);
+        const int off = swz<ROWB>(vc[i], vt[i] / VEC);
+        unpack16(*reinterpret_cast<const uint4*>(ring + S::kU + off), uv);
+        if (p.has_z) unpack16(*reinterpret_cast<const uint4*>(ring + S::kZ + off), zv);
         const float2 D2 = make_float2(vD[i], vD[i]);
 #pragma unroll
         for (int j = 0; j < VEC; j += 2) {
@@ -364,9 +400,16 @@ __global__ void __launch_bounds__(32 * K, min_blocks(K, NS))
           yo[j] = o.x;
           yo[j + 1] = o.y;
         }
-        IO* yp = static_cast<IO*>(p.y) + b * p.sy0 + dv * p.sy1 + t0 + vt[i];
-        stg_v4(yp, pack16(yo));
+        *reinterpret_cast<uint4*>(smem + S::kY + (k & 1) * S::kSeqTile + off) = pack16(yo);
       }
+      fence_async_smem();   // the staging box is read by the TMA store issued after the next barrier
+    }
+  }
+  if (MODE == MODE_OUTPUT && ntiles > 0) {
+    __syncthreads();
+    if (tid == 0) {
+      store_y(ntiles - 1);
+      bulk_wait<0>();       // the staging boxes outlive their stores
     }
   }
 
@@ -447,8 +490,9 @@ cudaError_t launch_shape(const ScanProblem& p, const ScanPlan& plan, TiledParams
   return launch_one<IO, K, NS, MODE_OUTPUT, PRECISE>(tp, tm, grid, s);
 }
 
-// Tensor map of a (batch, rows, L) tensor with time stride 1, box (T steps x box_rows).
-// rank 3 (t, row, b) when the batch stride is used, else rank 2 (t, row).
+// Tensor map of a (batch, rows, L) tensor with time stride 1, box (T steps x
+// box_rows), swizzled (see swz).  Rank 3 (t, row, b) when the batch stride is
+// used, else rank 2 (t, row).
 bool encode_map(CUtensorMap* map, const void* base, const int64_t* strides, int64_t rows, uint32_t box_rows,
                 const ScanProblem& p, bool rank3) {
   EncodeTiledFn enc = get_encode_tiled();
@@ -462,8 +506,9 @@ bool encode_map(CUtensorMap* map, const void* base, const int64_t* strides, int6
   cuuint64_t gstr[2] = {(cuuint64_t)(row_stride * es), (cuuint64_t)(batch_stride * es)};
   cuuint32_t box[3] = {(cuuint32_t)T, box_rows, 1};
   cuuint32_t estr[3] = {1, 1, 1};
+  const CUtensorMapSwizzle swz = es == 2 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B;
   CUresult r = enc(map, dt, rank3 ? 3 : 2, const_cast<void*>(base), dims, gstr, box, estr,
-                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
@@ -487,8 +532,6 @@ cudaError_t launch_scan_tiled(const ScanProblem& p, const ScanPlan& plan, void* 
   tp.B = p.B; tp.D = p.D; tp.L = p.L; tp.N = (int)p.N;
   tp.nchunks = (int)plan.nchunks;
   tp.chunk_len = plan.nchunks > 1 ? plan.chunk_len : p.L;
-  tp.y = p.y;
-  tp.sy0 = p.sy[0]; tp.sy1 = p.sy[1];
   tp.A = p.A; tp.sA0 = p.sA[0]; tp.sA1 = p.sA[1];
   tp.Dskip = p.Dskip; tp.bias = p.bias;
   tp.h0 = p.h0; tp.sh00 = p.sh0[0]; tp.sh01 = p.sh0[1]; tp.sh02 = p.sh0[2];
@@ -503,14 +546,16 @@ cudaError_t launch_scan_tiled(const ScanProblem& p, const ScanPlan& plan, void* 
     tp.rec_s = ws + p.B * p.D * plan.nchunks * NP;
   }
   // the planner only picks this path when u, delta, z share one batch layout
-  // kind and B, C share another (see tiled_eligible)
+  // kind and B, C share another (see tiled_eligible); y, an output, is
+  // batched whenever B > 1
   tp.seq_rank3 = (p.su[0] != 0 && p.B > 1) ? 1 : 0;
   tp.bc_rank3 = (p.sB[0] != 0 && p.B > 1) ? 1 : 0;
+  tp.y_rank3 = p.B > 1 ? 1 : 0;
   TensorMaps tm;
   std::memset(&tm, 0, sizeof(tm));
-  const bool r3 = tp.seq_rank3 == 1, b3 = tp.bc_rank3 == 1;
+  const bool r3 = tp.seq_rank3 == 1, b3 = tp.bc_rank3 == 1, y3 = tp.y_rank3 == 1;
   if (!encode_map(&tm.u, p.u, p.su, p.D, CH, p, r3) || !encode_map(&tm.delta, p.delta, p.sd, p.D, CH, p, r3) ||
-      (p.z && !encode_map(&tm.z, p.z, p.sz, p.D, CH, p, r3)) ||
+      (p.z && !encode_map(&tm.z, p.z, p.sz, p.D, CH, p, r3)) || !encode_map(&tm.y, p.y, p.sy, p.D, CH, p, y3) ||
       !encode_map(&tm.B, p.Bm, p.sB, p.N, (uint32_t)p.N, p, b3) ||
       !encode_map(&tm.C, p.Cm, p.sC, p.N, (uint32_t)p.N, p, b3))
     return cudaErrorInvalidValue;

@@ -193,10 +193,9 @@ bool tiled_eligible(const ScanProblem& p) {
 // threads per channel (8 states each) is the better balance of per-thread
 // parallelism against shared-memory traffic, except when the whole grid fits
 // on the GPU at 4 CTAs of 128 threads per SM: then 4 threads per channel give
-// twice the warps.  SSM_SCAN_KERNEL (k1, k2, k4, lane) overrides the choice
-// for tuning.
-TiledShape pick_shape(const ScanProblem& p, int64_t ctas, int sms, bool* lane) {
-  *lane = false;
+// twice the warps.  SSM_SCAN_KERNEL (k1, k2, k4) overrides the choice for
+// tuning.
+TiledShape pick_shape(const ScanProblem& p, int64_t ctas, int sms) {
   if (p.N > 32) return TiledShape{4, 16, 32};
   if (p.N > 16) return TiledShape{4, 8, 32};
   const char* env = getenv("SSM_SCAN_KERNEL");
@@ -204,10 +203,6 @@ TiledShape pick_shape(const ScanProblem& p, int64_t ctas, int sms, bool* lane) {
     if (!strcmp(env, "k1")) return TiledShape{1, 16, 32};
     if (!strcmp(env, "k2")) return TiledShape{2, 8, 32};
     if (!strcmp(env, "k4")) return TiledShape{4, 4, 32};
-    if (!strcmp(env, "lane")) {
-      *lane = true;
-      return TiledShape{1, 16, 32};
-    }
   }
   if (ctas <= 4 * (int64_t)sms) return TiledShape{4, 4, 32};
   return TiledShape{2, 8, 32};
@@ -235,7 +230,7 @@ ssm_status_t plan_scan(const ssm_scan_args_t* a, const ScanProblem& p, ScanPlan*
   if (flags & SSM_SCAN_FORCE_CHUNKED) chunk_wanted = true;
   else if (!(flags & SSM_SCAN_FORCE_TILED)) chunk_wanted = ctas < 2 * sms && p.L >= 8 * 1024;
   // the chunked path launches many more CTAs than the single pass
-  plan->shape = pick_shape(p, chunk_wanted ? 8 * (int64_t)sms : ctas, sms, &plan->lane);
+  plan->shape = pick_shape(p, chunk_wanted ? 8 * (int64_t)sms : ctas, sms);
   const int NP = plan->shape.K * plan->shape.NS;
   int64_t chunk_len = 0;
   if (chunk_wanted) {
@@ -367,7 +362,7 @@ ssm_status_t ssm_scan_fwd(const ssm_scan_args_t* args, void* stream) {
         return fail(SSM_ERR_WORKSPACE, "workspace %zu < %zu bytes", args->workspace_bytes, plan.workspace_bytes);
       if (!aligned(args->workspace, 16)) return fail(SSM_ERR_WORKSPACE, "workspace not 16-byte aligned");
     }
-    e = plan.lane ? launch_scan_lane(p, plan, args->workspace, s) : launch_scan_tiled(p, plan, args->workspace, s);
+    e = launch_scan_tiled(p, plan, args->workspace, s);
   }
   if (e != cudaSuccess) return cuda_fail(e);
   return ok();
@@ -500,8 +495,7 @@ ssm_status_t ssm_scan_fwd_noalloc(const ssm_scan_args_t* args, void* stream) {
   cudaError_t e = cudaSuccess;
   void* scratch = noalloc_scratch(&e);
   if (!scratch) return cuda_fail(e);
-  e = plan.lane ? launch_scan_lane(p, plan, scratch, static_cast<cudaStream_t>(stream))
-                : launch_scan_tiled(p, plan, scratch, static_cast<cudaStream_t>(stream));
+  e = launch_scan_tiled(p, plan, scratch, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e);
   return ok();
 }

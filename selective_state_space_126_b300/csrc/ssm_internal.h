@@ -44,7 +44,6 @@ struct TiledShape {
 
 struct ScanPlan {
   ScanPath path;
-  bool lane;              // tiled / chunked paths: the one-warp lane kernel (N <= 16)
   TiledShape shape;
   int64_t chunk_len;      // chunked path: timesteps per chunk (multiple of the tile)
   int64_t nchunks;
@@ -57,7 +56,6 @@ int* device_status_ptr();
 // launchers (return a cudaError_t from the launch)
 cudaError_t launch_scan_generic(const ScanProblem& p, cudaStream_t s);
 cudaError_t launch_scan_tiled(const ScanProblem& p, const ScanPlan& plan, void* workspace, cudaStream_t s);
-cudaError_t launch_scan_lane(const ScanProblem& p, const ScanPlan& plan, void* workspace, cudaStream_t s);
 cudaError_t launch_state_update(const StepProblem& p, cudaStream_t s);
 
 // tile length of the tiled kernel (timesteps)
