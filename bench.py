@@ -39,7 +39,7 @@ UNIT = "state-updates/s"
 SCAN_SOURCES = ["selective_state_space_126_b300/csrc/scan_tiled.cu",
                 "selective_state_space_126_b300/csrc/async_copy.cuh",
                 "selective_state_space_126_b300/csrc/device_math.cuh"]
-TRAFFIC_FILE = os.path.join(ROOT, "profiles", "scan_tiled_traffic.json")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "scan_tiled_traffic.txt")   # JSON text written from an ncu capture
 
 
 def parse():
@@ -53,6 +53,7 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--no-rows", action="store_true", help="skip the other workloads' timing rows")
     return ap.parse_args()
 
 
@@ -157,8 +158,9 @@ class ClockSampler:
                 "samples": len(mhz), "window": window}
 
 
-def cpu_baseline(cfg, target_s=12.0):
-    """The fp64 oracle, as it stands, on a bounded sample of the workload (whole rows of channels)."""
+def cpu_baseline(cfg, target_s=10.0):
+    """The fp64 oracle, as it stands, on a bounded sample of the workload: whole batch rows
+    (every channel, full L), taken in order and repeated until about ``target_s`` of CPU time."""
     import oracle
     from selective_state_space_126_b300 import synthetic as syn
     threads = oracle.default_threads()
@@ -168,28 +170,162 @@ def cpu_baseline(cfg, target_s=12.0):
         cores = os.cpu_count() or 1
     L, N = cfg.seqlen, cfg.dstate
     A, Dskip, bias = syn.layer_params(cfg.dim, N, cfg.dt_min, cfg.dt_max)
-    chans = 64
-    elapsed, done = 0.0, 0
-    while True:
-        d1 = min(cfg.dim, chans)
-        u = syn.channel_rows(cfg, syn.T_U, 0, 0, d1)[None]
-        dl = syn.channel_rows(cfg, syn.T_DELTA, 0, 0, d1)[None]
-        z = syn.channel_rows(cfg, syn.T_Z, 0, 0, d1)[None] if cfg.gate else None
-        Bm = syn.bc_rows(cfg, syn.T_B, 0)[None]
-        Cm = syn.bc_rows(cfg, syn.T_C, 0)[None]
+    chans = cfg.dim if cfg.seqlen * cfg.dim <= (1 << 24) else max(threads, (1 << 24) // cfg.seqlen)
+    elapsed, updates, rows = 0.0, 0, 0
+    while elapsed < target_s and rows < 64:
+        b = rows % cfg.batch
+        u = syn.channel_rows(cfg, syn.T_U, b, 0, chans)[None]
+        dl = syn.channel_rows(cfg, syn.T_DELTA, b, 0, chans)[None]
+        z = syn.channel_rows(cfg, syn.T_Z, b, 0, chans)[None] if cfg.gate else None
+        Bm = syn.bc_rows(cfg, syn.T_B, b)[None]
+        Cm = syn.bc_rows(cfg, syn.T_C, b)[None]
         t0 = time.perf_counter()
-        oracle.selective_scan(u, dl, A[:d1], Bm, Cm, Dskip=Dskip[:d1] if cfg.dskip else None, z=z,
-                              delta_bias=bias[:d1], nthreads=threads)
-        elapsed = time.perf_counter() - t0
-        done = d1
-        if elapsed >= target_s / 4 or d1 == cfg.dim:
-            break
-        chans = min(cfg.dim, int(chans * max(2.0, min(8.0, target_s / 4 / max(elapsed, 1e-3)))))
-    updates = done * L * N
+        oracle.selective_scan(u, dl, A[:chans], Bm, Cm, Dskip=Dskip[:chans] if cfg.dskip else None, z=z,
+                              delta_bias=bias[:chans], nthreads=threads)
+        elapsed += time.perf_counter() - t0
+        updates += chans * L * N
+        rows += 1
     return {"value": updates / elapsed, "unit": UNIT, "cores": threads, "host_cores_visible": cores,
             "kind": "oracle",
-            "sample": f"batch row 0, channels 0..{done - 1} of {cfg.dim}, full L={L}, N={N} "
-                      f"({updates} state updates, {elapsed:.2f} s)"}
+            "sample": f"{rows} batch rows of the workload (channels 0..{chans - 1} of {cfg.dim} each, full L={L}, "
+                      f"N={N}), {updates} state updates in {elapsed:.1f} s of oracle time"}
+
+
+def random_device_inputs(cfg, seed, device):
+    """Inputs with the workload's shapes and value distributions drawn on the GPU (seeded); used for
+    the timing-only rows, where the host-side per-row recipe would take minutes to generate."""
+    import torch
+    from selective_state_space_126_b300 import synthetic as syn
+    g = torch.Generator(device=device)
+    g.manual_seed(1000 + seed)
+    dt = torch.float32 if cfg.io_dtype == "f32" else torch.bfloat16
+    B, D, L, N = cfg.batch, cfg.dim, cfg.seqlen, cfg.dstate
+
+    def randn(*shape):
+        return torch.randn(*shape, generator=g, device=device, dtype=torch.float32).to(dt)
+
+    out = {"u": randn(B, D, L), "z": randn(B, D, L) if cfg.gate else None}
+    nb = 1 if cfg.shared_bc else B
+    if cfg.time_invariant:
+        out["delta"] = randn(B, D, 1).expand(B, D, L).contiguous()
+        out["Bm"] = randn(nb, N, 1).expand(nb, N, L).contiguous()
+        out["Cm"] = randn(nb, N, 1).expand(nb, N, L).contiguous()
+    else:
+        out["delta"] = randn(B, D, L)
+        out["Bm"], out["Cm"] = randn(nb, N, L), randn(nb, N, L)
+    if cfg.shared_bc:
+        out["Bm"], out["Cm"] = out["Bm"][0], out["Cm"][0]
+    A, Dskip, bias = syn.layer_params(D, N, cfg.dt_min, cfg.dt_max, seed)
+    out["A"] = torch.from_numpy(A).to(device)
+    out["Dskip"] = torch.from_numpy(Dskip).to(device) if cfg.dskip else None
+    out["delta_bias"] = torch.from_numpy(bias).to(device)
+    return out
+
+
+def time_launches(run, n, stream, flush=None):
+    """Mean device time of ``run`` over n launches (CUDA events on the launching stream), with an
+    optional L2 flush between launches outside the timed events."""
+    import torch
+    ms = []
+    for _ in range(n):
+        if flush is not None:
+            flush()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        run()
+        e1.record(stream)
+        ms.append((e0, e1))
+    torch.cuda.synchronize()
+    return float(np.mean([a.elapsed_time(b) for a, b in ms]))
+
+
+def decode_bytes(cfg) -> int:
+    """Bytes one decode step must move: the fp32 state read and written; u, delta, z read and y
+    written (B*D each, I/O dtype); B, C (B*N each); A (D*N) and D, delta_bias (D) in fp32."""
+    es = 4 if cfg.io_dtype == "f32" else 2
+    bd = cfg.batch * cfg.dim
+    return (2 * bd * cfg.dstate * 4 + ((3 if cfg.gate else 2) + 1) * bd * es + 2 * cfg.batch * cfg.dstate * es
+            + cfg.dim * cfg.dstate * 4 + 2 * cfg.dim * 4)
+
+
+def other_rows(lib, ssm, peak, stream, dev):
+    """The remaining rows of the hot path, each timed on its own full-size workload: the other
+    scan shapes (single pass, time-invariant, the 2^20-step chunked scan) and 1000 decode steps."""
+    import torch
+    from selective_state_space_126_b300 import synthetic as syn
+    sh = ctypes.c_void_p(stream.cuda_stream)
+    # Reading 2x the L2 evicts the previous launch's lines and leaves only clean ones behind (a
+    # write-based flush would leave dirty lines whose write-back lands in the timed launch).
+    flush_buf = torch.ones(64 << 20, dtype=torch.float32, device=dev)
+    flush_sink = torch.empty(1, dtype=torch.float32, device=dev)
+
+    def flush():
+        torch.sum(flush_buf, dim=0, out=flush_sink)
+
+    rows = {}
+    for name, n in (("mamba130m_bf16_b8_d1536_l2048_n16", 200), ("mamba2.8b_ti_bf16_b1_d5120_l2048_n16", 200),
+                    ("long_bf16_b1_d1536_l1048576_n16", 5)):
+        cfg = syn.SCAN_CONFIGS[name]
+        inp = random_device_inputs(cfg, 0, dev)
+        y = torch.empty_like(inp["u"])
+        a = ssm.make_scan_args(inp["u"], inp["delta"], inp["A"], inp["Bm"], inp["Cm"], y, inp["Dskip"], inp["z"],
+                               inp["delta_bias"])
+        wsb = ssm.ssm_scan_workspace_size(a)
+        ws = torch.empty(max(wsb, 16), dtype=torch.uint8, device=dev)
+        a.workspace, a.workspace_bytes = ws.data_ptr(), wsb
+        path = ssm.ssm_scan_plan_path(a)
+        argp = ctypes.byref(a)
+
+        def run():
+            rc = lib.ssm_scan_fwd(argp, sh)
+            if rc != 0:
+                raise RuntimeError(ssm.status_name(rc))
+
+        for _ in range(3):
+            run()
+        algo = algorithmic_bytes(cfg)
+        ms = time_launches(run, n, stream, flush if algo < (256 << 20) else None)
+        gbs = algo / (ms * 1e-3) / 1e9
+        rows[name] = {"ms": ms, "value": cfg.updates / (ms * 1e-3), "unit": UNIT, "path": path,
+                      "launches": {"tiled": 1, "chunked": 3, "generic": 1}[path],
+                      "hbm_gbs_algorithmic": gbs, "frac": gbs / peak, "algorithmic_bytes": algo,
+                      "l2": "flushed between launches" if algo < (256 << 20) else "inputs larger than L2"}
+        del inp, y, ws
+        torch.cuda.empty_cache()
+
+    # decode: 1000 consecutive steps against one persistent fp32 state
+    dc = syn.DECODE
+    g = torch.Generator(device=dev)
+    g.manual_seed(2000)
+    Bsz, D, N, steps = dc.batch, dc.dim, dc.dstate, dc.steps
+    bf = torch.bfloat16 if dc.io_dtype == "bf16" else torch.float32
+    state = torch.randn(Bsz, D, N, generator=g, device=dev)
+    toks = {k: torch.randn(steps, Bsz, D, generator=g, device=dev).to(bf) for k in ("u", "delta", "z")}
+    bcs = {k: torch.randn(steps, Bsz, N, generator=g, device=dev).to(bf) for k in ("Bm", "Cm")}
+    A, Dskip, bias = syn.decode_params(dc)
+    A, Dskip, bias = (torch.from_numpy(x).to(dev) for x in (A, Dskip, bias))
+    yd = torch.empty(Bsz, D, dtype=bf, device=dev)
+    sargs = [ssm.make_step_args(state, toks["u"][i], toks["delta"][i], A, bcs["Bm"][i], bcs["Cm"][i], yd, Dskip,
+                                toks["z"][i], bias) for i in range(steps)]
+    it = iter(range(10 ** 9))
+
+    def dstep():
+        i = next(it) % steps
+        rc = lib.ssm_state_update(ctypes.byref(sargs[i]), sh)
+        if rc != 0:
+            raise RuntimeError(ssm.status_name(rc))
+
+    for _ in range(3):
+        dstep()
+    ms = time_launches(dstep, steps, stream, flush)
+    byt = decode_bytes(dc)
+    gbs = byt / (ms * 1e-3) / 1e9
+    rows[dc.name] = {"ms_per_step": ms, "value": dc.updates_per_step / (ms * 1e-3), "unit": UNIT,
+                     "steps": steps, "hbm_gbs_algorithmic": gbs, "frac": gbs / peak, "algorithmic_bytes": byt,
+                     "l2": "flushed between steps (the 84 MB state would otherwise stay in the 126 MB L2)"}
+    del flush_buf, flush_sink, state, toks, bcs
+    torch.cuda.empty_cache()
+    return rows
 
 
 def run_reference(args, rank, world):
@@ -385,6 +521,8 @@ def main():
         "clocks": clocks,
         "e2e": e2e,
     }
+    if not args.no_rows:
+        line["rows"] = other_rows(lib, ssm, peak, stream, dev)
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(cfg)
     print(json.dumps(line), flush=True)
