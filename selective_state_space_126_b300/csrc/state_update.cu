@@ -31,7 +31,10 @@ namespace ssm {
 namespace {
 
 constexpr int ITEMS = 1;   // (channel, quad) items per thread of the per-item kernel
-constexpr int kRowSlots = 8;   // bulk-copy ring depth of the fast path (batch rows in flight per CTA)
+#ifndef SSM_DECODE_SLOTS
+#define SSM_DECODE_SLOTS 16
+#endif
+constexpr int kRowSlots = SSM_DECODE_SLOTS;   // bulk-copy ring depth of the fast path (batch rows in flight per CTA)
 
 __device__ __forceinline__ void load4(const __nv_bfloat16* p, int64_t stride, int n0, int N, bool vec, float (&v)[4]) {
   if (vec) {
