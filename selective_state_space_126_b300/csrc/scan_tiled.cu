@@ -47,9 +47,7 @@
 #include <cstdio>
 #include <cstring>
 
-#include "async_copy.cuh"
-#include "device_math.cuh"
-#include "ssm_internal.h"
+#include "scan_common.cuh"
 
 namespace ssm {
 namespace {
@@ -64,38 +62,7 @@ constexpr int CH = 32;   // channels per CTA, one per lane
 constexpr int min_blocks(int K, int NS) { return (K * NS <= 16) ? SSM_TILED_MIN_BLOCKS : 2; }
 constexpr int T = kTileT;
 constexpr int kStages = 2;
-constexpr int MODE_OUTPUT = 0;
-constexpr int MODE_RECORD = 1;
-#ifndef SSM_EXP_AHEAD
-#define SSM_EXP_AHEAD 0
-#endif
 
-struct TiledParams {
-  int64_t B, D, L;
-  int N;
-  int nchunks;
-  int64_t chunk_len;
-  const float* A;
-  int64_t sA0, sA1;
-  const float* Dskip;
-  const float* bias;
-  const float* h0;
-  int64_t sh00, sh01, sh02;
-  float* h_last;
-  int64_t shl0, shl1, shl2;
-  float* rec_h;     // [B][D][nchunks][NP]: chunk end state (record pass) / chunk initial state (output pass)
-  float* rec_s;     // [B][D][nchunks]: sum of Delta over the chunk
-  int softplus;
-  int has_z;
-  int seq_rank3;    // u / delta / z tensor maps carry a batch dimension (else shared across the batch)
-  int bc_rank3;     // B / C tensor maps carry a batch dimension
-  int y_rank3;      // the y tensor map carries a batch dimension
-  int* status;
-};
-
-struct TensorMaps {
-  CUtensorMap u, delta, z, B, C, y;
-};
 
 // Shared-memory layout of one CTA (byte offsets from a 1024-aligned base;
 // every TMA box starts on a 1024-byte boundary, as the swizzled layouts need).
@@ -121,18 +88,10 @@ struct Smem {
   static_assert(kSeqTile % 1024 == 0 && kBCTile % 1024 == 0, "box alignment");
 };
 
-// Byte offset of 16-byte piece `chunk` of row `row` in a box that TMA wrote
-// with the 64-byte (rows of 64 bytes) or 128-byte (rows of 128 bytes)
-// swizzle: the piece index is XOR-ed with address bits 7.. of the row.
-template <int ROWB>
-__device__ __forceinline__ int swz(int row, int chunk) {
-  if (ROWB == 64) return row * 64 + ((chunk ^ ((row >> 1) & 3)) << 4);
-  return row * 128 + ((chunk ^ (row & 7)) << 4);
-}
 
 template <typename IO, int K, int NS, int MODE, bool PRECISE>
 __global__ void __launch_bounds__(32 * K, min_blocks(K, NS))
-    scan_tiled_kernel(const __grid_constant__ TiledParams p, const __grid_constant__ TensorMaps tm) {
+    scan_tiled_kernel(const __grid_constant__ ScanKernelParams p, const __grid_constant__ ScanMaps tm) {
   using S = Smem<IO, K, NS>;
   constexpr int kThreads = 32 * K;
   constexpr int NP = S::NP;
@@ -239,138 +198,50 @@ __global__ void __launch_bounds__(32 * K, min_blocks(K, NS))
     vD[i] = p.Dskip ? p.Dskip[dvc] : 0.f;
   }
 
-  float dsum = 0.f;
-  for (int k = 0; k < ntiles; ++k) {
+  // ---- stage A of tile k: Delta and Delta*u -> dt_s; B / C widened to fp32 -> bc_s ----
+  auto stage_a = [&](int k) {
     const int64_t t0 = t_begin + (int64_t)k * T;
-    const int slot = k % kStages;
-    const uint32_t phase = (uint32_t)(k / kStages) & 1u;
-    const unsigned char* ring = smem + S::kRing + slot * S::kStage;
-
-    // ---- stage A: Delta and Delta*u for this tile; B / C widened to fp32 ----
-    const bool ok = mbar_wait(bar_base + 8 * slot, phase);
-    if (ok) {
+    const unsigned char* ring = smem + S::kRing + (k % kStages) * S::kStage;
 #pragma unroll
-      for (int i = 0; i < NV; ++i) {
-        if (!vec_thread) break;
-        float uv[VEC], dv[VEC];
-        const int off = swz<ROWB>(vc[i], vt[i] / VEC);
-        unpack16(*reinterpret_cast<const uint4*>(ring + S::kU + off), uv);
-        unpack16(*reinterpret_cast<const uint4*>(ring + S::kDelta + off), dv);
-        const bool full = t0 + vt[i] + VEC <= t_end;      // else a ragged chunk end: mask per step
-        float4* dst = reinterpret_cast<float4*>(dt_s + vc[i] * S::kDTRow + vt[i]);
+    for (int i = 0; i < NV; ++i) {
+      if (!vec_thread) break;
+      float uv[VEC], dv[VEC];
+      const int off = swz<ROWB>(vc[i], vt[i] / VEC);
+      unpack16(*reinterpret_cast<const uint4*>(ring + S::kU + off), uv);
+      unpack16(*reinterpret_cast<const uint4*>(ring + S::kDelta + off), dv);
+      const bool full = t0 + vt[i] + VEC <= t_end;      // else a ragged chunk end: mask per step
+      float4* dst = reinterpret_cast<float4*>(dt_s + vc[i] * S::kDTRow + vt[i]);
 #pragma unroll
-        for (int j = 0; j < VEC; j += 2) {
-          float2 dt = delta_of2<PRECISE>(make_float2(dv[j], dv[j + 1]), vbias[i], p.softplus);
-          if (!full) {
-            if (t0 + vt[i] + j >= t_end) dt.x = 0.f;
-            if (t0 + vt[i] + j + 1 >= t_end) dt.y = 0.f;
-          }
-          const float2 du = __fmul2_rn(dt, make_float2(uv[j], uv[j + 1]));
-          dst[j / 2] = make_float4(dt.x, du.x, dt.y, du.y);
+      for (int j = 0; j < VEC; j += 2) {
+        float2 dt = delta_of2<PRECISE>(make_float2(dv[j], dv[j + 1]), vbias[i], p.softplus);
+        if (!full) {
+          if (t0 + vt[i] + j >= t_end) dt.x = 0.f;
+          if (t0 + vt[i] + j + 1 >= t_end) dt.y = 0.f;
         }
+        const float2 du = __fmul2_rn(dt, make_float2(uv[j], uv[j + 1]));
+        dst[j / 2] = make_float4(dt.x, du.x, dt.y, du.y);
       }
-      // B and C rows -> fp32 [t][B|C][n]: thread v takes row v % ACT (B rows
-      // first, then C rows; the record pass needs only B) and piece v / ACT
-      // of it, so that a warp writes consecutive floats per step
-      constexpr int ROWS = 2 * NP;
-      constexpr int ACT = MODE == MODE_OUTPUT ? ROWS : NP;
-      for (int v = tid; v < ACT * VPR; v += kThreads) {
-        const int row = v % ACT, piece = v / ACT;
-        const int tensor = row / NP, n = row % NP;
-        if (n >= N) continue;
-        float f[VEC];
-        unpack16(*reinterpret_cast<const uint4*>(ring + S::kB + tensor * S::kBCTile + swz<ROWB>(n, piece)), f);
+    }
+    // B and C rows -> fp32 [t][B|C][n]: thread v takes row v % ACT (B rows
+    // first, then C rows; the record pass needs only B) and piece v / ACT
+    // of it, so that a warp writes consecutive floats per step
+    constexpr int ROWS = 2 * NP;
+    constexpr int ACT = MODE == MODE_OUTPUT ? ROWS : NP;
+    for (int v = tid; v < ACT * VPR; v += kThreads) {
+      const int row = v % ACT, piece = v / ACT;
+      const int tensor = row / NP, n = row % NP;
+      if (n >= N) continue;
+      float f[VEC];
+      unpack16(*reinterpret_cast<const uint4*>(ring + S::kB + tensor * S::kBCTile + swz<ROWB>(n, piece)), f);
 #pragma unroll
-        for (int e = 0; e < VEC; ++e) bc_s[(piece * VEC + e) * ROWS + row] = f[e];
-      }
-    } else {
-      record_status(p.status, SSM_ERR_TIMEOUT);
+      for (int e = 0; e < VEC; ++e) bc_s[(piece * VEC + e) * ROWS + row] = f[e];
     }
-    // the y store of tile k-2 (issued at tile k-1) must be done reading its
-    // staging box before stage C of this tile rewrites it
-    if (MODE == MODE_OUTPUT && tid == 0 && k >= 2) bulk_wait_read<0>();
-    if (__syncthreads_or(!ok)) {   // a TMA copy never completed (the next tile is not issued yet)
-      if (MODE == MODE_OUTPUT && tid == 0) bulk_wait<0>();
-      return;
-    }
+  };
 
-    // Every thread is past stage C of tile k-1 and stage A of tile k: the
-    // other ring slot is free, so the next tile's copies go out now; the
-    // staging box of tile k-1 is complete, so its store goes out too.
-    if (tid == 0) {
-      if (k + 1 < ntiles) issue(k + 1);
-      if (MODE == MODE_OUTPUT && k >= 1) store_y(k - 1);
-    }
-
-    // ---- stage B: the recurrence over the T steps of the tile ----
-    {
-      const float4* dt4 = reinterpret_cast<const float4*>(dt_s + c * S::kDTRow);
-      const float* bcg = bc_s + g * NS;
-      float* prow = part_s + (g * CH + c) * S::kPartRow;
-      float yv[4];
-#if SSM_EXP_AHEAD
-      // Abar of the next step is computed one step ahead, so that its SFU
-      // latency overlaps the dependent FMAs of the current step.
-      float2 an[NS / 2];
-      {
-        const float dt0 = dt4[0].x;
-#pragma unroll
-        for (int q = 0; q < NS / 2; ++q) {
-          const float2 x = __fmul2_rn(make_float2(dt0, dt0), A2[q]);
-          an[q] = make_float2(ex2_approx(x.x), ex2_approx(x.y));
-        }
-      }
-#endif
-#pragma unroll
-      for (int t = 0; t < T; t += 2) {
-        const float4 dd = dt4[t / 2];
-#pragma unroll
-        for (int s = 0; s < 2; ++s) {
-          const float dt = s ? dd.z : dd.x;
-          const float du = s ? dd.w : dd.y;
-          const float* Bt = bcg + (t + s) * 2 * NP;
-          const float2 du2 = make_float2(du, du);
-          float2 a[NS / 2];
-#if SSM_EXP_AHEAD
-#pragma unroll
-          for (int q = 0; q < NS / 2; ++q) a[q] = an[q];
-          if (t + s + 1 < T) {
-            const float dtn = s ? dt4[t / 2 + 1].x : dd.z;
-#pragma unroll
-            for (int q = 0; q < NS / 2; ++q) {
-              const float2 x = __fmul2_rn(make_float2(dtn, dtn), A2[q]);
-              an[q] = make_float2(ex2_approx(x.x), ex2_approx(x.y));
-            }
-          }
-#else
-#pragma unroll
-          for (int q = 0; q < NS / 2; ++q) {
-            const float2 x = __fmul2_rn(make_float2(dt, dt), A2[q]);
-            a[q] = make_float2(ex2_approx(x.x), ex2_approx(x.y));
-          }
-#endif
-          float2 acc = make_float2(0.f, 0.f);
-#pragma unroll
-          for (int q = 0; q < NS; q += 4) {
-            const float4 bq = *reinterpret_cast<const float4*>(Bt + q);
-            h[q / 2] = __ffma2_rn(a[q / 2], h[q / 2], __fmul2_rn(du2, make_float2(bq.x, bq.y)));
-            h[q / 2 + 1] = __ffma2_rn(a[q / 2 + 1], h[q / 2 + 1], __fmul2_rn(du2, make_float2(bq.z, bq.w)));
-            if (MODE == MODE_OUTPUT) {
-              const float4 cq = *reinterpret_cast<const float4*>(Bt + NP + q);
-              acc = __ffma2_rn(make_float2(cq.x, cq.y), h[q / 2], acc);
-              acc = __ffma2_rn(make_float2(cq.z, cq.w), h[q / 2 + 1], acc);
-            }
-          }
-          yv[(t + s) & 3] = acc.x + acc.y;
-          if (MODE == MODE_RECORD) dsum += dt;
-        }
-        if (MODE == MODE_OUTPUT && (t & 3) == 2)
-          *reinterpret_cast<float4*>(prow + t - 2) = make_float4(yv[0], yv[1], yv[2], yv[3]);
-      }
-    }
-    __syncthreads();
-
-    // ---- stage C: sum the K partials, D skip, gate, store ----
+  // ---- stage C of tile k: sum the K partials, D skip, gate -> staging box ----
+  auto stage_c = [&](int k) {
+    const int64_t t0 = t_begin + (int64_t)k * T;
+    const unsigned char* ring = smem + S::kRing + (k % kStages) * S::kStage;
     if (MODE == MODE_OUTPUT) {
 #pragma unroll
       for (int i = 0; i < NV; ++i) {
@@ -404,14 +275,79 @@ __global__ void __launch_bounds__(32 * K, min_blocks(K, NS))
       }
       fence_async_smem();   // the staging box is read by the TMA store issued after the next barrier
     }
-  }
-  if (MODE == MODE_OUTPUT && ntiles > 0) {
+  };
+
+  // Tile loop.  Stage C of tile k and stage A of tile k+1 form one phase
+  // between the barriers that bracket stage B, so that their latency chains
+  // overlap:  A(0) | B(0) | C(0) A(1) | B(1) | C(1) A(2) | ...
+  // Ring slot k % 2 is free after the phase that holds C(k); the TMA loads of
+  // tile k+2 go into it, and the TMA store of tile k's staging box goes out.
+  float dsum = 0.f;
+  bool ok = ntiles > 0 ? mbar_wait(bar_base, 0) : true;
+  if (ok && ntiles > 0) stage_a(0);
+  if (!ok) record_status(p.status, SSM_ERR_TIMEOUT);
+  if (__syncthreads_or(!ok)) return;   // nothing else is in flight
+  if (tid == 0 && ntiles > 1) issue(1);
+  for (int k = 0; k < ntiles; ++k) {
+    // ---- stage B: the recurrence over the T steps of the tile ----
+    {
+      const float4* dt4 = reinterpret_cast<const float4*>(dt_s + c * S::kDTRow);
+      const float* bcg = bc_s + g * NS;
+      float* prow = part_s + (g * CH + c) * S::kPartRow;
+      float yv[4];
+#pragma unroll
+      for (int t = 0; t < T; t += 2) {
+        const float4 dd = dt4[t / 2];
+#pragma unroll
+        for (int s = 0; s < 2; ++s) {
+          const float dt = s ? dd.z : dd.x;
+          const float du = s ? dd.w : dd.y;
+          const float* Bt = bcg + (t + s) * 2 * NP;
+          const float2 du2 = make_float2(du, du);
+          float2 a[NS / 2];
+#pragma unroll
+          for (int q = 0; q < NS / 2; ++q) {
+            const float2 x = __fmul2_rn(make_float2(dt, dt), A2[q]);
+            a[q] = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+          }
+          float2 acc = make_float2(0.f, 0.f);
+#pragma unroll
+          for (int q = 0; q < NS; q += 4) {
+            const float4 bq = *reinterpret_cast<const float4*>(Bt + q);
+            h[q / 2] = __ffma2_rn(a[q / 2], h[q / 2], __fmul2_rn(du2, make_float2(bq.x, bq.y)));
+            h[q / 2 + 1] = __ffma2_rn(a[q / 2 + 1], h[q / 2 + 1], __fmul2_rn(du2, make_float2(bq.z, bq.w)));
+            if (MODE == MODE_OUTPUT) {
+              const float4 cq = *reinterpret_cast<const float4*>(Bt + NP + q);
+              acc = __ffma2_rn(make_float2(cq.x, cq.y), h[q / 2], acc);
+              acc = __ffma2_rn(make_float2(cq.z, cq.w), h[q / 2 + 1], acc);
+            }
+          }
+          yv[(t + s) & 3] = acc.x + acc.y;
+          if (MODE == MODE_RECORD) dsum += dt;
+        }
+        if (MODE == MODE_OUTPUT && (t & 3) == 2)
+          *reinterpret_cast<float4*>(prow + t - 2) = make_float4(yv[0], yv[1], yv[2], yv[3]);
+      }
+    }
+    // the store of tile k-2 must be done reading the staging box that C(k) rewrites
+    if (MODE == MODE_OUTPUT && tid == 0 && k >= 2) bulk_wait_read<1>();
     __syncthreads();
+
+    const bool next = k + 1 < ntiles;
+    ok = next ? mbar_wait(bar_base + 8 * ((k + 1) % kStages), (uint32_t)((k + 1) / kStages) & 1u) : true;
+    if (MODE == MODE_OUTPUT) stage_c(k);
+    if (ok && next) stage_a(k + 1);
+    if (!ok) record_status(p.status, SSM_ERR_TIMEOUT);
+    if (__syncthreads_or(!ok)) {   // tile k+1's copy never completed; only tile k's store may be in flight
+      if (MODE == MODE_OUTPUT && tid == 0) bulk_wait<0>();
+      return;
+    }
     if (tid == 0) {
-      store_y(ntiles - 1);
-      bulk_wait<0>();       // the staging boxes outlive their stores
+      if (k + 2 < ntiles) issue(k + 2);
+      if (MODE == MODE_OUTPUT) store_y(k);
     }
   }
+  if (MODE == MODE_OUTPUT && tid == 0 && ntiles > 0) bulk_wait<0>();   // the staging boxes outlive their stores
 
   // ---- epilogue: final state or chunk record ----
   if (MODE == MODE_OUTPUT) {
@@ -435,28 +371,8 @@ __global__ void __launch_bounds__(32 * K, min_blocks(K, NS))
   }
 }
 
-// Chunk carry: turns the per-chunk end states (from zero) into each chunk's
-// true initial state, in chunk order.  One thread per (b, d, n).
-__global__ void __launch_bounds__(256) chunk_carry_kernel(const TiledParams p, int NP) {
-  const int64_t gid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  const int64_t total = p.B * p.D * NP;
-  if (gid >= total) return;
-  const int n = (int)(gid % NP);
-  const int64_t c = gid / NP;
-  const int64_t b = c / p.D, d = c % p.D;
-  if (n >= p.N) return;
-  const float a2 = p.A[d * p.sA0 + n * p.sA1] * kLog2e;
-  float hcur = p.h0 ? p.h0[b * p.sh00 + d * p.sh01 + n * p.sh02] : 0.f;
-  for (int k = 0; k < p.nchunks; ++k) {
-    const int64_t r = c * p.nchunks + k;
-    const float hend = p.rec_h[r * NP + n];
-    p.rec_h[r * NP + n] = hcur;
-    hcur = fmaf(ex2_approx(a2 * p.rec_s[r]), hcur, hend);
-  }
-}
-
 template <typename IO, int K, int NS, int MODE, bool PRECISE>
-cudaError_t launch_one(const TiledParams& tp, const TensorMaps& tm, dim3 grid, cudaStream_t s) {
+cudaError_t launch_one(const ScanKernelParams& tp, const ScanMaps& tm, dim3 grid, cudaStream_t s) {
   using S = Smem<IO, K, NS>;
   auto kern = scan_tiled_kernel<IO, K, NS, MODE, PRECISE>;
   static unsigned long long attr_set = 0;   // one bit per device; a racing duplicate set is harmless
@@ -474,7 +390,7 @@ cudaError_t launch_one(const TiledParams& tp, const TensorMaps& tm, dim3 grid, c
 }
 
 template <typename IO, int K, int NS, bool PRECISE>
-cudaError_t launch_shape(const ScanProblem& p, const ScanPlan& plan, TiledParams& tp, const TensorMaps& tm,
+cudaError_t launch_shape(const ScanProblem& p, const ScanPlan& plan, ScanKernelParams& tp, const ScanMaps& tm,
                          cudaStream_t s) {
   constexpr int NP = K * NS;
   const dim3 grid((unsigned)((p.D + CH - 1) / CH), (unsigned)plan.nchunks, (unsigned)p.B);
@@ -490,31 +406,8 @@ cudaError_t launch_shape(const ScanProblem& p, const ScanPlan& plan, TiledParams
   return launch_one<IO, K, NS, MODE_OUTPUT, PRECISE>(tp, tm, grid, s);
 }
 
-// Tensor map of a (batch, rows, L) tensor with time stride 1, box (T steps x
-// box_rows), swizzled (see swz).  Rank 3 (t, row, b) when the batch stride is
-// used, else rank 2 (t, row).
-bool encode_map(CUtensorMap* map, const void* base, const int64_t* strides, int64_t rows, uint32_t box_rows,
-                const ScanProblem& p, bool rank3) {
-  EncodeTiledFn enc = get_encode_tiled();
-  if (!enc) return false;
-  const int es = p.io == SSM_F32 ? 4 : 2;
-  const CUtensorMapDataType dt = p.io == SSM_F32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
-  // a stride over an extent of 1 is never used; give the encoder a valid one
-  const int64_t row_stride = rows > 1 ? strides[1] : (p.L + 7) / 8 * 8;
-  const int64_t batch_stride = strides[0];
-  cuuint64_t dims[3] = {(cuuint64_t)p.L, (cuuint64_t)rows, (cuuint64_t)p.B};
-  cuuint64_t gstr[2] = {(cuuint64_t)(row_stride * es), (cuuint64_t)(batch_stride * es)};
-  cuuint32_t box[3] = {(cuuint32_t)T, box_rows, 1};
-  cuuint32_t estr[3] = {1, 1, 1};
-  const CUtensorMapSwizzle swz = es == 2 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B;
-  CUresult r = enc(map, dt, rank3 ? 3 : 2, const_cast<void*>(base), dims, gstr, box, estr,
-                   CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
-                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS;
-}
-
 template <typename IO, bool PRECISE>
-cudaError_t launch_typed(const ScanProblem& p, const ScanPlan& plan, TiledParams& tp, const TensorMaps& tm,
+cudaError_t launch_typed(const ScanProblem& p, const ScanPlan& plan, ScanKernelParams& tp, const ScanMaps& tm,
                          cudaStream_t s) {
   const int K = plan.shape.K, NS = plan.shape.NS;
   if (K == 1 && NS == 16) return launch_shape<IO, 1, 16, PRECISE>(p, plan, tp, tm, s);
@@ -528,36 +421,9 @@ cudaError_t launch_typed(const ScanProblem& p, const ScanPlan& plan, TiledParams
 }  // namespace
 
 cudaError_t launch_scan_tiled(const ScanProblem& p, const ScanPlan& plan, void* workspace, cudaStream_t s) {
-  TiledParams tp{};
-  tp.B = p.B; tp.D = p.D; tp.L = p.L; tp.N = (int)p.N;
-  tp.nchunks = (int)plan.nchunks;
-  tp.chunk_len = plan.nchunks > 1 ? plan.chunk_len : p.L;
-  tp.A = p.A; tp.sA0 = p.sA[0]; tp.sA1 = p.sA[1];
-  tp.Dskip = p.Dskip; tp.bias = p.bias;
-  tp.h0 = p.h0; tp.sh00 = p.sh0[0]; tp.sh01 = p.sh0[1]; tp.sh02 = p.sh0[2];
-  tp.h_last = p.h_last; tp.shl0 = p.shl[0]; tp.shl1 = p.shl[1]; tp.shl2 = p.shl[2];
-  tp.softplus = p.softplus ? 1 : 0;
-  tp.has_z = p.z ? 1 : 0;
-  tp.status = device_status_ptr();
-  const int NP = plan.shape.K * plan.shape.NS;
-  if (plan.nchunks > 1) {
-    float* ws = static_cast<float*>(workspace);
-    tp.rec_h = ws;
-    tp.rec_s = ws + p.B * p.D * plan.nchunks * NP;
-  }
-  // the planner only picks this path when u, delta, z share one batch layout
-  // kind and B, C share another (see tiled_eligible); y, an output, is
-  // batched whenever B > 1
-  tp.seq_rank3 = (p.su[0] != 0 && p.B > 1) ? 1 : 0;
-  tp.bc_rank3 = (p.sB[0] != 0 && p.B > 1) ? 1 : 0;
-  tp.y_rank3 = p.B > 1 ? 1 : 0;
-  TensorMaps tm;
-  std::memset(&tm, 0, sizeof(tm));
-  const bool r3 = tp.seq_rank3 == 1, b3 = tp.bc_rank3 == 1, y3 = tp.y_rank3 == 1;
-  if (!encode_map(&tm.u, p.u, p.su, p.D, CH, p, r3) || !encode_map(&tm.delta, p.delta, p.sd, p.D, CH, p, r3) ||
-      (p.z && !encode_map(&tm.z, p.z, p.sz, p.D, CH, p, r3)) || !encode_map(&tm.y, p.y, p.sy, p.D, CH, p, y3) ||
-      !encode_map(&tm.B, p.Bm, p.sB, p.N, (uint32_t)p.N, p, b3) ||
-      !encode_map(&tm.C, p.Cm, p.sC, p.N, (uint32_t)p.N, p, b3))
+  ScanKernelParams tp;
+  ScanMaps tm;
+  if (!make_scan_kernel_args(p, plan, workspace, plan.shape.K * plan.shape.NS, T, &tp, &tm))
     return cudaErrorInvalidValue;
   if (p.io == SSM_F32) return launch_typed<float, true>(p, plan, tp, tm, s);
   return launch_typed<__nv_bfloat16, false>(p, plan, tp, tm, s);
