@@ -54,6 +54,10 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--no-rows", action="store_true", help="skip the other workloads' timing rows")
+    ap.add_argument("--only-rows", action="store_true",
+                    help="time only the other workloads' rows (one line of JSON; for profiling their kernels)")
+    ap.add_argument("--rows", default="all", help="comma-separated subset of rows: m130, ti, long, decode")
+    ap.add_argument("--decode-steps", type=int, default=1000, help="decode steps of the decode row")
     return ap.parse_args()
 
 
@@ -248,7 +252,11 @@ def decode_bytes(cfg) -> int:
             + cfg.dim * cfg.dstate * 4 + 2 * cfg.dim * 4)
 
 
-def other_rows(lib, ssm, peak, stream, dev):
+ROW_KEYS = {"m130": "mamba130m_bf16_b8_d1536_l2048_n16", "ti": "mamba2.8b_ti_bf16_b1_d5120_l2048_n16",
+            "long": "long_bf16_b1_d1536_l1048576_n16", "decode": "decode_bf16_b256_d5120_n16_x1000"}
+
+
+def other_rows(lib, ssm, peak, stream, dev, which="all", decode_steps=1000):
     """The remaining rows of the hot path, each timed on its own full-size workload: the other
     scan shapes (single pass, time-invariant, the 2^20-step chunked scan) and 1000 decode steps."""
     import torch
@@ -262,9 +270,12 @@ def other_rows(lib, ssm, peak, stream, dev):
     def flush():
         torch.sum(flush_buf, dim=0, out=flush_sink)
 
+    sel = set(ROW_KEYS) if which == "all" else set(which.split(","))
     rows = {}
-    for name, n in (("mamba130m_bf16_b8_d1536_l2048_n16", 200), ("mamba2.8b_ti_bf16_b1_d5120_l2048_n16", 200),
-                    ("long_bf16_b1_d1536_l1048576_n16", 5)):
+    for key, n in (("m130", 200), ("ti", 200), ("long", 5)):
+        if key not in sel:
+            continue
+        name = ROW_KEYS[key]
         cfg = syn.SCAN_CONFIGS[name]
         inp = random_device_inputs(cfg, 0, dev)
         y = torch.empty_like(inp["u"])
@@ -293,8 +304,11 @@ def other_rows(lib, ssm, peak, stream, dev):
         del inp, y, ws
         torch.cuda.empty_cache()
 
-    # decode: 1000 consecutive steps against one persistent fp32 state
-    dc = syn.DECODE
+    if "decode" not in sel:
+        del flush_buf, flush_sink
+        return rows
+    # decode: consecutive steps (1000 by default) against one persistent fp32 state
+    dc = syn.with_decode_steps(syn.DECODE, decode_steps) if decode_steps != syn.DECODE.steps else syn.DECODE
     g = torch.Generator(device=dev)
     g.manual_seed(2000)
     Bsz, D, N, steps = dc.batch, dc.dim, dc.dstate, dc.steps
@@ -395,6 +409,12 @@ def main():
     lib = ssm.load_library()
     cfg = workload(args)
     dev = torch.device("cuda", torch.cuda.current_device())
+    if args.only_rows:
+        if rank == 0:
+            peak, _ = measured_peaks()
+            print(json.dumps({"rows": other_rows(lib, ssm, peak, torch.cuda.current_stream(), dev, args.rows,
+                                                 args.decode_steps)}), flush=True)
+        return
 
     # ---- inputs resident in HBM (each rank its own replica, seeded by rank) ----
     inp = device_inputs(cfg, seed=rank)
@@ -522,7 +542,7 @@ def main():
         "e2e": e2e,
     }
     if not args.no_rows:
-        line["rows"] = other_rows(lib, ssm, peak, stream, dev)
+        line["rows"] = other_rows(lib, ssm, peak, stream, dev, args.rows, args.decode_steps)
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(cfg)
     print(json.dumps(line), flush=True)

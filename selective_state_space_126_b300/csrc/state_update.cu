@@ -35,6 +35,11 @@ constexpr int ITEMS = 1;   // (channel, quad) items per thread of the per-item k
 #define SSM_DECODE_SLOTS 16
 #endif
 constexpr int kRowSlots = SSM_DECODE_SLOTS;   // bulk-copy ring depth of the fast path (batch rows in flight per CTA)
+#ifndef SSM_DECODE_GROUP
+#define SSM_DECODE_GROUP 8
+#endif
+constexpr int kRowGroup = SSM_DECODE_GROUP;   // batch rows per barrier of the fast path
+static_assert(kRowSlots % kRowGroup == 0 && kRowSlots >= 2 * kRowGroup, "ring of whole groups");
 
 __device__ __forceinline__ void load4(const __nv_bfloat16* p, int64_t stride, int n0, int N, bool vec, float (&v)[4]) {
   if (vec) {
@@ -207,45 +212,60 @@ __global__ void __launch_bounds__(128) state_update_bulk_kernel(const StepProble
   if (tid == 0)
     for (int k = 0; k < kRowSlots && k < rows; ++k) issue(k);
 
-  for (int k = 0; k < rows; ++k) {
-    const int s = k % kRowSlots;
-    const bool ok = mbar_wait(bar0 + 8 * s, (uint32_t)(k / kRowSlots) & 1u);
+  // Rows go in groups of kRowGroup per barrier: every thread waits for the
+  // group's slots, updates its quad of each row, then (after one barrier)
+  // thread 0 refills the group's slots with rows kRowSlots further on.
+  for (int k0 = 0; k0 < rows; k0 += kRowGroup) {
+    bool ok = true;
+#pragma unroll
+    for (int r = 0; r < kRowGroup; ++r) {
+      const int k = k0 + r;
+      if (k < rows) ok = ok && mbar_wait(bar0 + 8 * (k % kRowSlots), (uint32_t)(k / kRowSlots) & 1u);
+    }
     if (__syncthreads_or(!ok)) {
       // a copy never completed: record it, let the others in flight land (bounded), leave
       if (tid == 0) {
         record_status(status, SSM_ERR_TIMEOUT);
-        for (int j = k + 1; j < k + kRowSlots && j < rows; ++j)
+        const int issued = k0 >= kRowGroup ? k0 - kRowGroup + kRowSlots : kRowSlots;   // rows [0, issued) went out
+        for (int j = k0; j < issued && j < rows; ++j)
           (void)mbar_wait(bar0 + 8 * (j % kRowSlots), (uint32_t)(j / kRowSlots) & 1u);
       }
       return;
     }
-    // every thread is done with row k-1: its slot takes row k-1+kRowSlots
-    if (tid == 0 && k >= 1 && k - 1 + kRowSlots < rows) issue(k - 1 + kRowSlots);
-    const unsigned char* sl = slots[s];
-    const int64_t b = g + (int64_t)k * row_groups;
-    const float4 hv = *reinterpret_cast<const float4*>(sl + R::kState + (c * R::N + n0) * 4);
-    const float uv = to_f32(reinterpret_cast<const IO*>(sl + R::kU)[c]);
-    const float dv = to_f32(reinterpret_cast<const IO*>(sl + R::kDelta)[c]);
-    const float zv = has_z ? to_f32(reinterpret_cast<const IO*>(sl + R::kZ)[c]) : 0.f;
-    const IO* Bs = reinterpret_cast<const IO*>(sl + R::kB);
-    const IO* Cs = reinterpret_cast<const IO*>(sl + R::kC);
-    const float dt = delta_of<PRECISE>(dv, bias, p.softplus);
-    const float du = dt * uv;
-    float h[4] = {hv.x, hv.y, hv.z, hv.w};
-    float acc = 0.f;
+    // every thread is done with the previous group: its slots take the rows kRowSlots further on
+    if (tid == 0 && k0 >= kRowGroup)
+      for (int k = k0 - kRowGroup; k < k0; ++k)
+        if (k + kRowSlots < rows) issue(k + kRowSlots);
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const float a = ex2_approx(dt * A4[i]);
-      h[i] = fmaf(a, h[i], du * to_f32(Bs[n0 + i]));
-      acc = fmaf(to_f32(Cs[n0 + i]), h[i], acc);
-    }
+    for (int r = 0; r < kRowGroup; ++r) {
+      const int k = k0 + r;
+      if (k >= rows) break;
+      const unsigned char* sl = slots[k % kRowSlots];
+      const int64_t b = g + (int64_t)k * row_groups;
+      const float4 hv = *reinterpret_cast<const float4*>(sl + R::kState + (c * R::N + n0) * 4);
+      const float uv = to_f32(reinterpret_cast<const IO*>(sl + R::kU)[c]);
+      const float dv = to_f32(reinterpret_cast<const IO*>(sl + R::kDelta)[c]);
+      const float zv = has_z ? to_f32(reinterpret_cast<const IO*>(sl + R::kZ)[c]) : 0.f;
+      const IO* Bs = reinterpret_cast<const IO*>(sl + R::kB);
+      const IO* Cs = reinterpret_cast<const IO*>(sl + R::kC);
+      const float dt = delta_of<PRECISE>(dv, bias, p.softplus);
+      const float du = dt * uv;
+      float h[4] = {hv.x, hv.y, hv.z, hv.w};
+      float acc = 0.f;
 #pragma unroll
-    for (int off = 1; off < Q; off <<= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-    *reinterpret_cast<float4*>(p.state + b * p.sst[0] + d * R::N + n0) = make_float4(h[0], h[1], h[2], h[3]);
-    if (q == 0) {
-      float out = fmaf(Dd, uv, acc);
-      if (has_z) out *= silu<PRECISE>(zv);
-      static_cast<IO*>(p.y)[b * p.sy[0] + d] = from_f32<IO>(out);
+      for (int i = 0; i < 4; ++i) {
+        const float a = ex2_approx(dt * A4[i]);
+        h[i] = fmaf(a, h[i], du * to_f32(Bs[n0 + i]));
+        acc = fmaf(to_f32(Cs[n0 + i]), h[i], acc);
+      }
+#pragma unroll
+      for (int off = 1; off < Q; off <<= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+      *reinterpret_cast<float4*>(p.state + b * p.sst[0] + d * R::N + n0) = make_float4(h[0], h[1], h[2], h[3]);
+      if (q == 0) {
+        float out = fmaf(Dd, uv, acc);
+        if (has_z) out *= silu<PRECISE>(zv);
+        static_cast<IO*>(p.y)[b * p.sy[0] + d] = from_f32<IO>(out);
+      }
     }
   }
 }

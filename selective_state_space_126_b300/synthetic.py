@@ -80,6 +80,11 @@ DECODE = DecodeConfig("decode_bf16_b256_d5120_n16_x1000", 256, 5120, 16, 1000)
 SCAN_CONFIGS = {c.name: c for c in (TINY, M130, M2P8, M2P8_TI, LONG)}
 
 
+def with_decode_steps(cfg: DecodeConfig, steps: int) -> DecodeConfig:
+    """A copy of the decode workload with another number of steps (same shapes and distributions)."""
+    return replace(cfg, steps=steps, name=f"{cfg.name}_steps{steps}")
+
+
 def with_shape(cfg: ScanConfig, **kw) -> ScanConfig:
     """A copy of ``cfg`` with some fields replaced (same distributions)."""
     return replace(cfg, **kw)
