@@ -270,6 +270,130 @@ __global__ void __launch_bounds__(128) state_update_bulk_kernel(const StepProble
   }
 }
 
+// Wide fast path for N = 16: one thread per channel with all 16 states, 128
+// channels per CTA, so that a batch row is one 8 KB state copy plus three
+// 256-byte copies of u, delta, z and two 32-byte copies of B, C.  Thread c
+// visits its four 16-byte state pieces in an order rotated by (c / 2) % 4,
+// which spreads a quarter-warp's shared-memory reads over all bank groups; A,
+// B and C are read in the same rotated order, so no piece is ever moved back.
+template <typename IO>
+struct WideSlot {
+  static constexpr int CH = 128;
+  static constexpr int kState = 0;                                      // float [128][16]: 8 KB
+  static constexpr int kU = CH * 16 * 4;                                // IO [128] each for u, delta, z
+  static constexpr int kSeq = CH * (int)sizeof(IO);
+  static constexpr int kDelta = kU + kSeq, kZ = kU + 2 * kSeq;
+  static constexpr int kB = kU + 3 * kSeq;                              // IO [16] each for B, C
+  static constexpr int kBC = 16 * (int)sizeof(IO);
+  static constexpr int kC = kB + kBC;
+  static constexpr int kBytes = (kC + kBC + 127) / 128 * 128;
+};
+constexpr int kWideSlots = 4;
+
+__device__ __forceinline__ void load_piece(const __nv_bfloat16* p, float (&v)[4]) {
+  const uint2 r = *reinterpret_cast<const uint2*>(p);
+  v[0] = __uint_as_float(r.x << 16);
+  v[1] = __uint_as_float(r.x & 0xffff0000u);
+  v[2] = __uint_as_float(r.y << 16);
+  v[3] = __uint_as_float(r.y & 0xffff0000u);
+}
+__device__ __forceinline__ void load_piece(const float* p, float (&v)[4]) {
+  const float4 r = *reinterpret_cast<const float4*>(p);
+  v[0] = r.x; v[1] = r.y; v[2] = r.z; v[3] = r.w;
+}
+
+template <typename IO, bool PRECISE>
+__global__ void __launch_bounds__(128) state_update_wide_kernel(const StepProblem p, int row_groups, int* status) {
+  using W = WideSlot<IO>;
+  __shared__ __align__(128) unsigned char slots[kWideSlots][W::kBytes];
+  __shared__ __align__(8) uint64_t bars[kWideSlots];
+
+  const int c = threadIdx.x;
+  const int rot = (c >> 1) & 3;
+  const int64_t d0 = (int64_t)blockIdx.x * W::CH;
+  const int64_t d = d0 + c;
+  const int g = blockIdx.y;
+  const int rows = (int)((p.B - g + row_groups - 1) / row_groups);   // rows g, g + G, g + 2G, ...
+
+  float2 A2[8];   // A * log2(e), pieces in rotated order
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const float4 a = *reinterpret_cast<const float4*>(p.A + d * p.sA[0] + 4 * ((j + rot) & 3));
+    A2[2 * j] = make_float2(a.x * kLog2e, a.y * kLog2e);
+    A2[2 * j + 1] = make_float2(a.z * kLog2e, a.w * kLog2e);
+  }
+  const float bias = p.bias ? p.bias[d] : 0.f;
+  const float Dd = p.Dskip ? p.Dskip[d] : 0.f;
+  const bool has_z = p.z != nullptr;
+
+  const uint32_t bar0 = smem_u32(&bars[0]);
+  if (c == 0) {
+    for (int s = 0; s < kWideSlots; ++s) mbar_init(bar0 + 8 * s, 1);
+    mbar_init_fence();
+  }
+  __syncthreads();
+  const uint32_t tile_bytes = (uint32_t)(W::CH * 16 * 4 + (2 + (has_z ? 1 : 0)) * W::kSeq + 2 * W::kBC);
+  auto issue = [&](int k) {
+    const int64_t b = g + (int64_t)k * row_groups;
+    const int s = k % kWideSlots;
+    const uint32_t dst = smem_u32(&slots[s][0]), bar = bar0 + 8 * s;
+    mbar_expect_tx(bar, tile_bytes);
+    bulk_load(dst + W::kState, p.state + b * p.sst[0] + d0 * 16, W::CH * 16 * 4, bar);
+    bulk_load(dst + W::kU, static_cast<const IO*>(p.u) + b * p.su[0] + d0, W::kSeq, bar);
+    bulk_load(dst + W::kDelta, static_cast<const IO*>(p.delta) + b * p.sd[0] + d0, W::kSeq, bar);
+    if (has_z) bulk_load(dst + W::kZ, static_cast<const IO*>(p.z) + b * p.sz[0] + d0, W::kSeq, bar);
+    bulk_load(dst + W::kB, static_cast<const IO*>(p.Bm) + b * p.sB[0], W::kBC, bar);
+    bulk_load(dst + W::kC, static_cast<const IO*>(p.Cm) + b * p.sC[0], W::kBC, bar);
+  };
+  if (c == 0)
+    for (int k = 0; k < kWideSlots && k < rows; ++k) issue(k);
+
+  for (int k = 0; k < rows; ++k) {
+    const int s = k % kWideSlots;
+    const bool ok = mbar_wait(bar0 + 8 * s, (uint32_t)(k / kWideSlots) & 1u);
+    if (__syncthreads_or(!ok)) {
+      // a copy never completed: record it, let the others in flight land (bounded), leave
+      if (c == 0) {
+        record_status(status, SSM_ERR_TIMEOUT);
+        const int issued = k >= 1 ? k - 1 + kWideSlots : kWideSlots;   // rows [0, issued) went out
+        for (int j = k; j < issued && j < rows; ++j)
+          (void)mbar_wait(bar0 + 8 * (j % kWideSlots), (uint32_t)(j / kWideSlots) & 1u);
+      }
+      return;
+    }
+    // every thread is done with row k-1: its slot takes row k-1+kWideSlots
+    if (c == 0 && k >= 1 && k - 1 + kWideSlots < rows) issue(k - 1 + kWideSlots);
+    const unsigned char* sl = slots[s];
+    const int64_t b = g + (int64_t)k * row_groups;
+    const float uv = to_f32(reinterpret_cast<const IO*>(sl + W::kU)[c]);
+    const float dv = to_f32(reinterpret_cast<const IO*>(sl + W::kDelta)[c]);
+    const float zv = has_z ? to_f32(reinterpret_cast<const IO*>(sl + W::kZ)[c]) : 0.f;
+    const float dt = delta_of<PRECISE>(dv, bias, p.softplus);
+    const float2 dt2 = make_float2(dt, dt), du2 = make_float2(dt * uv, dt * uv);
+    float2 acc = make_float2(0.f, 0.f);
+    float* st = p.state + b * p.sst[0] + d * 16;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int piece = (j + rot) & 3;
+      const float4 hv = *reinterpret_cast<const float4*>(sl + W::kState + (c * 16 + 4 * piece) * 4);
+      float Bv[4], Cv[4];
+      load_piece(reinterpret_cast<const IO*>(sl + W::kB) + 4 * piece, Bv);
+      load_piece(reinterpret_cast<const IO*>(sl + W::kC) + 4 * piece, Cv);
+      const float2 x0 = __fmul2_rn(dt2, A2[2 * j]), x1 = __fmul2_rn(dt2, A2[2 * j + 1]);
+      const float2 a0 = make_float2(ex2_approx(x0.x), ex2_approx(x0.y));
+      const float2 a1 = make_float2(ex2_approx(x1.x), ex2_approx(x1.y));
+      const float2 h0 = __ffma2_rn(a0, make_float2(hv.x, hv.y), __fmul2_rn(du2, make_float2(Bv[0], Bv[1])));
+      const float2 h1 = __ffma2_rn(a1, make_float2(hv.z, hv.w), __fmul2_rn(du2, make_float2(Bv[2], Bv[3])));
+      acc = __ffma2_rn(make_float2(Cv[0], Cv[1]), h0, acc);
+      acc = __ffma2_rn(make_float2(Cv[2], Cv[3]), h1, acc);
+      *reinterpret_cast<float4*>(st + 4 * piece) = make_float4(h0.x, h0.y, h1.x, h1.y);
+    }
+    float out = fmaf(Dd, uv, acc.x + acc.y);
+    if (has_z) out *= silu<PRECISE>(zv);
+    static_cast<IO*>(p.y)[b * p.sy[0] + d] = from_f32<IO>(out);
+  }
+}
+
 // Whether the fast path takes these arguments (dense rows, 16-byte aligned bulk copies).
 template <typename IO>
 bool bulk_eligible(const StepProblem& p, int* Qout) {
@@ -318,9 +442,25 @@ cudaError_t launch_bulk(const StepProblem& p, cudaStream_t s) {
 }
 
 template <typename IO, bool PRECISE>
+cudaError_t launch_wide(const StepProblem& p, cudaStream_t s) {
+  int dev = 0, sms = 148;
+  if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int64_t ranges = p.D / WideSlot<IO>::CH;
+  // about 5 resident CTAs per SM; every CTA walks B / G batch rows
+  int64_t G = (5 * (int64_t)sms + ranges - 1) / ranges;
+  G = std::max<int64_t>(1, std::min<int64_t>(G, std::min<int64_t>(p.B, 65535)));
+  state_update_wide_kernel<IO, PRECISE><<<dim3((unsigned)ranges, (unsigned)G), 128, 0, s>>>(p, (int)G,
+                                                                                          device_status_ptr());
+  return cudaGetLastError();
+}
+
+template <typename IO, bool PRECISE>
 cudaError_t launch_typed(const StepProblem& p, cudaStream_t s) {
   int Qb = 0;
-  if (bulk_eligible<IO>(p, &Qb) && getenv("SSM_DECODE_PER_ITEM") == nullptr) {
+  const bool bulk = bulk_eligible<IO>(p, &Qb) && getenv("SSM_DECODE_PER_ITEM") == nullptr;
+  if (bulk && p.N == 16 && p.D % WideSlot<IO>::CH == 0 && getenv("SSM_DECODE_QUAD") == nullptr)
+    return launch_wide<IO, PRECISE>(p, s);
+  if (bulk) {
     switch (Qb) {
       case 1:
         if constexpr (sizeof(IO) == 4) return launch_bulk<IO, 1, PRECISE>(p, s);

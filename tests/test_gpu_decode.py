@@ -26,7 +26,8 @@ def step_inputs(B, D, N, io, seed, gate=True, dskip=True):
 
 
 @pytest.mark.parametrize("io", ["f32", "bf16"])
-@pytest.mark.parametrize("shape", [(1, 1, 1), (3, 17, 5), (4, 64, 16), (2, 33, 13), (2, 8, 64), (5, 300, 32)])
+@pytest.mark.parametrize("shape", [(1, 1, 1), (3, 17, 5), (4, 64, 16), (2, 33, 13), (2, 8, 64), (5, 300, 32),
+                                   (3, 256, 16), (7, 384, 16)])
 def test_step_shapes(io, shape):
     B, D, N = shape
     p = step_inputs(B, D, N, io, seed=sum(shape))
@@ -39,6 +40,28 @@ def test_step_shapes(io, shape):
                                  z=p["z"], delta_bias=p["delta_bias"])
     assert_close(io, host(y), yr, f"y {shape}")
     assert_close(io, host(st), sr, f"state {shape}")
+
+
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+@pytest.mark.parametrize("kernel", ["wide", "quad", "per_item"])
+def test_step_every_kernel(io, kernel, monkeypatch):
+    """The three decode kernels (one thread per channel and 128 channels per CTA; four lanes per
+    channel with bulk-copied rows; per-item global loads) on the same dense N = 16 inputs."""
+    if kernel == "quad":
+        monkeypatch.setenv("SSM_DECODE_QUAD", "1")
+    if kernel == "per_item":
+        monkeypatch.setenv("SSM_DECODE_PER_ITEM", "1")
+    B, D, N = 37, 256, 16
+    p = step_inputs(B, D, N, io, seed=11)
+    st = to_dev(p["state"])
+    y = ssm.ssm_state_update(st, to_dev(p["u"], io), to_dev(p["delta"], io), to_dev(p["A"]),
+                             to_dev(p["Bm"], io), to_dev(p["Cm"], io), Dskip=to_dev(p["Dskip"]),
+                             z=to_dev(p["z"], io), delta_bias=to_dev(p["delta_bias"]))
+    torch.cuda.synchronize()
+    sr, yr = oracle.state_update(p["state"], p["u"], p["delta"], p["A"], p["Bm"], p["Cm"], Dskip=p["Dskip"],
+                                 z=p["z"], delta_bias=p["delta_bias"])
+    assert_close(io, host(y), yr, f"y {kernel}")
+    assert_close(io, host(st), sr, f"state {kernel}")
 
 
 def test_step_strided_state():
