@@ -4,11 +4,12 @@
 //  * the state recurrence, the C contraction and every intermediate are fp32;
 //  * exp(Delta * A) uses the SFU base-2 exponential (ex2.approx.ftz) on
 //    Delta * A * log2(e), relative error a few ulp;
-//  * softplus has two forms.  For bf16 I/O the SFU form
-//    max(s,0) + ln2 * lg2(1 + 2^(-|s| log2 e)) is used (absolute error
-//    ~1e-7, far inside bf16 rounding).  For fp32 I/O the accurate library
-//    log1pf/expf form is used, because lg2.approx has an absolute (not
-//    relative) error bound near 1 and Delta can be as small as ~1e-5;
+//  * softplus has two forms.  For bf16 I/O:
+//    max(s,0) + log1p(e) with e = 2^(-|s| log2 e) from the SFU and
+//    log1p(e) = e * q(e) evaluated as a polynomial on the FMA pipe (q fitted
+//    on [0, 1] by fit_log1p.py, relative error 2.3e-7), so Delta keeps its
+//    relative accuracy however small it is.  For fp32 I/O the library
+//    log1pf/expf form is used;
 //  * silu(z) = z / (1 + 2^(-z log2 e)) with the SFU reciprocal.
 #pragma once
 
@@ -18,17 +19,10 @@
 namespace ssm {
 
 constexpr float kLog2e = 1.4426950408889634f;
-constexpr float kLn2 = 0.6931471805599453f;
 
 __device__ __forceinline__ float ex2_approx(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
-
-__device__ __forceinline__ float lg2_approx(float x) {
-  float y;
-  asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
 
@@ -38,14 +32,40 @@ __device__ __forceinline__ float rcp_approx(float x) {
   return y;
 }
 
+// log1p(e) for e in [0, 1] as e * (1 + e * r(e)); r is the degree-7
+// polynomial printed by fit_log1p.py (relative error 2.3e-7 in fp32).
+__device__ __forceinline__ float log1p_unit(float e) {
+  float r = 6.479088217e-03f;
+  r = fmaf(r, e, -3.448650241e-02f);
+  r = fmaf(r, e, 8.630371094e-02f);
+  r = fmaf(r, e, -1.434402466e-01f);
+  r = fmaf(r, e, 1.942283958e-01f);
+  r = fmaf(r, e, -2.492260784e-01f);
+  r = fmaf(r, e, 3.332882226e-01f);
+  r = fmaf(r, e, -4.999993443e-01f);
+  return e * fmaf(e, r, 1.f);
+}
+
+// Two-lane form of log1p_unit on packed f32x2 FMAs.
+__device__ __forceinline__ float2 log1p_unit2(float2 e) {
+  float2 r = make_float2(6.479088217e-03f, 6.479088217e-03f);
+  r = __ffma2_rn(r, e, make_float2(-3.448650241e-02f, -3.448650241e-02f));
+  r = __ffma2_rn(r, e, make_float2(8.630371094e-02f, 8.630371094e-02f));
+  r = __ffma2_rn(r, e, make_float2(-1.434402466e-01f, -1.434402466e-01f));
+  r = __ffma2_rn(r, e, make_float2(1.942283958e-01f, 1.942283958e-01f));
+  r = __ffma2_rn(r, e, make_float2(-2.492260784e-01f, -2.492260784e-01f));
+  r = __ffma2_rn(r, e, make_float2(3.332882226e-01f, 3.332882226e-01f));
+  r = __ffma2_rn(r, e, make_float2(-4.999993443e-01f, -4.999993443e-01f));
+  return __fmul2_rn(e, __ffma2_rn(e, r, make_float2(1.f, 1.f)));
+}
+
 // softplus(s) = log(1 + e^s) = max(s, 0) + log1p(e^{-|s|})
 template <bool PRECISE>
 __device__ __forceinline__ float softplus(float s) {
   if (PRECISE) {
     return fmaxf(s, 0.f) + log1pf(expf(-fabsf(s)));
   } else {
-    const float e = ex2_approx(-fabsf(s) * kLog2e);
-    return fmaf(lg2_approx(1.f + e), kLn2, fmaxf(s, 0.f));
+    return fmaxf(s, 0.f) + log1p_unit(ex2_approx(-fabsf(s) * kLog2e));
   }
 }
 
@@ -58,13 +78,12 @@ __device__ __forceinline__ float silu(float z) {
   }
 }
 
-// Two-lane forms of the SFU softplus and silu above, with the FMA-pipe work
+// Two-lane forms of the fast softplus and silu above, with the FMA-pipe work
 // on packed f32x2 instructions (same arithmetic, half the issue slots).
 __device__ __forceinline__ float2 softplus2_fast(float2 s) {
   const float2 x = __fmul2_rn(make_float2(fabsf(s.x), fabsf(s.y)), make_float2(-kLog2e, -kLog2e));
-  const float2 ope = __fadd2_rn(make_float2(ex2_approx(x.x), ex2_approx(x.y)), make_float2(1.f, 1.f));
-  return __ffma2_rn(make_float2(lg2_approx(ope.x), lg2_approx(ope.y)), make_float2(kLn2, kLn2),
-                    make_float2(fmaxf(s.x, 0.f), fmaxf(s.y, 0.f)));
+  return __fadd2_rn(make_float2(fmaxf(s.x, 0.f), fmaxf(s.y, 0.f)),
+                    log1p_unit2(make_float2(ex2_approx(x.x), ex2_approx(x.y))));
 }
 
 __device__ __forceinline__ float2 silu2_fast(float2 z) {

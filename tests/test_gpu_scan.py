@@ -119,6 +119,18 @@ def test_options(io, opt):
         assert_close(io, hl, hr, f"h_last {opt} {path}")
 
 
+def test_small_delta_relative_accuracy():
+    """Delta around 1e-5 (long memory): the final state, which is never rounded to the I/O dtype, keeps
+    fp32 relative accuracy.  The fast softplus must be accurate relative to Delta, not just absolutely."""
+    case = rand_case(2, 64, 1024, 16, "bf16", seed=5)
+    case["delta_bias"] = np.full(64, float(syn.softplus_inverse(1e-5)), dtype=np.float32)
+    case["delta"] = case["delta"] * 0.25
+    y, hl = gpu_scan(case, "bf16")
+    yr, hr = oracle_case(case)
+    assert rel_l2(hl, hr) <= 1e-4, rel_l2(hl, hr)
+    assert_close("bf16", y, yr, "y")
+
+
 def test_padded_row_strides():
     """Rows stored with padding (row stride 104 for L = 100), seen through strides."""
     case = rand_case(2, 24, 100, 16, "f32", seed=3)
