@@ -84,12 +84,36 @@ def algorithmic_bytes(cfg) -> int:
     return (seq + bc) * es + params
 
 
+def bench_config(cfg, world) -> dict:
+    """The workload description both arms print (the reference arm runs a bounded sample of it)."""
+    algo = algorithmic_bytes(cfg)
+    return {"workload": cfg.name, "batch": cfg.batch, "dim": cfg.dim, "seqlen": cfg.seqlen, "dstate": cfg.dstate,
+            "io_dtype": cfg.io_dtype, "l2": f"inputs larger than L2 ({algo / 1e6:.0f} MB moved per step vs 126 MB L2)",
+            "parallelism": f"replicas x{world}" if world > 1 else "single GPU"}
+
+
 def source_sha() -> str:
     h = hashlib.sha256()
     for f in SCAN_SOURCES:
         with open(os.path.join(ROOT, f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
+
+
+def max_over_ranks(x: float, world: int, device) -> float:
+    """The largest of every rank's x (the job's step time is its slowest rank's); x itself at N = 1."""
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_value(updates_per_rank: int, world: int, ms_per_step: float) -> float:
+    """Whole-job throughput: every rank's state updates over the job's (slowest rank's) step time."""
+    return updates_per_rank * world / (ms_per_step * 1e-3)
 
 
 def measured_peaks():
@@ -376,8 +400,7 @@ def run_reference(args, rank, world):
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": cfg.name, "batch": cfg.batch, "dim": cfg.dim, "seqlen": cfg.seqlen,
-                   "dstate": cfg.dstate, "io_dtype": cfg.io_dtype},
+        "config": bench_config(cfg, world),
         "cpu_baseline": {"kind": "oracle", "cores": threads, "sample": sample, "value": value, "unit": UNIT},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }), flush=True)
@@ -461,13 +484,10 @@ def main():
     sampler.stop()
     total_ms = start.elapsed_time(stop)
     launch_ms = float(np.mean([s.elapsed_time(e) for s, e in ev]))
-    if world > 1:
-        t = torch.tensor([total_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(total_ms, world, dev)
     ms_per_step = total_ms / args.steps
     updates_per_step = cfg.updates * world
-    value = updates_per_step / (ms_per_step * 1e-3)
+    value = job_value(cfg.updates, world, ms_per_step)
 
     # ---- end to end through the C ABI from pinned host buffers ----
     e2e = None
@@ -494,10 +514,7 @@ def main():
         s1.record(stream)
         torch.cuda.synchronize()
         e2e_ms = s0.elapsed_time(s1) / args.e2e_steps
-        if world > 1:
-            t = torch.tensor([e2e_ms], device=dev)
-            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-            e2e_ms = float(t.item())
+        e2e_ms = max_over_ranks(e2e_ms, world, dev)
         e2e = {"value": updates_per_step / (e2e_ms * 1e-3), "unit": UNIT, "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms, "steps": args.e2e_steps,
                "host_memory": "pinned"}
@@ -527,10 +544,7 @@ def main():
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": max(3, args.warmup), "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": {"workload": cfg.name, "batch": cfg.batch, "dim": cfg.dim, "seqlen": cfg.seqlen,
-                   "dstate": cfg.dstate, "io_dtype": cfg.io_dtype, "path": path,
-                   "l2": f"inputs larger than L2 ({algo / 1e6:.0f} MB moved per step vs 126 MB L2)",
-                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "config": bench_config(cfg, world), "path": path,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "traffic": traffic, "peak_kind": peak_kind, "algorithmic_bytes_per_launch": algo,
                      "kernel_ms": kernel_ms},
