@@ -72,12 +72,14 @@ struct Smem {
   static constexpr int ROWB = T * (int)sizeof(IO);                   // bytes per box row
   static constexpr int kSeqTile = CH * ROWB;                         // one (32 ch x 32 t) box
   static constexpr int kBCTile = NP * ROWB;                          // one (N x 32 t) box, N <= NP rows
-  static constexpr int kU = 0, kDelta = kSeqTile, kZ = 2 * kSeqTile, kB = 3 * kSeqTile;
-  static constexpr int kC = kB + kBCTile;
-  static constexpr int kStage = (kC + kBCTile + 1023) / 1024 * 1024; // bytes per ring slot
+  static constexpr int kSeqBox = (kSeqTile + 1023) / 1024 * 1024;    // boxes start on 1024-byte boundaries
+  static constexpr int kBCBox = (kBCTile + 1023) / 1024 * 1024;
+  static constexpr int kU = 0, kDelta = kSeqBox, kZ = 2 * kSeqBox, kB = 3 * kSeqBox;
+  static constexpr int kC = kB + kBCBox;
+  static constexpr int kStage = kC + kBCBox;                         // bytes per ring slot
   static constexpr int kRing = 0;
   static constexpr int kY = kRing + kStages * kStage;                // two y staging boxes
-  static constexpr int kBC = kY + 2 * kSeqTile;                      // float [T][2][NP]
+  static constexpr int kBC = kY + 2 * kSeqBox;                       // float [T][2][NP]
   static constexpr int kDT = kBC + T * 2 * NP * 4;                   // float2 [CH][T+2]
   static constexpr int kDTRow = T + 2;
   static constexpr int kPart = kDT + CH * kDTRow * 8;                // float [K][CH][T+4]
@@ -85,7 +87,6 @@ struct Smem {
   static constexpr int kBar = kPart + K * CH * kPartRow * 4;         // kStages x uint64
   static constexpr int kBytes = kBar + 8 * kStages;
   static constexpr int kAlloc = kBytes + 1024;                       // slack for the 1024-byte alignment
-  static_assert(kSeqTile % 1024 == 0 && kBCTile % 1024 == 0, "box alignment");
 };
 
 
@@ -177,7 +178,7 @@ __global__ void __launch_bounds__(32 * K, min_blocks(K, NS))
   };
   const int y_z = p.y_rank3 ? (int)b : 0;
   auto store_y = [&](int tile) {
-    tma_store(&tm.y, smem_u32(smem + S::kY + (tile & 1) * S::kSeqTile), (int)(t_begin + (int64_t)tile * T),
+    tma_store(&tm.y, smem_u32(smem + S::kY + (tile & 1) * S::kSeqBox), (int)(t_begin + (int64_t)tile * T),
               (int)d0, y_z, p.y_rank3);
     bulk_commit();
   };
@@ -232,7 +233,7 @@ __global__ void __launch_bounds__(32 * K, min_blocks(K, NS))
       const int tensor = row / NP, n = row % NP;
       if (n >= N) continue;
       float f[VEC];
-      unpack16(*reinterpret_cast<const uint4*>(ring + S::kB + tensor * S::kBCTile + swz<ROWB>(n, piece)), f);
+      unpack16(*reinterpret_cast<const uint4*>(ring + S::kB + tensor * S::kBCBox + swz<ROWB>(n, piece)), f);
 #pragma unroll
       for (int e = 0; e < VEC; ++e) bc_s[(piece * VEC + e) * ROWS + row] = f[e];
     }
@@ -271,7 +272,7 @@ __global__ void __launch_bounds__(32 * K, min_blocks(K, NS))
           yo[j] = o.x;
           yo[j + 1] = o.y;
         }
-        *reinterpret_cast<uint4*>(smem + S::kY + (k & 1) * S::kSeqTile + off) = pack16(yo);
+        *reinterpret_cast<uint4*>(smem + S::kY + (k & 1) * S::kSeqBox + off) = pack16(yo);
       }
       fence_async_smem();   // the staging box is read by the TMA store issued after the next barrier
     }
