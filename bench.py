@@ -37,6 +37,7 @@ sys.path.insert(0, ROOT)
 METRIC = "selective-scan state-updates/s (B·D·L·N/s); achieved HBM GB/s vs B300 peak"
 UNIT = "state-updates/s"
 SCAN_SOURCES = ["selective_state_space_126_b300/csrc/scan_tiled.cu",
+                "selective_state_space_126_b300/csrc/scan_common.cuh",
                 "selective_state_space_126_b300/csrc/async_copy.cuh",
                 "selective_state_space_126_b300/csrc/device_math.cuh"]
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "scan_tiled_traffic.txt")   # JSON text written from an ncu capture
