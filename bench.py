@@ -117,6 +117,11 @@ def job_value(updates_per_rank: int, world: int, ms_per_step: float) -> float:
     return updates_per_rank * world / (ms_per_step * 1e-3)
 
 
+def ssm_launches(lib, ssm, args) -> int:
+    """Kernel launches one ssm_scan_fwd makes for these arguments."""
+    return {"tiled": 1, "chunked": 3, "generic": 1}[ssm.ssm_scan_plan_path(args)]
+
+
 def measured_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -449,7 +454,7 @@ def main():
     ws_bytes = ssm.ssm_scan_workspace_size(a)
     ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
     a.workspace, a.workspace_bytes = ws.data_ptr(), ws_bytes
-    launches_per_step = {"tiled": 1, "chunked": 3, "generic": 1}[path]
+    launches_per_step = ssm_launches(lib, ssm, a)
     stream = torch.cuda.current_stream()
     sh = ctypes.c_void_p(stream.cuda_stream)
     argp = ctypes.byref(a)
@@ -491,34 +496,102 @@ def main():
     value = job_value(cfg.updates, world, ms_per_step)
 
     # ---- end to end through the C ABI from pinned host buffers ----
+    # Batch rows are independent scans, so the step is pipelined over chunks of rows on three streams:
+    # the host-to-device copies of chunk i+1 overlap the scan of chunk i and the read-back of chunk i-1,
+    # and both copy directions run at once.  Every byte of input and of y crosses the link every step.
     e2e = None
     if not args.no_e2e:
-        names = ["u", "delta", "z", "Bm", "Cm", "A", "Dskip", "delta_bias"]
-        hbuf = {k: inp[k].cpu().pin_memory() for k in names if inp[k] is not None}
+        seq_names = ["u", "delta", "z"] + (["Bm", "Cm"] if inp["Bm"].dim() == 3 else [])
+        par_names = ["A", "Dskip", "delta_bias"] + ([] if inp["Bm"].dim() == 3 else ["Bm", "Cm"])
+        hbuf = {k: inp[k].cpu().pin_memory() for k in seq_names + par_names if inp[k] is not None}
+        y_resident = y.float().cpu()
         hy = torch.empty(y.shape, dtype=y.dtype).pin_memory()
         h2d = sum(t.numel() * t.element_size() for t in hbuf.values())
         d2h = hy.numel() * hy.element_size()
+        nchunk = min(cfg.batch, 4)
+        bounds = [(i * cfg.batch // nchunk, (i + 1) * cfg.batch // nchunk) for i in range(nchunk)]
+        s_in, s_run, s_out = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
+        # the small per-channel parameters are double-buffered across steps, so that copying the next
+        # step's never waits for this step's last scan
+        par = [{k: inp[k] if inp[k] is None else torch.empty_like(inp[k]) for k in par_names} for _ in range(2)]
+        chunk_args, chunk_ws = [[], []], []
+        for b0, b1 in bounds:
+            wsb = 0
+            for q in range(2):
+                src = dict(inp, **par[q])
+                rows = lambda k: src[k][b0:b1] if src[k] is not None else None
+                bc = (lambda k: src[k][b0:b1]) if src["Bm"].dim() == 3 else (lambda k: src[k])
+                ca = ssm.make_scan_args(rows("u"), rows("delta"), src["A"], bc("Bm"), bc("Cm"), y[b0:b1],
+                                        src["Dskip"], rows("z"), src["delta_bias"])
+                if q == 0:
+                    wsb = ssm.ssm_scan_workspace_size(ca)
+                    chunk_ws.append(torch.empty(max(wsb, 16), dtype=torch.uint8, device=dev))
+                ca.workspace, ca.workspace_bytes = chunk_ws[-1].data_ptr(), wsb
+                chunk_args[q].append(ca)
+        ev_in = [torch.cuda.Event() for _ in bounds]
+        ev_run = [torch.cuda.Event() for _ in bounds]
+        ev_out = [torch.cuda.Event() for _ in bounds]
+        ev_par = [torch.cuda.Event() for _ in range(2)]
+        ev_par_used = [torch.cuda.Event() for _ in range(2)]
+        h_run = ctypes.c_void_p(s_run.cuda_stream)
+        n_e2e = [0]
 
-        def e2e_step():
-            for k, t in hbuf.items():
-                inp[k].copy_(t, non_blocking=True)
-            step()
-            hy.copy_(y, non_blocking=True)
+        def e2e_step(first):
+            q = n_e2e[0] % 2
+            n_e2e[0] += 1
+            with torch.cuda.stream(s_in):
+                if n_e2e[0] > 2:
+                    s_in.wait_event(ev_par_used[q])     # the scans of two steps ago are done with this buffer
+                for k in par_names:
+                    if inp[k] is not None:
+                        par[q][k].copy_(hbuf[k], non_blocking=True)
+                ev_par[q].record(s_in)
+            for i, (b0, b1) in enumerate(bounds):
+                with torch.cuda.stream(s_in):
+                    if not first:
+                        s_in.wait_event(ev_run[i])      # the previous step's scan of these rows has read them
+                    for k in seq_names:
+                        if inp[k] is not None:
+                            inp[k][b0:b1].copy_(hbuf[k][b0:b1], non_blocking=True)
+                    ev_in[i].record(s_in)
+                s_run.wait_event(ev_in[i])
+                s_run.wait_event(ev_par[q])
+                if not first:
+                    s_run.wait_event(ev_out[i])     # the previous step's read-back of these rows is done
+                rc = lib.ssm_scan_fwd(ctypes.byref(chunk_args[q][i]), h_run)
+                if rc != 0:
+                    raise RuntimeError(ssm.status_name(rc) + " " + lib.ssm_last_error_detail().decode())
+                ev_run[i].record(s_run)
+                s_out.wait_event(ev_run[i])
+                with torch.cuda.stream(s_out):
+                    hy[b0:b1].copy_(y[b0:b1], non_blocking=True)
+                    ev_out[i].record(s_out)
+            ev_par_used[q].record(s_run)
 
-        for _ in range(3):
-            e2e_step()
+        for w in range(3):
+            e2e_step(w == 0)
         torch.cuda.synchronize()
         s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         s0.record(stream)
+        for st in (s_in, s_run, s_out):
+            st.wait_event(s0)
         for _ in range(args.e2e_steps):
-            e2e_step()
+            e2e_step(False)
+        for e in ev_out:
+            stream.wait_event(e)
         s1.record(stream)
         torch.cuda.synchronize()
         e2e_ms = s0.elapsed_time(s1) / args.e2e_steps
         e2e_ms = max_over_ranks(e2e_ms, world, dev)
+        # the pipelined, host-to-host result must be the device-resident one
+        e2e_diff = float((hy.float() - y_resident).abs().max())
+        if not e2e_diff <= 1e-2 * max(1.0, float(y_resident.abs().max())):
+            raise RuntimeError(f"pipelined end-to-end y differs from the resident run by {e2e_diff}")
         e2e = {"value": updates_per_step / (e2e_ms * 1e-3), "unit": UNIT, "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms, "steps": args.e2e_steps,
-               "host_memory": "pinned"}
+               "host_memory": "pinned", "pipeline": f"{nchunk} chunks of batch rows on 3 streams",
+               "max_abs_diff_vs_resident": e2e_diff,
+               "gpu_launches_per_step": sum(ssm_launches(lib, ssm, ca) for ca in chunk_args[0])}
 
     if rank != 0:
         if world > 1:
