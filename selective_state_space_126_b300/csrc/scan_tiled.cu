@@ -46,6 +46,7 @@
 // rescans each chunk from its true initial state and emits y.
 #include <cstdio>
 #include <cstring>
+#include <type_traits>
 
 #include "scan_common.cuh"
 
@@ -53,6 +54,9 @@ namespace ssm {
 namespace {
 
 constexpr int CH = 32;   // channels per CTA, one per lane
+
+template <bool V>
+using Bool = std::integral_constant<bool, V>;
 
 // Resident CTAs per SM the register budget is sized for: enough that every
 // CTA of a 4 x 5120-channel problem (640 CTAs) is resident at once on 148 SMs.
@@ -200,9 +204,15 @@ __global__ void __launch_bounds__(32 * K, min_blocks(K, NS))
   }
 
   // ---- stage A of tile k: Delta and Delta*u -> dt_s; B / C widened to fp32 -> bc_s ----
-  auto stage_a = [&](int k) {
+  // The FAST form (a full tile, softplus on, N == NP, every channel of the CTA
+  // inside D) has no data-dependent branch, so that stage C of one tile and
+  // stage A of the next compile into one basic block the scheduler can
+  // interleave; the general form handles ragged ends, padding and options.
+  auto stage_a = [&](int k, auto fast_tag) {
+    constexpr bool FAST = decltype(fast_tag)::value;
     const int64_t t0 = t_begin + (int64_t)k * T;
     const unsigned char* ring = smem + S::kRing + (k % kStages) * S::kStage;
+    const bool use_sp = FAST || p.softplus;
 #pragma unroll
     for (int i = 0; i < NV; ++i) {
       if (!vec_thread) break;
@@ -210,11 +220,11 @@ __global__ void __launch_bounds__(32 * K, min_blocks(K, NS))
       const int off = swz<ROWB>(vc[i], vt[i] / VEC);
       unpack16(*reinterpret_cast<const uint4*>(ring + S::kU + off), uv);
       unpack16(*reinterpret_cast<const uint4*>(ring + S::kDelta + off), dv);
-      const bool full = t0 + vt[i] + VEC <= t_end;      // else a ragged chunk end: mask per step
+      const bool full = FAST || t0 + vt[i] + VEC <= t_end;   // else a ragged chunk end: mask per step
       float4* dst = reinterpret_cast<float4*>(dt_s + vc[i] * S::kDTRow + vt[i]);
 #pragma unroll
       for (int j = 0; j < VEC; j += 2) {
-        float2 dt = delta_of2<PRECISE>(make_float2(dv[j], dv[j + 1]), vbias[i], p.softplus);
+        float2 dt = delta_of2<PRECISE>(make_float2(dv[j], dv[j + 1]), vbias[i], use_sp);
         if (!full) {
           if (t0 + vt[i] + j >= t_end) dt.x = 0.f;
           if (t0 + vt[i] + j + 1 >= t_end) dt.y = 0.f;
@@ -228,10 +238,14 @@ __global__ void __launch_bounds__(32 * K, min_blocks(K, NS))
     // of it, so that a warp writes consecutive floats per step
     constexpr int ROWS = 2 * NP;
     constexpr int ACT = MODE == MODE_OUTPUT ? ROWS : NP;
-    for (int v = tid; v < ACT * VPR; v += kThreads) {
+    constexpr int NBC = (ACT * VPR + kThreads - 1) / kThreads;
+#pragma unroll
+    for (int ib = 0; ib < NBC; ++ib) {
+      const int v = tid + ib * kThreads;
+      if ((ACT * VPR) % kThreads != 0 && v >= ACT * VPR) break;
       const int row = v % ACT, piece = v / ACT;
       const int tensor = row / NP, n = row % NP;
-      if (n >= N) continue;
+      if (!FAST && n >= N) continue;
       float f[VEC];
       unpack16(*reinterpret_cast<const uint4*>(ring + S::kB + tensor * S::kBCBox + swz<ROWB>(n, piece)), f);
 #pragma unroll
@@ -240,14 +254,17 @@ __global__ void __launch_bounds__(32 * K, min_blocks(K, NS))
   };
 
   // ---- stage C of tile k: sum the K partials, D skip, gate -> staging box ----
-  auto stage_c = [&](int k) {
+  // (FAST as for stage A; HZ: the gate is on, fixed at compile time in the FAST form)
+  auto stage_c = [&](int k, auto fast_tag, auto hz_tag) {
+    constexpr bool FAST = decltype(fast_tag)::value;
     const int64_t t0 = t_begin + (int64_t)k * T;
     const unsigned char* ring = smem + S::kRing + (k % kStages) * S::kStage;
+    const bool gate = FAST ? decltype(hz_tag)::value : p.has_z != 0;
     if (MODE == MODE_OUTPUT) {
 #pragma unroll
       for (int i = 0; i < NV; ++i) {
         const int64_t dv = d0 + vc[i];
-        if (!(vec_thread && dv < p.D && t0 + vt[i] < t_end)) continue;
+        if (!FAST && !(vec_thread && dv < p.D && t0 + vt[i] < t_end)) continue;
         float yo[VEC], uv[VEC], zv[VEC];
 #pragma unroll
         for (int j = 0; j < VEC; j += 4) {
@@ -263,12 +280,12 @@ __global__ void __launch_bounds__(32 * K, min_blocks(K, NS))
         }
         const int off = swz<ROWB>(vc[i], vt[i] / VEC);
         unpack16(*reinterpret_cast<const uint4*>(ring + S::kU + off), uv);
-        if (p.has_z) unpack16(*reinterpret_cast<const uint4*>(ring + S::kZ + off), zv);
+        if (gate) unpack16(*reinterpret_cast<const uint4*>(ring + S::kZ + off), zv);
         const float2 D2 = make_float2(vD[i], vD[i]);
 #pragma unroll
         for (int j = 0; j < VEC; j += 2) {
           float2 o = __ffma2_rn(D2, make_float2(uv[j], uv[j + 1]), make_float2(yo[j], yo[j + 1]));
-          if (p.has_z) o = __fmul2_rn(o, silu2<PRECISE>(make_float2(zv[j], zv[j + 1])));
+          if (gate) o = __fmul2_rn(o, silu2<PRECISE>(make_float2(zv[j], zv[j + 1])));
           yo[j] = o.x;
           yo[j + 1] = o.y;
         }
@@ -283,9 +300,11 @@ __global__ void __launch_bounds__(32 * K, min_blocks(K, NS))
   // overlap:  A(0) | B(0) | C(0) A(1) | B(1) | C(1) A(2) | ...
   // Ring slot k % 2 is free after the phase that holds C(k); the TMA loads of
   // tile k+2 go into it, and the TMA store of tile k's staging box goes out.
+  // every tile but a ragged last one takes the branch-free stage A / C forms
+  const bool cta_fast = p.softplus && N == NP && d0 + CH <= p.D;
   float dsum = 0.f;
   bool ok = ntiles > 0 ? mbar_wait(bar_base, 0) : true;
-  if (ok && ntiles > 0) stage_a(0);
+  if (ok && ntiles > 0) stage_a(0, Bool<false>{});
   if (!ok) record_status(p.status, SSM_ERR_TIMEOUT);
   if (__syncthreads_or(!ok)) return;   // nothing else is in flight
   if (tid == 0 && ntiles > 1) issue(1);
@@ -336,8 +355,18 @@ __global__ void __launch_bounds__(32 * K, min_blocks(K, NS))
 
     const bool next = k + 1 < ntiles;
     ok = next ? mbar_wait(bar_base + 8 * ((k + 1) % kStages), (uint32_t)((k + 1) / kStages) & 1u) : true;
-    if (MODE == MODE_OUTPUT) stage_c(k);
-    if (ok && next) stage_a(k + 1);
+    if (cta_fast && ok && next && t_begin + (int64_t)(k + 2) * T <= t_end) {
+      if (MODE == MODE_OUTPUT && p.has_z) {
+        stage_c(k, Bool<true>{}, Bool<true>{});
+        stage_a(k + 1, Bool<true>{});
+      } else {
+        stage_c(k, Bool<true>{}, Bool<false>{});
+        stage_a(k + 1, Bool<true>{});
+      }
+    } else {
+      stage_c(k, Bool<false>{}, Bool<false>{});
+      if (ok && next) stage_a(k + 1, Bool<false>{});
+    }
     if (!ok) record_status(p.status, SSM_ERR_TIMEOUT);
     if (__syncthreads_or(!ok)) {   // tile k+1's copy never completed; only tile k's store may be in flight
       if (MODE == MODE_OUTPUT && tid == 0) bulk_wait<0>();
