@@ -71,6 +71,8 @@ def _bind(lib):
     lib.oracle_state_update.restype = ctypes.c_int
     lib.oracle_state_update.argtypes = [i64, i64, i64, dp] + [dp] * 8 + [
         ctypes.c_int, ctypes.c_int, dp]
+    lib.oracle_causal_conv1d.restype = ctypes.c_int
+    lib.oracle_causal_conv1d.argtypes = [i64, i64, i64, i64] + [dp] * 4 + [ctypes.c_int, dp]
     lib.oracle_default_threads.restype = ctypes.c_int
     lib.oracle_default_threads.argtypes = []
     return lib
@@ -151,3 +153,25 @@ def state_update(state, u, delta, A, Bm, Cm, Dskip=None, z=None, delta_bias=None
     if rc != 0:
         raise RuntimeError("oracle_state_update failed")
     return st, y
+
+
+def causal_conv1d(x, w, bias=None, x_hist=None, silu=True, lib=None):
+    """fp64 causal depthwise convolution along time, then SiLU if ``silu``.
+
+    x: (B, D, L); w: (D, W), tap W-1 on the current step; bias: (D,);
+    x_hist: (B, D, W-1), the inputs before t = 0 (oldest first), zero if None.
+    Returns out (B, D, L) float64.
+    """
+    lib = lib or load()
+    x = _f64(x)
+    Bsz, D, L = x.shape
+    w = _f64(w)
+    W = w.shape[1]
+    bias = _f64(bias, (D,))
+    x_hist = _f64(x_hist, (Bsz, D, W - 1)) if W > 1 else None
+    out = np.empty((Bsz, D, L), dtype=np.float64)
+    rc = lib.oracle_causal_conv1d(Bsz, D, L, W, _ptr(x), _ptr(w), _ptr(bias), _ptr(x_hist),
+                                  int(bool(silu)), _ptr(out))
+    if rc != 0:
+        raise RuntimeError("oracle_causal_conv1d failed")
+    return out

@@ -21,7 +21,10 @@
  *     ("docs.ifdog.com", sections "Continuous state space model" and
  *     "Discretisation"; "gitcode", section 2, recurrent mode);
  *   - optional gate y_t *= silu(z_t) = z_t * sigmoid(z_t) ("docs.ifdog.com",
- *     section "Mamba architecture", steps 4-5).
+ *     section "Mamba architecture", steps 4-5);
+ *   - the causal depthwise convolution (with optional SiLU) that feeds the
+ *     SSM branch ("docs.ifdog.com", section "Mamba architecture", step 3a),
+ *     as a separate function.
  * The hardware-aware scan of "gitcode" section 3.3.2 is an exact reordering
  * of this recurrence, so the oracle is the sequential definition itself.  A
  * second evaluation order (work-efficient tree scan of the associative
@@ -292,6 +295,47 @@ int oracle_state_update(int64_t B, int64_t D, int64_t N, double *state,
             double v = acc + (Dskip ? Dskip[d] : 0.0) * u[c];
             if (z) v *= z[c] * sigmoid(z[c]);
             y[c] = v;
+        }
+    }
+    return 0;
+}
+
+/*
+ * Causal depthwise 1-D convolution along time, optionally followed by SiLU:
+ * the step in front of the selective SSM ("docs.ifdog.com", section "Mamba
+ * architecture", step 3a: every channel is convolved on its own, with a
+ * kernel of d_conv taps, typically 4, so that each position sees itself and
+ * the d_conv - 1 positions before it; step 3b: that output enters the SSM).
+ *
+ *   out[b,d,t] = act(bias[d] + sum_{k=0}^{W-1} w[d,k] * x[b,d,t-(W-1)+k])
+ *
+ * Tap k = W-1 multiplies the current step (the order of a framework Conv1d
+ * with W-1 steps of left padding, cut to the first L outputs).  Inputs before
+ * t = 0 are x_hist[b,d,0..W-2] (oldest first) when given, else zero.
+ * act is SiLU, v * sigmoid(v) ("docs.ifdog.com", same section, step 4), or
+ * the identity.
+ *   x, out : (B, D, L)   w : (D, W)   bias : (D) nullable
+ *   x_hist : (B, D, W-1) nullable
+ */
+int oracle_causal_conv1d(int64_t B, int64_t D, int64_t L, int64_t W, const double *x,
+                         const double *w, const double *bias, const double *x_hist,
+                         int use_silu, double *out) {
+    if (B < 0 || D < 0 || L < 0 || W < 1) return -1;
+    if (B * D * L > 0 && (!x || !w || !out)) return -1;
+    for (int64_t b = 0; b < B; ++b) {
+        for (int64_t d = 0; d < D; ++d) {
+            const int64_t row = b * D + d;
+            for (int64_t t = 0; t < L; ++t) {
+                double v = bias ? bias[d] : 0.0;
+                for (int64_t k = 0; k < W; ++k) {
+                    const int64_t src = t - (W - 1) + k;   /* the input step tap k reads */
+                    double xv;
+                    if (src >= 0) xv = x[row * L + src];
+                    else xv = x_hist ? x_hist[row * (W - 1) + (W - 1) + src] : 0.0;
+                    v += w[d * W + k] * xv;
+                }
+                out[row * L + t] = use_silu ? v * sigmoid(v) : v;
+            }
         }
     }
     return 0;

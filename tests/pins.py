@@ -307,7 +307,91 @@ def pin_zoh_to_euler_small_delta(lib):
     _close(yz, ye, rtol=1e-10, atol=1e-14, what="zoh -> euler")
 
 
-ALL_PINS = [
+# ---------------------------------------------------------------------------
+# The causal depthwise convolution in front of the SSM branch ("Mamba and state
+# space models", docs.ifdog.com, section "Mamba architecture", step 3a).
+# ---------------------------------------------------------------------------
+
+def pin_conv_golden(lib):
+    """Hand-worked outputs of a 4-tap convolution, with and without history."""
+    g = _read_golden("hand_conv_w4_l5.txt")
+    x = g["x"].reshape(1, 1, -1)
+    w = g["w"].reshape(1, -1)
+    bias = g["bias"]
+    out = oracle.causal_conv1d(x, w, bias, silu=False, lib=lib)
+    _close(out.ravel(), g["out"], what="conv without history")
+    out = oracle.causal_conv1d(x, w, bias, x_hist=g["hist"].reshape(1, 1, -1), silu=False, lib=lib)
+    _close(out.ravel(), g["out_hist"], what="conv with history")
+
+
+def pin_conv_unit_taps_shift(lib):
+    """A kernel with one tap j set to 1 is a causal delay by W-1-j steps (zeros shifted in)."""
+    rng = np.random.default_rng(11)
+    W, L = 4, 23
+    x = rng.standard_normal((2, 3, L))
+    for j in range(W):
+        w = np.zeros((3, W))
+        w[:, j] = 1.0
+        out = oracle.causal_conv1d(x, w, silu=False, lib=lib)
+        lag = W - 1 - j
+        want = np.zeros_like(x)
+        want[..., lag:] = x[..., :L - lag]
+        assert np.array_equal(out, want), f"tap {j} is not a delay of {lag}"
+
+
+def pin_conv_matches_numpy_convolve(lib):
+    """Against numpy's full linear convolution cut to the first L samples (kernel reversed,
+    since the taps are in cross-correlation order), then SiLU v * sigmoid(v) in closed form."""
+    rng = np.random.default_rng(12)
+    Bsz, D, L, W = 2, 5, 37, 4
+    x = rng.standard_normal((Bsz, D, L))
+    w = rng.standard_normal((D, W))
+    bias = rng.standard_normal(D)
+    lin = np.empty_like(x)
+    for b in range(Bsz):
+        for d in range(D):
+            lin[b, d] = np.convolve(x[b, d], w[d, ::-1])[:L] + bias[d]
+    _close(oracle.causal_conv1d(x, w, bias, silu=False, lib=lib), lin, what="linear conv")
+    _close(oracle.causal_conv1d(x, w, bias, silu=True, lib=lib), lin * _sigmoid(lin), what="conv + silu")
+
+
+def pin_conv_silu_values(lib):
+    """One tap of weight 1: out = silu(x); silu(0) = 0, silu(ln 3) = (3/4) ln 3 and
+    silu(-ln 3) = -(1/4) ln 3, since sigmoid(ln 3) = 3/4."""
+    ln3 = math.log(3.0)
+    x = np.array([0.0, ln3, -ln3]).reshape(1, 1, 3)
+    out = oracle.causal_conv1d(x, np.ones((1, 1)), silu=True, lib=lib).ravel()
+    _close(out, np.array([0.0, 0.75 * ln3, -0.25 * ln3]), what="silu values")
+
+
+def pin_conv_history_continuation(lib):
+    """Convolving [x1, x2] in one call equals convolving x2 with the last W-1 inputs of x1 as
+    its history (a sequence split at any step)."""
+    rng = np.random.default_rng(13)
+    W = 4
+    x = rng.standard_normal((1, 3, 30))
+    w = rng.standard_normal((3, W))
+    bias = rng.standard_normal(3)
+    whole = oracle.causal_conv1d(x, w, bias, lib=lib)
+    for cut in (1, 2, 3, 17):
+        head = oracle.causal_conv1d(x[..., :cut], w, bias, lib=lib)
+        hist = np.zeros((1, 3, W - 1))
+        k = min(cut, W - 1)
+        hist[..., W - 1 - k:] = x[..., cut - k:cut]
+        tail = oracle.causal_conv1d(x[..., cut:], w, bias, x_hist=hist, lib=lib)
+        _close(np.concatenate([head, tail], axis=-1), whole, what=f"split at {cut}")
+
+
+CONV_PINS = [
+    pin_conv_golden,
+    pin_conv_unit_taps_shift,
+    pin_conv_matches_numpy_convolve,
+    pin_conv_silu_values,
+    pin_conv_history_continuation,
+]
+
+
+ALL_PINS = CONV_PINS + [
     pin_golden_recurrence, pin_golden_gated, pin_lti_equals_convolution, pin_theorem1_gated_rnn,
     pin_unrolled_sum, pin_single_step_closed_form, pin_tree_order_matches_sequential,
     pin_boundary_reset, pin_ignore_window, pin_chunk_invariance, pin_step_matches_scan,

@@ -48,6 +48,12 @@ MUTANTS = [
     ("xb[r] = la * pb + lb;", "xb[r] = pa * lb + pb;"),
     ("eb[t] = a[t] * xb[t] + b[t];", "eb[t] = xb[t] + b[t];"),
     ("acc += Cb[n * L + t] * hs[t * N + n];", "acc += Cb[n * L + t] * hs[n];"),
+    # the causal convolution
+    ("const int64_t src = t - (W - 1) + k;", "const int64_t src = t - W + k;"),
+    ("v += w[d * W + k] * xv;", "v += w[d * W + (W - 1 - k)] * xv;"),
+    ("double v = bias ? bias[d] : 0.0;\n                for", "double v = 0.0;\n                for"),
+    ("x_hist[row * (W - 1) + (W - 1) + src]", "x_hist[row * (W - 1) - src - 1]"),
+    ("out[row * L + t] = use_silu ? v * sigmoid(v) : v;", "out[row * L + t] = use_silu ? sigmoid(v) : v;"),
 ]
 
 
