@@ -57,7 +57,7 @@ def parse():
     ap.add_argument("--no-rows", action="store_true", help="skip the other workloads' timing rows")
     ap.add_argument("--only-rows", action="store_true",
                     help="time only the other workloads' rows (one line of JSON; for profiling their kernels)")
-    ap.add_argument("--rows", default="all", help="comma-separated subset of rows: m130, ti, long, decode")
+    ap.add_argument("--rows", default="all", help="comma-separated subset of rows: m130, ti, long, decode, conv")
     ap.add_argument("--decode-steps", type=int, default=1000, help="decode steps of the decode row")
     return ap.parse_args()
 
@@ -283,7 +283,8 @@ def decode_bytes(cfg) -> int:
 
 
 ROW_KEYS = {"m130": "mamba130m_bf16_b8_d1536_l2048_n16", "ti": "mamba2.8b_ti_bf16_b1_d5120_l2048_n16",
-            "long": "long_bf16_b1_d1536_l1048576_n16", "decode": "decode_bf16_b256_d5120_n16_x1000"}
+            "long": "long_bf16_b1_d1536_l1048576_n16", "decode": "decode_bf16_b256_d5120_n16_x1000",
+            "conv": "conv1d_silu_bf16_b4_d5120_l2048_w4"}
 
 
 def other_rows(lib, ssm, peak, stream, dev, which="all", decode_steps=1000):
@@ -332,6 +333,35 @@ def other_rows(lib, ssm, peak, stream, dev, which="all", decode_steps=1000):
                       "hbm_gbs_algorithmic": gbs, "frac": gbs / peak, "algorithmic_bytes": algo,
                       "l2": "flushed between launches" if algo < (256 << 20) else "inputs larger than L2"}
         del inp, y, ws
+        torch.cuda.empty_cache()
+
+    if "conv" in sel:
+        # the causal depthwise convolution + SiLU in front of the scan, on the 2.8B-shaped layer
+        name = ROW_KEYS["conv"]
+        Bsz, D, L, W = 4, 5120, 2048, 4
+        g = torch.Generator(device=dev)
+        g.manual_seed(3000)
+        x = torch.randn(Bsz, D, L, generator=g, device=dev).to(torch.bfloat16)
+        bound = 1.0 / W ** 0.5
+        wt = (torch.rand(D, W, generator=g, device=dev) * 2 - 1) * bound
+        cb = (torch.rand(D, generator=g, device=dev) * 2 - 1) * bound
+        xo = torch.empty_like(x)
+        ca = ssm.make_conv_args(x, wt, xo, cb, None, True)
+
+        def crun():
+            rc = lib.ssm_causal_conv1d_fwd(ctypes.byref(ca), sh)
+            if rc != 0:
+                raise RuntimeError(ssm.status_name(rc))
+
+        for _ in range(3):
+            crun()
+        ms = time_launches(crun, 200, stream, flush)
+        byt = 2 * x.numel() * x.element_size() + wt.numel() * 4 + cb.numel() * 4
+        gbs = byt / (ms * 1e-3) / 1e9
+        rows[name] = {"ms": ms, "value": x.numel() / (ms * 1e-3), "unit": "outputs/s", "launches": 1,
+                      "hbm_gbs_algorithmic": gbs, "frac": gbs / peak, "algorithmic_bytes": byt,
+                      "l2": "flushed between launches"}
+        del x, xo, wt, cb
         torch.cuda.empty_cache()
 
     if "decode" not in sel:

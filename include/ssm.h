@@ -1,7 +1,7 @@
 /*
  * ssm.h -- C ABI of the B300 selective state space (S6) library (libssm.so).
  *
- * Two operations, both defined by the Mamba paper (arXiv 2312.00752) as
+ * Three operations, all from the Mamba paper (arXiv 2312.00752) as
  * restated on the pages this library follows:
  *
  *   ssm_scan_fwd      the selective-scan forward pass.  For every batch b,
@@ -23,6 +23,12 @@
  *   ssm_state_update  one recurrent (decode) step of the same recurrence
  *                     against a persistent fp32 state ("gitcode", section 1
  *                     and section 2: constant time per generated token).
+ *   ssm_causal_conv1d_fwd
+ *                     the causal depthwise convolution along time, with an
+ *                     optional SiLU, that produces the SSM branch's input
+ *                     ("docs.ifdog.com", section "Mamba architecture", step
+ *                     3a; step 3b feeds its output to the projections that
+ *                     make Delta, B and C and to the scan as u).
  *
  * Conventions for every entry point
  *   - All tensor pointers are DEVICE pointers unless stated otherwise; the
@@ -125,6 +131,41 @@ typedef struct ssm_step_args {
     int64_t stride_A[2];                       /* (d, n) */
 } ssm_step_args_t;
 
+/*
+ * Arguments of ssm_causal_conv1d_fwd.  Per batch b, channel d and step t:
+ *   out[b,d,t] = act(bias[d] + sum_{k=0}^{width-1} weight[d,k] * x[b,d,t-(width-1)+k])
+ * Tap width-1 multiplies the current step (the tap order of a framework
+ * Conv1d with width-1 steps of left padding).  Inputs before t = 0 are
+ * x_hist[b,d,0..width-2], oldest first, or zero when x_hist is NULL, so a
+ * sequence split at any step continues exactly when the next call gets the
+ * last width-1 inputs of the previous one.  act is SiLU, v * sigmoid(v), when
+ * silu != 0, else the identity.
+ *   x, out  : (batch, dim, seqlen)   io_dtype, time stride 1
+ *   weight  : (dim, width)           fp32
+ *   bias    : (dim,)                 fp32, contiguous, nullable (no bias)
+ *   x_hist  : (batch, dim, width-1)  io_dtype, nullable
+ * Limits: 1 <= width <= 16; batch, dim, seqlen >= 0 (empty is a no-op).
+ * out must not overlap x, weight, bias or x_hist.  Arithmetic is fp32; a
+ * bf16 out is rounded to nearest even.
+ */
+typedef struct ssm_conv_args {
+    int64_t batch, dim, seqlen;                /* B, D, L */
+    int32_t width;                             /* taps, W */
+    ssm_dtype_t io_dtype;                      /* x, x_hist, out */
+    int32_t silu;                              /* 1: SiLU after the bias */
+    int32_t reserved0;
+    const void *x;
+    const float *weight, *bias;
+    const void *x_hist;
+    void *out;
+    int64_t stride_x[3], stride_out[3];        /* (b, d, t) */
+    int64_t stride_weight[2];                  /* (d, k) */
+    int64_t stride_x_hist[3];                  /* (b, d, k) */
+} ssm_conv_args_t;
+
+/* Causal depthwise convolution (+ SiLU) along time (see ssm_conv_args_t). */
+ssm_status_t ssm_causal_conv1d_fwd(const ssm_conv_args_t *args, void *stream);
+
 /* Bytes of device workspace ssm_scan_fwd needs for these arguments (0 for
  * the single-pass paths).  Host-only; validates the arguments first.  The
  * plan it reflects depends on the current device's SM count. */
@@ -188,7 +229,7 @@ int ssm_version(void);
 
 /* sizeof of the argument structs as compiled into the library, so that a
  * binding can check its mirror of them: which = 0 -> ssm_scan_args_t,
- * 1 -> ssm_step_args_t; 0 for any other value. */
+ * 1 -> ssm_step_args_t, 2 -> ssm_conv_args_t; 0 for any other value. */
 size_t ssm_abi_sizeof(int which);
 
 #ifdef __cplusplus

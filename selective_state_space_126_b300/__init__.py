@@ -9,6 +9,7 @@ device is present, the calls raise.
 Public API (same names as the C entry points):
   ssm_scan_fwd(u, delta, A, Bm, Cm, Dskip=None, z=None, delta_bias=None, h0=None, ...)
   ssm_state_update(state, u, delta, A, Bm, Cm, Dskip=None, z=None, delta_bias=None, ...)
+  ssm_causal_conv1d_fwd(x, weight, bias=None, x_hist=None, silu=True, ...)
   ssm_scan_workspace_size(...), ssm_status_string(code), ssm_version()
 """
 from __future__ import annotations
@@ -28,7 +29,7 @@ PATH_NAMES = {0: "generic", 1: "tiled", 2: "chunked"}
 # every symbol include/ssm.h declares
 EXPORTED_SYMBOLS = ["ssm_scan_workspace_size", "ssm_scan_fwd", "ssm_state_update", "ssm_status_string",
                     "ssm_last_error_detail", "ssm_get_device_status", "ssm_scan_plan_path", "ssm_version",
-                    "ssm_abi_sizeof", "ssm_scan_fwd_noalloc"]
+                    "ssm_abi_sizeof", "ssm_scan_fwd_noalloc", "ssm_causal_conv1d_fwd"]
 
 _i64 = ctypes.c_int64
 _vp = ctypes.c_void_p
@@ -59,6 +60,18 @@ class StepArgs(ctypes.Structure):
         ("stride_state", _i64 * 3), ("stride_u", _i64 * 2), ("stride_delta", _i64 * 2),
         ("stride_z", _i64 * 2), ("stride_y", _i64 * 2), ("stride_B", _i64 * 2), ("stride_C", _i64 * 2),
         ("stride_A", _i64 * 2),
+    ]
+
+
+class ConvArgs(ctypes.Structure):
+    """Mirror of ssm_conv_args_t."""
+    _fields_ = [
+        ("batch", _i64), ("dim", _i64), ("seqlen", _i64),
+        ("width", ctypes.c_int32), ("io_dtype", ctypes.c_int), ("silu", ctypes.c_int32),
+        ("reserved0", ctypes.c_int32),
+        ("x", _vp), ("weight", _vp), ("bias", _vp), ("x_hist", _vp), ("out", _vp),
+        ("stride_x", _i64 * 3), ("stride_out", _i64 * 3), ("stride_weight", _i64 * 2),
+        ("stride_x_hist", _i64 * 3),
     ]
 
 
@@ -101,7 +114,10 @@ def load_library(path: str = LIB_PATH):
         lib.ssm_scan_fwd_noalloc.restype = ctypes.c_int
         lib.ssm_abi_sizeof.argtypes = [ctypes.c_int]
         lib.ssm_abi_sizeof.restype = ctypes.c_size_t
-        if lib.ssm_abi_sizeof(0) != ctypes.sizeof(ScanArgs) or lib.ssm_abi_sizeof(1) != ctypes.sizeof(StepArgs):
+        lib.ssm_causal_conv1d_fwd.argtypes = [ctypes.POINTER(ConvArgs), _vp]
+        lib.ssm_causal_conv1d_fwd.restype = ctypes.c_int
+        if (lib.ssm_abi_sizeof(0) != ctypes.sizeof(ScanArgs) or lib.ssm_abi_sizeof(1) != ctypes.sizeof(StepArgs)
+                or lib.ssm_abi_sizeof(2) != ctypes.sizeof(ConvArgs)):
             raise ImportError("libssm.so argument structs do not match this binding")
         if path == LIB_PATH:
             _lib = lib
@@ -289,6 +305,44 @@ def ssm_state_update(state, u, delta, A, Bm, Cm, Dskip=None, z=None, delta_bias=
     args = make_step_args(state, u, delta, A, Bm, Cm, y, Dskip, z, delta_bias, delta_softplus)
     _check(lib.ssm_state_update(ctypes.byref(args), _vp(_stream_handle(stream))))
     return y
+
+
+def make_conv_args(x, weight, out, bias=None, x_hist=None, silu=True) -> ConvArgs:
+    """Fill an ssm_conv_args_t from torch tensors (no copies, strides passed through)."""
+    Bsz, D, L = x.shape
+    a = ConvArgs()
+    a.batch, a.dim, a.seqlen, a.width = Bsz, D, L, weight.shape[1]
+    a.io_dtype = _io_dtype(x)
+    a.silu = 1 if silu else 0
+    a.x, a.weight, a.bias, a.x_hist, a.out = _ptr(x), _ptr(weight), _ptr(bias), _ptr(x_hist), _ptr(out)
+    a.stride_x[:] = _strides(x, 3)
+    a.stride_out[:] = _strides(out, 3)
+    a.stride_weight[:] = _strides(weight, 2)
+    a.stride_x_hist[:] = _strides(x_hist, 3)
+    return a
+
+
+def ssm_causal_conv1d_fwd(x, weight, bias=None, x_hist=None, silu=True, out=None, stream=None):
+    """Causal depthwise convolution along time, then SiLU if ``silu``.
+
+    x: (B, D, L) float32 or bfloat16; weight: (D, W) fp32, tap W-1 on the current step;
+    bias: (D,) fp32; x_hist: (B, D, W-1) in x's dtype, the inputs before t = 0 (zero if None).
+    Returns out (B, D, L) in x's dtype.
+    """
+    torch = _torch()
+    lib = load_library()
+    if not x.is_cuda:
+        raise ValueError("x must be a CUDA tensor")
+    _f32(weight, "weight"); _f32(bias, "bias")
+    if bias is not None:
+        bias = bias.contiguous()
+    if x_hist is not None and x_hist.dtype != x.dtype:
+        raise TypeError("x_hist must have x's dtype")
+    if out is None:
+        out = torch.empty(x.shape, dtype=x.dtype, device=x.device)
+    args = make_conv_args(x, weight, out, bias, x_hist, silu)
+    _check(lib.ssm_causal_conv1d_fwd(ctypes.byref(args), _vp(_stream_handle(stream))))
+    return out
 
 
 def ssm_get_device_status(clear=True, stream=None) -> int:

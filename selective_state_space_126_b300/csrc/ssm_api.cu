@@ -298,11 +298,12 @@ using namespace ssm;
 
 extern "C" {
 
-int ssm_version(void) { return (1 << 16) | 0; }
+int ssm_version(void) { return (1 << 16) | 1; }
 
 size_t ssm_abi_sizeof(int which) {
   if (which == 0) return sizeof(ssm_scan_args_t);
   if (which == 1) return sizeof(ssm_step_args_t);
+  if (which == 2) return sizeof(ssm_conv_args_t);
   return 0;
 }
 
@@ -430,6 +431,57 @@ ssm_status_t ssm_state_update(const ssm_step_args_t* a, void* stream) {
       return fail(SSM_ERR_INVALID_ARG, "an output overlaps an input");
   }
   cudaError_t e = launch_state_update(p, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e);
+  return ok();
+}
+
+ssm_status_t ssm_causal_conv1d_fwd(const ssm_conv_args_t* a, void* stream) {
+  if (!a) return fail(SSM_ERR_INVALID_ARG, "args is NULL");
+  if (a->io_dtype != SSM_F32 && a->io_dtype != SSM_BF16) return fail(SSM_ERR_INVALID_ARG, "io_dtype");
+  if (a->batch < 0 || a->dim < 0 || a->seqlen < 0) return fail(SSM_ERR_INVALID_ARG, "negative size");
+  if (a->width < 1 || a->width > 16) return fail(SSM_ERR_UNSUPPORTED, "width outside [1, 16]");
+  ConvProblem p;
+  std::memset(&p, 0, sizeof(p));
+  p.B = a->batch; p.D = a->dim; p.L = a->seqlen; p.W = a->width; p.io = a->io_dtype; p.silu = a->silu != 0;
+  p.x = a->x; p.w = a->weight; p.bias = a->bias; p.x_hist = a->x_hist; p.out = a->out;
+  std::memcpy(p.sx, a->stride_x, sizeof(p.sx));
+  std::memcpy(p.so, a->stride_out, sizeof(p.so));
+  std::memcpy(p.sw, a->stride_weight, sizeof(p.sw));
+  std::memcpy(p.sxh, a->stride_x_hist, sizeof(p.sxh));
+  if (p.B == 0 || p.D == 0 || p.L == 0) return ok();
+  if (!p.x || !p.w || !p.out) return fail(SSM_ERR_INVALID_ARG, "required pointer is NULL");
+  for (int i = 0; i < 3; ++i)
+    if (p.sx[i] < 0 || p.so[i] < 0 || p.sxh[i] < 0) return fail(SSM_ERR_INVALID_ARG, "negative stride");
+  if (p.sw[0] < 0 || p.sw[1] < 0) return fail(SSM_ERR_INVALID_ARG, "negative stride");
+  if (p.sx[2] != 1 || p.so[2] != 1) return fail(SSM_ERR_UNSUPPORTED, "time stride must be 1");
+  const int es = elem_size(p.io);
+  if (!aligned(p.x, es) || !aligned(p.out, es) || (p.x_hist && !aligned(p.x_hist, es)))
+    return fail(SSM_ERR_INVALID_ARG, "misaligned pointer");
+  if (!aligned(p.w, 4) || (p.bias && !aligned(p.bias, 4))) return fail(SSM_ERR_INVALID_ARG, "misaligned fp32 pointer");
+  int64_t eo[3] = {p.B, p.D, p.L};
+  if (!injective(3, eo, p.so)) return fail(SSM_ERR_INVALID_ARG, "out strides overlap");
+  uintptr_t o0, o1;
+  tensor_range(p.out, 3, eo, p.so, es, &o0, &o1);
+  struct In {
+    const void* ptr;
+    int rank;
+    int64_t ext[3];
+    const int64_t* str;
+    int es;
+  } ins[] = {{p.x, 3, {p.B, p.D, p.L}, p.sx, es},
+             {p.w, 2, {p.D, p.W, 1}, p.sw, 4},
+             {p.x_hist, 3, {p.B, p.D, p.W - 1}, p.sxh, es}};
+  for (const In& in : ins) {
+    if (!in.ptr || in.ext[in.rank - 1] == 0) continue;
+    uintptr_t i0, i1;
+    tensor_range(in.ptr, in.rank, in.ext, in.str, in.es, &i0, &i1);
+    if (overlaps(o0, o1, i0, i1)) return fail(SSM_ERR_INVALID_ARG, "out overlaps an input");
+  }
+  if (p.bias) {
+    uintptr_t i0 = reinterpret_cast<uintptr_t>(p.bias), i1 = i0 + (uintptr_t)p.D * 4;
+    if (overlaps(o0, o1, i0, i1)) return fail(SSM_ERR_INVALID_ARG, "out overlaps an input");
+  }
+  cudaError_t e = launch_causal_conv1d(p, device_sm_count(), static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e);
   return ok();
 }

@@ -33,6 +33,18 @@ struct StepProblem {
   int64_t sst[3], su[2], sd[2], sz[2], sy[2], sB[2], sC[2], sA[2];
 };
 
+struct ConvProblem {
+  int64_t B, D, L;
+  int W;
+  ssm_dtype_t io;
+  bool silu;
+  const void* x;
+  const float *w, *bias;
+  const void* x_hist;
+  void* out;
+  int64_t sx[3], so[3], sw[2], sxh[3];
+};
+
 enum ScanPath { kPathGeneric = 0, kPathTiled = 1, kPathChunked = 2 };
 
 // Tiled-kernel shape: K threads share one channel's states, NS states per thread.
@@ -57,6 +69,7 @@ int* device_status_ptr();
 cudaError_t launch_scan_generic(const ScanProblem& p, cudaStream_t s);
 cudaError_t launch_scan_tiled(const ScanProblem& p, const ScanPlan& plan, void* workspace, cudaStream_t s);
 cudaError_t launch_state_update(const StepProblem& p, cudaStream_t s);
+cudaError_t launch_causal_conv1d(const ConvProblem& p, int sms, cudaStream_t s);
 
 // tile length of the tiled kernel (timesteps)
 #ifndef SSM_TILE_T

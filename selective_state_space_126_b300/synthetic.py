@@ -11,7 +11,10 @@ Recipe (the distributions of the Mamba layer workloads):
   * A[d, n] = -(n + 1) (S4D-Real initialisation, same page, section 3.6
     "Initialization");
   * tensors whose I/O dtype is bf16 are rounded once, round-to-nearest-even,
-    and both sides consume exactly those values.
+    and both sides consume exactly those values;
+  * the causal convolution in front of the scan: input x ~ N(0, 1) (a stream
+    of its own), taps and bias ~ U(-1/sqrt(W), 1/sqrt(W)), the default
+    initialisation of a framework's depthwise Conv1d (fan-in W).
 
 Every row of every tensor has its own PCG64 stream, keyed by
 (seed, tensor id, batch index, row index[, step]).  Any channel can therefore
@@ -25,7 +28,7 @@ from dataclasses import dataclass, replace
 import numpy as np
 
 # tensor ids of the per-row streams
-T_U, T_DELTA, T_Z, T_B, T_C, T_D, T_DT0, T_STATE = range(8)
+T_U, T_DELTA, T_Z, T_B, T_C, T_D, T_DT0, T_STATE, T_X, T_CONVW, T_CONVB = range(11)
 
 
 @dataclass(frozen=True)
@@ -158,6 +161,14 @@ def layer_params(dim: int, dstate: int, dt_min: float, dt_max: float, seed: int 
     dt0 = np.exp(_rng(seed, T_DT0).uniform(lo, hi, dim))
     delta_bias = softplus_inverse(dt0).astype(np.float32)
     return A, Dskip, delta_bias
+
+
+def conv_params(dim: int, width: int, seed: int = 0):
+    """Conv taps (D, W) and bias (D,) as float32, uniform in +-1/sqrt(W)."""
+    bound = 1.0 / np.sqrt(width)
+    w = _rng(seed, T_CONVW).uniform(-bound, bound, (dim, width)).astype(np.float32)
+    bias = _rng(seed, T_CONVB).uniform(-bound, bound, dim).astype(np.float32)
+    return w, bias
 
 
 def scan_inputs(cfg: ScanConfig, seed: int = 0, batches=None) -> dict:

@@ -22,7 +22,7 @@ FAKE = {k: 0x10_0000_0000 + i * 0x1_0000_0000 for i, k in enumerate(
 def header_functions():
     text = open(HEADER).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(ssm_[a-z_]+)\s*\(", text)))
+    return sorted(set(re.findall(r"\b(ssm_[a-z0-9_]+)\s*\(", text)))
 
 
 def scan_args(B=2, D=64, L=256, N=16, io=ssm.SSM_BF16, **over):
@@ -66,6 +66,7 @@ def test_every_header_symbol_is_exported(lib):
 def test_struct_sizes_match(lib):
     assert lib.ssm_abi_sizeof(0) == ctypes.sizeof(ssm.ScanArgs)
     assert lib.ssm_abi_sizeof(1) == ctypes.sizeof(ssm.StepArgs)
+    assert lib.ssm_abi_sizeof(2) == ctypes.sizeof(ssm.ConvArgs)
     assert lib.ssm_abi_sizeof(7) == 0
     assert ssm.ssm_version() >> 16 == 1
 
@@ -195,3 +196,50 @@ def test_workspace_size_formula(lib):
     chunk = 1024                       # rounded up to the 32-step tile
     nchunks = -(-4096 // chunk)
     assert ws == 2 * 64 * nchunks * (16 + 1) * 4
+
+
+def conv_args(B=2, D=64, L=256, W=4, io=ssm.SSM_BF16, **over):
+    a = ssm.ConvArgs()
+    a.batch, a.dim, a.seqlen, a.width = B, D, L, W
+    a.io_dtype = io
+    a.silu = 1
+    a.x, a.weight, a.bias, a.out = FAKE["u"], FAKE["A"], FAKE["bias"], FAKE["y"]
+    a.stride_x[:] = [D * L, L, 1]
+    a.stride_out[:] = [D * L, L, 1]
+    a.stride_weight[:] = [W, 1]
+    for k, v in over.items():
+        if isinstance(v, list):
+            getattr(a, k)[:] = v
+        else:
+            setattr(a, k, v)
+    return a
+
+
+def call_conv(a):
+    return ssm.load_library().ssm_causal_conv1d_fwd(ctypes.byref(a), None)
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(x=None), ssm.SSM_ERR_INVALID_ARG),
+    (dict(weight=None), ssm.SSM_ERR_INVALID_ARG),
+    (dict(out=None), ssm.SSM_ERR_INVALID_ARG),
+    (dict(width=0), ssm.SSM_ERR_UNSUPPORTED),
+    (dict(width=17), ssm.SSM_ERR_UNSUPPORTED),
+    (dict(io_dtype=7), ssm.SSM_ERR_INVALID_ARG),
+    (dict(seqlen=-1), ssm.SSM_ERR_INVALID_ARG),
+    (dict(stride_x=[64 * 256, 256, 2]), ssm.SSM_ERR_UNSUPPORTED),
+    (dict(stride_out=[64 * 256, 256, 2]), ssm.SSM_ERR_UNSUPPORTED),
+    (dict(stride_out=[0, 256, 1]), ssm.SSM_ERR_INVALID_ARG),          # two batch rows on one output row
+    (dict(stride_weight=[-4, 1]), ssm.SSM_ERR_INVALID_ARG),
+    (dict(out=FAKE["u"] + 512), ssm.SSM_ERR_INVALID_ARG),              # out overlaps x
+    (dict(out=FAKE["A"]), ssm.SSM_ERR_INVALID_ARG),                    # out overlaps the weights
+    (dict(x=FAKE["u"] + 1), ssm.SSM_ERR_INVALID_ARG),                  # not element-aligned
+])
+def test_conv_validation(lib, over, code):
+    assert call_conv(conv_args(**over)) == code
+
+
+@pytest.mark.parametrize("over", [dict(batch=0), dict(dim=0), dict(seqlen=0),
+                                  dict(seqlen=0, x=None, weight=None, out=None)])
+def test_conv_empty_is_a_no_op(lib, over):
+    assert call_conv(conv_args(**over)) == ssm.SSM_OK
