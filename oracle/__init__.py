@@ -71,6 +71,8 @@ def _bind(lib):
     lib.oracle_state_update.restype = ctypes.c_int
     lib.oracle_state_update.argtypes = [i64, i64, i64, dp] + [dp] * 8 + [
         ctypes.c_int, ctypes.c_int, dp]
+    lib.oracle_selective_scan_bwd.restype = ctypes.c_int
+    lib.oracle_selective_scan_bwd.argtypes = [i64, i64, i64, i64] + [dp] * 9 + [ctypes.c_int] + [dp] * 11
     lib.oracle_causal_conv1d.restype = ctypes.c_int
     lib.oracle_causal_conv1d.argtypes = [i64, i64, i64, i64] + [dp] * 4 + [ctypes.c_int, dp]
     lib.oracle_default_threads.restype = ctypes.c_int
@@ -174,4 +176,47 @@ def causal_conv1d(x, w, bias=None, x_hist=None, silu=True, lib=None):
                                   int(bool(silu)), _ptr(out))
     if rc != 0:
         raise RuntimeError("oracle_causal_conv1d failed")
+    return out
+
+
+def selective_scan_bwd(u, delta, A, Bm, Cm, dy, Dskip=None, z=None, delta_bias=None, h0=None,
+                       delta_softplus=True, dh_last=None, lib=None):
+    """fp64 gradients of the (Euler) selective scan for an upstream gradient dy (B, D, L) of y and,
+    optionally, dh_last (B, D, N) of the final state.
+
+    Returns a dict with du, ddelta (B, D, L); dz (B, D, L) if z is given; dBm, dCm shaped like the
+    given Bm, Cm (a leading batch of 1 gets the sum over the batch); dA (D, N); dDskip (D,) if Dskip is
+    given; ddelta_bias (D,); dh0 (B, D, N).
+    """
+    lib = lib or load()
+    u = _f64(u)
+    Bsz, D, L = u.shape
+    A = _f64(A)
+    N = A.shape[1]
+    bc_shared = np.asarray(Bm).shape[0] == 1 and Bsz != 1
+    delta = _f64(delta, (Bsz, D, L))
+    z = _f64(z, (Bsz, D, L))
+    Bm = _f64(Bm, (Bsz, N, L))
+    Cm = _f64(Cm, (Bsz, N, L))
+    Dskip = _f64(Dskip, (D,))
+    delta_bias = _f64(delta_bias, (D,))
+    h0 = _f64(h0, (Bsz, D, N))
+    dy = _f64(dy, (Bsz, D, L))
+    dh_last = _f64(dh_last, (Bsz, D, N))
+    out = {k: np.empty(s, dtype=np.float64) for k, s in (
+        ("du", (Bsz, D, L)), ("ddelta", (Bsz, D, L)), ("dBm", (Bsz, N, L)), ("dCm", (Bsz, N, L)),
+        ("dA", (D, N)), ("ddelta_bias", (D,)), ("dh0", (Bsz, D, N)))}
+    out["dz"] = np.empty((Bsz, D, L)) if z is not None else None
+    out["dDskip"] = np.empty(D) if Dskip is not None else None
+    rc = lib.oracle_selective_scan_bwd(Bsz, D, L, N, _ptr(u), _ptr(delta), _ptr(z), _ptr(Bm), _ptr(Cm),
+                                       _ptr(A), _ptr(Dskip), _ptr(delta_bias), _ptr(h0),
+                                       int(bool(delta_softplus)), _ptr(dy), _ptr(dh_last),
+                                       _ptr(out["du"]), _ptr(out["ddelta"]), _ptr(out["dz"]), _ptr(out["dBm"]),
+                                       _ptr(out["dCm"]), _ptr(out["dA"]), _ptr(out["dDskip"]),
+                                       _ptr(out["ddelta_bias"]), _ptr(out["dh0"]))
+    if rc != 0:
+        raise RuntimeError("oracle_selective_scan_bwd failed")
+    if bc_shared:
+        out["dBm"] = out["dBm"].sum(axis=0, keepdims=True)
+        out["dCm"] = out["dCm"].sum(axis=0, keepdims=True)
     return out

@@ -340,3 +340,101 @@ int oracle_causal_conv1d(int64_t B, int64_t D, int64_t L, int64_t W, const doubl
     }
     return 0;
 }
+
+/*
+ * Reverse-mode derivative of the scan above (Euler input term), for training
+ * with recomputation ("gitcode", section 3.3.2: the backward pass recomputes
+ * the intermediate states instead of storing them; the oracle, being slow and
+ * plain, simply keeps every state of one channel).  Given the upstream
+ * gradient dy of y (and optionally dh_last of the final state) it returns the
+ * gradient of every input.  Written out from the chain rule on
+ *   Delta_t = softplus(s_t), s_t = delta_t + bias       dDelta/ds = sigmoid(s_t)
+ *   a_t[n]  = exp(Delta_t A[n])                          da/dDelta = a A, da/dA = a Delta
+ *   h_t[n]  = a_t[n] h_{t-1}[n] + Delta_t B_t[n] u_t
+ *   p_t     = sum_n C_t[n] h_t[n] + D u_t,   y_t = p_t silu(z_t)
+ *   silu'(z) = sigmoid(z) (1 + z (1 - sigmoid(z)))
+ * with the adjoint lambda_t[n] = dL/dh_t[n] = (dy_t silu(z_t)) C_t[n]
+ * + a_{t+1}[n] lambda_{t+1}[n], run backwards from lambda_{L-1} = dh_last
+ * contributions.  dh0 = a_0 lambda_0.
+ * Outputs, each overwritten (accumulated from zero over the batch and time):
+ *   du, ddelta : (B, D, L)   dz : (B, D, L), only if z   dBm, dCm : (B, N, L)
+ *   dA : (D, N)   dDskip : (D), only if Dskip   ddelta_bias : (D)   dh0 : (B, D, N) nullable
+ */
+int oracle_selective_scan_bwd(int64_t B, int64_t D, int64_t L, int64_t N,
+                              const double *u, const double *delta, const double *z,
+                              const double *Bm, const double *Cm, const double *A,
+                              const double *Dskip, const double *delta_bias,
+                              const double *h0, int delta_softplus,
+                              const double *dy, const double *dh_last,
+                              double *du, double *ddelta, double *dz, double *dBm, double *dCm,
+                              double *dA, double *dDskip, double *ddelta_bias, double *dh0) {
+    if (B < 0 || D < 0 || L < 0 || N < 0) return -1;
+    if (!u || !delta || !Bm || !Cm || !A || !dy || !du || !ddelta || !dBm || !dCm || !dA || !ddelta_bias)
+        return -1;
+    if (z && !dz) return -1;
+    if (Dskip && !dDskip) return -1;
+    memset(dBm, 0, sizeof(double) * (size_t)(B * N * L));
+    memset(dCm, 0, sizeof(double) * (size_t)(B * N * L));
+    memset(dA, 0, sizeof(double) * (size_t)(D * N));
+    memset(ddelta_bias, 0, sizeof(double) * (size_t)D);
+    if (dDskip) memset(dDskip, 0, sizeof(double) * (size_t)D);
+    double *hs = (double *)malloc(sizeof(double) * (size_t)((L + 1) * N + 1));   /* h_{t-1} at row t */
+    double *dts = (double *)malloc(sizeof(double) * (size_t)(L + 1));
+    double *pre = (double *)malloc(sizeof(double) * (size_t)(L + 1));
+    double *lam = (double *)malloc(sizeof(double) * (size_t)(N + 1));
+    if (!hs || !dts || !pre || !lam) { free(hs); free(dts); free(pre); free(lam); return -1; }
+    for (int64_t b = 0; b < B; ++b) {
+        for (int64_t d = 0; d < D; ++d) {
+            const int64_t c = b * D + d;
+            const double *uc = u + c * L, *dl = delta + c * L, *zc = z ? z + c * L : NULL;
+            const double *dyc = dy + c * L;
+            const double *Bb = Bm + b * N * L, *Cb = Cm + b * N * L, *Ad = A + d * N;
+            const double bias = delta_bias ? delta_bias[d] : 0.0;
+            const double Dd = Dskip ? Dskip[d] : 0.0;
+            /* forward, keeping every state: hs[t*N + n] = h_{t-1}[n] */
+            for (int64_t n = 0; n < N; ++n) hs[n] = h0 ? h0[c * N + n] : 0.0;
+            for (int64_t t = 0; t < L; ++t) {
+                dts[t] = discretisation_step(dl[t], bias, delta_softplus);
+                double acc = 0.0;
+                for (int64_t n = 0; n < N; ++n) {
+                    double hn = exp(dts[t] * Ad[n]) * hs[t * N + n] + dts[t] * Bb[n * L + t] * uc[t];
+                    hs[(t + 1) * N + n] = hn;
+                    acc += Cb[n * L + t] * hn;
+                }
+                pre[t] = acc + Dd * uc[t];
+            }
+            /* backward */
+            for (int64_t n = 0; n < N; ++n) lam[n] = dh_last ? dh_last[c * N + n] : 0.0;
+            for (int64_t t = L - 1; t >= 0; --t) {
+                double gate = 1.0;
+                if (zc) {
+                    const double sg = sigmoid(zc[t]);
+                    gate = zc[t] * sg;
+                    dz[c * L + t] = dyc[t] * pre[t] * sg * (1.0 + zc[t] * (1.0 - sg));
+                }
+                const double yt = dyc[t] * gate;   /* dL/dp_t */
+                if (dDskip) dDskip[d] += yt * uc[t];
+                double du_acc = yt * Dd, dDelta = 0.0;
+                for (int64_t n = 0; n < N; ++n) {
+                    const double lt = lam[n] + yt * Cb[n * L + t];   /* lambda_t */
+                    const double at = exp(dts[t] * Ad[n]);   /* Abar_t[n] */
+                    const double hprev = hs[t * N + n];
+                    dCm[b * N * L + n * L + t] += yt * hs[(t + 1) * N + n];
+                    dA[d * N + n] += lt * hprev * at * dts[t];
+                    dDelta += lt * (hprev * at * Ad[n] + Bb[n * L + t] * uc[t]);
+                    dBm[b * N * L + n * L + t] += lt * dts[t] * uc[t];
+                    du_acc += lt * dts[t] * Bb[n * L + t];
+                    lam[n] = lt * at;                               /* carried to step t-1 */
+                }
+                du[c * L + t] = du_acc;
+                const double dd = delta_softplus ? dDelta * sigmoid(dl[t] + bias) : dDelta;
+                ddelta[c * L + t] = dd;
+                ddelta_bias[d] += dd;
+            }
+            if (dh0)
+                for (int64_t n = 0; n < N; ++n) dh0[c * N + n] = lam[n];
+        }
+    }
+    free(hs); free(dts); free(pre); free(lam);
+    return 0;
+}

@@ -308,6 +308,77 @@ def pin_zoh_to_euler_small_delta(lib):
 
 
 # ---------------------------------------------------------------------------
+# The backward pass (gradients of the scan, for training with recomputation,
+# "Mamba paper translation", gitcode.csdn.net, section 3.3.2).  Pinned to the
+# forward oracle (itself pinned above) by central finite differences of the
+# scalar objective sum(dy * y) + sum(dh_last * h_last), element by element.
+# ---------------------------------------------------------------------------
+
+def _fd_check_bwd(lib, gate, dskip, bias, softplus, h0, dh_last, bc_shared=False, seed=21):
+    rng = np.random.default_rng(seed)
+    Bsz, D, L, N = 2, 3, 7, 4
+    p = dict(u=rng.standard_normal((Bsz, D, L)), delta=rng.standard_normal((Bsz, D, L)) * 0.7,
+             z=rng.standard_normal((Bsz, D, L)) if gate else None,
+             Bm=rng.standard_normal((1 if bc_shared else Bsz, N, L)),
+             Cm=rng.standard_normal((1 if bc_shared else Bsz, N, L)),
+             A=-rng.uniform(0.3, 2.0, (D, N)), Dskip=rng.standard_normal(D) if dskip else None,
+             delta_bias=rng.standard_normal(D) * 0.5 if bias else None,
+             h0=rng.standard_normal((Bsz, D, N)) if h0 else None)
+    dy = rng.standard_normal((Bsz, D, L))
+    dhl = rng.standard_normal((Bsz, D, N)) if dh_last else None
+
+    def objective(q):
+        y, hl = oracle.selective_scan(q["u"], q["delta"], q["A"], q["Bm"], q["Cm"], Dskip=q["Dskip"], z=q["z"],
+                                      delta_bias=q["delta_bias"], h0=q["h0"], delta_softplus=softplus,
+                                      return_last_state=True, nthreads=1, lib=lib)
+        v = float(np.sum(dy * y))
+        if dhl is not None:
+            v += float(np.sum(dhl * hl))
+        return v
+
+    g = oracle.selective_scan_bwd(p["u"], p["delta"], p["A"], p["Bm"], p["Cm"], dy, Dskip=p["Dskip"], z=p["z"],
+                                  delta_bias=p["delta_bias"], h0=p["h0"], delta_softplus=softplus, dh_last=dhl,
+                                  lib=lib)
+    names = {"u": "du", "delta": "ddelta", "z": "dz", "Bm": "dBm", "Cm": "dCm", "A": "dA", "Dskip": "dDskip",
+             "delta_bias": "ddelta_bias", "h0": "dh0"}
+    for key, gname in names.items():
+        if p[key] is None:
+            continue
+        got = g[gname]
+        fd = np.empty_like(p[key])
+        for idx in np.ndindex(p[key].shape):
+            eps = 1e-6 * max(1.0, abs(p[key][idx]))
+            qp = dict(p); qp[key] = p[key].copy(); qp[key][idx] += eps
+            qm = dict(p); qm[key] = p[key].copy(); qm[key][idx] -= eps
+            fd[idx] = (objective(qp) - objective(qm)) / (2 * eps)
+        scale = max(1.0, float(np.max(np.abs(fd))))
+        err = float(np.max(np.abs(got - fd)))
+        assert err <= 1e-6 * scale, f"{gname}: max |analytic - finite difference| = {err:.3e} (scale {scale:.2e})"
+    if p["h0"] is None:
+        # the gradient of a zero initial state is still defined: dh0 = a_0 lambda_0
+        assert g["dh0"].shape == (Bsz, D, N)
+
+
+def pin_bwd_finite_differences_full(lib):
+    """Gate, D skip, bias, softplus, h0 and dh_last all on."""
+    _fd_check_bwd(lib, gate=True, dskip=True, bias=True, softplus=True, h0=True, dh_last=True)
+
+
+def pin_bwd_finite_differences_bare(lib):
+    """No gate, no D skip, no bias, Delta = delta (no softplus), zero h0, dy only."""
+    _fd_check_bwd(lib, gate=False, dskip=False, bias=False, softplus=False, h0=False, dh_last=False, seed=22)
+
+
+def pin_bwd_finite_differences_shared_bc(lib):
+    """B, C shared across the batch: their gradients are the sums over the batch."""
+    _fd_check_bwd(lib, gate=True, dskip=True, bias=True, softplus=True, h0=False, dh_last=True, bc_shared=True,
+                  seed=23)
+
+
+BWD_PINS = [pin_bwd_finite_differences_full, pin_bwd_finite_differences_bare, pin_bwd_finite_differences_shared_bc]
+
+
+# ---------------------------------------------------------------------------
 # The causal depthwise convolution in front of the SSM branch ("Mamba and state
 # space models", docs.ifdog.com, section "Mamba architecture", step 3a).
 # ---------------------------------------------------------------------------
@@ -391,7 +462,7 @@ CONV_PINS = [
 ]
 
 
-ALL_PINS = CONV_PINS + [
+ALL_PINS = CONV_PINS + BWD_PINS + [
     pin_golden_recurrence, pin_golden_gated, pin_lti_equals_convolution, pin_theorem1_gated_rnn,
     pin_unrolled_sum, pin_single_step_closed_form, pin_tree_order_matches_sequential,
     pin_boundary_reset, pin_ignore_window, pin_chunk_invariance, pin_step_matches_scan,

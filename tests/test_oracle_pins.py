@@ -54,6 +54,16 @@ MUTANTS = [
     ("double v = bias ? bias[d] : 0.0;\n                for", "double v = 0.0;\n                for"),
     ("x_hist[row * (W - 1) + (W - 1) + src]", "x_hist[row * (W - 1) - src - 1]"),
     ("out[row * L + t] = use_silu ? v * sigmoid(v) : v;", "out[row * L + t] = use_silu ? sigmoid(v) : v;"),
+    # the backward pass
+    ("lam[n] = lt * at;", "lam[n] = lt;"),
+    ("dDelta += lt * (hprev * at * Ad[n] + Bb[n * L + t] * uc[t]);", "dDelta += lt * hprev * at * Ad[n];"),
+    ("dz[c * L + t] = dyc[t] * pre[t] * sg * (1.0 + zc[t] * (1.0 - sg));", "dz[c * L + t] = dyc[t] * pre[t] * sg;"),
+    ("dA[d * N + n] += lt * hprev * at * dts[t];", "dA[d * N + n] += lt * hprev * at;"),
+    ("if (dDskip) dDskip[d] += yt * uc[t];", "if (dDskip) dDskip[d] += dyc[t] * uc[t];"),
+    ("dCm[b * N * L + n * L + t] += yt * hs[(t + 1) * N + n];", "dCm[b * N * L + n * L + t] += yt * hs[t * N + n];"),
+    ("const double dd = delta_softplus ? dDelta * sigmoid(dl[t] + bias) : dDelta;",
+     "const double dd = dDelta;"),
+    ("du_acc += lt * dts[t] * Bb[n * L + t];", "du_acc += lt * Bb[n * L + t];"),
 ]
 
 
