@@ -1,7 +1,7 @@
 /*
  * ssm.h -- C ABI of the B300 selective state space (S6) library (libssm.so).
  *
- * Three operations, all from the Mamba paper (arXiv 2312.00752) as
+ * Four operations, all from the Mamba paper (arXiv 2312.00752) as
  * restated on the pages this library follows:
  *
  *   ssm_scan_fwd      the selective-scan forward pass.  For every batch b,
@@ -23,6 +23,9 @@
  *   ssm_state_update  one recurrent (decode) step of the same recurrence
  *                     against a persistent fp32 state ("gitcode", section 1
  *                     and section 2: constant time per generated token).
+ *   ssm_scan_bwd      the gradients of the scan for training, with the
+ *                     forward states recomputed rather than stored
+ *                     ("gitcode", section 3.3.2).
  *   ssm_causal_conv1d_fwd
  *                     the causal depthwise convolution along time, with an
  *                     optional SiLU, that produces the SSM branch's input
@@ -132,6 +135,52 @@ typedef struct ssm_step_args {
 } ssm_step_args_t;
 
 /*
+ * Arguments of ssm_scan_bwd: the gradients of ssm_scan_fwd (training).  With
+ * L the scalar being differentiated, dy = dL/dy and dh_last = dL/dh_last,
+ * it writes dL/d(every input) of the forward call described by `fwd`, by the
+ * chain rule through the recurrence run backwards in time (the adjoint
+ * lambda_t = dL/dh_t = dy_t silu(z_t) C_t + Abar_{t+1} lambda_{t+1}).  The
+ * forward states are not stored by ssm_scan_fwd: this call recomputes them
+ * ("gitcode", section 3.3.2, recomputation), keeping one state checkpoint
+ * every SSM_BWD_SEGMENT steps in the caller's workspace.
+ *   fwd           : the forward call's inputs; its y, h_last, flags and chunk_len
+ *                   are ignored, its workspace fields are used for the checkpoints
+ *   dy            : (batch, dim, seqlen)   io_dtype
+ *   dh_last       : (batch, dim, dstate)   fp32, nullable (zero)
+ *   du, ddelta    : (batch, dim, seqlen)   io_dtype
+ *   dz            : (batch, dim, seqlen)   io_dtype, required exactly when fwd.z is set
+ *   dA            : (dim, dstate)          fp32
+ *   dB, dC        : (batch, dstate, seqlen) fp32; batch stride 0 (a single row) when
+ *                   fwd's B / C are shared across the batch (their batch stride is 0)
+ *   dDskip        : (dim,) fp32 contiguous, required exactly when fwd.Dskip is set
+ *   ddelta_bias   : (dim,) fp32 contiguous, nullable
+ *   dh0           : (batch, dim, dstate)   fp32, nullable
+ * dA, dB, dC, dDskip and ddelta_bias are sums over the batch (and time, and
+ * for dB/dC over the channels): the call overwrites them (zeroes, then adds
+ * with atomics, so the order of the fp32 sums is not fixed).  Limits:
+ * 1 <= dstate <= 16; the gradient outputs must not overlap each other or any
+ * input.
+ */
+#define SSM_BWD_SEGMENT 8
+typedef struct ssm_scan_bwd_args {
+    ssm_scan_args_t fwd;
+    const void *dy;
+    const float *dh_last;
+    void *du, *ddelta, *dz;
+    float *dA, *dB, *dC, *dDskip, *ddelta_bias, *dh0;
+    int64_t stride_dy[3], stride_du[3], stride_ddelta[3], stride_dz[3];   /* (b, d, t) */
+    int64_t stride_dB[3], stride_dC[3];                                  /* (b, n, t) */
+    int64_t stride_dh_last[3], stride_dh0[3];                            /* (b, d, n) */
+} ssm_scan_bwd_args_t;
+
+/* Bytes of device workspace ssm_scan_bwd needs (the state checkpoints:
+ * batch * dim * ceil(seqlen / SSM_BWD_SEGMENT) * 16 floats).  Host-only. */
+ssm_status_t ssm_scan_bwd_workspace_size(const ssm_scan_bwd_args_t *args, size_t *bytes);
+
+/* Gradients of the selective scan (see ssm_scan_bwd_args_t). */
+ssm_status_t ssm_scan_bwd(const ssm_scan_bwd_args_t *args, void *stream);
+
+/*
  * Arguments of ssm_causal_conv1d_fwd.  Per batch b, channel d and step t:
  *   out[b,d,t] = act(bias[d] + sum_{k=0}^{width-1} weight[d,k] * x[b,d,t-(width-1)+k])
  * Tap width-1 multiplies the current step (the tap order of a framework
@@ -229,7 +278,8 @@ int ssm_version(void);
 
 /* sizeof of the argument structs as compiled into the library, so that a
  * binding can check its mirror of them: which = 0 -> ssm_scan_args_t,
- * 1 -> ssm_step_args_t, 2 -> ssm_conv_args_t; 0 for any other value. */
+ * 1 -> ssm_step_args_t, 2 -> ssm_conv_args_t, 3 -> ssm_scan_bwd_args_t; 0 for
+ * any other value. */
 size_t ssm_abi_sizeof(int which);
 
 #ifdef __cplusplus

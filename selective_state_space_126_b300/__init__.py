@@ -9,6 +9,7 @@ device is present, the calls raise.
 Public API (same names as the C entry points):
   ssm_scan_fwd(u, delta, A, Bm, Cm, Dskip=None, z=None, delta_bias=None, h0=None, ...)
   ssm_state_update(state, u, delta, A, Bm, Cm, Dskip=None, z=None, delta_bias=None, ...)
+  ssm_scan_bwd(u, delta, A, Bm, Cm, dy, Dskip=None, z=None, delta_bias=None, h0=None, dh_last=None, ...)
   ssm_causal_conv1d_fwd(x, weight, bias=None, x_hist=None, silu=True, ...)
   ssm_scan_workspace_size(...), ssm_status_string(code), ssm_version()
 """
@@ -29,7 +30,8 @@ PATH_NAMES = {0: "generic", 1: "tiled", 2: "chunked"}
 # every symbol include/ssm.h declares
 EXPORTED_SYMBOLS = ["ssm_scan_workspace_size", "ssm_scan_fwd", "ssm_state_update", "ssm_status_string",
                     "ssm_last_error_detail", "ssm_get_device_status", "ssm_scan_plan_path", "ssm_version",
-                    "ssm_abi_sizeof", "ssm_scan_fwd_noalloc", "ssm_causal_conv1d_fwd"]
+                    "ssm_abi_sizeof", "ssm_scan_fwd_noalloc", "ssm_causal_conv1d_fwd",
+                    "ssm_scan_bwd_workspace_size", "ssm_scan_bwd"]
 
 _i64 = ctypes.c_int64
 _vp = ctypes.c_void_p
@@ -75,6 +77,18 @@ class ConvArgs(ctypes.Structure):
     ]
 
 
+class BwdArgs(ctypes.Structure):
+    """Mirror of ssm_scan_bwd_args_t."""
+    _fields_ = [
+        ("fwd", ScanArgs),
+        ("dy", _vp), ("dh_last", _vp),
+        ("du", _vp), ("ddelta", _vp), ("dz", _vp),
+        ("dA", _vp), ("dB", _vp), ("dC", _vp), ("dDskip", _vp), ("ddelta_bias", _vp), ("dh0", _vp),
+        ("stride_dy", _i64 * 3), ("stride_du", _i64 * 3), ("stride_ddelta", _i64 * 3), ("stride_dz", _i64 * 3),
+        ("stride_dB", _i64 * 3), ("stride_dC", _i64 * 3), ("stride_dh_last", _i64 * 3), ("stride_dh0", _i64 * 3),
+    ]
+
+
 class SsmError(RuntimeError):
     def __init__(self, code, detail=""):
         self.code = code
@@ -116,8 +130,12 @@ def load_library(path: str = LIB_PATH):
         lib.ssm_abi_sizeof.restype = ctypes.c_size_t
         lib.ssm_causal_conv1d_fwd.argtypes = [ctypes.POINTER(ConvArgs), _vp]
         lib.ssm_causal_conv1d_fwd.restype = ctypes.c_int
+        lib.ssm_scan_bwd_workspace_size.argtypes = [ctypes.POINTER(BwdArgs), ctypes.POINTER(ctypes.c_size_t)]
+        lib.ssm_scan_bwd_workspace_size.restype = ctypes.c_int
+        lib.ssm_scan_bwd.argtypes = [ctypes.POINTER(BwdArgs), _vp]
+        lib.ssm_scan_bwd.restype = ctypes.c_int
         if (lib.ssm_abi_sizeof(0) != ctypes.sizeof(ScanArgs) or lib.ssm_abi_sizeof(1) != ctypes.sizeof(StepArgs)
-                or lib.ssm_abi_sizeof(2) != ctypes.sizeof(ConvArgs)):
+                or lib.ssm_abi_sizeof(2) != ctypes.sizeof(ConvArgs) or lib.ssm_abi_sizeof(3) != ctypes.sizeof(BwdArgs)):
             raise ImportError("libssm.so argument structs do not match this binding")
         if path == LIB_PATH:
             _lib = lib
@@ -172,6 +190,8 @@ def _strides(t, rank, dims=None):
     s = list(t.stride())
     if dims is not None and t.dim() == rank - 1:   # broadcast over a missing batch dimension
         s = [0] + s
+    elif dims is not None and t.dim() == rank and t.shape[0] == 1:   # a batch of one is broadcast
+        s[0] = 0
     if len(s) != rank:
         raise ValueError(f"expected a {rank}-d tensor, got shape {tuple(t.shape)}")
     return s
@@ -305,6 +325,75 @@ def ssm_state_update(state, u, delta, A, Bm, Cm, Dskip=None, z=None, delta_bias=
     args = make_step_args(state, u, delta, A, Bm, Cm, y, Dskip, z, delta_bias, delta_softplus)
     _check(lib.ssm_state_update(ctypes.byref(args), _vp(_stream_handle(stream))))
     return y
+
+
+SSM_BWD_SEGMENT = 8
+
+
+def make_bwd_args(fwd: ScanArgs, dy, grads: dict, dh_last=None) -> BwdArgs:
+    """Fill an ssm_scan_bwd_args_t: ``fwd`` from make_scan_args (its y may be None), ``grads`` a dict of
+    output tensors du, ddelta, dz, dA, dB, dC, dDskip, ddelta_bias, dh0 (missing keys = NULL)."""
+    a = BwdArgs()
+    a.fwd = fwd
+    a.dy, a.dh_last = _ptr(dy), _ptr(dh_last)
+    a.stride_dy[:] = _strides(dy, 3)
+    a.stride_dh_last[:] = _strides(dh_last, 3)
+    for k in ("du", "ddelta", "dz", "dA", "dB", "dC", "dDskip", "ddelta_bias", "dh0"):
+        setattr(a, k, _ptr(grads.get(k)))
+    for k in ("du", "ddelta", "dz", "dh0"):
+        getattr(a, "stride_" + k)[:] = _strides(grads.get(k), 3)
+    for k in ("dB", "dC"):
+        getattr(a, "stride_" + k)[:] = _strides(grads.get(k), 3, dims="b")
+    return a
+
+
+def ssm_scan_bwd(u, delta, A, Bm, Cm, dy, Dskip=None, z=None, delta_bias=None, h0=None, delta_softplus=True,
+                 dh_last=None, return_dh0=True, workspace=None, stream=None):
+    """Gradients of ssm_scan_fwd for an upstream gradient ``dy`` (B, D, L) of y (and ``dh_last``
+    (B, D, N) fp32 of the final state, optional).
+
+    Returns a dict: du, ddelta (and dz if z is given) in the I/O dtype, (B, D, L); dA (D, N); dB, dC
+    fp32 shaped like Bm, Cm ((N, L) when they are shared across the batch); dDskip (D,) if Dskip is
+    given; ddelta_bias (D,) if delta_bias is given; dh0 (B, D, N) if ``return_dh0``.
+    """
+    torch = _torch()
+    lib = load_library()
+    for name, t in (("u", u), ("delta", delta), ("Bm", Bm), ("Cm", Cm), ("z", z), ("dy", dy)):
+        if t is not None and not t.is_cuda:
+            raise ValueError(f"{name} must be a CUDA tensor")
+    if dy.dtype != u.dtype:
+        raise TypeError("dy must have u's dtype")
+    _f32(A, "A"); _f32(Dskip, "Dskip"); _f32(delta_bias, "delta_bias"); _f32(h0, "h0"); _f32(dh_last, "dh_last")
+    if Dskip is not None:
+        Dskip = Dskip.contiguous()
+    if delta_bias is not None:
+        delta_bias = delta_bias.contiguous()
+    Bsz, D, L = u.shape
+    N = A.shape[1]
+    dev = u.device
+    g = {"du": torch.empty_like(u), "ddelta": torch.empty_like(u),
+         "dA": torch.empty((D, N), dtype=torch.float32, device=dev),
+         "dB": torch.empty(tuple(Bm.shape), dtype=torch.float32, device=dev),
+         "dC": torch.empty(tuple(Cm.shape), dtype=torch.float32, device=dev)}
+    if z is not None:
+        g["dz"] = torch.empty_like(u)
+    if Dskip is not None:
+        g["dDskip"] = torch.empty(D, dtype=torch.float32, device=dev)
+    if delta_bias is not None:
+        g["ddelta_bias"] = torch.empty(D, dtype=torch.float32, device=dev)
+    if return_dh0:
+        g["dh0"] = torch.empty((Bsz, D, N), dtype=torch.float32, device=dev)
+    fwd = make_scan_args(u, delta, A, Bm, Cm, None, Dskip, z, delta_bias, h0, None, delta_softplus)
+    args = make_bwd_args(fwd, dy, g, dh_last)
+    need = ctypes.c_size_t(0)
+    _check(lib.ssm_scan_bwd_workspace_size(ctypes.byref(args), ctypes.byref(need)))
+    if need.value > 0:
+        if workspace is None or workspace.numel() * workspace.element_size() < need.value:
+            workspace = torch.empty(need.value, dtype=torch.uint8, device=dev)
+        args.fwd.workspace = workspace.data_ptr()
+        args.fwd.workspace_bytes = workspace.numel() * workspace.element_size()
+    _check(lib.ssm_scan_bwd(ctypes.byref(args), _vp(_stream_handle(stream))))
+    return g
 
 
 def make_conv_args(x, weight, out, bias=None, x_hist=None, silu=True) -> ConvArgs:

@@ -298,12 +298,13 @@ using namespace ssm;
 
 extern "C" {
 
-int ssm_version(void) { return (1 << 16) | 1; }
+int ssm_version(void) { return (1 << 16) | 2; }
 
 size_t ssm_abi_sizeof(int which) {
   if (which == 0) return sizeof(ssm_scan_args_t);
   if (which == 1) return sizeof(ssm_step_args_t);
   if (which == 2) return sizeof(ssm_conv_args_t);
+  if (which == 3) return sizeof(ssm_scan_bwd_args_t);
   return 0;
 }
 
@@ -431,6 +432,152 @@ ssm_status_t ssm_state_update(const ssm_step_args_t* a, void* stream) {
       return fail(SSM_ERR_INVALID_ARG, "an output overlaps an input");
   }
   cudaError_t e = launch_state_update(p, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e);
+  return ok();
+}
+
+}  // extern "C"
+
+namespace ssm {
+namespace {
+
+// Validates the backward arguments: the forward inputs (with dy standing in
+// for y as a read-only sequence tensor) and every gradient output.
+ssm_status_t validate_bwd(const ssm_scan_bwd_args_t* a, BwdProblem* p) {
+  if (!a) return fail(SSM_ERR_INVALID_ARG, "args is NULL");
+  ssm_scan_args_t fa = a->fwd;
+  fa.y = const_cast<void*>(a->dy);
+  std::memcpy(fa.stride_y, a->stride_dy, sizeof(fa.stride_y));
+  fa.h_last = nullptr;
+  std::memset(p, 0, sizeof(*p));
+  ssm_status_t st = validate_scan(&fa, &p->f);
+  if (st != SSM_OK) return st;
+  const ScanProblem& f = p->f;
+  if (f.N > 16) return fail(SSM_ERR_UNSUPPORTED, "the backward pass takes dstate <= 16");
+  p->dy = a->dy; p->dhl = a->dh_last;
+  p->du = a->du; p->ddelta = a->ddelta; p->dz = a->dz;
+  p->dA = a->dA; p->dB = a->dB; p->dC = a->dC; p->dD = a->dDskip; p->dbias = a->ddelta_bias; p->dh0 = a->dh0;
+  std::memcpy(p->sdy, a->stride_dy, sizeof(p->sdy));
+  std::memcpy(p->sdu, a->stride_du, sizeof(p->sdu));
+  std::memcpy(p->sdd, a->stride_ddelta, sizeof(p->sdd));
+  std::memcpy(p->sdz, a->stride_dz, sizeof(p->sdz));
+  std::memcpy(p->sdB, a->stride_dB, sizeof(p->sdB));
+  std::memcpy(p->sdC, a->stride_dC, sizeof(p->sdC));
+  std::memcpy(p->sdhl, a->stride_dh_last, sizeof(p->sdhl));
+  std::memcpy(p->sdh0, a->stride_dh0, sizeof(p->sdh0));
+  p->nseg = (f.L + SSM_BWD_SEGMENT - 1) / SSM_BWD_SEGMENT;
+  const bool shared_b = f.sB[0] == 0 && f.B > 1, shared_c = f.sC[0] == 0 && f.B > 1;
+  if (shared_b != shared_c) return fail(SSM_ERR_UNSUPPORTED, "B and C must be both shared or both per batch row");
+  p->bc_rows = shared_b ? 1 : f.B;
+  if (f.B == 0 || f.D == 0) return ok();
+  if (!p->dA) return fail(SSM_ERR_INVALID_ARG, "dA is NULL");
+  if (f.L > 0 && (!p->dy || !p->du || !p->ddelta || !p->dB || !p->dC))
+    return fail(SSM_ERR_INVALID_ARG, "dy, du, ddelta, dB or dC is NULL");
+  if ((f.z != nullptr) != (p->dz != nullptr) && f.L > 0) return fail(SSM_ERR_INVALID_ARG, "dz must be given exactly when z is");
+  if ((f.Dskip != nullptr) != (p->dD != nullptr)) return fail(SSM_ERR_INVALID_ARG, "dDskip must be given exactly when Dskip is");
+  if (shared_b && (p->sdB[0] != 0 || p->sdC[0] != 0))
+    return fail(SSM_ERR_INVALID_ARG, "B/C are shared across the batch: dB/dC need batch stride 0");
+  const int es = elem_size(f.io);
+  struct Out {
+    const char* name;
+    const void* ptr;
+    int rank;
+    int64_t ext[3];
+    const int64_t* str;
+    int es;
+  };
+  const int64_t sA[2] = {f.N, 1}, s1[1] = {1};
+  int64_t sdB[3] = {p->sdB[0], p->sdB[1], p->sdB[2]}, sdC[3] = {p->sdC[0], p->sdC[1], p->sdC[2]};
+  const Out outs[] = {{"du", p->du, 3, {f.B, f.D, f.L}, p->sdu, es},
+                      {"ddelta", p->ddelta, 3, {f.B, f.D, f.L}, p->sdd, es},
+                      {"dz", p->dz, 3, {f.B, f.D, f.L}, p->sdz, es},
+                      {"dB", p->dB, 3, {p->bc_rows, f.N, f.L}, sdB, 4},
+                      {"dC", p->dC, 3, {p->bc_rows, f.N, f.L}, sdC, 4},
+                      {"dA", p->dA, 2, {f.D, f.N, 1}, sA, 4},
+                      {"dDskip", p->dD, 1, {f.D, 1, 1}, s1, 4},
+                      {"ddelta_bias", p->dbias, 1, {f.D, 1, 1}, s1, 4},
+                      {"dh0", p->dh0, 3, {f.B, f.D, f.N}, p->sdh0, 4}};
+  uintptr_t lo[9], hi[9];
+  int m = 0;
+  for (const Out& o : outs) {
+    if (!o.ptr || o.ext[o.rank - 1] == 0) continue;
+    for (int i = 0; i < o.rank; ++i)
+      if (o.str[i] < 0) return fail(SSM_ERR_INVALID_ARG, "%s has a negative stride", o.name);
+    const bool seq = o.ptr == p->du || o.ptr == p->ddelta || o.ptr == p->dz;   // written along t with stride 1
+    if (seq && o.str[2] != 1 && f.L > 1) return fail(SSM_ERR_UNSUPPORTED, "%s time stride must be 1", o.name);
+    if (!aligned(o.ptr, o.es)) return fail(SSM_ERR_INVALID_ARG, "%s misaligned", o.name);
+    if (o.rank == 3 && !injective(3, o.ext, o.str)) return fail(SSM_ERR_INVALID_ARG, "%s strides overlap", o.name);
+    tensor_range(o.ptr, o.rank, o.ext, o.str, o.es, &lo[m], &hi[m]);
+    ++m;
+  }
+  for (int i = 0; i < m; ++i)
+    for (int j = i + 1; j < m; ++j)
+      if (overlaps(lo[i], hi[i], lo[j], hi[j])) return fail(SSM_ERR_INVALID_ARG, "two gradient outputs overlap");
+  // no gradient output may overlap an input
+  struct In {
+    const void* ptr;
+    int rank;
+    int64_t ext[3];
+    int64_t str[3];
+    int es;
+  } ins[] = {
+      {f.u, 3, {f.B, f.D, f.L}, {f.su[0], f.su[1], 1}, es},
+      {f.delta, 3, {f.B, f.D, f.L}, {f.sd[0], f.sd[1], 1}, es},
+      {f.z, 3, {f.B, f.D, f.L}, {f.sz[0], f.sz[1], 1}, es},
+      {p->dy, 3, {f.B, f.D, f.L}, {p->sdy[0], p->sdy[1], 1}, es},
+      {f.Bm, 3, {f.B, f.N, f.L}, {f.sB[0], f.sB[1], 1}, es},
+      {f.Cm, 3, {f.B, f.N, f.L}, {f.sC[0], f.sC[1], 1}, es},
+      {f.A, 2, {f.D, f.N, 1}, {f.sA[0], f.sA[1], 0}, 4},
+      {f.Dskip, 1, {f.D, 1, 1}, {1, 0, 0}, 4},
+      {f.bias, 1, {f.D, 1, 1}, {1, 0, 0}, 4},
+      {f.h0, 3, {f.B, f.D, f.N}, {f.sh0[0], f.sh0[1], f.sh0[2]}, 4},
+      {p->dhl, 3, {f.B, f.D, f.N}, {p->sdhl[0], p->sdhl[1], p->sdhl[2]}, 4},
+  };
+  for (const In& in : ins) {
+    if (!in.ptr || in.ext[in.rank - 1] == 0) continue;
+    for (int i = 0; i < in.rank; ++i)
+      if (in.str[i] < 0) return fail(SSM_ERR_INVALID_ARG, "negative input stride");
+    uintptr_t i0, i1;
+    tensor_range(in.ptr, in.rank, in.ext, in.str, in.es, &i0, &i1);
+    for (int k = 0; k < m; ++k)
+      if (overlaps(lo[k], hi[k], i0, i1)) return fail(SSM_ERR_INVALID_ARG, "a gradient output overlaps an input");
+  }
+  return ok();
+}
+
+size_t bwd_workspace_bytes(const BwdProblem& p) {
+  return (size_t)(p.f.B * p.f.D * p.nseg) * 16 * sizeof(float);
+}
+
+}  // namespace
+}  // namespace ssm
+
+extern "C" {
+
+ssm_status_t ssm_scan_bwd_workspace_size(const ssm_scan_bwd_args_t* args, size_t* bytes) {
+  if (!bytes) return fail(SSM_ERR_INVALID_ARG, "bytes is NULL");
+  *bytes = 0;
+  BwdProblem p;
+  ssm_status_t st = validate_bwd(args, &p);
+  if (st != SSM_OK) return st;
+  *bytes = bwd_workspace_bytes(p);
+  return ok();
+}
+
+ssm_status_t ssm_scan_bwd(const ssm_scan_bwd_args_t* args, void* stream) {
+  BwdProblem p;
+  ssm_status_t st = validate_bwd(args, &p);
+  if (st != SSM_OK) return st;
+  if (p.f.B == 0 || p.f.D == 0) return ok();
+  const size_t need = bwd_workspace_bytes(p);
+  if (need > 0) {
+    if (!args->fwd.workspace) return fail(SSM_ERR_WORKSPACE, "workspace of %zu bytes required", need);
+    if (args->fwd.workspace_bytes < need)
+      return fail(SSM_ERR_WORKSPACE, "workspace %zu < %zu bytes", args->fwd.workspace_bytes, need);
+    if (!aligned(args->fwd.workspace, 16)) return fail(SSM_ERR_WORKSPACE, "workspace not 16-byte aligned");
+  }
+  p.ckpt = static_cast<float*>(args->fwd.workspace);
+  cudaError_t e = launch_scan_bwd(p, device_sm_count(), static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e);
   return ok();
 }

@@ -33,6 +33,20 @@ struct StepProblem {
   int64_t sst[3], su[2], sd[2], sz[2], sy[2], sB[2], sC[2], sA[2];
 };
 
+// Validated backward problem: the forward inputs, the upstream gradients and
+// the gradient outputs (strides in elements).
+struct BwdProblem {
+  ScanProblem f;
+  const void* dy;
+  const float* dhl;
+  void *du, *ddelta, *dz;
+  float *dA, *dB, *dC, *dD, *dbias, *dh0;
+  int64_t sdy[3], sdu[3], sdd[3], sdz[3], sdB[3], sdC[3], sdhl[3], sdh0[3];
+  int64_t bc_rows;     // rows of dB / dC: 1 when B / C are shared across the batch
+  int64_t nseg;        // checkpoints per channel
+  float* ckpt;         // [B][D][nseg][16] fp32
+};
+
 struct ConvProblem {
   int64_t B, D, L;
   int W;
@@ -70,6 +84,7 @@ cudaError_t launch_scan_generic(const ScanProblem& p, cudaStream_t s);
 cudaError_t launch_scan_tiled(const ScanProblem& p, const ScanPlan& plan, void* workspace, cudaStream_t s);
 cudaError_t launch_state_update(const StepProblem& p, cudaStream_t s);
 cudaError_t launch_causal_conv1d(const ConvProblem& p, int sms, cudaStream_t s);
+cudaError_t launch_scan_bwd(const BwdProblem& p, int sms, cudaStream_t s);
 
 // tile length of the tiled kernel (timesteps)
 #ifndef SSM_TILE_T

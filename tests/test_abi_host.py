@@ -243,3 +243,60 @@ def test_conv_validation(lib, over, code):
                                   dict(seqlen=0, x=None, weight=None, out=None)])
 def test_conv_empty_is_a_no_op(lib, over):
     assert call_conv(conv_args(**over)) == ssm.SSM_OK
+
+
+def bwd_args(B=2, D=64, L=256, N=16, **over):
+    a = ssm.BwdArgs()
+    a.fwd = scan_args(B, D, L, N)
+    a.fwd.y = None
+    a.dy = FAKE["y"]
+    a.stride_dy[:] = [D * L, L, 1]
+    base = 0x40_0000_0000
+    for i, k in enumerate(("du", "ddelta", "dz", "dA", "dB", "dC", "dDskip", "ddelta_bias", "dh0")):
+        setattr(a, k, base + i * 0x1_0000_0000)
+    for k in ("stride_du", "stride_ddelta", "stride_dz"):
+        getattr(a, k)[:] = [D * L, L, 1]
+    a.stride_dB[:] = [N * L, L, 1]
+    a.stride_dC[:] = [N * L, L, 1]
+    a.stride_dh0[:] = [D * N, N, 1]
+    for k, v in over.items():
+        if isinstance(v, list):
+            getattr(a, k)[:] = v
+        else:
+            setattr(a, k, v)
+    return a
+
+
+def bwd_ws(a):
+    n = ctypes.c_size_t(0)
+    rc = ssm.load_library().ssm_scan_bwd_workspace_size(ctypes.byref(a), ctypes.byref(n))
+    return rc, n.value
+
+
+def test_bwd_workspace_size(lib):
+    rc, n = bwd_ws(bwd_args(B=2, D=64, L=250, N=16))
+    assert rc == ssm.SSM_OK and n == 2 * 64 * 32 * 16 * 4   # ceil(250 / 8) = 32 checkpoints per channel
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(dA=None), ssm.SSM_ERR_INVALID_ARG),
+    (dict(du=None), ssm.SSM_ERR_INVALID_ARG),
+    (dict(dz=None), ssm.SSM_ERR_INVALID_ARG),          # z is set
+    (dict(dDskip=None), ssm.SSM_ERR_INVALID_ARG),      # Dskip is set
+    (dict(dy=None), ssm.SSM_ERR_INVALID_ARG),
+    (dict(stride_du=[64 * 256, 256, 2]), ssm.SSM_ERR_UNSUPPORTED),
+    (dict(stride_dB=[0, 256, 1]), ssm.SSM_ERR_INVALID_ARG),   # two batch rows of dB on one row
+    (dict(ddelta=0x40_0000_0000), ssm.SSM_ERR_INVALID_ARG),   # ddelta on du
+    (dict(du=FAKE["u"]), ssm.SSM_ERR_INVALID_ARG),            # a gradient on an input
+    (dict(dy=FAKE["u"] + 2), ssm.SSM_ERR_INVALID_ARG),        # dy overlaps u (read-only, but y's checks apply)
+])
+def test_bwd_validation(lib, over, code):
+    assert bwd_ws(bwd_args(**over))[0] == code
+
+
+def test_bwd_rejects_large_dstate(lib):
+    a = bwd_args(N=32)
+    a.stride_dB[:] = [32 * 256, 256, 1]
+    a.stride_dC[:] = [32 * 256, 256, 1]
+    a.stride_dh0[:] = [64 * 32, 32, 1]
+    assert bwd_ws(a)[0] == ssm.SSM_ERR_UNSUPPORTED
