@@ -57,7 +57,7 @@ def parse():
     ap.add_argument("--no-rows", action="store_true", help="skip the other workloads' timing rows")
     ap.add_argument("--only-rows", action="store_true",
                     help="time only the other workloads' rows (one line of JSON; for profiling their kernels)")
-    ap.add_argument("--rows", default="all", help="comma-separated subset of rows: m130, ti, long, decode, conv")
+    ap.add_argument("--rows", default="all", help="comma-separated subset of rows: m130, ti, long, decode, conv, bwd")
     ap.add_argument("--decode-steps", type=int, default=1000, help="decode steps of the decode row")
     return ap.parse_args()
 
@@ -284,7 +284,7 @@ def decode_bytes(cfg) -> int:
 
 ROW_KEYS = {"m130": "mamba130m_bf16_b8_d1536_l2048_n16", "ti": "mamba2.8b_ti_bf16_b1_d5120_l2048_n16",
             "long": "long_bf16_b1_d1536_l1048576_n16", "decode": "decode_bf16_b256_d5120_n16_x1000",
-            "conv": "conv1d_silu_bf16_b4_d5120_l2048_w4"}
+            "conv": "conv1d_silu_bf16_b4_d5120_l2048_w4", "bwd": "scan_bwd_mamba2.8b_bf16_b4_d5120_l2048_n16"}
 
 
 def other_rows(lib, ssm, peak, stream, dev, which="all", decode_steps=1000):
@@ -362,6 +362,45 @@ def other_rows(lib, ssm, peak, stream, dev, which="all", decode_steps=1000):
                       "hbm_gbs_algorithmic": gbs, "frac": gbs / peak, "algorithmic_bytes": byt,
                       "l2": "flushed between launches"}
         del x, xo, wt, cb
+        torch.cuda.empty_cache()
+
+    if "bwd" in sel:
+        # the backward pass (all gradients, states recomputed) on the 2.8B-shaped layer
+        name = ROW_KEYS["bwd"]
+        cfg = syn.M2P8
+        inp = random_device_inputs(cfg, 0, dev)
+        dy = torch.randn(inp["u"].shape, generator=torch.Generator(device=dev).manual_seed(4000), device=dev).to(
+            inp["u"].dtype)
+        Bsz, D, L, N = cfg.batch, cfg.dim, cfg.seqlen, cfg.dstate
+        grads = {k: torch.empty_like(inp["u"]) for k in ("du", "ddelta", "dz")}
+        grads.update(dA=torch.empty(D, N, device=dev), dB=torch.empty(Bsz, N, L, device=dev),
+                     dC=torch.empty(Bsz, N, L, device=dev), dDskip=torch.empty(D, device=dev),
+                     ddelta_bias=torch.empty(D, device=dev), dh0=torch.empty(Bsz, D, N, device=dev))
+        fa = ssm.make_scan_args(inp["u"], inp["delta"], inp["A"], inp["Bm"], inp["Cm"], None, inp["Dskip"], inp["z"],
+                                inp["delta_bias"])
+        ba = ssm.make_bwd_args(fa, dy, grads)
+        need = ctypes.c_size_t(0)
+        if lib.ssm_scan_bwd_workspace_size(ctypes.byref(ba), ctypes.byref(need)) != 0:
+            raise RuntimeError("ssm_scan_bwd_workspace_size failed")
+        bws = torch.empty(max(need.value, 16), dtype=torch.uint8, device=dev)
+        ba.fwd.workspace, ba.fwd.workspace_bytes = bws.data_ptr(), need.value
+
+        def brun():
+            rc = lib.ssm_scan_bwd(ctypes.byref(ba), sh)
+            if rc != 0:
+                raise RuntimeError(ssm.status_name(rc) + " " + lib.ssm_last_error_detail().decode())
+
+        for _ in range(3):
+            brun()
+        ms = time_launches(brun, 20, stream, None)
+        # read u, delta, z, dy and write du, ddelta, dz once; B, C read and dB, dC written (fp32) once
+        es = inp["u"].element_size()
+        byt = 7 * Bsz * D * L * es + 2 * Bsz * N * L * es + 2 * Bsz * N * L * 4 + (D * N + 2 * D) * 4
+        gbs = byt / (ms * 1e-3) / 1e9
+        rows[name] = {"ms": ms, "value": cfg.updates / (ms * 1e-3), "unit": UNIT, "launches": 2,
+                      "hbm_gbs_algorithmic": gbs, "frac": gbs / peak, "algorithmic_bytes": byt,
+                      "workspace_bytes": need.value, "l2": "inputs larger than L2"}
+        del inp, dy, grads, bws
         torch.cuda.empty_cache()
 
     if "decode" not in sel:
