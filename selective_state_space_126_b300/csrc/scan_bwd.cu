@@ -118,8 +118,9 @@ __global__ void __launch_bounds__(32) scan_bwd_kernel(const BwdProblem p) {
     __syncwarp();
   };
 
-  // ---- forward sweep: a checkpoint of the state before every segment ----
-  for (int64_t seg = 0; seg < p.nseg; ++seg) {
+  // ---- forward sweep: a checkpoint of the state before every segment (unless the
+  // tiled forward kernel has written them already) ----
+  for (int64_t seg = 0; p.sweep && seg < p.nseg; ++seg) {
     stage_bc(seg);
     if (valid) {
 #pragma unroll

@@ -14,6 +14,7 @@ namespace {
 
 constexpr int MODE_OUTPUT = 0;   // scan and emit y (and h_last)
 constexpr int MODE_RECORD = 1;   // chunked path, first pass: scan from zero, record end state and sum of Delta
+constexpr int MODE_CKPT = 2;     // backward pass, first step: scan from h0, keep the state every SSM_BWD_SEGMENT steps
 
 struct ScanKernelParams {
   int64_t B, D, L;
@@ -36,6 +37,8 @@ struct ScanKernelParams {
   int bc_rank3;     // B / C tensor maps carry a batch dimension
   int y_rank3;      // the y tensor map carries a batch dimension
   int* status;
+  float* ckpt;      // MODE_CKPT: [B][D][nseg][16], the state before every segment
+  int64_t nseg;
 };
 
 struct ScanMaps {

@@ -44,6 +44,10 @@
 // h_in[c] + h_end[c] (the associative combine of "docs.ifdog.com", section
 // "Hardware-aware parallel scan", applied to whole chunks); (3) MODE_OUTPUT
 // rescans each chunk from its true initial state and emits y.
+//
+// MODE_CKPT serves the backward pass: one pass from h0 that writes the state
+// before every SSM_BWD_SEGMENT-th step to a checkpoint array and emits nothing
+// else.
 #include <cstdio>
 #include <cstring>
 #include <type_traits>
@@ -142,7 +146,7 @@ __global__ void __launch_bounds__(32 * K, min_blocks(K, NS))
     float a = 0.f, hv = 0.f;
     if (valid && n < N) {
       a = p.A[d * p.sA0 + n * p.sA1] * kLog2e;
-      if (MODE == MODE_OUTPUT) {
+      if (MODE == MODE_OUTPUT || MODE == MODE_CKPT) {
         if (chunk == 0) {
           if (p.h0) hv = p.h0[b * p.sh00 + d * p.sh01 + n * p.sh02];
         } else {
@@ -320,6 +324,15 @@ __global__ void __launch_bounds__(32 * K, min_blocks(K, NS))
         const float4 dd = dt4[t / 2];
 #pragma unroll
         for (int s = 0; s < 2; ++s) {
+          if (MODE == MODE_CKPT && (t + s) % SSM_BWD_SEGMENT == 0) {   // the state before this step
+            const int64_t tg = t_begin + (int64_t)k * T + t + s;
+            if (valid && tg < p.L) {
+              float4* dst = reinterpret_cast<float4*>(p.ckpt + ((b * p.D + d) * p.nseg + tg / SSM_BWD_SEGMENT) * 16 + g * NS);
+#pragma unroll
+              for (int q = 0; q < NS / 4; ++q)
+                dst[q] = make_float4(h[2 * q].x, h[2 * q].y, h[2 * q + 1].x, h[2 * q + 1].y);
+            }
+          }
           const float dt = s ? dd.z : dd.x;
           const float du = s ? dd.w : dd.y;
           const float* Bt = bcg + (t + s) * 2 * NP;
@@ -388,7 +401,7 @@ __global__ void __launch_bounds__(32 * K, min_blocks(K, NS))
         if (n < N) p.h_last[b * p.shl0 + d * p.shl1 + n * p.shl2] = (i & 1) ? h[i / 2].y : h[i / 2].x;
       }
     }
-  } else {
+  } else if (MODE == MODE_RECORD) {
     if (valid) {
       const int64_t r = (b * p.D + d) * p.nchunks + chunk;
 #pragma unroll
@@ -437,6 +450,17 @@ cudaError_t launch_shape(const ScanProblem& p, const ScanPlan& plan, ScanKernelP
 }
 
 template <typename IO, bool PRECISE>
+cudaError_t launch_ckpt_typed(const ScanPlan& plan, const ScanKernelParams& tp, const ScanMaps& tm,
+                              const ScanProblem& p, cudaStream_t s) {
+  const dim3 grid((unsigned)((p.D + CH - 1) / CH), 1, (unsigned)p.B);
+  const int K = plan.shape.K, NS = plan.shape.NS;
+  if (K == 1 && NS == 16) return launch_one<IO, 1, 16, MODE_CKPT, PRECISE>(tp, tm, grid, s);
+  if (K == 2 && NS == 8) return launch_one<IO, 2, 8, MODE_CKPT, PRECISE>(tp, tm, grid, s);
+  if (K == 4 && NS == 4) return launch_one<IO, 4, 4, MODE_CKPT, PRECISE>(tp, tm, grid, s);
+  return cudaErrorInvalidValue;
+}
+
+template <typename IO, bool PRECISE>
 cudaError_t launch_typed(const ScanProblem& p, const ScanPlan& plan, ScanKernelParams& tp, const ScanMaps& tm,
                          cudaStream_t s) {
   const int K = plan.shape.K, NS = plan.shape.NS;
@@ -457,6 +481,17 @@ cudaError_t launch_scan_tiled(const ScanProblem& p, const ScanPlan& plan, void* 
     return cudaErrorInvalidValue;
   if (p.io == SSM_F32) return launch_typed<float, true>(p, plan, tp, tm, s);
   return launch_typed<__nv_bfloat16, false>(p, plan, tp, tm, s);
+}
+
+cudaError_t launch_scan_ckpt(const ScanProblem& p, const ScanPlan& plan, float* ckpt, int64_t nseg, cudaStream_t s) {
+  if (plan.nchunks != 1 || plan.shape.K * plan.shape.NS != 16) return cudaErrorInvalidValue;
+  ScanKernelParams tp;
+  ScanMaps tm;
+  if (!make_scan_kernel_args(p, plan, nullptr, 16, T, &tp, &tm)) return cudaErrorInvalidValue;
+  tp.ckpt = ckpt;
+  tp.nseg = nseg;
+  if (p.io == SSM_F32) return launch_ckpt_typed<float, true>(plan, tp, tm, p, s);
+  return launch_ckpt_typed<__nv_bfloat16, false>(plan, tp, tm, p, s);
 }
 
 size_t tiled_smem_bytes(ssm_dtype_t io, int K, int NS) {

@@ -577,7 +577,23 @@ ssm_status_t ssm_scan_bwd(const ssm_scan_bwd_args_t* args, void* stream) {
     if (!aligned(args->fwd.workspace, 16)) return fail(SSM_ERR_WORKSPACE, "workspace not 16-byte aligned");
   }
   p.ckpt = static_cast<float*>(args->fwd.workspace);
-  cudaError_t e = launch_scan_bwd(p, device_sm_count(), static_cast<cudaStream_t>(stream));
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // the checkpoints come from the tiled forward kernel when the layout allows it (one pass, from h0)
+  p.sweep = 1;
+  if (p.f.L > 0 && tiled_eligible(p.f) && !getenv("SSM_BWD_SWEEP")) {
+    ssm_scan_args_t fa = args->fwd;
+    fa.y = const_cast<void*>(args->dy);
+    std::memcpy(fa.stride_y, args->stride_dy, sizeof(fa.stride_y));
+    fa.h_last = nullptr;
+    fa.flags = SSM_SCAN_FORCE_TILED;
+    ScanPlan plan;
+    if (plan_scan(&fa, p.f, &plan) == SSM_OK && plan.path == kPathTiled && plan.shape.K * plan.shape.NS == 16) {
+      cudaError_t e = launch_scan_ckpt(p.f, plan, p.ckpt, p.nseg, s);
+      if (e != cudaSuccess) return cuda_fail(e);
+      p.sweep = 0;
+    }
+  }
+  cudaError_t e = launch_scan_bwd(p, device_sm_count(), s);
   if (e != cudaSuccess) return cuda_fail(e);
   return ok();
 }

@@ -45,6 +45,7 @@ struct BwdProblem {
   int64_t bc_rows;     // rows of dB / dC: 1 when B / C are shared across the batch
   int64_t nseg;        // checkpoints per channel
   float* ckpt;         // [B][D][nseg][16] fp32
+  int sweep;           // 1: the backward kernel writes the checkpoints itself; 0: they are already there
 };
 
 struct ConvProblem {
@@ -85,6 +86,7 @@ cudaError_t launch_scan_tiled(const ScanProblem& p, const ScanPlan& plan, void* 
 cudaError_t launch_state_update(const StepProblem& p, cudaStream_t s);
 cudaError_t launch_causal_conv1d(const ConvProblem& p, int sms, cudaStream_t s);
 cudaError_t launch_scan_bwd(const BwdProblem& p, int sms, cudaStream_t s);
+cudaError_t launch_scan_ckpt(const ScanProblem& p, const ScanPlan& plan, float* ckpt, int64_t nseg, cudaStream_t s);
 
 // tile length of the tiled kernel (timesteps)
 #ifndef SSM_TILE_T
