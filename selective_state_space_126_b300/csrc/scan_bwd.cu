@@ -12,17 +12,20 @@
 // the state every SEG steps, and the reverse sweep recomputes each SEG-step
 // segment from its checkpoint before running the adjoint through it.
 //
-// Design: one warp per CTA covers 32 channels of one batch row, one channel per
-// lane, all (up to 16) states of a channel in that lane's registers.
+// Design: one warp per CTA covers 16 channels of one batch row, two lanes per
+// channel (8 states each, as f32x2 pairs), so that twice as many warps share
+// the work; the sums over a channel's states take one shuffle between its two
+// lanes.  A segment's inputs of a channel arrive as one 128-bit load per
+// tensor when the rows allow it.
 //   * B_t and C_t of a segment are staged in shared memory by the lanes and
 //     read as warp-wide broadcasts;
 //   * the recomputed states of a segment go to shared memory, laid out
 //     [step][4 states][lane] as 16-byte pieces so that every access is
 //     conflict-free;
 //   * dB_t[n] and dC_t[n] are sums over the channels: per step each lane
-//     writes its 32 contributions to a row of a shared 32 x 32 block, every
-//     lane then sums one column, and one atomic add per (t, n) per warp goes
-//     to global memory;
+//     writes its 16 contributions to its channel's row of a shared 16 x 32
+//     block, every lane then sums one column, and one atomic add per (t, n)
+//     per warp goes to global memory;
 //   * dA, dD and the Delta-bias gradient accumulate in registers over the
 //     whole sequence and are added atomically at the end (several batch rows
 //     share a channel).
@@ -35,7 +38,6 @@ namespace ssm {
 namespace {
 
 constexpr int SEG = SSM_BWD_SEGMENT;   // steps per checkpoint
-constexpr int NPL = 16;                // states per lane
 constexpr float kLn2 = 0.69314718055994531f;
 
 template <bool PRECISE>
@@ -79,33 +81,74 @@ __global__ void __launch_bounds__(256) bwd_zero_kernel(const BwdProblem p) {
   }
 }
 
+// SEG steps of one row starting at `ptr` (time stride 1) as fp32: one or two
+// 128-bit loads when the row is 16-byte aligned and the segment is whole,
+// element loads otherwise.
+template <typename IO>
+__device__ __forceinline__ void load_seg(const void* base, int64_t off, bool vec, int steps, float (&out)[SEG]) {
+  const IO* ptr = static_cast<const IO*>(base) + off;
+  if (vec) {
+    if (sizeof(IO) == 2) {
+      float f[8];
+      unpack16(ldg_nc_v4(ptr), f);
+#pragma unroll
+      for (int t = 0; t < SEG; ++t) out[t] = f[t];
+    } else {
+      float f0[4], f1[4];
+      unpack16(ldg_nc_v4(ptr), f0);
+      unpack16(ldg_nc_v4(ptr + 4), f1);
+#pragma unroll
+      for (int t = 0; t < 4; ++t) { out[t] = f0[t]; out[t + 4] = f1[t]; }
+    }
+  } else {
+#pragma unroll
+    for (int t = 0; t < SEG; ++t) out[t] = t < steps ? to_f32(ptr[t]) : 0.f;
+  }
+}
+
+__device__ __forceinline__ float2 f2(float v) { return make_float2(v, v); }
+
+// One warp per CTA: 16 channels of one batch row, two lanes per channel
+// (lanes c and c + 16), each lane holding 8 of the channel's states as four
+// f32x2 pairs.  Sums over the states (the C contraction, dDelta, du) take one
+// shuffle between the two lanes of a channel.
 template <typename IO, bool PRECISE>
 __global__ void __launch_bounds__(32) scan_bwd_kernel(const BwdProblem p) {
-  __shared__ float4 hist[(SEG + 1) * 4 * 32];   // [row][state quad][lane]; row 0 = state before the segment
-  __shared__ float bcs[SEG][32];                // [t][B_t[0..15] | C_t[0..15]]
-  __shared__ __align__(16) float red[32][36];   // per-step transpose block for the channel sums (16-byte rows)
+  constexpr int CHW = 16;                            // channels per warp
+  __shared__ float4 hist[(SEG + 1) * 2 * 32];        // [row][half of the lane's 8 states][lane]
+  __shared__ __align__(16) float bcs[SEG][32];       // [t][B_t[0..15] | C_t[0..15]]
+  __shared__ __align__(16) float red[CHW][36];       // [channel][dB_t[0..15] | dC_t[0..15]]
   const ScanProblem& f = p.f;
   const int lane = threadIdx.x;
+  const int ch = lane & 15, g = lane >> 4;           // channel within the warp, half of its states
   const int64_t b = blockIdx.y;
-  const int64_t d = (int64_t)blockIdx.x * 32 + lane;
+  const int64_t d = (int64_t)blockIdx.x * CHW + ch;
   const bool valid = d < f.D;
+  const bool lead = g == 0;                          // writes the channel's per-step outputs
   const int N = (int)f.N;
   const int64_t L = f.L;
   const int64_t c = b * f.D + (valid ? d : 0);
 
-  float A2[NPL], h[NPL];
+  float2 A2[4], h[4];
 #pragma unroll
-  for (int n = 0; n < NPL; ++n) {
-    A2[n] = (valid && n < N) ? f.A[d * f.sA[0] + n * f.sA[1]] * kLog2e : 0.f;
-    h[n] = (valid && n < N && f.h0) ? f.h0[b * f.sh0[0] + d * f.sh0[1] + n * f.sh0[2]] : 0.f;
+  for (int q = 0; q < 4; ++q) {
+    float av[2], hv[2];
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const int n = g * 8 + 2 * q + e;
+      av[e] = (valid && n < N) ? f.A[d * f.sA[0] + n * f.sA[1]] * kLog2e : 0.f;
+      hv[e] = (valid && n < N && f.h0) ? f.h0[b * f.sh0[0] + d * f.sh0[1] + n * f.sh0[2]] : 0.f;
+    }
+    A2[q] = make_float2(av[0], av[1]);
+    h[q] = make_float2(hv[0], hv[1]);
   }
   const float bias = (valid && f.bias) ? f.bias[d] : 0.f;
   const float Dd = (valid && f.Dskip) ? f.Dskip[d] : 0.f;
   const int64_t ou = b * f.su[0] + d * f.su[1], odl = b * f.sd[0] + d * f.sd[1], oz = b * f.sz[0] + d * f.sz[1];
   const int64_t ody = b * p.sdy[0] + d * p.sdy[1];
-  float4* ck = reinterpret_cast<float4*>(p.ckpt + c * p.nseg * NPL);
+  // this lane's half of each 16-float checkpoint record
+  float4* ck = reinterpret_cast<float4*>(p.ckpt + c * p.nseg * 16 + g * 8);
 
-  // B_t and C_t of segment `seg` into shared memory (lane j: row j % 16 of B for j < 16, of C otherwise)
   auto stage_bc = [&](int64_t seg) {
     __syncwarp();
     const int n = lane & 15;
@@ -117,14 +160,19 @@ __global__ void __launch_bounds__(32) scan_bwd_kernel(const BwdProblem p) {
       bcs[t][lane] = (n < N && t0 + t < L) ? ld<IO>(base, b * sb[0] + n * sb[1] + t0 + t) : 0.f;
     __syncwarp();
   };
+  auto bpair = [&](int t, int q) { return *reinterpret_cast<const float2*>(&bcs[t][g * 8 + 2 * q]); };
+  auto cpair = [&](int t, int q) { return *reinterpret_cast<const float2*>(&bcs[t][16 + g * 8 + 2 * q]); };
+  auto abar = [&](float dt, int q) {
+    const float2 x = __fmul2_rn(f2(dt), A2[q]);
+    return make_float2(ex2_approx(x.x), ex2_approx(x.y));
+  };
 
-  // ---- forward sweep: a checkpoint of the state before every segment (unless the
-  // tiled forward kernel has written them already) ----
+  // ---- forward sweep: the checkpoints, unless the tiled forward kernel wrote them ----
   for (int64_t seg = 0; p.sweep && seg < p.nseg; ++seg) {
     stage_bc(seg);
     if (valid) {
-#pragma unroll
-      for (int q = 0; q < 4; ++q) ck[seg * 4 + q] = make_float4(h[4 * q], h[4 * q + 1], h[4 * q + 2], h[4 * q + 3]);
+      ck[seg * 4] = make_float4(h[0].x, h[0].y, h[1].x, h[1].y);
+      ck[seg * 4 + 1] = make_float4(h[2].x, h[2].y, h[3].x, h[3].y);
     }
     const int64_t t0 = seg * SEG;
 #pragma unroll
@@ -133,64 +181,75 @@ __global__ void __launch_bounds__(32) scan_bwd_kernel(const BwdProblem p) {
       const float dt = valid ? delta_of<PRECISE>(ld<IO>(f.delta, odl + t0 + t), bias, f.softplus) : 0.f;
       const float du = valid ? dt * ld<IO>(f.u, ou + t0 + t) : 0.f;
 #pragma unroll
-      for (int n = 0; n < NPL; ++n) h[n] = fmaf(ex2_approx(dt * A2[n]), h[n], du * bcs[t][n]);
+      for (int q = 0; q < 4; ++q) h[q] = __ffma2_rn(abar(dt, q), h[q], __fmul2_rn(f2(du), bpair(t, q)));
     }
   }
 
   // ---- reverse sweep ----
-  float lam[NPL], dA[NPL];
+  float2 lam[4], dA[4];
 #pragma unroll
-  for (int n = 0; n < NPL; ++n) {
-    lam[n] = (valid && n < N && p.dhl) ? p.dhl[b * p.sdhl[0] + d * p.sdhl[1] + n * p.sdhl[2]] : 0.f;
-    dA[n] = 0.f;
+  for (int q = 0; q < 4; ++q) {
+    float lv[2];
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const int n = g * 8 + 2 * q + e;
+      lv[e] = (valid && n < N && p.dhl) ? p.dhl[b * p.sdhl[0] + d * p.sdhl[1] + n * p.sdhl[2]] : 0.f;
+    }
+    lam[q] = make_float2(lv[0], lv[1]);
+    dA[q] = make_float2(0.f, 0.f);
   }
   float dD = 0.f, dbias = 0.f;
   for (int64_t seg = p.nseg - 1; seg >= 0; --seg) {
     stage_bc(seg);
     const int64_t t0 = seg * SEG;
     const int steps = L - t0 < SEG ? (int)(L - t0) : SEG;
-    // recompute the segment's states from its checkpoint
     if (valid) {
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const float4 v = ck[seg * 4 + q];
-        h[4 * q] = v.x; h[4 * q + 1] = v.y; h[4 * q + 2] = v.z; h[4 * q + 3] = v.w;
-      }
+      const float4 v0 = ck[seg * 4], v1 = ck[seg * 4 + 1];
+      h[0] = make_float2(v0.x, v0.y); h[1] = make_float2(v0.z, v0.w);
+      h[2] = make_float2(v1.x, v1.y); h[3] = make_float2(v1.z, v1.w);
     }
-#pragma unroll
-    for (int q = 0; q < 4; ++q) hist[q * 32 + lane] = make_float4(h[4 * q], h[4 * q + 1], h[4 * q + 2], h[4 * q + 3]);
-    float dts[SEG], us[SEG], yts[SEG], ss[SEG];
+    hist[lane] = make_float4(h[0].x, h[0].y, h[1].x, h[1].y);
+    hist[32 + lane] = make_float4(h[2].x, h[2].y, h[3].x, h[3].y);
+    // the segment's inputs of this channel
+    float us[SEG], ss[SEG], zs[SEG], dys[SEG];
+    const bool vec = valid && p.vec && steps == SEG;
+    if (valid) {
+      load_seg<IO>(f.u, ou + t0, vec, steps, us);
+      load_seg<IO>(f.delta, odl + t0, vec, steps, ss);
+      load_seg<IO>(p.dy, ody + t0, vec, steps, dys);
+      if (f.z) load_seg<IO>(f.z, oz + t0, vec, steps, zs);
+    }
+    float dts[SEG], yts[SEG];
+    // recompute the segment's states from its checkpoint
 #pragma unroll
     for (int t = 0; t < SEG; ++t) {
-      dts[t] = 0.f; us[t] = 0.f; yts[t] = 0.f; ss[t] = 0.f;
+      dts[t] = 0.f; yts[t] = 0.f;
       if (t >= steps) continue;
-      const int64_t tg = t0 + t;
-      float uv = 0.f, s = 0.f, dyv = 0.f, zv = 0.f;
-      if (valid) {
-        uv = ld<IO>(f.u, ou + tg);
-        s = ld<IO>(f.delta, odl + tg) + bias;
-        dyv = ld<IO>(p.dy, ody + tg);
-        if (f.z) zv = ld<IO>(f.z, oz + tg);
-      }
+      const float uv = valid ? us[t] : 0.f;
+      const float s = valid ? ss[t] + bias : 0.f;
+      ss[t] = s;
       const float dt = valid ? (f.softplus ? softplus<PRECISE>(s) : s) : 0.f;
       const float du = dt * uv;
-      float acc = 0.f;
+      float2 acc = make_float2(0.f, 0.f);
 #pragma unroll
-      for (int n = 0; n < NPL; ++n) {
-        h[n] = fmaf(ex2_approx(dt * A2[n]), h[n], du * bcs[t][n]);
-        acc = fmaf(bcs[t][16 + n], h[n], acc);
+      for (int q = 0; q < 4; ++q) {
+        h[q] = __ffma2_rn(abar(dt, q), h[q], __fmul2_rn(f2(du), bpair(t, q)));
+        acc = __ffma2_rn(cpair(t, q), h[q], acc);
       }
-#pragma unroll
-      for (int q = 0; q < 4; ++q)
-        hist[((t + 1) * 4 + q) * 32 + lane] = make_float4(h[4 * q], h[4 * q + 1], h[4 * q + 2], h[4 * q + 3]);
+      hist[((t + 1) * 2) * 32 + lane] = make_float4(h[0].x, h[0].y, h[1].x, h[1].y);
+      hist[((t + 1) * 2 + 1) * 32 + lane] = make_float4(h[2].x, h[2].y, h[3].x, h[3].y);
+      float part = acc.x + acc.y;
+      part += __shfl_xor_sync(0xffffffffu, part, 16);   // the other half of the channel's states
+      const float dyv = valid ? dys[t] : 0.f;
       float yt = dyv;
       if (f.z) {
-        const float pre = fmaf(Dd, uv, acc);
+        const float zv = valid ? zs[t] : 0.f;
         const float sg = sigmoid_f<PRECISE>(zv);
         yt = dyv * zv * sg;
-        if (valid) st<IO>(p.dz, b * p.sdz[0] + d * p.sdz[1] + tg, dyv * pre * sg * fmaf(zv, 1.f - sg, 1.f));
+        if (valid && lead)
+          st<IO>(p.dz, b * p.sdz[0] + d * p.sdz[1] + t0 + t, dyv * fmaf(Dd, uv, part) * sg * fmaf(zv, 1.f - sg, 1.f));
       }
-      dts[t] = dt; us[t] = uv; yts[t] = yt; ss[t] = s;
+      dts[t] = dt; yts[t] = yt;
     }
     __syncwarp();
     // the adjoint through the segment, last step first
@@ -198,48 +257,48 @@ __global__ void __launch_bounds__(32) scan_bwd_kernel(const BwdProblem p) {
     for (int t = SEG - 1; t >= 0; --t) {
       if (t >= steps) continue;
       const int64_t tg = t0 + t;
-      const float dt = dts[t], uv = us[t], yt = yts[t], du = dt * uv;
-      float sq = 0.f, sb = 0.f;
-      float vb[NPL], vc[NPL];
+      const float dt = dts[t], yt = yts[t];
+      const float uv = valid ? us[t] : 0.f;
+      const float du = dt * uv;
+      const float4 hp0 = hist[(t * 2) * 32 + lane], hp1 = hist[(t * 2 + 1) * 32 + lane];
+      const float4 ht0 = hist[((t + 1) * 2) * 32 + lane], ht1 = hist[((t + 1) * 2 + 1) * 32 + lane];
+      const float2 hp[4] = {make_float2(hp0.x, hp0.y), make_float2(hp0.z, hp0.w), make_float2(hp1.x, hp1.y),
+                            make_float2(hp1.z, hp1.w)};
+      const float2 ht[4] = {make_float2(ht0.x, ht0.y), make_float2(ht0.z, ht0.w), make_float2(ht1.x, ht1.y),
+                            make_float2(ht1.z, ht1.w)};
+      float2 sq = make_float2(0.f, 0.f), sb = make_float2(0.f, 0.f), vb[4], vc[4];
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
-        const float4 hp4 = hist[(t * 4 + q) * 32 + lane];
-        const float4 ht4 = hist[((t + 1) * 4 + q) * 32 + lane];
-        const float hp[4] = {hp4.x, hp4.y, hp4.z, hp4.w};
-        const float ht[4] = {ht4.x, ht4.y, ht4.z, ht4.w};
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int n = 4 * q + i;
-          const float l = fmaf(yt, bcs[t][16 + n], lam[n]);   // lambda_t[n]
-          const float a = ex2_approx(dt * A2[n]);
-          const float qv = l * hp[i] * a;
-          dA[n] = fmaf(qv, dt, dA[n]);
-          sq = fmaf(qv, A2[n], sq);
-          sb = fmaf(l, bcs[t][n], sb);
-          vb[n] = l * du;
-          vc[n] = yt * ht[i];
-          lam[n] = l * a;
-        }
+        const float2 l = __ffma2_rn(f2(yt), cpair(t, q), lam[q]);   // lambda_t
+        const float2 a = abar(dt, q);
+        const float2 qv = __fmul2_rn(__fmul2_rn(l, hp[q]), a);
+        dA[q] = __ffma2_rn(qv, f2(dt), dA[q]);
+        sq = __ffma2_rn(qv, A2[q], sq);
+        sb = __ffma2_rn(l, bpair(t, q), sb);
+        vb[q] = __fmul2_rn(l, f2(du));
+        vc[q] = __fmul2_rn(f2(yt), ht[q]);
+        lam[q] = __fmul2_rn(l, a);
       }
-      if (valid) {
-        const float dDelta = fmaf(sq, kLn2, sb * uv);
-        st<IO>(p.du, b * p.sdu[0] + d * p.sdu[1] + tg, fmaf(sb, dt, yt * Dd));
+      float sqs = sq.x + sq.y, sbs = sb.x + sb.y;
+      sqs += __shfl_xor_sync(0xffffffffu, sqs, 16);
+      sbs += __shfl_xor_sync(0xffffffffu, sbs, 16);
+      if (valid && lead) {
+        const float dDelta = fmaf(sqs, kLn2, sbs * uv);
+        st<IO>(p.du, b * p.sdu[0] + d * p.sdu[1] + tg, fmaf(sbs, dt, yt * Dd));
         const float dd = f.softplus ? dDelta * sigmoid_f<PRECISE>(ss[t]) : dDelta;
         st<IO>(p.ddelta, b * p.sdd[0] + d * p.sdd[1] + tg, dd);
         dbias += dd;
         dD = fmaf(yt, uv, dD);
       }
-      // channel sums of dB_t[n], dC_t[n]: transpose through shared memory
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        *reinterpret_cast<float4*>(&red[lane][4 * q]) = make_float4(vb[4 * q], vb[4 * q + 1], vb[4 * q + 2], vb[4 * q + 3]);
-        *reinterpret_cast<float4*>(&red[lane][16 + 4 * q]) =
-            make_float4(vc[4 * q], vc[4 * q + 1], vc[4 * q + 2], vc[4 * q + 3]);
-      }
+      // channel sums of dB_t[n] and dC_t[n]: transpose through shared memory
+      *reinterpret_cast<float4*>(&red[ch][g * 8]) = make_float4(vb[0].x, vb[0].y, vb[1].x, vb[1].y);
+      *reinterpret_cast<float4*>(&red[ch][g * 8 + 4]) = make_float4(vb[2].x, vb[2].y, vb[3].x, vb[3].y);
+      *reinterpret_cast<float4*>(&red[ch][16 + g * 8]) = make_float4(vc[0].x, vc[0].y, vc[1].x, vc[1].y);
+      *reinterpret_cast<float4*>(&red[ch][16 + g * 8 + 4]) = make_float4(vc[2].x, vc[2].y, vc[3].x, vc[3].y);
       __syncwarp();
       float sum = 0.f;
 #pragma unroll
-      for (int r = 0; r < 32; ++r) sum += red[r][lane];
+      for (int r = 0; r < CHW; ++r) sum += red[r][lane];
       __syncwarp();
       const int n = lane & 15;
       if (n < N) {
@@ -251,13 +310,19 @@ __global__ void __launch_bounds__(32) scan_bwd_kernel(const BwdProblem p) {
   if (!valid) return;
   // ---- the summed parameter gradients and dh0 ----
 #pragma unroll
-  for (int n = 0; n < NPL; ++n) {
-    if (n >= N) break;
-    atomicAdd(p.dA + d * N + n, dA[n]);
-    if (p.dh0) p.dh0[b * p.sdh0[0] + d * p.sdh0[1] + n * p.sdh0[2]] = lam[n];
+  for (int q = 0; q < 4; ++q) {
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const int n = g * 8 + 2 * q + e;
+      if (n >= N) continue;
+      atomicAdd(p.dA + d * N + n, e ? dA[q].y : dA[q].x);
+      if (p.dh0) p.dh0[b * p.sdh0[0] + d * p.sdh0[1] + n * p.sdh0[2]] = e ? lam[q].y : lam[q].x;
+    }
   }
-  if (p.dD) atomicAdd(p.dD + d, dD);
-  if (p.dbias) atomicAdd(p.dbias + d, dbias);
+  if (lead) {
+    if (p.dD) atomicAdd(p.dD + d, dD);
+    if (p.dbias) atomicAdd(p.dbias + d, dbias);
+  }
 }
 
 template <typename IO, bool PRECISE>
@@ -267,7 +332,7 @@ cudaError_t launch_typed(const BwdProblem& p, int sms, cudaStream_t s) {
   bwd_zero_kernel<<<zb, 256, 0, s>>>(p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  const dim3 grid((unsigned)((p.f.D + 31) / 32), (unsigned)p.f.B);
+  const dim3 grid((unsigned)((p.f.D + 15) / 16), (unsigned)p.f.B);
   scan_bwd_kernel<IO, PRECISE><<<grid, 32, 0, s>>>(p);
   return cudaGetLastError();
 }

@@ -578,6 +578,17 @@ ssm_status_t ssm_scan_bwd(const ssm_scan_bwd_args_t* args, void* stream) {
   }
   p.ckpt = static_cast<float*>(args->fwd.workspace);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  {
+    const int es = elem_size(p.f.io);
+    auto rows16 = [&](const void* ptr, const int64_t* st) {
+      if (!ptr) return true;
+      if (!aligned(ptr, 16)) return false;
+      if (p.f.D > 1 && (st[1] * es) % 16) return false;
+      if (p.f.B > 1 && (st[0] * es) % 16) return false;
+      return true;
+    };
+    p.vec = rows16(p.f.u, p.f.su) && rows16(p.f.delta, p.f.sd) && rows16(p.f.z, p.f.sz) && rows16(p.dy, p.sdy) ? 1 : 0;
+  }
   // the checkpoints come from the tiled forward kernel when the layout allows it (one pass, from h0)
   p.sweep = 1;
   if (p.f.L > 0 && tiled_eligible(p.f) && !getenv("SSM_BWD_SWEEP")) {

@@ -46,6 +46,7 @@ struct BwdProblem {
   int64_t nseg;        // checkpoints per channel
   float* ckpt;         // [B][D][nseg][16] fp32
   int sweep;           // 1: the backward kernel writes the checkpoints itself; 0: they are already there
+  int vec;             // u, delta, z, dy rows start on 16-byte boundaries (128-bit segment loads)
 };
 
 struct ConvProblem {
