@@ -155,9 +155,16 @@ __global__ void __launch_bounds__(32) scan_bwd_kernel(const BwdProblem p) {
     const void* base = lane < 16 ? f.Bm : f.Cm;
     const int64_t* sb = lane < 16 ? f.sB : f.sC;
     const int64_t t0 = seg * SEG;
+    const int steps = L - t0 < SEG ? (int)(L - t0) : SEG;
+    float v[SEG];
+    if (n < N) {
+      load_seg<IO>(base, b * sb[0] + n * sb[1] + t0, p.vecbc && steps == SEG, steps, v);
+    } else {
 #pragma unroll
-    for (int t = 0; t < SEG; ++t)
-      bcs[t][lane] = (n < N && t0 + t < L) ? ld<IO>(base, b * sb[0] + n * sb[1] + t0 + t) : 0.f;
+      for (int t = 0; t < SEG; ++t) v[t] = 0.f;
+    }
+#pragma unroll
+    for (int t = 0; t < SEG; ++t) bcs[t][lane] = v[t];
     __syncwarp();
   };
   auto bpair = [&](int t, int q) { return *reinterpret_cast<const float2*>(&bcs[t][g * 8 + 2 * q]); };
@@ -252,16 +259,17 @@ __global__ void __launch_bounds__(32) scan_bwd_kernel(const BwdProblem p) {
       dts[t] = dt; yts[t] = yt;
     }
     __syncwarp();
-    // the adjoint through the segment, last step first
+    // the adjoint through the segment, last step first; h_t of a step is h_{t-1} of the one after
+    // it, so each step reads one state from shared memory
+    float4 ht0 = make_float4(h[0].x, h[0].y, h[1].x, h[1].y), ht1 = make_float4(h[2].x, h[2].y, h[3].x, h[3].y);
 #pragma unroll
     for (int t = SEG - 1; t >= 0; --t) {
-      if (t >= steps) continue;
+      if (t >= steps) continue;   // (the first step taken is steps-1, whose h_t is the recompute's last h)
       const int64_t tg = t0 + t;
       const float dt = dts[t], yt = yts[t];
       const float uv = valid ? us[t] : 0.f;
       const float du = dt * uv;
       const float4 hp0 = hist[(t * 2) * 32 + lane], hp1 = hist[(t * 2 + 1) * 32 + lane];
-      const float4 ht0 = hist[((t + 1) * 2) * 32 + lane], ht1 = hist[((t + 1) * 2 + 1) * 32 + lane];
       const float2 hp[4] = {make_float2(hp0.x, hp0.y), make_float2(hp0.z, hp0.w), make_float2(hp1.x, hp1.y),
                             make_float2(hp1.z, hp1.w)};
       const float2 ht[4] = {make_float2(ht0.x, ht0.y), make_float2(ht0.z, ht0.w), make_float2(ht1.x, ht1.y),
@@ -279,6 +287,8 @@ __global__ void __launch_bounds__(32) scan_bwd_kernel(const BwdProblem p) {
         vc[q] = __fmul2_rn(f2(yt), ht[q]);
         lam[q] = __fmul2_rn(l, a);
       }
+      ht0 = hp0;
+      ht1 = hp1;
       float sqs = sq.x + sq.y, sbs = sb.x + sb.y;
       sqs += __shfl_xor_sync(0xffffffffu, sqs, 16);
       sbs += __shfl_xor_sync(0xffffffffu, sbs, 16);

@@ -588,6 +588,13 @@ ssm_status_t ssm_scan_bwd(const ssm_scan_bwd_args_t* args, void* stream) {
       return true;
     };
     p.vec = rows16(p.f.u, p.f.su) && rows16(p.f.delta, p.f.sd) && rows16(p.f.z, p.f.sz) && rows16(p.dy, p.sdy) ? 1 : 0;
+    auto bc16 = [&](const void* ptr, const int64_t* st) {   // rows n of B / C: batch stride 0 allowed
+      if (!aligned(ptr, 16)) return false;
+      if (p.f.N > 1 && (st[1] * es) % 16) return false;
+      if (p.f.B > 1 && (st[0] * es) % 16) return false;
+      return true;
+    };
+    p.vecbc = bc16(p.f.Bm, p.f.sB) && bc16(p.f.Cm, p.f.sC) ? 1 : 0;
   }
   // the checkpoints come from the tiled forward kernel when the layout allows it (one pass, from h0)
   p.sweep = 1;

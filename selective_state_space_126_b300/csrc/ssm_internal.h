@@ -47,6 +47,7 @@ struct BwdProblem {
   float* ckpt;         // [B][D][nseg][16] fp32
   int sweep;           // 1: the backward kernel writes the checkpoints itself; 0: they are already there
   int vec;             // u, delta, z, dy rows start on 16-byte boundaries (128-bit segment loads)
+  int vecbc;           // the same for the rows of B and C
 };
 
 struct ConvProblem {
