@@ -106,6 +106,22 @@ __device__ __forceinline__ void load_seg(const void* base, int64_t off, bool vec
   }
 }
 
+// The inverse of load_seg: SEG values to a 16-byte aligned row piece.
+template <typename IO>
+__device__ __forceinline__ void store_seg(void* base, int64_t off, const float (&v)[SEG]) {
+  IO* ptr = static_cast<IO*>(base) + off;
+  if (sizeof(IO) == 2) {
+    float f[8];
+#pragma unroll
+    for (int t = 0; t < 8; ++t) f[t] = v[t];
+    stg_v4(ptr, pack16(f));
+  } else {
+    float f0[4] = {v[0], v[1], v[2], v[3]}, f1[4] = {v[4], v[5], v[6], v[7]};
+    stg_v4(ptr, pack16(f0));
+    stg_v4(ptr + 4, pack16(f1));
+  }
+}
+
 __device__ __forceinline__ float2 f2(float v) { return make_float2(v, v); }
 
 // One warp per CTA: 16 channels of one batch row, two lanes per channel
@@ -227,6 +243,7 @@ __global__ void __launch_bounds__(32) scan_bwd_kernel(const BwdProblem p) {
       if (f.z) load_seg<IO>(f.z, oz + t0, vec, steps, zs);
     }
     float dts[SEG], yts[SEG];
+    float dzo[SEG], duo[SEG], ddo[SEG], sums[SEG];   // the segment's outputs, written once it is done
     // recompute the segment's states from its checkpoint
 #pragma unroll
     for (int t = 0; t < SEG; ++t) {
@@ -254,7 +271,7 @@ __global__ void __launch_bounds__(32) scan_bwd_kernel(const BwdProblem p) {
         const float sg = sigmoid_f<PRECISE>(zv);
         yt = dyv * zv * sg;
         if (valid && lead)
-          st<IO>(p.dz, b * p.sdz[0] + d * p.sdz[1] + t0 + t, dyv * fmaf(Dd, uv, part) * sg * fmaf(zv, 1.f - sg, 1.f));
+          dzo[t] = dyv * fmaf(Dd, uv, part) * sg * fmaf(zv, 1.f - sg, 1.f);
       }
       dts[t] = dt; yts[t] = yt;
     }
@@ -294,9 +311,9 @@ __global__ void __launch_bounds__(32) scan_bwd_kernel(const BwdProblem p) {
       sbs += __shfl_xor_sync(0xffffffffu, sbs, 16);
       if (valid && lead) {
         const float dDelta = fmaf(sqs, kLn2, sbs * uv);
-        st<IO>(p.du, b * p.sdu[0] + d * p.sdu[1] + tg, fmaf(sbs, dt, yt * Dd));
+        duo[t] = fmaf(sbs, dt, yt * Dd);
         const float dd = f.softplus ? dDelta * sigmoid_f<PRECISE>(ss[t]) : dDelta;
-        st<IO>(p.ddelta, b * p.sdd[0] + d * p.sdd[1] + tg, dd);
+        ddo[t] = dd;
         dbias += dd;
         dD = fmaf(yt, uv, dD);
       }
@@ -310,10 +327,44 @@ __global__ void __launch_bounds__(32) scan_bwd_kernel(const BwdProblem p) {
 #pragma unroll
       for (int r = 0; r < CHW; ++r) sum += red[r][lane];
       __syncwarp();
+      sums[t] = sum;
+      (void)tg;
+    }
+    // the segment's outputs: per-step values of this channel (lead lane) and the channel sums of
+    // dB / dC (lane j: row j % 16 of dB for j < 16, of dC otherwise), as 16-byte pieces when the
+    // rows allow it
+    if (valid && lead) {
+      const int64_t odu = b * p.sdu[0] + d * p.sdu[1] + t0, odd = b * p.sdd[0] + d * p.sdd[1] + t0;
+      const int64_t odz = b * p.sdz[0] + d * p.sdz[1] + t0;
+      if (p.vecout && steps == SEG) {
+        store_seg<IO>(p.du, odu, duo);
+        store_seg<IO>(p.ddelta, odd, ddo);
+        if (f.z) store_seg<IO>(p.dz, odz, dzo);
+      } else {
+#pragma unroll
+        for (int t = 0; t < SEG; ++t) {
+          if (t >= steps) break;
+          st<IO>(p.du, odu + t, duo[t]);
+          st<IO>(p.ddelta, odd + t, ddo[t]);
+          if (f.z) st<IO>(p.dz, odz + t, dzo[t]);
+        }
+      }
+    }
+    {
       const int n = lane & 15;
       if (n < N) {
-        if (lane < 16) atomicAdd(p.dB + b * p.sdB[0] + n * p.sdB[1] + tg * p.sdB[2], sum);
-        else atomicAdd(p.dC + b * p.sdC[0] + n * p.sdC[1] + tg * p.sdC[2], sum);
+        float* dst = lane < 16 ? p.dB + b * p.sdB[0] + n * p.sdB[1] : p.dC + b * p.sdC[0] + n * p.sdC[1];
+        const int64_t st2 = lane < 16 ? p.sdB[2] : p.sdC[2];
+        if (p.vecdbc && steps == SEG) {
+          atomicAdd(reinterpret_cast<float4*>(dst + t0), make_float4(sums[0], sums[1], sums[2], sums[3]));
+          atomicAdd(reinterpret_cast<float4*>(dst + t0 + 4), make_float4(sums[4], sums[5], sums[6], sums[7]));
+        } else {
+#pragma unroll
+          for (int t = 0; t < SEG; ++t) {
+            if (t >= steps) break;
+            atomicAdd(dst + (t0 + t) * st2, sums[t]);
+          }
+        }
       }
     }
   }

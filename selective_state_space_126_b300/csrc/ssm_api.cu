@@ -595,6 +595,14 @@ ssm_status_t ssm_scan_bwd(const ssm_scan_bwd_args_t* args, void* stream) {
       return true;
     };
     p.vecbc = bc16(p.f.Bm, p.f.sB) && bc16(p.f.Cm, p.f.sC) ? 1 : 0;
+    p.vecout = rows16(p.du, p.sdu) && rows16(p.ddelta, p.sdd) && rows16(p.dz, p.sdz) ? 1 : 0;
+    auto g16 = [&](const float* ptr, const int64_t* st) {   // fp32 rows (b, n) of dB / dC
+      if (!aligned(ptr, 16) || st[2] != 1) return false;
+      if (p.f.N > 1 && (st[1] * 4) % 16) return false;
+      if (p.bc_rows > 1 && (st[0] * 4) % 16) return false;
+      return true;
+    };
+    p.vecdbc = g16(p.dB, p.sdB) && g16(p.dC, p.sdC) ? 1 : 0;
   }
   // the checkpoints come from the tiled forward kernel when the layout allows it (one pass, from h0)
   p.sweep = 1;

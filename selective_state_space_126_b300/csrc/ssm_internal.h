@@ -48,6 +48,8 @@ struct BwdProblem {
   int sweep;           // 1: the backward kernel writes the checkpoints itself; 0: they are already there
   int vec;             // u, delta, z, dy rows start on 16-byte boundaries (128-bit segment loads)
   int vecbc;           // the same for the rows of B and C
+  int vecout;          // du, ddelta, dz rows start on 16-byte boundaries (128-bit segment stores)
+  int vecdbc;          // dB, dC rows start on 16-byte boundaries with time stride 1 (float4 atomic adds)
 };
 
 struct ConvProblem {
