@@ -81,6 +81,16 @@ __global__ void __launch_bounds__(256) bwd_zero_kernel(const BwdProblem p) {
   }
 }
 
+// 128-bit read-only load of segment data.  It is L1-cached (a 128-byte line
+// holds eight segments of a row, read one after another, and the two lanes of
+// a channel read the same piece) and asks L2 for 256 bytes on a miss.
+__device__ __forceinline__ uint4 ld_seg16(const void* p) {
+  uint4 r;
+  asm volatile("ld.global.nc.L2::256B.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "l"(p));
+  return r;
+}
+
 // SEG steps of one row starting at `ptr` (time stride 1) as fp32: one or two
 // 128-bit loads when the row is 16-byte aligned and the segment is whole,
 // element loads otherwise.
@@ -90,13 +100,13 @@ __device__ __forceinline__ void load_seg(const void* base, int64_t off, bool vec
   if (vec) {
     if (sizeof(IO) == 2) {
       float f[8];
-      unpack16(ldg_nc_v4(ptr), f);
+      unpack16(ld_seg16(ptr), f);
 #pragma unroll
       for (int t = 0; t < SEG; ++t) out[t] = f[t];
     } else {
       float f0[4], f1[4];
-      unpack16(ldg_nc_v4(ptr), f0);
-      unpack16(ldg_nc_v4(ptr + 4), f1);
+      unpack16(ld_seg16(ptr), f0);
+      unpack16(ld_seg16(ptr + 4), f1);
 #pragma unroll
       for (int t = 0; t < 4; ++t) { out[t] = f0[t]; out[t + 4] = f1[t]; }
     }
