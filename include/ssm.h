@@ -9,6 +9,7 @@
  *                       Delta_t   = softplus(delta[b,d,t] + delta_bias[d])
  *                       Abar_t[n] = exp(Delta_t * A[d,n])
  *                       h_t[n]    = Abar_t[n] h_{t-1}[n] + Delta_t B[b,n,t] u[b,d,t]
+ *                                   (or the exact zero-order-hold input term, SSM_DISC_ZOH)
  *                       y[b,d,t]  = (sum_n C[b,n,t] h_t[n] + Dskip[d] u[b,d,t]) * silu(z[b,d,t])
  *                     ("Mamba paper translation", gitcode.csdn.net: section 2
  *                     "State Space Models" for the recurrence and the
@@ -75,6 +76,13 @@ typedef enum {
     SSM_BF16 = 1               /* bfloat16; the state and all arithmetic stay fp32 */
 } ssm_dtype_t;
 
+/* discretisation of the input term ("docs.ifdog.com", section "Discretisation"):
+ * Euler Bbar x = Delta B u (the default), or the exact zero-order hold
+ * Bbar x = (exp(Delta A) - 1) / A * B u (Delta B u where A = 0).  Abar = exp(Delta A)
+ * in both. */
+#define SSM_DISC_EULER 0
+#define SSM_DISC_ZOH   1
+
 /* flags for ssm_scan_args_t.flags (testing and tuning; 0 = automatic) */
 #define SSM_SCAN_FORCE_GENERIC 0x1   /* use the stride-general kernel */
 #define SSM_SCAN_FORCE_TILED   0x2   /* use the tiled single-pass kernel (error if impossible) */
@@ -106,7 +114,7 @@ typedef struct ssm_scan_args {
     int64_t stride_A[2];                                              /* (d, n)    */
     int64_t stride_h0[3], stride_h_last[3];                           /* (b, d, n) */
     int32_t flags;                             /* SSM_SCAN_FORCE_*; 0 = automatic */
-    int32_t reserved0;
+    int32_t discretization;                    /* SSM_DISC_EULER (0) or SSM_DISC_ZOH */
     int64_t chunk_len;                         /* chunked path: timesteps per chunk; 0 = automatic */
     void *workspace;                           /* device scratch, caller-owned, nullable if 0 bytes needed */
     size_t workspace_bytes;
@@ -132,6 +140,8 @@ typedef struct ssm_step_args {
     int64_t stride_u[2], stride_delta[2], stride_z[2], stride_y[2];   /* (b, d) */
     int64_t stride_B[2], stride_C[2];          /* (b, n) */
     int64_t stride_A[2];                       /* (d, n) */
+    int32_t discretization;                    /* SSM_DISC_EULER (0) or SSM_DISC_ZOH */
+    int32_t reserved0;
 } ssm_step_args_t;
 
 /*

@@ -25,6 +25,7 @@ LIB_PATH = os.path.join(_HERE, "libssm.so")
 SSM_OK, SSM_ERR_INVALID_ARG, SSM_ERR_UNSUPPORTED, SSM_ERR_CUDA, SSM_ERR_TIMEOUT, SSM_ERR_WORKSPACE = range(6)
 SSM_F32, SSM_BF16 = 0, 1
 SSM_SCAN_FORCE_GENERIC, SSM_SCAN_FORCE_TILED, SSM_SCAN_FORCE_CHUNKED = 0x1, 0x2, 0x4
+SSM_DISC_EULER, SSM_DISC_ZOH = 0, 1
 PATH_NAMES = {0: "generic", 1: "tiled", 2: "chunked"}
 
 # every symbol include/ssm.h declares
@@ -47,7 +48,7 @@ class ScanArgs(ctypes.Structure):
         ("stride_u", _i64 * 3), ("stride_delta", _i64 * 3), ("stride_z", _i64 * 3), ("stride_y", _i64 * 3),
         ("stride_B", _i64 * 3), ("stride_C", _i64 * 3), ("stride_A", _i64 * 2),
         ("stride_h0", _i64 * 3), ("stride_h_last", _i64 * 3),
-        ("flags", ctypes.c_int32), ("reserved0", ctypes.c_int32), ("chunk_len", _i64),
+        ("flags", ctypes.c_int32), ("discretization", ctypes.c_int32), ("chunk_len", _i64),
         ("workspace", _vp), ("workspace_bytes", ctypes.c_size_t),
     ]
 
@@ -61,7 +62,7 @@ class StepArgs(ctypes.Structure):
         ("A", _vp), ("Dskip", _vp), ("delta_bias", _vp), ("y", _vp),
         ("stride_state", _i64 * 3), ("stride_u", _i64 * 2), ("stride_delta", _i64 * 2),
         ("stride_z", _i64 * 2), ("stride_y", _i64 * 2), ("stride_B", _i64 * 2), ("stride_C", _i64 * 2),
-        ("stride_A", _i64 * 2),
+        ("stride_A", _i64 * 2), ("discretization", ctypes.c_int32), ("reserved0", ctypes.c_int32),
     ]
 
 
@@ -216,7 +217,8 @@ def _f32(t, name):
 
 
 def make_scan_args(u, delta, A, Bm, Cm, y, Dskip=None, z=None, delta_bias=None, h0=None, h_last=None,
-                   delta_softplus=True, flags=0, chunk_len=0, workspace=None) -> ScanArgs:
+                   delta_softplus=True, flags=0, chunk_len=0, workspace=None,
+                   discretization=SSM_DISC_EULER) -> ScanArgs:
     """Fill an ssm_scan_args_t from torch tensors (no copies, strides passed through)."""
     Bsz, D, L = u.shape
     N = A.shape[1]
@@ -237,6 +239,7 @@ def make_scan_args(u, delta, A, Bm, Cm, y, Dskip=None, z=None, delta_bias=None, 
     a.stride_h0[:] = _strides(h0, 3)
     a.stride_h_last[:] = _strides(h_last, 3)
     a.flags = int(flags)
+    a.discretization = int(discretization)
     a.chunk_len = int(chunk_len)
     if workspace is not None:
         a.workspace = workspace.data_ptr()
@@ -256,8 +259,8 @@ def ssm_scan_plan_path(args: ScanArgs) -> str:
 
 def ssm_scan_fwd(u, delta, A, Bm, Cm, Dskip=None, z=None, delta_bias=None, h0=None, delta_softplus=True,
                  y=None, return_last_state=False, h_last=None, workspace=None, flags=0, chunk_len=0,
-                 stream=None):
-    """Selective-scan forward pass on the GPU.
+                 stream=None, discretization=SSM_DISC_EULER):
+    """Selective-scan forward pass on the GPU (``discretization``: SSM_DISC_EULER or SSM_DISC_ZOH).
 
     u, delta, z: (B, D, L); Bm, Cm: (B, N, L) or (N, L) (shared across the batch);
     A: (D, N) fp32; Dskip, delta_bias: (D,) fp32; h0: (B, D, N) fp32.
@@ -279,7 +282,7 @@ def ssm_scan_fwd(u, delta, A, Bm, Cm, Dskip=None, z=None, delta_bias=None, h0=No
     if return_last_state and h_last is None:
         h_last = torch.empty((u.shape[0], u.shape[1], A.shape[1]), dtype=torch.float32, device=u.device)
     args = make_scan_args(u, delta, A, Bm, Cm, y, Dskip, z, delta_bias, h0, h_last, delta_softplus, flags,
-                          chunk_len, None)
+                          chunk_len, None, discretization)
     need = ssm_scan_workspace_size(args)
     if need > 0:
         if workspace is None or workspace.numel() * workspace.element_size() < need:
@@ -291,7 +294,7 @@ def ssm_scan_fwd(u, delta, A, Bm, Cm, Dskip=None, z=None, delta_bias=None, h0=No
 
 
 def make_step_args(state, u, delta, A, Bm, Cm, y, Dskip=None, z=None, delta_bias=None,
-                   delta_softplus=True) -> StepArgs:
+                   delta_softplus=True, discretization=SSM_DISC_EULER) -> StepArgs:
     Bsz, D, N = state.shape
     a = StepArgs()
     a.batch, a.dim, a.dstate = Bsz, D, N
@@ -307,11 +310,12 @@ def make_step_args(state, u, delta, A, Bm, Cm, y, Dskip=None, z=None, delta_bias
     a.stride_B[:] = _strides(Bm, 2)
     a.stride_C[:] = _strides(Cm, 2)
     a.stride_A[:] = _strides(A, 2)
+    a.discretization = int(discretization)
     return a
 
 
 def ssm_state_update(state, u, delta, A, Bm, Cm, Dskip=None, z=None, delta_bias=None, delta_softplus=True,
-                     y=None, stream=None):
+                     y=None, stream=None, discretization=SSM_DISC_EULER):
     """One decode step: ``state`` (B, D, N) fp32 is updated in place; returns y (B, D)."""
     torch = _torch()
     lib = load_library()
@@ -322,7 +326,7 @@ def ssm_state_update(state, u, delta, A, Bm, Cm, Dskip=None, z=None, delta_bias=
         delta_bias = delta_bias.contiguous()
     if y is None:
         y = torch.empty(u.shape, dtype=u.dtype, device=u.device)
-    args = make_step_args(state, u, delta, A, Bm, Cm, y, Dskip, z, delta_bias, delta_softplus)
+    args = make_step_args(state, u, delta, A, Bm, Cm, y, Dskip, z, delta_bias, delta_softplus, discretization)
     _check(lib.ssm_state_update(ctypes.byref(args), _vp(_stream_handle(stream))))
     return y
 
@@ -446,7 +450,7 @@ SSM_NOALLOC_SCRATCH_BYTES = 8 << 20
 
 
 def ssm_scan_fwd_noalloc(u, delta, A, Bm, Cm, y, Dskip=None, z=None, delta_bias=None, h0=None, h_last=None,
-                         delta_softplus=True, chunk_len=0, stream=None):
+                         delta_softplus=True, chunk_len=0, stream=None, discretization=SSM_DISC_EULER):
     """The chunked scan without a caller workspace, for callers that cannot allocate.
 
     The caller passes every input and the outputs (``y`` and optionally
@@ -456,6 +460,6 @@ def ssm_scan_fwd_noalloc(u, delta, A, Bm, Cm, y, Dskip=None, z=None, delta_bias=
     two of them overlap on the GPU.
     """
     args = make_scan_args(u, delta, A, Bm, Cm, y, Dskip, z, delta_bias, h0, h_last, delta_softplus,
-                          SSM_SCAN_FORCE_CHUNKED, chunk_len, None)
+                          SSM_SCAN_FORCE_CHUNKED, chunk_len, None, discretization)
     _check(load_library().ssm_scan_fwd_noalloc(ctypes.byref(args), _vp(_stream_handle(stream))))
     return y

@@ -10,7 +10,8 @@
 //    on [0, 1] by fit_log1p.py, relative error 2.3e-7), so Delta keeps its
 //    relative accuracy however small it is.  For fp32 I/O the library
 //    log1pf/expf form is used;
-//  * silu(z) = z / (1 + 2^(-z log2 e)) with the SFU reciprocal.
+//  * silu(z) = z / (1 + 2^(-z log2 e)) with the SFU reciprocal;
+//  * the exact-ZOH input coefficient (exp(Delta A) - 1) / A: see zoh_coef.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -19,6 +20,7 @@
 namespace ssm {
 
 constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.69314718055994531f;
 
 __device__ __forceinline__ float ex2_approx(float x) {
   float y;
@@ -90,6 +92,47 @@ __device__ __forceinline__ float2 silu2_fast(float2 z) {
   const float2 x = __fmul2_rn(z, make_float2(-kLog2e, -kLog2e));
   const float2 den = __fadd2_rn(make_float2(ex2_approx(x.x), ex2_approx(x.y)), make_float2(1.f, 1.f));
   return __fmul2_rn(z, make_float2(rcp_approx(den.x), rcp_approx(den.y)));
+}
+
+// Exact zero-order-hold input coefficient of one state ("Mamba and state space
+// models", docs.ifdog.com, section "Discretisation": Bbar = (Delta A)^-1
+// (exp(Delta A) - 1) Delta B, so Bbar x = g B u with g = (exp(Delta A) - 1) / A
+// = Delta phi(Delta A), phi(x) = (e^x - 1) / x).  Given x = Delta A, a = e^x
+// and inv_a = 1 / A:
+//   |x| <  1/2 : g = Delta (1 + x/2! ... + x^7/8!), the Taylor series of phi
+//                (truncation below 1.1e-8), which stays accurate where e^x - 1
+//                cancels (and gives g = Delta at A = 0);
+//   |x| >= 1/2 : g = (a - 1) / A, where |a - 1| > 0.39 keeps the relative error
+//                of a within a few 1e-7 (the fp32-I/O form uses expm1f).
+__device__ __forceinline__ float phi_series(float x) {
+  float r = 2.4801587301587302e-05f;                 // 1/8!
+  r = fmaf(r, x, 1.9841269841269841e-04f);          // 1/7!
+  r = fmaf(r, x, 1.3888888888888889e-03f);          // 1/6!
+  r = fmaf(r, x, 8.3333333333333333e-03f);          // 1/5!
+  r = fmaf(r, x, 4.1666666666666667e-02f);          // 1/4!
+  r = fmaf(r, x, 1.6666666666666667e-01f);          // 1/3!
+  r = fmaf(r, x, 0.5f);                             // 1/2!
+  return fmaf(r, x, 1.f);
+}
+
+template <bool PRECISE>
+__device__ __forceinline__ float zoh_coef(float dt, float x, float a, float inv_a) {
+  const float large = PRECISE ? expm1f(x) * inv_a : (a - 1.f) * inv_a;
+  return fabsf(x) < 0.5f ? dt * phi_series(x) : large;
+}
+
+// Two-lane form of zoh_coef (fast path) on packed f32x2 FMAs.
+__device__ __forceinline__ float2 zoh_coef2_fast(float2 dt, float2 x, float2 a, float2 inv_a) {
+  float2 r = make_float2(2.4801587301587302e-05f, 2.4801587301587302e-05f);
+  r = __ffma2_rn(r, x, make_float2(1.9841269841269841e-04f, 1.9841269841269841e-04f));
+  r = __ffma2_rn(r, x, make_float2(1.3888888888888889e-03f, 1.3888888888888889e-03f));
+  r = __ffma2_rn(r, x, make_float2(8.3333333333333333e-03f, 8.3333333333333333e-03f));
+  r = __ffma2_rn(r, x, make_float2(4.1666666666666667e-02f, 4.1666666666666667e-02f));
+  r = __ffma2_rn(r, x, make_float2(1.6666666666666667e-01f, 1.6666666666666667e-01f));
+  r = __ffma2_rn(r, x, make_float2(0.5f, 0.5f));
+  const float2 small = __fmul2_rn(dt, __ffma2_rn(r, x, make_float2(1.f, 1.f)));
+  const float2 large = __fmul2_rn(__fadd2_rn(a, make_float2(-1.f, -1.f)), inv_a);
+  return make_float2(fabsf(x.x) < 0.5f ? small.x : large.x, fabsf(x.y) < 0.5f ? small.y : large.y);
 }
 
 // Delta for one element: softplus(delta + bias) or the plain sum.

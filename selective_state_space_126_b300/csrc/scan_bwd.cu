@@ -38,7 +38,6 @@ namespace ssm {
 namespace {
 
 constexpr int SEG = SSM_BWD_SEGMENT;   // steps per checkpoint
-constexpr float kLn2 = 0.69314718055994531f;
 
 template <bool PRECISE>
 __device__ __forceinline__ float sigmoid_f(float v) {

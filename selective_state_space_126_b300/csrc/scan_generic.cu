@@ -4,7 +4,7 @@
 // rows (seqlen not a multiple of the 16-byte vector), strided layouts, empty
 // sequences.  It runs the recurrence of the Mamba paper ("gitcode.csdn.net",
 // section 2, recurrent mode; Delta = softplus(delta + bias), Abar = exp(Delta A),
-// Bbar x = Delta B u) with the state in registers, the silu gate of the Mamba
+// Bbar x = Delta B u, or the exact zero-order hold) with the state in registers, the silu gate of the Mamba
 // block ("docs.ifdog.com", section "Mamba architecture") and the D skip term.
 #include "device_math.cuh"
 #include "ssm_internal.h"
@@ -25,10 +25,12 @@ __global__ void __launch_bounds__(128) scan_generic_kernel(const ScanProblem p) 
   const IO* Cm = static_cast<const IO*>(p.Cm) + b * p.sC[0];
   IO* y = static_cast<IO*>(p.y) + b * p.sy[0] + d * p.sy[1];
 
-  float A2[NB], h[NB];
+  float A2[NB], h[NB], Ai[NB];
 #pragma unroll
   for (int n = 0; n < NB; ++n) {
-    A2[n] = n < N ? p.A[d * p.sA[0] + n * p.sA[1]] * kLog2e : 0.f;
+    const float a = n < N ? p.A[d * p.sA[0] + n * p.sA[1]] : 0.f;
+    A2[n] = a * kLog2e;
+    Ai[n] = 1.f / a;   // ZOH: 1 / A (infinite at A = 0, where zoh_coef takes its series)
     h[n] = (n < N && p.h0) ? p.h0[b * p.sh0[0] + d * p.sh0[1] + n * p.sh0[2]] : 0.f;
   }
   const float bias = p.bias ? p.bias[d] : 0.f;
@@ -43,7 +45,8 @@ __global__ void __launch_bounds__(128) scan_generic_kernel(const ScanProblem p) 
     for (int n = 0; n < NB; ++n) {
       if (n < N) {
         const float a = ex2_approx(dt * A2[n]);
-        h[n] = fmaf(a, h[n], du * to_f32(Bm[n * p.sB[1] + t]));
+        const float bx = p.zoh ? zoh_coef<PRECISE>(dt, dt * A2[n] * kLn2, a, Ai[n]) * uv : du;
+        h[n] = fmaf(a, h[n], bx * to_f32(Bm[n * p.sB[1] + t]));
         acc = fmaf(to_f32(Cm[n * p.sC[1] + t]), h[n], acc);
       }
     }

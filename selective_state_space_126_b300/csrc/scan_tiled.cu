@@ -30,7 +30,9 @@
 //       B. the recurrence, fully unrolled over the tile so that the SFU ex2
 //          of later steps overlaps the dependent FMAs of earlier ones: per
 //          step one ex2 per state, Abar*h + (Delta u) B on packed f32x2 FMAs
-//          and the C contraction into a partial y;
+//          and the C contraction into a partial y (with the exact
+//          zero-order-hold term, a compile-time variant, the input
+//          coefficient is g u with g = (exp(Delta A) - 1) / A, see zoh_coef);
 //       C. the K partial outputs are summed, D*u added and multiplied by
 //          silu(z) into a swizzled staging box, which a TMA store writes back
 //          (issued after the next tile's first barrier; two boxes alternate).
@@ -98,7 +100,7 @@ struct Smem {
 };
 
 
-template <typename IO, int K, int NS, int MODE, bool PRECISE>
+template <typename IO, int K, int NS, int MODE, bool PRECISE, bool ZOH>
 __global__ void __launch_bounds__(32 * K, min_blocks(K, NS))
     scan_tiled_kernel(const __grid_constant__ ScanKernelParams p, const __grid_constant__ ScanMaps tm) {
   using S = Smem<IO, K, NS>;
@@ -139,13 +141,14 @@ __global__ void __launch_bounds__(32 * K, min_blocks(K, NS))
   const int ntiles = (int)((t_end - t_begin + T - 1) / T);
 
   // ---- per-thread state: A * log2(e) and h for this thread's NS states ----
-  float2 A2[NS / 2], h[NS / 2];
+  float2 A2[NS / 2], h[NS / 2], Ai[NS / 2];   // Ai: 1 / A, for the exact-ZOH input term
 #pragma unroll
   for (int i = 0; i < NS; ++i) {
     const int n = g * NS + i;
-    float a = 0.f, hv = 0.f;
+    float a = 0.f, hv = 0.f, ai = 0.f;
     if (valid && n < N) {
       a = p.A[d * p.sA0 + n * p.sA1] * kLog2e;
+      ai = kLog2e / a;
       if (MODE == MODE_OUTPUT || MODE == MODE_CKPT) {
         if (chunk == 0) {
           if (p.h0) hv = p.h0[b * p.sh00 + d * p.sh01 + n * p.sh02];
@@ -154,8 +157,8 @@ __global__ void __launch_bounds__(32 * K, min_blocks(K, NS))
         }
       }
     }
-    if (i & 1) { A2[i / 2].y = a; h[i / 2].y = hv; }
-    else { A2[i / 2].x = a; h[i / 2].x = hv; }
+    if (i & 1) { A2[i / 2].y = a; h[i / 2].y = hv; Ai[i / 2].y = ai; }
+    else { A2[i / 2].x = a; h[i / 2].x = hv; Ai[i / 2].x = ai; }
   }
 
   // ---- one-time set-up: zero the B/C tile (padded states stay zero), barriers ----
@@ -233,7 +236,8 @@ __global__ void __launch_bounds__(32 * K, min_blocks(K, NS))
           if (t0 + vt[i] + j >= t_end) dt.x = 0.f;
           if (t0 + vt[i] + j + 1 >= t_end) dt.y = 0.f;
         }
-        const float2 du = __fmul2_rn(dt, make_float2(uv[j], uv[j + 1]));
+        // (Delta, Delta u) for the Euler term; (Delta, u) for the exact ZOH term
+        const float2 du = ZOH ? make_float2(uv[j], uv[j + 1]) : __fmul2_rn(dt, make_float2(uv[j], uv[j + 1]));
         dst[j / 2] = make_float4(dt.x, du.x, dt.y, du.y);
       }
     }
@@ -343,12 +347,29 @@ __global__ void __launch_bounds__(32 * K, min_blocks(K, NS))
             const float2 x = __fmul2_rn(make_float2(dt, dt), A2[q]);
             a[q] = make_float2(ex2_approx(x.x), ex2_approx(x.y));
           }
+          // input coefficient per state: Delta u (Euler), or g u with the exact-ZOH g (du holds u)
+          float2 bx[NS / 2];
+#pragma unroll
+          for (int q = 0; q < NS / 2; ++q) {
+            if (ZOH) {
+              const float2 x = __fmul2_rn(__fmul2_rn(make_float2(dt, dt), A2[q]), make_float2(kLn2, kLn2));
+              float2 gq;
+              if (PRECISE) {
+                gq = make_float2(zoh_coef<true>(dt, x.x, a[q].x, Ai[q].x), zoh_coef<true>(dt, x.y, a[q].y, Ai[q].y));
+              } else {
+                gq = zoh_coef2_fast(make_float2(dt, dt), x, a[q], Ai[q]);
+              }
+              bx[q] = __fmul2_rn(gq, du2);
+            } else {
+              bx[q] = du2;
+            }
+          }
           float2 acc = make_float2(0.f, 0.f);
 #pragma unroll
           for (int q = 0; q < NS; q += 4) {
             const float4 bq = *reinterpret_cast<const float4*>(Bt + q);
-            h[q / 2] = __ffma2_rn(a[q / 2], h[q / 2], __fmul2_rn(du2, make_float2(bq.x, bq.y)));
-            h[q / 2 + 1] = __ffma2_rn(a[q / 2 + 1], h[q / 2 + 1], __fmul2_rn(du2, make_float2(bq.z, bq.w)));
+            h[q / 2] = __ffma2_rn(a[q / 2], h[q / 2], __fmul2_rn(bx[q / 2], make_float2(bq.x, bq.y)));
+            h[q / 2 + 1] = __ffma2_rn(a[q / 2 + 1], h[q / 2 + 1], __fmul2_rn(bx[q / 2 + 1], make_float2(bq.z, bq.w)));
             if (MODE == MODE_OUTPUT) {
               const float4 cq = *reinterpret_cast<const float4*>(Bt + NP + q);
               acc = __ffma2_rn(make_float2(cq.x, cq.y), h[q / 2], acc);
@@ -414,10 +435,10 @@ __global__ void __launch_bounds__(32 * K, min_blocks(K, NS))
   }
 }
 
-template <typename IO, int K, int NS, int MODE, bool PRECISE>
+template <typename IO, int K, int NS, int MODE, bool PRECISE, bool ZOH>
 cudaError_t launch_one(const ScanKernelParams& tp, const ScanMaps& tm, dim3 grid, cudaStream_t s) {
   using S = Smem<IO, K, NS>;
-  auto kern = scan_tiled_kernel<IO, K, NS, MODE, PRECISE>;
+  auto kern = scan_tiled_kernel<IO, K, NS, MODE, PRECISE, ZOH>;
   static unsigned long long attr_set = 0;   // one bit per device; a racing duplicate set is harmless
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -432,21 +453,21 @@ cudaError_t launch_one(const ScanKernelParams& tp, const ScanMaps& tm, dim3 grid
   return cudaGetLastError();
 }
 
-template <typename IO, int K, int NS, bool PRECISE>
+template <typename IO, int K, int NS, bool PRECISE, bool ZOH>
 cudaError_t launch_shape(const ScanProblem& p, const ScanPlan& plan, ScanKernelParams& tp, const ScanMaps& tm,
                          cudaStream_t s) {
   constexpr int NP = K * NS;
   const dim3 grid((unsigned)((p.D + CH - 1) / CH), (unsigned)plan.nchunks, (unsigned)p.B);
   cudaError_t e;
   if (plan.nchunks > 1) {
-    e = launch_one<IO, K, NS, MODE_RECORD, PRECISE>(tp, tm, grid, s);
+    e = launch_one<IO, K, NS, MODE_RECORD, PRECISE, ZOH>(tp, tm, grid, s);
     if (e != cudaSuccess) return e;
     const int64_t total = p.B * p.D * NP;
     chunk_carry_kernel<<<(unsigned)((total + 255) / 256), 256, 0, s>>>(tp, NP);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
-  return launch_one<IO, K, NS, MODE_OUTPUT, PRECISE>(tp, tm, grid, s);
+  return launch_one<IO, K, NS, MODE_OUTPUT, PRECISE, ZOH>(tp, tm, grid, s);
 }
 
 template <typename IO, bool PRECISE>
@@ -454,21 +475,21 @@ cudaError_t launch_ckpt_typed(const ScanPlan& plan, const ScanKernelParams& tp, 
                               const ScanProblem& p, cudaStream_t s) {
   const dim3 grid((unsigned)((p.D + CH - 1) / CH), 1, (unsigned)p.B);
   const int K = plan.shape.K, NS = plan.shape.NS;
-  if (K == 1 && NS == 16) return launch_one<IO, 1, 16, MODE_CKPT, PRECISE>(tp, tm, grid, s);
-  if (K == 2 && NS == 8) return launch_one<IO, 2, 8, MODE_CKPT, PRECISE>(tp, tm, grid, s);
-  if (K == 4 && NS == 4) return launch_one<IO, 4, 4, MODE_CKPT, PRECISE>(tp, tm, grid, s);
+  if (K == 1 && NS == 16) return launch_one<IO, 1, 16, MODE_CKPT, PRECISE, false>(tp, tm, grid, s);
+  if (K == 2 && NS == 8) return launch_one<IO, 2, 8, MODE_CKPT, PRECISE, false>(tp, tm, grid, s);
+  if (K == 4 && NS == 4) return launch_one<IO, 4, 4, MODE_CKPT, PRECISE, false>(tp, tm, grid, s);
   return cudaErrorInvalidValue;
 }
 
-template <typename IO, bool PRECISE>
+template <typename IO, bool PRECISE, bool ZOH>
 cudaError_t launch_typed(const ScanProblem& p, const ScanPlan& plan, ScanKernelParams& tp, const ScanMaps& tm,
                          cudaStream_t s) {
   const int K = plan.shape.K, NS = plan.shape.NS;
-  if (K == 1 && NS == 16) return launch_shape<IO, 1, 16, PRECISE>(p, plan, tp, tm, s);
-  if (K == 2 && NS == 8) return launch_shape<IO, 2, 8, PRECISE>(p, plan, tp, tm, s);
-  if (K == 4 && NS == 4) return launch_shape<IO, 4, 4, PRECISE>(p, plan, tp, tm, s);
-  if (K == 4 && NS == 8) return launch_shape<IO, 4, 8, PRECISE>(p, plan, tp, tm, s);
-  if (K == 4 && NS == 16) return launch_shape<IO, 4, 16, PRECISE>(p, plan, tp, tm, s);
+  if (K == 1 && NS == 16) return launch_shape<IO, 1, 16, PRECISE, ZOH>(p, plan, tp, tm, s);
+  if (K == 2 && NS == 8) return launch_shape<IO, 2, 8, PRECISE, ZOH>(p, plan, tp, tm, s);
+  if (K == 4 && NS == 4) return launch_shape<IO, 4, 4, PRECISE, ZOH>(p, plan, tp, tm, s);
+  if (K == 4 && NS == 8) return launch_shape<IO, 4, 8, PRECISE, ZOH>(p, plan, tp, tm, s);
+  if (K == 4 && NS == 16) return launch_shape<IO, 4, 16, PRECISE, ZOH>(p, plan, tp, tm, s);
   return cudaErrorInvalidValue;
 }
 
@@ -479,8 +500,12 @@ cudaError_t launch_scan_tiled(const ScanProblem& p, const ScanPlan& plan, void* 
   ScanMaps tm;
   if (!make_scan_kernel_args(p, plan, workspace, plan.shape.K * plan.shape.NS, T, &tp, &tm))
     return cudaErrorInvalidValue;
-  if (p.io == SSM_F32) return launch_typed<float, true>(p, plan, tp, tm, s);
-  return launch_typed<__nv_bfloat16, false>(p, plan, tp, tm, s);
+  if (p.zoh) {
+    if (p.io == SSM_F32) return launch_typed<float, true, true>(p, plan, tp, tm, s);
+    return launch_typed<__nv_bfloat16, false, true>(p, plan, tp, tm, s);
+  }
+  if (p.io == SSM_F32) return launch_typed<float, true, false>(p, plan, tp, tm, s);
+  return launch_typed<__nv_bfloat16, false, false>(p, plan, tp, tm, s);
 }
 
 cudaError_t launch_scan_ckpt(const ScanProblem& p, const ScanPlan& plan, float* ckpt, int64_t nseg, cudaStream_t s) {

@@ -85,6 +85,9 @@ ssm_status_t validate_scan(const ssm_scan_args_t* a, ScanProblem* p) {
   p->B = a->batch; p->D = a->dim; p->L = a->seqlen; p->N = a->dstate;
   p->io = a->io_dtype;
   p->softplus = a->delta_softplus != 0;
+  if (a->discretization != SSM_DISC_EULER && a->discretization != SSM_DISC_ZOH)
+    return fail(SSM_ERR_INVALID_ARG, "discretization %d", (int)a->discretization);
+  p->zoh = a->discretization == SSM_DISC_ZOH;
   p->u = a->u; p->delta = a->delta; p->z = a->z; p->Bm = a->Bm; p->Cm = a->Cm;
   p->A = a->A; p->Dskip = a->Dskip; p->bias = a->delta_bias; p->h0 = a->h0; p->h_last = a->h_last; p->y = a->y;
   std::memcpy(p->su, a->stride_u, sizeof(p->su));
@@ -377,7 +380,10 @@ ssm_status_t ssm_state_update(const ssm_step_args_t* a, void* stream) {
   if (a->dstate < 1 || a->dstate > 64) return fail(SSM_ERR_UNSUPPORTED, "dstate outside [1, 64]");
   StepProblem p;
   std::memset(&p, 0, sizeof(p));
+  if (a->discretization != SSM_DISC_EULER && a->discretization != SSM_DISC_ZOH)
+    return fail(SSM_ERR_INVALID_ARG, "discretization %d", (int)a->discretization);
   p.B = a->batch; p.D = a->dim; p.N = a->dstate; p.io = a->io_dtype; p.softplus = a->delta_softplus != 0;
+  p.zoh = a->discretization == SSM_DISC_ZOH;
   p.state = a->state; p.u = a->u; p.delta = a->delta; p.z = a->z; p.Bm = a->Bm; p.Cm = a->Cm;
   p.A = a->A; p.Dskip = a->Dskip; p.bias = a->delta_bias; p.y = a->y;
   std::memcpy(p.sst, a->stride_state, sizeof(p.sst));
@@ -454,6 +460,7 @@ ssm_status_t validate_bwd(const ssm_scan_bwd_args_t* a, BwdProblem* p) {
   if (st != SSM_OK) return st;
   const ScanProblem& f = p->f;
   if (f.N > 16) return fail(SSM_ERR_UNSUPPORTED, "the backward pass takes dstate <= 16");
+  if (f.zoh) return fail(SSM_ERR_UNSUPPORTED, "the backward pass takes the Euler discretisation");
   p->dy = a->dy; p->dhl = a->dh_last;
   p->du = a->du; p->ddelta = a->ddelta; p->dz = a->dz;
   p->dA = a->dA; p->dB = a->dB; p->dC = a->dC; p->dD = a->dDskip; p->dbias = a->ddelta_bias; p->dh0 = a->dh0;

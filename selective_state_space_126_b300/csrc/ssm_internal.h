@@ -15,6 +15,7 @@ struct ScanProblem {
   int64_t B, D, L, N;
   ssm_dtype_t io;
   bool softplus;
+  bool zoh;               // exact zero-order-hold input term (else Euler)
   const void *u, *delta, *z, *Bm, *Cm;
   const float *A, *Dskip, *bias, *h0;
   float* h_last;
@@ -26,6 +27,7 @@ struct StepProblem {
   int64_t B, D, N;
   ssm_dtype_t io;
   bool softplus;
+  bool zoh;
   float* state;
   const void *u, *delta, *z, *Bm, *Cm;
   const float *A, *Dskip, *bias;

@@ -128,7 +128,8 @@ __global__ void __launch_bounds__(256) state_update_kernel(const StepProblem p, 
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       const float a = ex2_approx(dt * (Av[it][i] * kLog2e));
-      h[it][i] = fmaf(a, h[it][i], du * Bv[it][i]);
+      const float bx = p.zoh ? zoh_coef<PRECISE>(dt, dt * Av[it][i], a, 1.f / Av[it][i]) * uv[it] : du;
+      h[it][i] = fmaf(a, h[it][i], bx * Bv[it][i]);
       acc = fmaf(Cv[it][i], h[it][i], acc);
     }
 #pragma unroll
@@ -457,7 +458,8 @@ cudaError_t launch_wide(const StepProblem& p, cudaStream_t s) {
 template <typename IO, bool PRECISE>
 cudaError_t launch_typed(const StepProblem& p, cudaStream_t s) {
   int Qb = 0;
-  const bool bulk = bulk_eligible<IO>(p, &Qb) && getenv("SSM_DECODE_PER_ITEM") == nullptr;
+  // the exact-ZOH input term is implemented in the per-item kernel only
+  const bool bulk = !p.zoh && bulk_eligible<IO>(p, &Qb) && getenv("SSM_DECODE_PER_ITEM") == nullptr;
   if (bulk && p.N == 16 && p.D % WideSlot<IO>::CH == 0 && getenv("SSM_DECODE_QUAD") == nullptr)
     return launch_wide<IO, PRECISE>(p, s);
   if (bulk) {

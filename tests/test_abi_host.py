@@ -300,3 +300,23 @@ def test_bwd_rejects_large_dstate(lib):
     a.stride_dC[:] = [32 * 256, 256, 1]
     a.stride_dh0[:] = [64 * 32, 32, 1]
     assert bwd_ws(a)[0] == ssm.SSM_ERR_UNSUPPORTED
+
+
+def test_discretization_validation(lib):
+    assert call_scan(scan_args(discretization=2)) == ssm.SSM_ERR_INVALID_ARG
+    assert call_scan(scan_args(discretization=-1)) == ssm.SSM_ERR_INVALID_ARG
+    n = ctypes.c_size_t(0)
+    assert lib.ssm_scan_workspace_size(ctypes.byref(scan_args(discretization=ssm.SSM_DISC_ZOH)), ctypes.byref(n)) == 0
+
+
+def test_bwd_rejects_zoh(lib):
+    a = bwd_args()
+    a.fwd.discretization = ssm.SSM_DISC_ZOH
+    assert bwd_ws(a)[0] == ssm.SSM_ERR_UNSUPPORTED
+
+
+def test_step_discretization_validation(lib):
+    a = ssm.StepArgs()
+    a.batch, a.dim, a.dstate, a.io_dtype = 2, 8, 16, ssm.SSM_BF16
+    a.discretization = 3
+    assert lib.ssm_state_update(ctypes.byref(a), None) == ssm.SSM_ERR_INVALID_ARG

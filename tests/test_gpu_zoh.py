@@ -1,0 +1,108 @@
+"""GPU parity of the exact zero-order-hold input term (SSM_DISC_ZOH) against the oracle's ZOH mode.
+
+The oracle's ZOH mode is pinned by Theorem 1's gated RNN, the LTI convolution kernel and its Euler limit
+(tests/pins.py).  Here the scan (tiled single pass, chunked, stride-general) and the decode step take
+SSM_DISC_ZOH and are compared with it; A spans both forms of the coefficient (|Delta A| below and
+above 1/2), and a zero A, where the exact term reduces to the Euler one, is checked bit for bit.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import selective_state_space_126_b300 as ssm
+from selective_state_space_126_b300 import synthetic as syn
+from gpu_util import assert_close, host, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _setup(ssm_lib, cuda_ok):
+    yield
+
+
+def scan_inputs(B, D, L, N, io, seed, zero_a=False):
+    rng = np.random.default_rng(seed)
+    r = lambda *s: syn.round_io(rng.standard_normal(s, dtype=np.float32), io)
+    A, Dv, bv = syn.layer_params(D, N, 1e-3, 1e-1, seed)
+    A = A * rng.uniform(0.5, 1.5, A.shape).astype(np.float32)
+    if zero_a:
+        A[:, ::3] = 0.0
+    return dict(u=r(B, D, L), delta=r(B, D, L), z=r(B, D, L), Bm=r(B, N, L), Cm=r(B, N, L), A=A, Dskip=Dv,
+                delta_bias=bv, h0=rng.standard_normal((B, D, N)).astype(np.float32))
+
+
+def run_scan(p, io, flags=0, chunk_len=0, disc=ssm.SSM_DISC_ZOH):
+    d = {k: to_dev(v, io if k in ("u", "delta", "z", "Bm", "Cm") else None) for k, v in p.items()}
+    y, hl = ssm.ssm_scan_fwd(d["u"], d["delta"], d["A"], d["Bm"], d["Cm"], Dskip=d["Dskip"], z=d["z"],
+                             delta_bias=d["delta_bias"], h0=d["h0"], return_last_state=True, flags=flags,
+                             chunk_len=chunk_len, discretization=disc)
+    torch.cuda.synchronize()
+    return y, hl
+
+
+def oracle_scan(p):
+    return oracle.selective_scan(p["u"], p["delta"], p["A"], p["Bm"], p["Cm"], Dskip=p["Dskip"], z=p["z"],
+                                 delta_bias=p["delta_bias"], h0=p["h0"], disc=oracle.DISC_ZOH,
+                                 return_last_state=True)
+
+
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+@pytest.mark.parametrize("shape,flags", [((1, 16, 256, 16), 0), ((2, 64, 512, 16), 0), ((3, 96, 320, 8), 0),
+                                         ((2, 37, 100, 13), 0), ((2, 64, 512, 16), ssm.SSM_SCAN_FORCE_GENERIC)])
+def test_zoh_scan(io, shape, flags):
+    B, D, L, N = shape
+    p = scan_inputs(B, D, L, N, io, seed=sum(shape))
+    y, hl = run_scan(p, io, flags=flags)
+    yr, hr = oracle_scan(p)
+    assert_close(io, host(y), yr, f"y {shape}")
+    assert_close(io, host(hl), hr, f"h_last {shape}")
+
+
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+def test_zoh_chunked(io):
+    p = scan_inputs(2, 64, 1024, 16, io, seed=3)
+    y, hl = run_scan(p, io, flags=ssm.SSM_SCAN_FORCE_CHUNKED, chunk_len=128)
+    yr, hr = oracle_scan(p)
+    assert_close(io, host(y), yr, "y chunked")
+    assert_close(io, host(hl), hr, "h_last chunked")
+
+
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+def test_zoh_zero_a_is_euler(io):
+    """Where A = 0 the exact term is Delta B u: with every A zero, ZOH and Euler give the same bits."""
+    p = scan_inputs(2, 64, 256, 16, io, seed=8)
+    p["A"] = np.zeros_like(p["A"])
+    yz, hz = run_scan(p, io)
+    ye, he = run_scan(p, io, disc=ssm.SSM_DISC_EULER)
+    assert torch.equal(yz, ye) and torch.equal(hz, he)
+
+
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+def test_zoh_some_zero_a(io):
+    p = scan_inputs(2, 64, 256, 16, io, seed=9, zero_a=True)
+    y, hl = run_scan(p, io)
+    yr, hr = oracle_scan(p)
+    assert_close(io, host(y), yr, "y with zero A columns")
+    assert_close(io, host(hl), hr, "h_last with zero A columns")
+
+
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+@pytest.mark.parametrize("shape", [(3, 256, 16), (2, 33, 13), (4, 128, 8)])
+def test_zoh_decode(io, shape):
+    B, D, N = shape
+    rng = np.random.default_rng(sum(shape))
+    r = lambda *s: syn.round_io(rng.standard_normal(s, dtype=np.float32), io)
+    A, Dv, bv = syn.layer_params(D, N, 1e-3, 1e-1, 1)
+    A = A * rng.uniform(0.5, 1.5, A.shape).astype(np.float32)
+    st0 = rng.standard_normal((B, D, N)).astype(np.float32)
+    u, dl, z, Bm, Cm = r(B, D), r(B, D), r(B, D), r(B, N), r(B, N)
+    st = to_dev(st0)
+    y = ssm.ssm_state_update(st, to_dev(u, io), to_dev(dl, io), to_dev(A), to_dev(Bm, io), to_dev(Cm, io),
+                             Dskip=to_dev(Dv), z=to_dev(z, io), delta_bias=to_dev(bv),
+                             discretization=ssm.SSM_DISC_ZOH)
+    torch.cuda.synchronize()
+    sr, yr = oracle.state_update(st0, u, dl, A, Bm, Cm, Dskip=Dv, z=z, delta_bias=bv, disc=oracle.DISC_ZOH)
+    assert_close(io, host(y), yr, f"decode y {shape}")
+    assert_close(io, host(st), sr, f"decode state {shape}")
