@@ -98,12 +98,13 @@ __device__ __forceinline__ float2 silu2_fast(float2 z) {
 // models", docs.ifdog.com, section "Discretisation": Bbar = (Delta A)^-1
 // (exp(Delta A) - 1) Delta B, so Bbar x = g B u with g = (exp(Delta A) - 1) / A
 // = Delta phi(Delta A), phi(x) = (e^x - 1) / x).  Given x = Delta A, a = e^x
-// and inv_a = 1 / A:
-//   |x| <  1/2 : g = Delta (1 + x/2! ... + x^7/8!), the Taylor series of phi
-//                (truncation below 1.1e-8), which stays accurate where e^x - 1
-//                cancels (and gives g = Delta at A = 0);
-//   |x| >= 1/2 : g = (a - 1) / A, where |a - 1| > 0.39 keeps the relative error
-//                of a within a few 1e-7 (the fp32-I/O form uses expm1f).
+// and inv_a = 1 / A (infinite at A = 0, where the series branch is taken):
+//  * fp32 I/O: |x| < 1/2 : g = Delta (1 + x/2! + ... + x^7/8!), the Taylor
+//    series of phi (truncation below 1.1e-8); |x| >= 1/2 : g = expm1f(x) / A;
+//  * bf16 I/O: |x| < 1/64 : g = Delta (1 + x/2 + x^2/6) (truncation below
+//    1.6e-7); |x| >= 1/64 : g = (a - 1) / A with a from the SFU, whose error
+//    relative to |a - 1| >= 0.0155 stays below 2e-5 -- far inside the bf16
+//    rounding of the output, and a third of the series' work.
 __device__ __forceinline__ float phi_series(float x) {
   float r = 2.4801587301587302e-05f;                 // 1/8!
   r = fmaf(r, x, 1.9841269841269841e-04f);          // 1/7!
@@ -115,24 +116,21 @@ __device__ __forceinline__ float phi_series(float x) {
   return fmaf(r, x, 1.f);
 }
 
+constexpr float kZohFastCut = 0.015625f;   // 1/64
+
 template <bool PRECISE>
 __device__ __forceinline__ float zoh_coef(float dt, float x, float a, float inv_a) {
-  const float large = PRECISE ? expm1f(x) * inv_a : (a - 1.f) * inv_a;
-  return fabsf(x) < 0.5f ? dt * phi_series(x) : large;
+  if (PRECISE) return fabsf(x) < 0.5f ? dt * phi_series(x) : expm1f(x) * inv_a;
+  const float small = dt * fmaf(fmaf(x, 1.6666666666666667e-01f, 0.5f), x, 1.f);
+  return fabsf(x) < kZohFastCut ? small : (a - 1.f) * inv_a;
 }
 
-// Two-lane form of zoh_coef (fast path) on packed f32x2 FMAs.
+// Two-lane form of the bf16-I/O zoh_coef on packed f32x2 FMAs.
 __device__ __forceinline__ float2 zoh_coef2_fast(float2 dt, float2 x, float2 a, float2 inv_a) {
-  float2 r = make_float2(2.4801587301587302e-05f, 2.4801587301587302e-05f);
-  r = __ffma2_rn(r, x, make_float2(1.9841269841269841e-04f, 1.9841269841269841e-04f));
-  r = __ffma2_rn(r, x, make_float2(1.3888888888888889e-03f, 1.3888888888888889e-03f));
-  r = __ffma2_rn(r, x, make_float2(8.3333333333333333e-03f, 8.3333333333333333e-03f));
-  r = __ffma2_rn(r, x, make_float2(4.1666666666666667e-02f, 4.1666666666666667e-02f));
-  r = __ffma2_rn(r, x, make_float2(1.6666666666666667e-01f, 1.6666666666666667e-01f));
-  r = __ffma2_rn(r, x, make_float2(0.5f, 0.5f));
+  const float2 r = __ffma2_rn(x, make_float2(1.6666666666666667e-01f, 1.6666666666666667e-01f), make_float2(0.5f, 0.5f));
   const float2 small = __fmul2_rn(dt, __ffma2_rn(r, x, make_float2(1.f, 1.f)));
   const float2 large = __fmul2_rn(__fadd2_rn(a, make_float2(-1.f, -1.f)), inv_a);
-  return make_float2(fabsf(x.x) < 0.5f ? small.x : large.x, fabsf(x.y) < 0.5f ? small.y : large.y);
+  return make_float2(fabsf(x.x) < kZohFastCut ? small.x : large.x, fabsf(x.y) < kZohFastCut ? small.y : large.y);
 }
 
 // Delta for one element: softplus(delta + bias) or the plain sum.
