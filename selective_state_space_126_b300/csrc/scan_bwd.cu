@@ -8,24 +8,28 @@
 // with the adjoint lambda_t[n] = dL/dh_t[n] = (dy_t silu(z_t)) C_t[n]
 // + Abar_{t+1}[n] lambda_{t+1}[n], run backwards in time.  As in section 3.3.2
 // of the Mamba paper ("Mamba paper translation", gitcode.csdn.net) the forward
-// states are recomputed, not stored: a forward sweep keeps one checkpoint of
-// the state every SEG steps, and the reverse sweep recomputes each SEG-step
-// segment from its checkpoint before running the adjoint through it.
+// states are recomputed, not stored: one checkpoint of the state every SEG
+// steps comes from the tiled forward kernel's checkpoint mode (or, for layouts
+// it cannot take, from a forward sweep in this kernel), and the reverse sweep
+// recomputes each SEG-step segment from its checkpoint before running the
+// adjoint through it.
 //
 // Design: one warp per CTA covers 16 channels of one batch row, two lanes per
 // channel (8 states each, as f32x2 pairs), so that twice as many warps share
 // the work; the sums over a channel's states take one shuffle between its two
-// lanes.  A segment's inputs of a channel arrive as one 128-bit load per
-// tensor when the rows allow it.
-//   * B_t and C_t of a segment are staged in shared memory by the lanes and
-//     read as warp-wide broadcasts;
+// lanes.
+//   * A segment's inputs of a channel arrive as one 128-bit load per tensor
+//     when the rows allow it (L1-cached: a 128-byte line holds eight
+//     consecutive segments of a row);
+//   * B_t and C_t of a segment are staged in shared memory, one 128-bit load
+//     per row, and read as warp-wide broadcasts;
 //   * the recomputed states of a segment go to shared memory, laid out
-//     [step][4 states][lane] as 16-byte pieces so that every access is
-//     conflict-free;
+//     [step][half of the lane's states][lane] as 16-byte pieces;
 //   * dB_t[n] and dC_t[n] are sums over the channels: per step each lane
-//     writes its 16 contributions to its channel's row of a shared 16 x 32
-//     block, every lane then sums one column, and one atomic add per (t, n)
-//     per warp goes to global memory;
+//     writes its 16 contributions to its channel's row of a shared 16 x 36
+//     block and every lane sums one column; a segment's 8 sums per lane leave
+//     as two float4 atomic adds;
+//   * du, ddelta, dz of a segment leave as one 16-byte store per row;
 //   * dA, dD and the Delta-bias gradient accumulate in registers over the
 //     whole sequence and are added atomically at the end (several batch rows
 //     share a channel).
