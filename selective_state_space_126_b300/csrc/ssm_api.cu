@@ -231,7 +231,12 @@ ssm_status_t plan_scan(const ssm_scan_args_t* a, const ScanProblem& p, ScanPlan*
   const int64_t ctas = p.B * ((p.D + 31) / 32);
   bool chunk_wanted = false;
   if (flags & SSM_SCAN_FORCE_CHUNKED) chunk_wanted = true;
-  else if (!(flags & SSM_SCAN_FORCE_TILED)) chunk_wanted = ctas < 2 * sms && p.L >= 2048;
+  else if (!(flags & SSM_SCAN_FORCE_TILED)) {
+    // Long sequences on fewer than two CTAs per SM; from 2048 steps, grids of about one CTA per SM
+    // or fewer.  On B300 (148 SMs, L = 2048, D = 1536 or 5120): 96 CTAs 103 -> 91 us and 160 CTAs
+    // 129 -> 118 us chunked, but 192 CTAs 128 -> 155 us and 240 CTAs 129 -> 171 us.
+    chunk_wanted = (ctas < 2 * (int64_t)sms && p.L >= 8 * 1024) || (ctas <= sms + sms / 8 && p.L >= 2048);
+  }
   // the chunked path launches many more CTAs than the single pass
   plan->shape = pick_shape(p, chunk_wanted ? 8 * (int64_t)sms : ctas, sms);
   const int NP = plan->shape.K * plan->shape.NS;
