@@ -164,6 +164,10 @@ def test_step_empty_is_noop(lib):
     (dict(L=4096, flags=ssm.SSM_SCAN_FORCE_CHUNKED, chunk_len=1024), "chunked"),
     (dict(B=1, D=1536, L=1 << 20), "chunked"),       # long sequence, few channels
     (dict(B=4, D=5120, L=2048), "tiled"),
+    (dict(B=1, D=5120, L=2048), "chunked"),          # 160 CTAs: about one per SM
+    (dict(B=4, D=1536, L=2048), "tiled"),            # 192 CTAs: the single pass measured faster
+    (dict(B=1, D=5120, L=1024), "tiled"),            # too short to chunk
+    (dict(B=4, D=1536, L=8192), "chunked"),          # long and under two CTAs per SM
 ])
 def test_plan(lib, kw, path):
     kw = dict(kw)
