@@ -90,7 +90,8 @@ def bench_config(cfg, world) -> dict:
     algo = algorithmic_bytes(cfg)
     return {"workload": cfg.name, "batch": cfg.batch, "dim": cfg.dim, "seqlen": cfg.seqlen, "dstate": cfg.dstate,
             "io_dtype": cfg.io_dtype, "l2": f"inputs larger than L2 ({algo / 1e6:.0f} MB moved per step vs 126 MB L2)",
-            "parallelism": f"replicas x{world}" if world > 1 else "single GPU"}
+            "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+            "timing": "per-step CUDA events; L2 flushed between steps by a 256 MB read outside the events"}
 
 
 def source_sha() -> str:
@@ -192,37 +193,48 @@ class ClockSampler:
                 "samples": len(mhz), "window": window}
 
 
-def cpu_baseline(cfg, target_s=10.0):
-    """The fp64 oracle, as it stands, on a bounded sample of the workload: whole batch rows
-    (every channel, full L), taken in order and repeated until about ``target_s`` of CPU time."""
+def oracle_row(cfg, b, threads, max_chans=None):
+    """One bounded sample of the workload on the host: batch row b (every channel when the row has at
+    most 2^24 elements, else the first channels up to that size, and at most max_chans), full L, through
+    the fp64 oracle as it stands.  Returns (state updates, seconds of oracle time, channels)."""
     import oracle
     from selective_state_space_126_b300 import synthetic as syn
+    L, N = cfg.seqlen, cfg.dstate
+    A, Dskip, bias = syn.layer_params(cfg.dim, N, cfg.dt_min, cfg.dt_max)
+    chans = cfg.dim if cfg.seqlen * cfg.dim <= (1 << 24) else max(threads, (1 << 24) // cfg.seqlen)
+    if max_chans is not None:
+        chans = max(1, min(chans, max_chans))
+    u = syn.channel_rows(cfg, syn.T_U, b, 0, chans)[None]
+    dl = syn.channel_rows(cfg, syn.T_DELTA, b, 0, chans)[None]
+    z = syn.channel_rows(cfg, syn.T_Z, b, 0, chans)[None] if cfg.gate else None
+    Bm = syn.bc_rows(cfg, syn.T_B, b)[None]
+    Cm = syn.bc_rows(cfg, syn.T_C, b)[None]
+    t0 = time.perf_counter()
+    oracle.selective_scan(u, dl, A[:chans], Bm, Cm, Dskip=Dskip[:chans] if cfg.dskip else None, z=z,
+                          delta_bias=bias[:chans], nthreads=threads)
+    return chans * L * N, time.perf_counter() - t0, chans
+
+
+def cpu_baseline(cfg, target_s=10.0):
+    """The fp64 oracle, as it stands, on a bounded sample of the workload: whole batch rows
+    (see oracle_row), taken in order and repeated until about ``target_s`` of CPU time."""
+    import oracle
     threads = oracle.default_threads()
     try:
         cores = len(os.sched_getaffinity(0))
     except AttributeError:
         cores = os.cpu_count() or 1
-    L, N = cfg.seqlen, cfg.dstate
-    A, Dskip, bias = syn.layer_params(cfg.dim, N, cfg.dt_min, cfg.dt_max)
-    chans = cfg.dim if cfg.seqlen * cfg.dim <= (1 << 24) else max(threads, (1 << 24) // cfg.seqlen)
-    elapsed, updates, rows = 0.0, 0, 0
+    elapsed, updates, rows, chans = 0.0, 0, 0, 0
     while elapsed < target_s and rows < 64:
-        b = rows % cfg.batch
-        u = syn.channel_rows(cfg, syn.T_U, b, 0, chans)[None]
-        dl = syn.channel_rows(cfg, syn.T_DELTA, b, 0, chans)[None]
-        z = syn.channel_rows(cfg, syn.T_Z, b, 0, chans)[None] if cfg.gate else None
-        Bm = syn.bc_rows(cfg, syn.T_B, b)[None]
-        Cm = syn.bc_rows(cfg, syn.T_C, b)[None]
-        t0 = time.perf_counter()
-        oracle.selective_scan(u, dl, A[:chans], Bm, Cm, Dskip=Dskip[:chans] if cfg.dskip else None, z=z,
-                              delta_bias=bias[:chans], nthreads=threads)
-        elapsed += time.perf_counter() - t0
-        updates += chans * L * N
+        n, dt, chans = oracle_row(cfg, rows % cfg.batch, threads)
+        elapsed += dt
+        updates += n
         rows += 1
     return {"value": updates / elapsed, "unit": UNIT, "cores": threads, "host_cores_visible": cores,
             "kind": "oracle",
-            "sample": f"{rows} batch rows of the workload (channels 0..{chans - 1} of {cfg.dim} each, full L={L}, "
-                      f"N={N}), {updates} state updates in {elapsed:.1f} s of oracle time"}
+            "sample": f"{rows} batch rows of the workload (channels 0..{chans - 1} of {cfg.dim} each, "
+                      f"full L={cfg.seqlen}, N={cfg.dstate}), {updates} state updates in {elapsed:.1f} s "
+                      f"of oracle time"}
 
 
 def random_device_inputs(cfg, seed, device):
@@ -254,6 +266,52 @@ def random_device_inputs(cfg, seed, device):
     out["Dskip"] = torch.from_numpy(Dskip).to(device) if cfg.dskip else None
     out["delta_bias"] = torch.from_numpy(bias).to(device)
     return out
+
+
+def sfu_ops_per_update(cfg):
+    """SFU operations the bf16 scan kernel issues per state update: one ex2 for Abar per update, and per
+    (batch, channel, step) one ex2 in softplus and, with the gate, one ex2 and one rcp in silu."""
+    per_bdl_ex2 = 1 + (1 if cfg.gate else 0)
+    per_bdl_rcp = 1 if cfg.gate else 0
+    return 1.0 + per_bdl_ex2 / cfg.dstate, per_bdl_rcp / cfg.dstate
+
+
+def probe_sfu_rate(lib, op, sms, stream, dev):
+    """SFU operations per second on this GPU, measured with the library's probe kernel (8 independent
+    chains per thread, 8 blocks of 256 threads per SM), best of 5 launches after a warm-up."""
+    import torch
+    blocks, iters = 8 * sms, 2048
+    sink = torch.empty(blocks * 256, dtype=torch.float32, device=dev)
+    sh = ctypes.c_void_p(stream.cuda_stream)
+    run = lambda: lib.ssm_probe_sfu(op, blocks, iters, ctypes.c_void_p(sink.data_ptr()), sh)
+    if run() != 0:
+        raise RuntimeError("ssm_probe_sfu failed")
+    best = None
+    for _ in range(5):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        run()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1)
+        best = ms if best is None else min(best, ms)
+    return blocks * 256 * iters * 8 / (best * 1e-3)
+
+
+def sfu_roofline(lib, cfg, launch_ms, sms, mhz, stream, dev):
+    """The scan's second roofline: SFU work per launch in ex2-equivalents (an rcp counts as the ratio of
+    the measured ex2 and rcp rates) over the launch time, against the measured ex2 rate."""
+    ex2_rate = probe_sfu_rate(lib, 0, sms, stream, dev)
+    rcp_rate = probe_sfu_rate(lib, 1, sms, stream, dev)
+    ex2_pu, rcp_pu = sfu_ops_per_update(cfg)
+    equiv = ex2_pu + rcp_pu * ex2_rate / rcp_rate
+    achieved = cfg.updates * equiv / (launch_ms * 1e-3)
+    return {"bound": "alu", "achieved": achieved / 1e12, "peak": ex2_rate / 1e12, "unit": "Tex2-equiv/s",
+            "frac": achieved / ex2_rate, "ex2_per_update": ex2_pu, "rcp_per_update": rcp_pu,
+            "ex2_equiv_per_update": equiv,
+            "peak_basis": (f"measured by ssm_probe_sfu on this GPU: ex2 {ex2_rate / 1e12:.2f} T/s "
+                           f"({ex2_rate / (sms * mhz * 1e6):.1f}/clk/SM at the median {mhz:.0f} MHz), "
+                           f"rcp {rcp_rate / 1e12:.2f} T/s")}
 
 
 def time_launches(run, n, stream, flush=None):
@@ -297,7 +355,7 @@ def other_rows(lib, ssm, peak, stream, dev, which="all", decode_steps=1000):
     # Reading 2x the L2 evicts the previous launch's lines and leaves only clean ones behind (a
     # write-based flush would leave dirty lines whose write-back lands in the timed launch).
     flush_buf = torch.ones(64 << 20, dtype=torch.float32, device=dev)
-    flush_sink = torch.empty(1, dtype=torch.float32, device=dev)
+    flush_sink = torch.empty((), dtype=torch.float32, device=dev)
 
     def flush():
         torch.sum(flush_buf, dim=0, out=flush_sink)
@@ -445,38 +503,29 @@ def other_rows(lib, ssm, peak, stream, dev, which="all", decode_steps=1000):
 
 
 def run_reference(args, rank, world):
-    """--impl reference: the fp64 oracle timed on the host cores (rank 0 only)."""
+    """--impl reference: the fp64 oracle timed on the host cores (rank 0 only).  Each step is one
+    bounded sample of the workload, the same sample the cpu_baseline leg takes: one whole batch row
+    (every channel, full L), rows taken in order."""
     if rank != 0:
         return
     import oracle
-    from selective_state_space_126_b300 import synthetic as syn
     cfg = workload(args)
-    L, N = cfg.seqlen, cfg.dstate
-    A, Dskip, bias = syn.layer_params(cfg.dim, N, cfg.dt_min, cfg.dt_max)
     threads = oracle.default_threads()
-    chans = max(threads, 16)          # one bounded sample per step: `chans` full rows
-    u = syn.channel_rows(cfg, syn.T_U, 0, 0, chans)[None]
-    dl = syn.channel_rows(cfg, syn.T_DELTA, 0, 0, chans)[None]
-    z = syn.channel_rows(cfg, syn.T_Z, 0, 0, chans)[None] if cfg.gate else None
-    Bm = syn.bc_rows(cfg, syn.T_B, 0)[None]
-    Cm = syn.bc_rows(cfg, syn.T_C, 0)[None]
-
-    def step():
-        oracle.selective_scan(u, dl, A[:chans], Bm, Cm, Dskip=Dskip[:chans] if cfg.dskip else None, z=z,
-                              delta_bias=bias[:chans], nthreads=threads)
-
-    for _ in range(args.warmup):
-        step()
-    t0 = time.perf_counter()
-    for _ in range(args.steps):
-        step()
-    dt = time.perf_counter() - t0
-    updates = chans * L * N * args.steps
-    value = updates / dt
-    sample = f"each step: batch row 0, channels 0..{chans - 1} of {cfg.dim}, full L={L}, N={N}"
+    # whole rows unless the run would then exceed about a minute of oracle time (at ~6e8 updates/s)
+    cap = max(256, int(3.6e10 / max(1, args.steps + args.warmup) / (cfg.seqlen * cfg.dstate)))
+    for i in range(args.warmup):
+        oracle_row(cfg, i % cfg.batch, threads, cap)
+    updates, elapsed, chans = 0, 0.0, 0
+    for i in range(args.steps):
+        n, dt, chans = oracle_row(cfg, i % cfg.batch, threads, cap)
+        updates += n
+        elapsed += dt
+    value = updates / elapsed
+    sample = (f"each step: one batch row of the workload (channels 0..{chans - 1} of {cfg.dim}, full "
+              f"L={cfg.seqlen}, N={cfg.dstate}), rows in order; the cpu_baseline leg takes the same whole rows")
     print(json.dumps({
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": elapsed / args.steps * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": bench_config(cfg, world),
         "cpu_baseline": {"kind": "oracle", "cores": threads, "sample": sample, "value": value, "unit": UNIT},
@@ -540,6 +589,14 @@ def main():
         step()
     torch.cuda.synchronize()
 
+    # L2 flush between steps, outside the step events: a read of twice the L2 leaves only clean lines
+    # behind, so no write-back of the previous step's y lands in the next timed step
+    flush_buf = torch.ones(64 << 20, dtype=torch.float32, device=dev)
+    flush_sink = torch.empty((), dtype=torch.float32, device=dev)
+
+    def flush():
+        torch.sum(flush_buf, dim=0, out=flush_sink)
+
     sampler = ClockSampler(int(os.environ.get("CUDA_VISIBLE_DEVICES", "0").split(",")[0])
                            if os.environ.get("CUDA_VISIBLE_DEVICES", "").isdigit() else local)
     sampler.start()
@@ -551,6 +608,7 @@ def main():
     w0 = time.time()
     start.record(stream)
     for i in range(args.steps):
+        flush()
         ev[i][0].record(stream)
         step()
         ev[i][1].record(stream)
@@ -560,10 +618,11 @@ def main():
         torch.distributed.barrier()
     w1 = time.time()
     sampler.stop()
-    total_ms = start.elapsed_time(stop)
+    region_ms = start.elapsed_time(stop)
     launch_ms = float(np.mean([s.elapsed_time(e) for s, e in ev]))
-    total_ms = max_over_ranks(total_ms, world, dev)
-    ms_per_step = total_ms / args.steps
+    # a step is the scan between its events; the flushes between steps are not part of it
+    ms_per_step = max_over_ranks(launch_ms, world, dev)
+    del flush_buf, flush_sink
     updates_per_step = cfg.updates * world
     value = job_value(cfg.updates, world, ms_per_step)
 
@@ -684,19 +743,16 @@ def main():
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
     clocks = sampler.summary(w0, w1)
     mhz = (clocks or {}).get("sm_mhz") or 1900.0
-    ex2_rate = cfg.updates / (launch_ms * 1e-3)                 # one SFU ex2 per state update
-    ex2_peak = 32 * sms * mhz * 1e6                             # 32 ex2 / clk / SM on B300
+    sfu = sfu_roofline(lib, cfg, launch_ms, sms, mhz, stream, dev)
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
-        "warmup": max(3, args.warmup), "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "warmup": max(3, args.warmup), "ms_per_step": ms_per_step, "timed_region_ms": region_ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": bench_config(cfg, world), "path": path,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "traffic": traffic, "peak_kind": peak_kind, "algorithmic_bytes_per_launch": algo,
                      "kernel_ms": kernel_ms},
-        "sfu_roofline": {"bound": "alu", "achieved": ex2_rate / 1e12, "peak": ex2_peak / 1e12,
-                         "unit": "Tex2/s", "frac": ex2_rate / ex2_peak,
-                         "peak_basis": f"32 ex2/clk/SM x {sms} SMs x median {mhz:.0f} MHz"},
+        "sfu_roofline": sfu,
         "gpu_launches": args.steps * launches_per_step,
         "clocks": clocks,
         "e2e": e2e,

@@ -257,19 +257,21 @@ ssm_status_t ssm_get_device_status(void *stream, int clear, int *code);
  * an engine that owns every byte of device memory, a host that only holds
  * the raw input and output pointers, or code that must not take the implicit
  * device synchronisation of cudaMalloc/cudaFree.  This entry point takes the
- * same arguments as ssm_scan_fwd (args->workspace and args->workspace_bytes
- * are ignored) and keeps the chunk records in a scratch array that the
+ * same arguments as ssm_scan_fwd, except that args->workspace and
+ * args->workspace_bytes are ignored and args->flags must be 0 or
+ * SSM_SCAN_FORCE_CHUNKED (any other bit is SSM_ERR_INVALID_ARG): it always
+ * runs the chunked path.  The chunk records live in a scratch array that the
  * library reserves statically on every GPU it is loaded on, for the life of
  * the process: SSM_NOALLOC_SCRATCH_BYTES bytes.  It calls no allocator.
  *
  *   - The problem must fit: ssm_scan_workspace_size() with
  *     flags = SSM_SCAN_FORCE_CHUNKED must report at most
  *     SSM_NOALLOC_SCRATCH_BYTES, else SSM_ERR_WORKSPACE is returned and
- *     nothing is enqueued.  Layouts the chunked path cannot take return
- *     SSM_ERR_UNSUPPORTED.
- *   - The first call on each device resolves the scratch array's device
- *     address (cudaGetSymbolAddress) with that device current; make that
- *     first call before any stream capture on the device.
+ *     nothing is enqueued.  The 1 x 1536-channel, 2^20-step bf16 scan with
+ *     automatic chunking needs about 2.6 MB.  Layouts the chunked path cannot
+ *     take return SSM_ERR_UNSUPPORTED.
+ *   - Every call looks up the scratch array's address in the current
+ *     device's context (cudaGetSymbolAddress, a host-side query).
  *   - Every call on a device shares the one scratch array and leaves its
  *     records there.  No record needs to start at zero (each call writes
  *     every record before reading it), but calls whose kernels overlap on
@@ -278,6 +280,15 @@ ssm_status_t ssm_get_device_status(void *stream, int clear, int *code);
  */
 #define SSM_NOALLOC_SCRATCH_BYTES ((size_t)8 << 20)
 ssm_status_t ssm_scan_fwd_noalloc(const ssm_scan_args_t *args, void *stream);
+
+/* Measurement helper, not part of the method: enqueues blocks x 256 threads,
+ * each issuing iters x 8 independent SFU operations (op 0: ex2.approx.f32, the
+ * scan's exponential; op 1: rcp.approx.f32, the reciprocal in silu), and writes
+ * one float per thread to sink (device, blocks * 256 floats).  Timing the
+ * launch with events on `stream` gives the special-function-unit rate that
+ * bounds the scan's arithmetic (its second roofline).  Returns
+ * SSM_ERR_INVALID_ARG for a bad op, size or NULL sink. */
+ssm_status_t ssm_probe_sfu(int op, int blocks, int iters, float *sink, void *stream);
 
 /* Kernel path ssm_scan_fwd would take for these arguments:
  * 0 = generic, 1 = tiled single pass, 2 = chunked three-pass; -1 on error. */

@@ -32,7 +32,7 @@ PATH_NAMES = {0: "generic", 1: "tiled", 2: "chunked"}
 EXPORTED_SYMBOLS = ["ssm_scan_workspace_size", "ssm_scan_fwd", "ssm_state_update", "ssm_status_string",
                     "ssm_last_error_detail", "ssm_get_device_status", "ssm_scan_plan_path", "ssm_version",
                     "ssm_abi_sizeof", "ssm_scan_fwd_noalloc", "ssm_causal_conv1d_fwd",
-                    "ssm_scan_bwd_workspace_size", "ssm_scan_bwd"]
+                    "ssm_scan_bwd_workspace_size", "ssm_scan_bwd", "ssm_probe_sfu"]
 
 _i64 = ctypes.c_int64
 _vp = ctypes.c_void_p
@@ -135,6 +135,8 @@ def load_library(path: str = LIB_PATH):
         lib.ssm_scan_bwd_workspace_size.restype = ctypes.c_int
         lib.ssm_scan_bwd.argtypes = [ctypes.POINTER(BwdArgs), _vp]
         lib.ssm_scan_bwd.restype = ctypes.c_int
+        lib.ssm_probe_sfu.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, _vp, _vp]
+        lib.ssm_probe_sfu.restype = ctypes.c_int
         if (lib.ssm_abi_sizeof(0) != ctypes.sizeof(ScanArgs) or lib.ssm_abi_sizeof(1) != ctypes.sizeof(StepArgs)
                 or lib.ssm_abi_sizeof(2) != ctypes.sizeof(ConvArgs) or lib.ssm_abi_sizeof(3) != ctypes.sizeof(BwdArgs)):
             raise ImportError("libssm.so argument structs do not match this binding")

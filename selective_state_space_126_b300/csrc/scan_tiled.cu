@@ -314,7 +314,11 @@ __global__ void __launch_bounds__(32 * K, min_blocks(K, NS))
   bool ok = ntiles > 0 ? mbar_wait(bar_base, 0) : true;
   if (ok && ntiles > 0) stage_a(0, Bool<false>{});
   if (!ok) record_status(p.status, SSM_ERR_TIMEOUT);
-  if (__syncthreads_or(!ok)) return;   // nothing else is in flight
+  if (__syncthreads_or(!ok)) {
+    // tile 0's load may still be writing this CTA's shared memory: let it land (bounded) before exiting
+    if (tid == 0) mbar_wait(bar_base, 0);
+    return;
+  }
   if (tid == 0 && ntiles > 1) issue(1);
   for (int k = 0; k < ntiles; ++k) {
     // ---- stage B: the recurrence over the T steps of the tile ----
@@ -402,8 +406,13 @@ __global__ void __launch_bounds__(32 * K, min_blocks(K, NS))
       if (ok && next) stage_a(k + 1, Bool<false>{});
     }
     if (!ok) record_status(p.status, SSM_ERR_TIMEOUT);
-    if (__syncthreads_or(!ok)) {   // tile k+1's copy never completed; only tile k's store may be in flight
-      if (MODE == MODE_OUTPUT && tid == 0) bulk_wait<0>();
+    if (__syncthreads_or(!ok)) {
+      // Tile k+1's load (issued, not yet consumed) may still be writing shared memory, and the stores
+      // of tiles k-1 and k-2 may still be reading it: wait for all of them (bounded) before the CTA exits.
+      if (tid == 0) {
+        mbar_wait(bar_base + 8 * ((k + 1) % kStages), (uint32_t)((k + 1) / kStages) & 1u);
+        if (MODE == MODE_OUTPUT) bulk_wait<0>();
+      }
       return;
     }
     if (tid == 0) {

@@ -700,28 +700,15 @@ namespace {
 // One per device that loads the library, held until the process exits.
 static __device__ __align__(256) unsigned char g_noalloc_scratch[SSM_NOALLOC_SCRATCH_BYTES];
 
-constexpr int kMaxDevices = 64;
-std::mutex g_noalloc_mu;
-void* g_noalloc_ptr[kMaxDevices] = {nullptr};
-
-// Device address of the scratch array on the current device, resolved once per
-// device.  Returns nullptr (and fills *err) if the lookup fails.
+// Device address of the scratch array in the current device's context.  It is
+// looked up on every call (a host-side query, no allocation), so that a
+// context rebuilt after cudaDeviceReset, where the array may sit elsewhere,
+// never receives a stale address.  Returns nullptr (and fills *err) if the
+// lookup fails.
 void* noalloc_scratch(cudaError_t* err) {
-  int dev = 0;
-  *err = cudaGetDevice(&dev);
-  if (*err != cudaSuccess) return nullptr;
-  if (dev < 0 || dev >= kMaxDevices) {
-    *err = cudaErrorInvalidDevice;
-    return nullptr;
-  }
-  std::lock_guard<std::mutex> lk(g_noalloc_mu);
-  if (!g_noalloc_ptr[dev]) {
-    void* p = nullptr;
-    *err = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-    if (*err != cudaSuccess) return nullptr;
-    g_noalloc_ptr[dev] = p;
-  }
-  return g_noalloc_ptr[dev];
+  void* p = nullptr;
+  *err = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+  return *err == cudaSuccess ? p : nullptr;
 }
 
 }  // namespace
@@ -734,6 +721,8 @@ ssm_status_t ssm_scan_fwd_noalloc(const ssm_scan_args_t* args, void* stream) {
   ssm_status_t st = validate_scan(args, &p);
   if (st != SSM_OK) return st;
   if (p.B == 0 || p.D == 0) return ok();
+  if (args->flags & ~SSM_SCAN_FORCE_CHUNKED)
+    return fail(SSM_ERR_INVALID_ARG, "flags 0x%x: this entry point runs only the chunked path", (unsigned)args->flags);
   ssm_scan_args_t a = *args;
   a.flags = SSM_SCAN_FORCE_CHUNKED;
   a.workspace = nullptr;

@@ -170,6 +170,11 @@ def test_step_empty_is_noop(lib):
     (dict(B=4, D=1536, L=8192), "chunked"),          # long and under two CTAs per SM
 ])
 def test_plan(lib, kw, path):
+    # the planner's cut-offs are in CTAs per SM; these expected paths hold for 148 SMs (B300, and
+    # the value the library assumes when no GPU is present)
+    import torch
+    if torch.cuda.is_available() and torch.cuda.get_device_properties(0).multi_processor_count != 148:
+        pytest.skip("expected paths are for 148 SMs")
     kw = dict(kw)
     flags = kw.pop("flags", 0)
     chunk_len = kw.pop("chunk_len", 0)
