@@ -32,6 +32,12 @@
  * parallel scan"; Blelloch 1990) exists only so that tests can check the
  * two orders against each other.
  *
+ * Complex A (the S4D-Lin initialisation A_n = -1/2 + n i, "gitcode", section
+ * 3.6 "real vs complex" and "initialisation") is a separate function: the
+ * state h and Abar = exp(Delta A) are complex, the Euler input term
+ * Delta B u is real and enters the state as it is, and the output reads the
+ * real part of the C contraction, y = Re(sum_n C h) + D u (then the gate).
+ *
  * Readings where the pages are silent (each also listed in the design notes):
  *   - the gate multiplies the whole output C.h + D.u;
  *   - y_t uses the state after the update at step t;
@@ -43,6 +49,7 @@
  *   A : (D, N)    Dskip, delta_bias : (D)    h0, h_last, state : (B, D, N)
  * Nullable: z, Dskip, delta_bias, h0, h_last.
  */
+#include <complex.h>
 #include <math.h>
 #include <pthread.h>
 #include <stdint.h>
@@ -262,6 +269,55 @@ int oracle_selective_scan(int64_t B, int64_t D, int64_t L, int64_t N,
     free(jobs);
     free(tids);
     return rc;
+}
+
+/*
+ * Selective scan with a complex diagonal A (S4D-Lin, "gitcode" section 3.6):
+ * per channel the complex state runs
+ *     h_t[n] = exp(Delta_t A[d,n]) h_{t-1}[n] + Delta_t B[b,n,t] u[b,d,t]
+ *     y[b,d,t] = Re(sum_n C[b,n,t] h_t[n]) + Dskip[d] u[b,d,t]     (then * silu(z))
+ * with A = A_re + i A_im (the real arrays of the real scan's layout, (D, N)).
+ * h0 / h_last are complex (B, D, N), stored as interleaved (re, im) doubles;
+ * both nullable.  Single-threaded per call block, sequential order only.
+ */
+int oracle_selective_scan_complex(int64_t B, int64_t D, int64_t L, int64_t N,
+                                  const double *u, const double *delta, const double *z,
+                                  const double *Bm, const double *Cm, const double *A_re,
+                                  const double *A_im, const double *Dskip,
+                                  const double *delta_bias, const double *h0,
+                                  int delta_softplus, double *y, double *h_last) {
+    if (B < 0 || D < 0 || L < 0 || N < 0) return -1;
+    if (!u || !delta || !Bm || !Cm || !A_re || !A_im || !y) return -1;
+    double complex *h = (double complex *)malloc(sizeof(double complex) * (size_t)(N > 0 ? N : 1));
+    if (!h) return -1;
+    for (int64_t c = 0; c < B * D; ++c) {
+        const int64_t b = c / D, d = c % D;
+        const double bias = delta_bias ? delta_bias[d] : 0.0;
+        const double Dd = Dskip ? Dskip[d] : 0.0;
+        for (int64_t n = 0; n < N; ++n)
+            h[n] = h0 ? h0[2 * (c * N + n)] + I * h0[2 * (c * N + n) + 1] : 0.0;
+        for (int64_t t = 0; t < L; ++t) {
+            const double dt = discretisation_step(delta[c * L + t], bias, delta_softplus);
+            const double ut = u[c * L + t];
+            double complex acc = 0.0;
+            for (int64_t n = 0; n < N; ++n) {
+                const double complex a = A_re[d * N + n] + I * A_im[d * N + n];
+                const double complex abar = cexp(dt * a);
+                h[n] = abar * h[n] + dt * Bm[b * N * L + n * L + t] * ut;
+                acc += Cm[b * N * L + n * L + t] * h[n];
+            }
+            double v = creal(acc) + Dd * ut;
+            if (z) v *= z[c * L + t] * sigmoid(z[c * L + t]);
+            y[c * L + t] = v;
+        }
+        if (h_last)
+            for (int64_t n = 0; n < N; ++n) {
+                h_last[2 * (c * N + n)] = creal(h[n]);
+                h_last[2 * (c * N + n) + 1] = cimag(h[n]);
+            }
+    }
+    free(h);
+    return 0;
 }
 
 /*

@@ -462,7 +462,127 @@ CONV_PINS = [
 ]
 
 
-ALL_PINS = CONV_PINS + BWD_PINS + [
+# --------------------------------------------------------------------------
+# complex diagonal A (S4D-Lin, "Mamba paper translation" section 3.6): complex state,
+# real input term, y = Re(C . h) + D u
+# --------------------------------------------------------------------------
+
+def _complex_inputs(rng, Bsz, D, L, N):
+    x = _rand_inputs(rng, Bsz, D, L, N)
+    x["A"] = -rng.uniform(0.2, 1.5, (D, N)) + 1j * rng.uniform(-4.0, 4.0, (D, N))
+    x["h0"] = rng.standard_normal((Bsz, D, N)) + 1j * rng.standard_normal((Bsz, D, N))
+    return x
+
+
+def pin_complex_zero_imag_is_real(lib):
+    """With Im A = 0 and a real h0 the complex scan is the (pinned) real scan."""
+    rng = np.random.default_rng(41)
+    x = _rand_inputs(rng, 2, 3, 33, 5, h0=True)
+    yr, hr = oracle.selective_scan(x["u"], x["delta"], x["A"], x["Bm"], x["Cm"], Dskip=x["Dskip"], z=x["z"],
+                                   delta_bias=x["delta_bias"], h0=x["h0"], return_last_state=True, lib=lib)
+    yc, hc = oracle.selective_scan_complex(x["u"], x["delta"], x["A"] + 0j, x["Bm"], x["Cm"], Dskip=x["Dskip"],
+                                           z=x["z"], delta_bias=x["delta_bias"], h0=x["h0"] + 0j,
+                                           return_last_state=True, lib=lib)
+    _close(yc, yr, rtol=1e-12, atol=1e-12, what="complex scan with real A: y")
+    _close(hc.real, hr, rtol=1e-12, atol=1e-12, what="complex scan with real A: Re h_last")
+    _close(hc.imag, np.zeros_like(hr), atol=0.0, what="complex scan with real A: Im h_last")
+
+
+def pin_complex_lti_convolution(lib):
+    """Time-invariant complex case: y = K * u + D u (gated) with
+    K_k = Re(sum_n C[n] Abar[n]^k Delta B[n]), Abar = exp(Delta A) complex, as powers."""
+    rng = np.random.default_rng(42)
+    Bsz, D, L, N = 2, 3, 40, 4
+    delta_c = rng.standard_normal((Bsz, D, 1))
+    Bc = rng.standard_normal((Bsz, N, 1))
+    Cc = rng.standard_normal((Bsz, N, 1))
+    A = oracle.s4d_lin(D, N) * rng.uniform(0.5, 1.5, (D, N))
+    bias = rng.uniform(-3.0, 0.0, D)
+    Dskip = rng.standard_normal(D)
+    u = rng.standard_normal((Bsz, D, L))
+    z = rng.standard_normal((Bsz, D, L))
+    y = oracle.selective_scan_complex(u, np.repeat(delta_c, L, 2), A, np.repeat(Bc, L, 2), np.repeat(Cc, L, 2),
+                                      Dskip=Dskip, z=z, delta_bias=bias, lib=lib)
+    ks = np.arange(L)
+    for b in range(Bsz):
+        for d in range(D):
+            dt = _softplus(delta_c[b, d, 0] + bias[d])
+            abar = np.exp(dt * A[d])
+            K = (Cc[b, :, 0][None, :] * np.power(abar[None, :], ks[:, None]) * (dt * Bc[b, :, 0])[None, :]).sum(1).real
+            conv = np.array([np.dot(K[:t + 1][::-1], u[b, d, :t + 1]) for t in range(L)])
+            ref = (conv + Dskip[d] * u[b, d]) * z[b, d] * _sigmoid(z[b, d])
+            _close(y[b, d], ref, rtol=1e-11, atol=1e-12, what=f"complex LTI conv b{b} d{d}")
+
+
+def pin_complex_rotation_impulse(lib):
+    """Re A = 0: |Abar| = 1, the state only rotates.  An impulse u_0 = 1 from h0 = 0 gives
+    h_t[n] = Delta_0 B_0[n] exp(i A_im[n] (Delta_1 + ... + Delta_t)), so
+    y_t = sum_n C_t[n] Delta_0 B_0[n] cos(A_im[n] S_t) + D u_t (no gate)."""
+    rng = np.random.default_rng(43)
+    D, L, N = 2, 25, 3
+    A = 1j * rng.uniform(-3.0, 3.0, (D, N))
+    u = np.zeros((1, D, L))
+    u[0, :, 0] = 1.0
+    delta = rng.standard_normal((1, D, L))
+    bias = rng.uniform(-2.0, 0.5, D)
+    Bm, Cm = rng.standard_normal((1, N, L)), rng.standard_normal((1, N, L))
+    Dskip = rng.standard_normal(D)
+    y, hl = oracle.selective_scan_complex(u, delta, A, Bm, Cm, Dskip=Dskip, delta_bias=bias,
+                                          return_last_state=True, lib=lib)
+    for d in range(D):
+        dts = _softplus(delta[0, d] + bias[d])
+        S = np.concatenate([[0.0], np.cumsum(dts[1:])])            # S_t = Delta_1 + ... + Delta_t
+        amp = dts[0] * Bm[0, :, 0]                                   # (N,)
+        ref = (Cm[0] * amp[:, None] * np.cos(A[d].imag[:, None] * S[None, :])).sum(0) + Dskip[d] * u[0, d]
+        _close(y[0, d], ref, rtol=1e-11, atol=1e-12, what=f"rotation y d{d}")
+        h_ref = amp * np.exp(1j * A[d].imag * S[-1])
+        _close(hl[0, d].real, h_ref.real, rtol=1e-11, atol=1e-12, what=f"rotation Re h d{d}")
+        _close(hl[0, d].imag, h_ref.imag, rtol=1e-11, atol=1e-12, what=f"rotation Im h d{d}")
+
+
+def pin_complex_unrolled_sum(lib):
+    """Brute force with numpy complex arithmetic on tiny inputs: h_t = (prod Abar) h0 +
+    sum_s (prod_{r=s+1..t} Abar_r) Delta_s B_s u_s, y_t = (Re(C_t . h_t) + D u_t) silu(z_t)."""
+    rng = np.random.default_rng(44)
+    Bsz, D, L, N = 1, 2, 7, 3
+    x = _complex_inputs(rng, Bsz, D, L, N)
+    y, hl = oracle.selective_scan_complex(x["u"], x["delta"], x["A"], x["Bm"], x["Cm"], Dskip=x["Dskip"],
+                                          z=x["z"], delta_bias=x["delta_bias"], h0=x["h0"],
+                                          return_last_state=True, lib=lib)
+    for d in range(D):
+        dts = _softplus(x["delta"][0, d] + x["delta_bias"][d])
+        ab = np.exp(dts[:, None] * x["A"][d][None, :])                 # (L, N)
+        for t in range(L):
+            h = np.prod(ab[:t + 1], axis=0) * x["h0"][0, d]
+            for s_ in range(t + 1):
+                h = h + np.prod(ab[s_ + 1:t + 1], axis=0) * dts[s_] * x["Bm"][0, :, s_] * x["u"][0, d, s_]
+            v = np.sum(x["Cm"][0, :, t] * h).real + x["Dskip"][d] * x["u"][0, d, t]
+            v *= x["z"][0, d, t] * _sigmoid(x["z"][0, d, t])
+            _close(y[0, d, t], v, rtol=1e-11, atol=1e-12, what=f"complex unrolled y d{d} t{t}")
+        _close(hl[0, d].real, h.real, rtol=1e-11, atol=1e-12, what=f"complex unrolled Re h d{d}")
+        _close(hl[0, d].imag, h.imag, rtol=1e-11, atol=1e-12, what=f"complex unrolled Im h d{d}")
+
+
+def pin_complex_conjugate_symmetry(lib):
+    """Real inputs: replacing A by its conjugate conjugates the state and leaves y unchanged."""
+    rng = np.random.default_rng(45)
+    x = _complex_inputs(rng, 2, 3, 30, 4)
+    y1, h1 = oracle.selective_scan_complex(x["u"], x["delta"], x["A"], x["Bm"], x["Cm"], Dskip=x["Dskip"],
+                                           z=x["z"], delta_bias=x["delta_bias"], h0=x["h0"],
+                                           return_last_state=True, lib=lib)
+    y2, h2 = oracle.selective_scan_complex(x["u"], x["delta"], np.conj(x["A"]), x["Bm"], x["Cm"],
+                                           Dskip=x["Dskip"], z=x["z"], delta_bias=x["delta_bias"],
+                                           h0=np.conj(x["h0"]), return_last_state=True, lib=lib)
+    _close(y2, y1, rtol=1e-12, atol=1e-12, what="conjugate A: y")
+    _close(h2.real, h1.real, rtol=1e-12, atol=1e-12, what="conjugate A: Re h")
+    _close(h2.imag, -h1.imag, rtol=1e-12, atol=1e-12, what="conjugate A: Im h")
+
+
+COMPLEX_PINS = [pin_complex_zero_imag_is_real, pin_complex_lti_convolution, pin_complex_rotation_impulse,
+                pin_complex_unrolled_sum, pin_complex_conjugate_symmetry]
+
+
+ALL_PINS = CONV_PINS + BWD_PINS + COMPLEX_PINS + [
     pin_golden_recurrence, pin_golden_gated, pin_lti_equals_convolution, pin_theorem1_gated_rnn,
     pin_unrolled_sum, pin_single_step_closed_form, pin_tree_order_matches_sequential,
     pin_boundary_reset, pin_ignore_window, pin_chunk_invariance, pin_step_matches_scan,

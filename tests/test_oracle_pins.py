@@ -64,6 +64,15 @@ MUTANTS = [
     ("const double dd = delta_softplus ? dDelta * sigmoid(dl[t] + bias) : dDelta;",
      "const double dd = dDelta;"),
     ("du_acc += lt * dts[t] * Bb[n * L + t];", "du_acc += lt * Bb[n * L + t];"),
+    # the complex (S4D-Lin) scan
+    ("double v = creal(acc) + Dd * ut;", "double v = cimag(acc) + Dd * ut;"),
+    ("const double complex abar = cexp(dt * a);", "const double complex abar = cexp(dt * conj(a));"),
+    ("const double complex abar = cexp(dt * a);", "const double complex abar = exp(dt * creal(a));"),
+    ("h[n] = abar * h[n] + dt * Bm[b * N * L + n * L + t] * ut;",
+     "h[n] = abar * h[n] + I * dt * Bm[b * N * L + n * L + t] * ut;"),
+    ("h[n] = h0 ? h0[2 * (c * N + n)] + I * h0[2 * (c * N + n) + 1] : 0.0;",
+     "h[n] = h0 ? h0[2 * (c * N + n)] : 0.0;"),
+    ("h_last[2 * (c * N + n) + 1] = cimag(h[n]);", "h_last[2 * (c * N + n) + 1] = -cimag(h[n]);"),
 ]
 
 
