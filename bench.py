@@ -57,7 +57,8 @@ def parse():
     ap.add_argument("--no-rows", action="store_true", help="skip the other workloads' timing rows")
     ap.add_argument("--only-rows", action="store_true",
                     help="time only the other workloads' rows (one line of JSON; for profiling their kernels)")
-    ap.add_argument("--rows", default="all", help="comma-separated subset of rows: m130, ti, long, decode, conv, bwd, zoh")
+    ap.add_argument("--rows", default="all",
+                    help="comma-separated subset of rows: m130, ti, long, decode, conv, bwd, zoh, cplx")
     ap.add_argument("--decode-steps", type=int, default=1000, help="decode steps of the decode row")
     return ap.parse_args()
 
@@ -340,7 +341,8 @@ def decode_bytes(cfg) -> int:
             + cfg.dim * cfg.dstate * 4 + 2 * cfg.dim * 4)
 
 
-ROW_KEYS = {"m130": "mamba130m_bf16_b8_d1536_l2048_n16", "ti": "mamba2.8b_ti_bf16_b1_d5120_l2048_n16",
+ROW_KEYS = {"cplx": "mamba2.8b_s4dlin_complex_bf16_b4_d5120_l2048_n16",
+            "m130": "mamba130m_bf16_b8_d1536_l2048_n16", "ti": "mamba2.8b_ti_bf16_b1_d5120_l2048_n16",
             "long": "long_bf16_b1_d1536_l1048576_n16", "decode": "decode_bf16_b256_d5120_n16_x1000",
             "conv": "conv1d_silu_bf16_b4_d5120_l2048_w4", "bwd": "scan_bwd_mamba2.8b_bf16_b4_d5120_l2048_n16",
             "zoh": "mamba2.8b_zoh_bf16_b4_d5120_l2048_n16"}
@@ -363,16 +365,21 @@ def other_rows(lib, ssm, peak, stream, dev, which="all", decode_steps=1000):
     sel = set(ROW_KEYS) if which == "all" else set(which.split(","))
     rows = {}
     # (the "zoh" row: the 2.8B-shaped scan with the exact zero-order-hold input term)
-    for key, n in (("m130", 200), ("ti", 200), ("long", 5), ("zoh", 200)):
+    # (the "cplx" row: the 2.8B-shaped scan with a complex A, the S4D-Lin initialisation)
+    for key, n in (("m130", 200), ("ti", 200), ("long", 5), ("zoh", 200), ("cplx", 100)):
         if key not in sel:
             continue
         name = ROW_KEYS[key]
-        cfg = syn.M2P8 if key == "zoh" else syn.SCAN_CONFIGS[name]
+        cfg = syn.M2P8 if key in ("zoh", "cplx") else syn.SCAN_CONFIGS[name]
         disc = ssm.SSM_DISC_ZOH if key == "zoh" else ssm.SSM_DISC_EULER
         inp = random_device_inputs(cfg, 0, dev)
+        A_imag = None
+        if key == "cplx":
+            Ac = torch.from_numpy(syn.s4d_lin_A(cfg.dim, cfg.dstate)).to(dev)
+            inp["A"], A_imag = Ac.real.contiguous(), Ac.imag.contiguous()
         y = torch.empty_like(inp["u"])
         a = ssm.make_scan_args(inp["u"], inp["delta"], inp["A"], inp["Bm"], inp["Cm"], y, inp["Dskip"], inp["z"],
-                               inp["delta_bias"], discretization=disc)
+                               inp["delta_bias"], discretization=disc, A_imag=A_imag)
         wsb = ssm.ssm_scan_workspace_size(a)
         ws = torch.empty(max(wsb, 16), dtype=torch.uint8, device=dev)
         a.workspace, a.workspace_bytes = ws.data_ptr(), wsb

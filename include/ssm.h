@@ -99,6 +99,20 @@ typedef enum {
  *                                             final state not returned)
  *   z              : nullable (no gate)
  * Limits: 1 <= dstate <= 64; batch, dim, seqlen >= 0 (an empty problem is a no-op).
+ *
+ * Complex A ("gitcode", section 3.6: complex states, the S4D-Lin initialisation
+ * A[d,n] = -1/2 + n i): when A_imag is set, A + i A_imag is a complex diagonal
+ * (both fp32 with the strides stride_A), the state h is complex, Abar =
+ * exp(Delta A) is the complex exponential, the input term Delta B u is real
+ * and enters the state as it is, and the output reads the real part of the C
+ * contraction: y = (Re(sum_n C h) + Dskip u) * silu(z).  h0 and h_last then
+ * hold complex numbers as (re, im) fp32 pairs: element (b, d, n) has its real
+ * part at [b*s0 + d*s1 + n*s2] and its imaginary part one float after it
+ * (a dense (batch, dim, dstate, 2) array has strides (2*dim*dstate,
+ * 2*dstate, 2)).  Complex A takes the Euler input term, the single-pass or
+ * stride-general kernels (never the chunked path) and is not supported by
+ * ssm_scan_bwd, ssm_scan_fwd_noalloc or ssm_state_update
+ * (SSM_ERR_UNSUPPORTED).
  */
 typedef struct ssm_scan_args {
     int64_t batch, dim, seqlen, dstate;        /* B, D, L, N */
@@ -118,6 +132,7 @@ typedef struct ssm_scan_args {
     int64_t chunk_len;                         /* chunked path: timesteps per chunk; 0 = automatic */
     void *workspace;                           /* device scratch, caller-owned, nullable if 0 bytes needed */
     size_t workspace_bytes;
+    const float *A_imag;                       /* nullable: imaginary part of a complex A (see below) */
 } ssm_scan_args_t;
 
 /*

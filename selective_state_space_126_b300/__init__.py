@@ -50,6 +50,7 @@ class ScanArgs(ctypes.Structure):
         ("stride_h0", _i64 * 3), ("stride_h_last", _i64 * 3),
         ("flags", ctypes.c_int32), ("discretization", ctypes.c_int32), ("chunk_len", _i64),
         ("workspace", _vp), ("workspace_bytes", ctypes.c_size_t),
+        ("A_imag", _vp),
     ]
 
 
@@ -218,10 +219,19 @@ def _f32(t, name):
     return t
 
 
+def _state_strides(t):
+    """Strides of a (B, D, N) state tensor in floats: a complex tensor holds (re, im) float pairs."""
+    if t is None:
+        return [0, 0, 0]
+    s = _strides(t, 3)
+    return [2 * v for v in s] if t.is_complex() else s
+
+
 def make_scan_args(u, delta, A, Bm, Cm, y, Dskip=None, z=None, delta_bias=None, h0=None, h_last=None,
                    delta_softplus=True, flags=0, chunk_len=0, workspace=None,
-                   discretization=SSM_DISC_EULER) -> ScanArgs:
-    """Fill an ssm_scan_args_t from torch tensors (no copies, strides passed through)."""
+                   discretization=SSM_DISC_EULER, A_imag=None) -> ScanArgs:
+    """Fill an ssm_scan_args_t from torch tensors (no copies, strides passed through).  With A_imag (the
+    imaginary part of a complex A, strides of A) h0 / h_last are complex64 tensors."""
     Bsz, D, L = u.shape
     N = A.shape[1]
     a = ScanArgs()
@@ -238,8 +248,11 @@ def make_scan_args(u, delta, A, Bm, Cm, y, Dskip=None, z=None, delta_bias=None, 
     a.stride_B[:] = _strides(Bm, 3, dims="b")
     a.stride_C[:] = _strides(Cm, 3, dims="b")
     a.stride_A[:] = _strides(A, 2)
-    a.stride_h0[:] = _strides(h0, 3)
-    a.stride_h_last[:] = _strides(h_last, 3)
+    a.stride_h0[:] = _state_strides(h0)
+    a.stride_h_last[:] = _state_strides(h_last)
+    a.A_imag = _ptr(A_imag)
+    if A_imag is not None and tuple(A_imag.stride()) != tuple(A.stride()):
+        raise ValueError("A_imag must have the strides of A")
     a.flags = int(flags)
     a.discretization = int(discretization)
     a.chunk_len = int(chunk_len)
@@ -265,16 +278,28 @@ def ssm_scan_fwd(u, delta, A, Bm, Cm, Dskip=None, z=None, delta_bias=None, h0=No
     """Selective-scan forward pass on the GPU (``discretization``: SSM_DISC_EULER or SSM_DISC_ZOH).
 
     u, delta, z: (B, D, L); Bm, Cm: (B, N, L) or (N, L) (shared across the batch);
-    A: (D, N) fp32; Dskip, delta_bias: (D,) fp32; h0: (B, D, N) fp32.
+    A: (D, N) fp32, or complex64 for a complex diagonal (S4D-Lin); Dskip, delta_bias: (D,) fp32;
+    h0: (B, D, N) fp32 (complex64 with a complex A).
     I/O tensors are float32 or bfloat16 (all the same dtype), on one CUDA device.
-    Returns y (B, D, L) in the I/O dtype, and h_last (B, D, N) fp32 if requested.
+    Returns y (B, D, L) in the I/O dtype, and h_last (B, D, N) fp32 (complex64 with a complex A) if
+    requested.
     """
     torch = _torch()
     lib = load_library()
     for name, t in (("u", u), ("delta", delta), ("Bm", Bm), ("Cm", Cm), ("z", z)):
         if t is not None and not t.is_cuda:
             raise ValueError(f"{name} must be a CUDA tensor")
-    _f32(A, "A"); _f32(Dskip, "Dskip"); _f32(delta_bias, "delta_bias"); _f32(h0, "h0")
+    A_imag = None
+    cplx = A.is_complex()
+    if cplx:
+        if A.dtype != torch.complex64:
+            raise ValueError("a complex A must be complex64")
+        A, A_imag = A.real.contiguous(), A.imag.contiguous()
+        if h0 is not None and h0.dtype != torch.complex64:
+            raise ValueError("with a complex A, h0 must be complex64")
+    _f32(A, "A"); _f32(Dskip, "Dskip"); _f32(delta_bias, "delta_bias")
+    if not cplx:
+        _f32(h0, "h0")
     if Dskip is not None:
         Dskip = Dskip.contiguous()
     if delta_bias is not None:
@@ -282,9 +307,10 @@ def ssm_scan_fwd(u, delta, A, Bm, Cm, Dskip=None, z=None, delta_bias=None, h0=No
     if y is None:
         y = torch.empty(u.shape, dtype=u.dtype, device=u.device)
     if return_last_state and h_last is None:
-        h_last = torch.empty((u.shape[0], u.shape[1], A.shape[1]), dtype=torch.float32, device=u.device)
+        h_last = torch.empty((u.shape[0], u.shape[1], A.shape[1]), dtype=torch.complex64 if cplx else torch.float32,
+                             device=u.device)
     args = make_scan_args(u, delta, A, Bm, Cm, y, Dskip, z, delta_bias, h0, h_last, delta_softplus, flags,
-                          chunk_len, None, discretization)
+                          chunk_len, None, discretization, A_imag)
     need = ssm_scan_workspace_size(args)
     if need > 0:
         if workspace is None or workspace.numel() * workspace.element_size() < need:

@@ -133,6 +133,40 @@ __device__ __forceinline__ float2 zoh_coef2_fast(float2 dt, float2 x, float2 a, 
   return make_float2(fabsf(x.x) < kZohFastCut ? small.x : large.x, fabsf(x.y) < kZohFastCut ? small.y : large.y);
 }
 
+// cos and sin of theta, for the rotation part exp(i theta) of a complex Abar.
+// PRECISE: the library sincosf.  Fast form: Cody-Waite reduction (Cody and
+// Waite, "Software Manual for the Elementary Functions", 1980) of theta to
+// [-pi, pi] with 2 pi split as 6.28125 (exact in 8 bits, so k * 6.28125 is
+// exact for |k| < 2^16) plus the remainder 2 pi - 6.28125, then the SFU
+// sin / cos on the reduced argument.
+constexpr float kTwoPiHi = 6.28125f;
+constexpr float kTwoPiLo = 1.9353071795864769e-3f;
+constexpr float kInvTwoPi = 0.15915494309189535f;
+
+__device__ __forceinline__ float sin_approx(float x) {
+  float y;
+  asm("sin.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ float cos_approx(float x) {
+  float y;
+  asm("cos.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+template <bool PRECISE>
+__device__ __forceinline__ float2 cos_sin(float th) {
+  if (PRECISE) {
+    float s, c;
+    sincosf(th, &s, &c);
+    return make_float2(c, s);
+  }
+  const float k = rintf(th * kInvTwoPi);
+  const float r = fmaf(-k, kTwoPiLo, fmaf(-k, kTwoPiHi, th));
+  return make_float2(cos_approx(r), sin_approx(r));
+}
+
 // Delta for one element: softplus(delta + bias) or the plain sum.
 template <bool PRECISE>
 __device__ __forceinline__ float delta_of(float delta, float bias, bool use_softplus) {

@@ -22,6 +22,7 @@ struct ScanKernelParams {
   int nchunks;
   int64_t chunk_len;
   const float* A;
+  const float* Aim;  // imaginary part of a complex A (same strides), or null
   int64_t sA0, sA1;
   const float* Dskip;
   const float* bias;
@@ -110,7 +111,7 @@ inline bool make_scan_kernel_args(const ScanProblem& p, const ScanPlan& plan, vo
   kp->B = p.B; kp->D = p.D; kp->L = p.L; kp->N = (int)p.N;
   kp->nchunks = (int)plan.nchunks;
   kp->chunk_len = plan.nchunks > 1 ? plan.chunk_len : p.L;
-  kp->A = p.A; kp->sA0 = p.sA[0]; kp->sA1 = p.sA[1];
+  kp->A = p.A; kp->Aim = p.Aim; kp->sA0 = p.sA[0]; kp->sA1 = p.sA[1];
   kp->Dskip = p.Dskip; kp->bias = p.bias;
   kp->h0 = p.h0; kp->sh00 = p.sh0[0]; kp->sh01 = p.sh0[1]; kp->sh02 = p.sh0[2];
   kp->h_last = p.h_last; kp->shl0 = p.shl[0]; kp->shl1 = p.shl[1]; kp->shl2 = p.shl[2];

@@ -100,7 +100,7 @@ struct Smem {
 };
 
 
-template <typename IO, int K, int NS, int MODE, bool PRECISE, bool ZOH>
+template <typename IO, int K, int NS, int MODE, bool PRECISE, bool ZOH, bool CPLX>
 __global__ void __launch_bounds__(32 * K, min_blocks(K, NS))
     scan_tiled_kernel(const __grid_constant__ ScanKernelParams p, const __grid_constant__ ScanMaps tm) {
   using S = Smem<IO, K, NS>;
@@ -141,17 +141,22 @@ __global__ void __launch_bounds__(32 * K, min_blocks(K, NS))
   const int ntiles = (int)((t_end - t_begin + T - 1) / T);
 
   // ---- per-thread state: A * log2(e) and h for this thread's NS states ----
-  float2 A2[NS / 2], h[NS / 2], Ai[NS / 2];   // Ai: 1 / A, for the exact-ZOH input term
+  // Ai: 1 / A, for the exact-ZOH input term; with a complex A (CPLX) it holds Im A and hi the
+  // imaginary part of the state (h0 / h_last hold (re, im) pairs, the imaginary part one float on)
+  float2 A2[NS / 2], h[NS / 2], Ai[NS / 2], hi[CPLX ? NS / 2 : 1];
 #pragma unroll
   for (int i = 0; i < NS; ++i) {
     const int n = g * NS + i;
-    float a = 0.f, hv = 0.f, ai = 0.f;
+    float a = 0.f, hv = 0.f, ai = 0.f, hiv = 0.f;
     if (valid && n < N) {
       a = p.A[d * p.sA0 + n * p.sA1] * kLog2e;
-      ai = kLog2e / a;
+      ai = CPLX ? p.Aim[d * p.sA0 + n * p.sA1] : kLog2e / a;
       if (MODE == MODE_OUTPUT || MODE == MODE_CKPT) {
         if (chunk == 0) {
-          if (p.h0) hv = p.h0[b * p.sh00 + d * p.sh01 + n * p.sh02];
+          if (p.h0) {
+            hv = p.h0[b * p.sh00 + d * p.sh01 + n * p.sh02];
+            if (CPLX) hiv = p.h0[b * p.sh00 + d * p.sh01 + n * p.sh02 + 1];
+          }
         } else {
           hv = p.rec_h[((b * p.D + d) * p.nchunks + chunk) * NP + n];
         }
@@ -159,6 +164,10 @@ __global__ void __launch_bounds__(32 * K, min_blocks(K, NS))
     }
     if (i & 1) { A2[i / 2].y = a; h[i / 2].y = hv; Ai[i / 2].y = ai; }
     else { A2[i / 2].x = a; h[i / 2].x = hv; Ai[i / 2].x = ai; }
+    if (CPLX) {
+      if (i & 1) hi[i / 2].y = hiv;
+      else hi[i / 2].x = hiv;
+    }
   }
 
   // ---- one-time set-up: zero the B/C tile (padded states stay zero), barriers ----
@@ -345,43 +354,65 @@ __global__ void __launch_bounds__(32 * K, min_blocks(K, NS))
           const float du = s ? dd.w : dd.y;
           const float* Bt = bcg + (t + s) * 2 * NP;
           const float2 du2 = make_float2(du, du);
-          float2 a[NS / 2];
+          if constexpr (CPLX) {
+            // complex Abar = 2^(Delta Re A log2 e) (cos(Delta Im A) + i sin(Delta Im A)); the real input
+            // term enters the real part; y reads Re(C h)
+            float2 acc = make_float2(0.f, 0.f);
 #pragma unroll
-          for (int q = 0; q < NS / 2; ++q) {
-            const float2 x = __fmul2_rn(make_float2(dt, dt), A2[q]);
-            a[q] = make_float2(ex2_approx(x.x), ex2_approx(x.y));
-          }
-          // input coefficient per state: Delta u (Euler), or g u with the exact-ZOH g (du holds u)
-          float2 bx[NS / 2];
+            for (int q = 0; q < NS / 2; ++q) {
+              const float2 x = __fmul2_rn(make_float2(dt, dt), A2[q]);
+              const float2 mag = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+              const float2 th = __fmul2_rn(make_float2(dt, dt), Ai[q]);
+              const float2 cs0 = cos_sin<PRECISE>(th.x), cs1 = cos_sin<PRECISE>(th.y);
+              const float2 ar = __fmul2_rn(mag, make_float2(cs0.x, cs1.x));
+              const float2 ai = __fmul2_rn(mag, make_float2(cs0.y, cs1.y));
+              const float2 bq = *reinterpret_cast<const float2*>(Bt + 2 * q);
+              const float2 t1 = __ffma2_rn(make_float2(-ai.x, -ai.y), hi[q], __fmul2_rn(du2, bq));
+              const float2 hin = __ffma2_rn(ar, hi[q], __fmul2_rn(ai, h[q]));
+              h[q] = __ffma2_rn(ar, h[q], t1);
+              hi[q] = hin;
+              if (MODE == MODE_OUTPUT) acc = __ffma2_rn(*reinterpret_cast<const float2*>(Bt + NP + 2 * q), h[q], acc);
+            }
+            yv[(t + s) & 3] = acc.x + acc.y;
+          } else {
+            float2 a[NS / 2];
 #pragma unroll
-          for (int q = 0; q < NS / 2; ++q) {
-            if (ZOH) {
-              const float2 x = __fmul2_rn(__fmul2_rn(make_float2(dt, dt), A2[q]), make_float2(kLn2, kLn2));
-              float2 gq;
-              if (PRECISE) {
-                gq = make_float2(zoh_coef<true>(dt, x.x, a[q].x, Ai[q].x), zoh_coef<true>(dt, x.y, a[q].y, Ai[q].y));
+            for (int q = 0; q < NS / 2; ++q) {
+              const float2 x = __fmul2_rn(make_float2(dt, dt), A2[q]);
+              a[q] = make_float2(ex2_approx(x.x), ex2_approx(x.y));
+            }
+            // input coefficient per state: Delta u (Euler), or g u with the exact-ZOH g (du holds u)
+            float2 bx[NS / 2];
+#pragma unroll
+            for (int q = 0; q < NS / 2; ++q) {
+              if (ZOH) {
+                const float2 x = __fmul2_rn(__fmul2_rn(make_float2(dt, dt), A2[q]), make_float2(kLn2, kLn2));
+                float2 gq;
+                if (PRECISE) {
+                  gq = make_float2(zoh_coef<true>(dt, x.x, a[q].x, Ai[q].x), zoh_coef<true>(dt, x.y, a[q].y, Ai[q].y));
+                } else {
+                  gq = zoh_coef2_fast(make_float2(dt, dt), x, a[q], Ai[q]);
+                }
+                bx[q] = __fmul2_rn(gq, du2);
               } else {
-                gq = zoh_coef2_fast(make_float2(dt, dt), x, a[q], Ai[q]);
+                bx[q] = du2;
               }
-              bx[q] = __fmul2_rn(gq, du2);
-            } else {
-              bx[q] = du2;
             }
-          }
-          float2 acc = make_float2(0.f, 0.f);
+            float2 acc = make_float2(0.f, 0.f);
 #pragma unroll
-          for (int q = 0; q < NS; q += 4) {
-            const float4 bq = *reinterpret_cast<const float4*>(Bt + q);
-            h[q / 2] = __ffma2_rn(a[q / 2], h[q / 2], __fmul2_rn(bx[q / 2], make_float2(bq.x, bq.y)));
-            h[q / 2 + 1] = __ffma2_rn(a[q / 2 + 1], h[q / 2 + 1], __fmul2_rn(bx[q / 2 + 1], make_float2(bq.z, bq.w)));
-            if (MODE == MODE_OUTPUT) {
-              const float4 cq = *reinterpret_cast<const float4*>(Bt + NP + q);
-              acc = __ffma2_rn(make_float2(cq.x, cq.y), h[q / 2], acc);
-              acc = __ffma2_rn(make_float2(cq.z, cq.w), h[q / 2 + 1], acc);
+            for (int q = 0; q < NS; q += 4) {
+              const float4 bq = *reinterpret_cast<const float4*>(Bt + q);
+              h[q / 2] = __ffma2_rn(a[q / 2], h[q / 2], __fmul2_rn(bx[q / 2], make_float2(bq.x, bq.y)));
+              h[q / 2 + 1] = __ffma2_rn(a[q / 2 + 1], h[q / 2 + 1], __fmul2_rn(bx[q / 2 + 1], make_float2(bq.z, bq.w)));
+              if (MODE == MODE_OUTPUT) {
+                const float4 cq = *reinterpret_cast<const float4*>(Bt + NP + q);
+                acc = __ffma2_rn(make_float2(cq.x, cq.y), h[q / 2], acc);
+                acc = __ffma2_rn(make_float2(cq.z, cq.w), h[q / 2 + 1], acc);
+              }
             }
+            yv[(t + s) & 3] = acc.x + acc.y;
+            if (MODE == MODE_RECORD) dsum += dt;
           }
-          yv[(t + s) & 3] = acc.x + acc.y;
-          if (MODE == MODE_RECORD) dsum += dt;
         }
         if (MODE == MODE_OUTPUT && (t & 3) == 2)
           *reinterpret_cast<float4*>(prow + t - 2) = make_float4(yv[0], yv[1], yv[2], yv[3]);
@@ -428,7 +459,10 @@ __global__ void __launch_bounds__(32 * K, min_blocks(K, NS))
 #pragma unroll
       for (int i = 0; i < NS; ++i) {
         const int n = g * NS + i;
-        if (n < N) p.h_last[b * p.shl0 + d * p.shl1 + n * p.shl2] = (i & 1) ? h[i / 2].y : h[i / 2].x;
+        if (n < N) {
+          p.h_last[b * p.shl0 + d * p.shl1 + n * p.shl2] = (i & 1) ? h[i / 2].y : h[i / 2].x;
+          if (CPLX) p.h_last[b * p.shl0 + d * p.shl1 + n * p.shl2 + 1] = (i & 1) ? hi[i / 2].y : hi[i / 2].x;
+        }
       }
     }
   } else if (MODE == MODE_RECORD) {
@@ -444,10 +478,10 @@ __global__ void __launch_bounds__(32 * K, min_blocks(K, NS))
   }
 }
 
-template <typename IO, int K, int NS, int MODE, bool PRECISE, bool ZOH>
+template <typename IO, int K, int NS, int MODE, bool PRECISE, bool ZOH, bool CPLX = false>
 cudaError_t launch_one(const ScanKernelParams& tp, const ScanMaps& tm, dim3 grid, cudaStream_t s) {
   using S = Smem<IO, K, NS>;
-  auto kern = scan_tiled_kernel<IO, K, NS, MODE, PRECISE, ZOH>;
+  auto kern = scan_tiled_kernel<IO, K, NS, MODE, PRECISE, ZOH, CPLX>;
   static unsigned long long attr_set = 0;   // one bit per device; a racing duplicate set is harmless
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -490,6 +524,18 @@ cudaError_t launch_ckpt_typed(const ScanPlan& plan, const ScanKernelParams& tp, 
   return cudaErrorInvalidValue;
 }
 
+// complex A: single pass only (the planner never chunks it), Euler input term
+template <typename IO, bool PRECISE>
+cudaError_t launch_complex(const ScanProblem& p, const ScanPlan& plan, const ScanKernelParams& tp, const ScanMaps& tm,
+                           cudaStream_t s) {
+  if (plan.nchunks != 1) return cudaErrorInvalidValue;
+  const dim3 grid((unsigned)((p.D + CH - 1) / CH), 1, (unsigned)p.B);
+  const int K = plan.shape.K, NS = plan.shape.NS;
+  if (K == 2 && NS == 8) return launch_one<IO, 2, 8, MODE_OUTPUT, PRECISE, false, true>(tp, tm, grid, s);
+  if (K == 4 && NS == 4) return launch_one<IO, 4, 4, MODE_OUTPUT, PRECISE, false, true>(tp, tm, grid, s);
+  return cudaErrorInvalidValue;
+}
+
 template <typename IO, bool PRECISE, bool ZOH>
 cudaError_t launch_typed(const ScanProblem& p, const ScanPlan& plan, ScanKernelParams& tp, const ScanMaps& tm,
                          cudaStream_t s) {
@@ -509,6 +555,10 @@ cudaError_t launch_scan_tiled(const ScanProblem& p, const ScanPlan& plan, void* 
   ScanMaps tm;
   if (!make_scan_kernel_args(p, plan, workspace, plan.shape.K * plan.shape.NS, T, &tp, &tm))
     return cudaErrorInvalidValue;
+  if (p.cplx) {
+    if (p.io == SSM_F32) return launch_complex<float, true>(p, plan, tp, tm, s);
+    return launch_complex<__nv_bfloat16, false>(p, plan, tp, tm, s);
+  }
   if (p.zoh) {
     if (p.io == SSM_F32) return launch_typed<float, true, true>(p, plan, tp, tm, s);
     return launch_typed<__nv_bfloat16, false, true>(p, plan, tp, tm, s);

@@ -90,6 +90,9 @@ ssm_status_t validate_scan(const ssm_scan_args_t* a, ScanProblem* p) {
   p->zoh = a->discretization == SSM_DISC_ZOH;
   p->u = a->u; p->delta = a->delta; p->z = a->z; p->Bm = a->Bm; p->Cm = a->Cm;
   p->A = a->A; p->Dskip = a->Dskip; p->bias = a->delta_bias; p->h0 = a->h0; p->h_last = a->h_last; p->y = a->y;
+  p->Aim = a->A_imag;
+  p->cplx = a->A_imag != nullptr;
+  if (p->cplx && p->zoh) return fail(SSM_ERR_UNSUPPORTED, "complex A takes the Euler input term");
   std::memcpy(p->su, a->stride_u, sizeof(p->su));
   std::memcpy(p->sd, a->stride_delta, sizeof(p->sd));
   std::memcpy(p->sz, a->stride_z, sizeof(p->sz));
@@ -124,6 +127,7 @@ ssm_status_t validate_scan(const ssm_scan_args_t* a, ScanProblem* p) {
     if (!aligned(q.ptr, es)) return fail(SSM_ERR_INVALID_ARG, "%s is not %d-byte aligned", q.name, es);
   }
   if (!aligned(p->A, 4)) return fail(SSM_ERR_INVALID_ARG, "A misaligned");
+  if (p->cplx && !aligned(p->Aim, 4)) return fail(SSM_ERR_INVALID_ARG, "A_imag misaligned");
   for (int i = 0; i < 3; ++i)
     if ((p->h0 && p->sh0[i] < 0) || (p->h_last && p->shl[i] < 0))
       return fail(SSM_ERR_INVALID_ARG, "negative state stride");
@@ -131,28 +135,32 @@ ssm_status_t validate_scan(const ssm_scan_args_t* a, ScanProblem* p) {
   // outputs: one-to-one and disjoint from every input and from each other
   int64_t ey[3] = {p->B, p->D, p->L};
   int64_t sy[3] = {p->sy[0], p->sy[1], 1};
-  int64_t eh[3] = {p->B, p->D, p->N};
+  // a complex state is (B, D, N, 2): the imaginary part one float after the real part
+  const int hrank = p->cplx ? 4 : 3;
+  int64_t eh[4] = {p->B, p->D, p->N, 2};
+  int64_t shl[4] = {p->shl[0], p->shl[1], p->shl[2], 1};
   if (p->L > 0 && !injective(3, ey, sy)) return fail(SSM_ERR_INVALID_ARG, "y strides overlap");
-  if (p->h_last && !injective(3, eh, p->shl)) return fail(SSM_ERR_INVALID_ARG, "h_last strides overlap");
+  if (p->h_last && !injective(hrank, eh, shl)) return fail(SSM_ERR_INVALID_ARG, "h_last strides overlap");
   uintptr_t y0 = 0, y1 = 0, hl0 = 0, hl1 = 0;
   if (p->L > 0) tensor_range(p->y, 3, ey, sy, es, &y0, &y1);
-  if (p->h_last) tensor_range(p->h_last, 3, eh, p->shl, 4, &hl0, &hl1);
+  if (p->h_last) tensor_range(p->h_last, hrank, eh, shl, 4, &hl0, &hl1);
   struct In {
     const void* ptr;
     int rank;
-    int64_t ext[3];
-    int64_t str[3];
+    int64_t ext[4];
+    int64_t str[4];
     int es;
   } ins[] = {
-      {p->u, 3, {p->B, p->D, p->L}, {p->su[0], p->su[1], 1}, es},
-      {p->delta, 3, {p->B, p->D, p->L}, {p->sd[0], p->sd[1], 1}, es},
-      {p->z, 3, {p->B, p->D, p->L}, {p->sz[0], p->sz[1], 1}, es},
-      {p->Bm, 3, {p->B, p->N, p->L}, {p->sB[0], p->sB[1], 1}, es},
-      {p->Cm, 3, {p->B, p->N, p->L}, {p->sC[0], p->sC[1], 1}, es},
-      {p->A, 2, {p->D, p->N, 1}, {p->sA[0], p->sA[1], 0}, 4},
-      {p->Dskip, 1, {p->D, 1, 1}, {1, 0, 0}, 4},
-      {p->bias, 1, {p->D, 1, 1}, {1, 0, 0}, 4},
-      {p->h0, 3, {p->B, p->D, p->N}, {p->sh0[0], p->sh0[1], p->sh0[2]}, 4},
+      {p->u, 3, {p->B, p->D, p->L, 1}, {p->su[0], p->su[1], 1, 0}, es},
+      {p->delta, 3, {p->B, p->D, p->L, 1}, {p->sd[0], p->sd[1], 1, 0}, es},
+      {p->z, 3, {p->B, p->D, p->L, 1}, {p->sz[0], p->sz[1], 1, 0}, es},
+      {p->Bm, 3, {p->B, p->N, p->L, 1}, {p->sB[0], p->sB[1], 1, 0}, es},
+      {p->Cm, 3, {p->B, p->N, p->L, 1}, {p->sC[0], p->sC[1], 1, 0}, es},
+      {p->A, 2, {p->D, p->N, 1, 1}, {p->sA[0], p->sA[1], 0, 0}, 4},
+      {p->Aim, 2, {p->D, p->N, 1, 1}, {p->sA[0], p->sA[1], 0, 0}, 4},
+      {p->Dskip, 1, {p->D, 1, 1, 1}, {1, 0, 0, 0}, 4},
+      {p->bias, 1, {p->D, 1, 1, 1}, {1, 0, 0, 0}, 4},
+      {p->h0, hrank, {p->B, p->D, p->N, 2}, {p->sh0[0], p->sh0[1], p->sh0[2], 1}, 4},
   };
   for (const In& in : ins) {
     if (!in.ptr) continue;
@@ -225,6 +233,19 @@ ssm_status_t plan_scan(const ssm_scan_args_t* a, const ScanProblem& p, ScanPlan*
     if (flags & (SSM_SCAN_FORCE_TILED | SSM_SCAN_FORCE_CHUNKED))
       return fail(SSM_ERR_UNSUPPORTED, "layout not eligible for the tiled kernels (alignment / strides / seqlen)");
     plan->path = kPathGeneric;
+    return ok();
+  }
+  if (p.cplx) {
+    // complex A: the single-pass tiled kernel for N <= 16, else the stride-general one; no chunked path
+    if (flags & SSM_SCAN_FORCE_CHUNKED) return fail(SSM_ERR_UNSUPPORTED, "complex A has no chunked path");
+    if (p.N > 16) {
+      if (flags & SSM_SCAN_FORCE_TILED) return fail(SSM_ERR_UNSUPPORTED, "complex A on the tiled kernel takes dstate <= 16");
+      plan->path = kPathGeneric;
+      return ok();
+    }
+    plan->path = kPathTiled;
+    plan->shape = pick_shape(p, p.B * ((p.D + 31) / 32), device_sm_count());
+    if (plan->shape.K == 1) plan->shape = TiledShape{2, 8, 32};   // the complex variant exists for K = 2 and 4
     return ok();
   }
   const int sms = device_sm_count();
@@ -307,7 +328,7 @@ using namespace ssm;
 
 extern "C" {
 
-int ssm_version(void) { return (1 << 16) | 2; }
+int ssm_version(void) { return (1 << 16) | 3; }
 
 size_t ssm_abi_sizeof(int which) {
   if (which == 0) return sizeof(ssm_scan_args_t);
@@ -467,6 +488,7 @@ ssm_status_t validate_bwd(const ssm_scan_bwd_args_t* a, BwdProblem* p) {
   const ScanProblem& f = p->f;
   if (f.N > 16) return fail(SSM_ERR_UNSUPPORTED, "the backward pass takes dstate <= 16");
   if (f.zoh) return fail(SSM_ERR_UNSUPPORTED, "the backward pass takes the Euler discretisation");
+  if (f.cplx) return fail(SSM_ERR_UNSUPPORTED, "the backward pass takes a real A");
   p->dy = a->dy; p->dhl = a->dh_last;
   p->du = a->du; p->ddelta = a->ddelta; p->dz = a->dz;
   p->dA = a->dA; p->dB = a->dB; p->dC = a->dC; p->dD = a->dDskip; p->dbias = a->ddelta_bias; p->dh0 = a->dh0;

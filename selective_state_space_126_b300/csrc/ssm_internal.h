@@ -16,8 +16,9 @@ struct ScanProblem {
   ssm_dtype_t io;
   bool softplus;
   bool zoh;               // exact zero-order-hold input term (else Euler)
+  bool cplx;              // complex A (A + i Aim): complex state, y = Re(C h) + D u
   const void *u, *delta, *z, *Bm, *Cm;
-  const float *A, *Dskip, *bias, *h0;
+  const float *A, *Aim, *Dskip, *bias, *h0;
   float* h_last;
   void* y;
   int64_t su[3], sd[3], sz[3], sy[3], sB[3], sC[3], sA[2], sh0[3], shl[3];

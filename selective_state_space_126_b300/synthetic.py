@@ -163,6 +163,12 @@ def layer_params(dim: int, dstate: int, dt_min: float, dt_max: float, seed: int 
     return A, Dskip, delta_bias
 
 
+def s4d_lin_A(dim: int, dstate: int):
+    """The S4D-Lin initialisation of a complex diagonal A ("Mamba paper translation", section 3.6):
+    A[d, n] = -1/2 + n i, as complex64 (D, N)."""
+    return np.tile((-0.5 + 1j * np.arange(dstate)).astype(np.complex64), (dim, 1))
+
+
 def conv_params(dim: int, width: int, seed: int = 0):
     """Conv taps (D, W) and bias (D,) as float32, uniform in +-1/sqrt(W)."""
     bound = 1.0 / np.sqrt(width)

@@ -329,3 +329,25 @@ def test_step_discretization_validation(lib):
     a.batch, a.dim, a.dstate, a.io_dtype = 2, 8, 16, ssm.SSM_BF16
     a.discretization = 3
     assert lib.ssm_state_update(ctypes.byref(a), None) == ssm.SSM_ERR_INVALID_ARG
+
+
+def test_complex_validation(lib):
+    # complex A: chunked and ZOH are refused, the plan is single pass or generic, no workspace
+    a = scan_args(B=1, D=1536, L=1 << 20, A_imag=FAKE["ws"])
+    assert ssm.ssm_scan_plan_path(a) == "tiled"
+    assert ssm.ssm_scan_workspace_size(a) == 0
+    a = scan_args(L=4096, flags=ssm.SSM_SCAN_FORCE_CHUNKED, chunk_len=1024, A_imag=FAKE["ws"])
+    assert call_scan(a) == ssm.SSM_ERR_UNSUPPORTED
+    a = scan_args(discretization=ssm.SSM_DISC_ZOH, A_imag=FAKE["ws"])
+    assert call_scan(a) == ssm.SSM_ERR_UNSUPPORTED
+    a = scan_args(N=24, A_imag=FAKE["ws"])
+    assert ssm.ssm_scan_plan_path(a) == "generic"
+    a = scan_args(A_imag=FAKE["ws"] + 2)
+    assert call_scan(a) == ssm.SSM_ERR_INVALID_ARG
+    # a complex h_last is (B, D, N, 2): (re, im) pairs that must not overlap
+    B, D, N = 2, 64, 16
+    a = scan_args(A_imag=FAKE["ws"], h_last=FAKE["h_last"], stride_h_last=[D * N, N, 1])
+    assert call_scan(a) == ssm.SSM_ERR_INVALID_ARG
+    # the backward pass and the no-allocation entry point take a real A
+    assert lib.ssm_scan_fwd_noalloc(ctypes.byref(scan_args(L=4096, A_imag=FAKE["ws"])), None) == \
+        ssm.SSM_ERR_UNSUPPORTED
