@@ -77,6 +77,8 @@ def _bind(lib):
     lib.oracle_causal_conv1d.argtypes = [i64, i64, i64, i64] + [dp] * 4 + [ctypes.c_int, dp]
     lib.oracle_selective_scan_complex.restype = ctypes.c_int
     lib.oracle_selective_scan_complex.argtypes = [i64, i64, i64, i64] + [dp] * 10 + [ctypes.c_int, dp, dp]
+    lib.oracle_ssd_scan.restype = ctypes.c_int
+    lib.oracle_ssd_scan.argtypes = [i64] * 5 + [dp] * 9 + [ctypes.c_int, dp, dp]
     lib.oracle_default_threads.restype = ctypes.c_int
     lib.oracle_default_threads.argtypes = []
     return lib
@@ -165,6 +167,36 @@ def selective_scan_complex(u, delta, A, Bm, Cm, Dskip=None, z=None, delta_bias=N
                                            int(bool(delta_softplus)), _ptr(y), cp(h_last))
     if rc != 0:
         raise RuntimeError("oracle_selective_scan_complex failed")
+    return (y, h_last) if return_last_state else y
+
+
+def ssd_scan(x, delta, a, Bm, Cm, Dskip=None, z=None, delta_bias=None, h0=None, delta_softplus=True,
+             return_last_state=False, lib=None):
+    """fp64 Mamba-2 SSD layer (scalar A per head, B / C shared by the heads).
+
+    x, z: (B, H*P, L); delta: (B, H, L); a, Dskip, delta_bias: (H,); Bm, Cm: (B, L, N);
+    h0: (B, H, P, N).  Returns y (B, H*P, L), and h_last (B, H, P, N) if ``return_last_state``.
+    """
+    lib = lib or load()
+    delta = _f64(delta)
+    Bsz, H, L = delta.shape
+    x = _f64(x)
+    P = x.shape[1] // H
+    Bm = _f64(Bm)
+    N = Bm.shape[2]
+    Cm = _f64(Cm, (Bsz, L, N))
+    z = _f64(z, x.shape)
+    a = _f64(a, (H,))
+    Dskip = _f64(Dskip, (H,))
+    delta_bias = _f64(delta_bias, (H,))
+    h0 = _f64(h0, (Bsz, H, P, N))
+    y = np.empty(x.shape, dtype=np.float64)
+    h_last = np.empty((Bsz, H, P, N), dtype=np.float64) if return_last_state else None
+    rc = lib.oracle_ssd_scan(Bsz, H, P, L, N, _ptr(x), _ptr(delta), _ptr(z), _ptr(Bm), _ptr(Cm), _ptr(a),
+                             _ptr(Dskip), _ptr(delta_bias), _ptr(h0), int(bool(delta_softplus)), _ptr(y),
+                             _ptr(h_last))
+    if rc != 0:
+        raise RuntimeError("oracle_ssd_scan failed")
     return (y, h_last) if return_last_state else y
 
 

@@ -321,6 +321,63 @@ int oracle_selective_scan_complex(int64_t B, int64_t D, int64_t L, int64_t N,
 }
 
 /*
+ * Mamba-2 state-space-dual (SSD) layer: the same selective recurrence with A a
+ * scalar times the identity per head ("Mamba close reading", section on SSD
+ * and Mamba-2: A simplified to a scalar times I, heads like multi-head
+ * attention, larger states; "Mamba and state space models", section
+ * "Mamba-2 and structured duality").  Heads h < H of P channels each
+ * (channel d = h P + p), states n < N, per batch b and step t:
+ *     Delta_t  = softplus(delta[b,h,t] + delta_bias[h])      (or the plain sum)
+ *     abar_t   = exp(Delta_t a[h])                            (one scalar per head)
+ *     h_t[p,n] = abar_t h_{t-1}[p,n] + Delta_t B[b,t,n] x[b,d,t]
+ *     y[b,d,t] = (sum_n C[b,t,n] h_t[p,n] + Dskip[h] x[b,d,t]) * silu(z[b,d,t])
+ * B and C are shared by all heads.  Layout (dense, row-major):
+ *     x, z, y : (B, H*P, L)   delta : (B, H, L)   Bm, Cm : (B, L, N)
+ *     a, Dskip, delta_bias : (H)   h0, h_last : (B, H, P, N)
+ * Nullable: z, Dskip, delta_bias, h0, h_last.  Sequential in time, one
+ * thread.  The pages' dual (masked-attention) form is a second evaluation
+ * order of the same map, used by the tests as a pin.
+ */
+int oracle_ssd_scan(int64_t B, int64_t H, int64_t P, int64_t L, int64_t N,
+                    const double *x, const double *delta, const double *z,
+                    const double *Bm, const double *Cm, const double *a,
+                    const double *Dskip, const double *delta_bias, const double *h0,
+                    int delta_softplus, double *y, double *h_last) {
+    if (B < 0 || H < 0 || P < 0 || L < 0 || N < 0) return -1;
+    if (!x || !delta || !Bm || !Cm || !a || !y) return -1;
+    double *h = (double *)malloc(sizeof(double) * (size_t)(P * N > 0 ? P * N : 1));
+    if (!h) return -1;
+    for (int64_t b = 0; b < B; ++b) {
+        for (int64_t hd = 0; hd < H; ++hd) {
+            const double bias = delta_bias ? delta_bias[hd] : 0.0;
+            const double Dh = Dskip ? Dskip[hd] : 0.0;
+            for (int64_t i = 0; i < P * N; ++i)
+                h[i] = h0 ? h0[((b * H + hd) * P) * N + i] : 0.0;
+            for (int64_t t = 0; t < L; ++t) {
+                const double dt = discretisation_step(delta[(b * H + hd) * L + t], bias, delta_softplus);
+                const double abar = exp(dt * a[hd]);
+                for (int64_t p = 0; p < P; ++p) {
+                    const int64_t row = (b * H + hd) * P + p;   /* channel row of x, z, y */
+                    const double xt = x[row * L + t];
+                    double acc = 0.0;
+                    for (int64_t n = 0; n < N; ++n) {
+                        h[p * N + n] = abar * h[p * N + n] + dt * Bm[(b * L + t) * N + n] * xt;
+                        acc += Cm[(b * L + t) * N + n] * h[p * N + n];
+                    }
+                    double v = acc + Dh * xt;
+                    if (z) v *= z[row * L + t] * sigmoid(z[row * L + t]);
+                    y[row * L + t] = v;
+                }
+            }
+            if (h_last)
+                for (int64_t i = 0; i < P * N; ++i) h_last[((b * H + hd) * P) * N + i] = h[i];
+        }
+    }
+    free(h);
+    return 0;
+}
+
+/*
  * One recurrent (decode) step for every channel, the loop body of the scan
  * applied once ("gitcode", section 1: constant time per step; section 2: the
  * recurrent mode used for autoregressive inference).

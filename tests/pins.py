@@ -578,11 +578,99 @@ def pin_complex_conjugate_symmetry(lib):
     _close(h2.imag, -h1.imag, rtol=1e-12, atol=1e-12, what="conjugate A: Im h")
 
 
+# --------------------------------------------------------------------------
+# Mamba-2 SSD (scalar A per head; "Mamba close reading", SSD section; "Mamba and state space
+# models", section "Mamba-2 and structured duality"): the map is multiplication by a
+# semiseparable matrix, (L o C B^T) acting on Delta x, with L the data-dependent decay mask
+# --------------------------------------------------------------------------
+
+def _ssd_inputs(rng, Bsz, H, P, L, N, gate=True, h0=False):
+    return dict(
+        x=rng.standard_normal((Bsz, H * P, L)),
+        delta=rng.standard_normal((Bsz, H, L)),
+        z=rng.standard_normal((Bsz, H * P, L)) if gate else None,
+        Bm=rng.standard_normal((Bsz, L, N)),
+        Cm=rng.standard_normal((Bsz, L, N)),
+        a=-rng.uniform(0.2, 2.0, H),
+        Dskip=rng.standard_normal(H),
+        delta_bias=rng.uniform(-3.0, -0.5, H),
+        h0=rng.standard_normal((Bsz, H, P, N)) if h0 else None,
+    )
+
+
+def pin_ssd_dual_form(lib):
+    """The quadratic (dual) form computed directly: y_t = sum_{s<=t} exp(a (S_t - S_s)) (C_t . B_s) Delta_s x_s
+    + exp(a S_t) C_t . h0 + D x_t, gated, with S_t = Delta_0 + ... + Delta_t."""
+    rng = np.random.default_rng(51)
+    Bsz, H, P, L, N = 2, 3, 2, 24, 4
+    x = _ssd_inputs(rng, Bsz, H, P, L, N, h0=True)
+    y, hl = oracle.ssd_scan(x["x"], x["delta"], x["a"], x["Bm"], x["Cm"], Dskip=x["Dskip"], z=x["z"],
+                            delta_bias=x["delta_bias"], h0=x["h0"], return_last_state=True, lib=lib)
+    for b in range(Bsz):
+        G = x["Cm"][b] @ x["Bm"][b].T                                   # (L, L): C_t . B_s
+        for hd in range(H):
+            dts = _softplus(x["delta"][b, hd] + x["delta_bias"][hd])
+            S = np.cumsum(dts)
+            mask = np.tril(np.exp(x["a"][hd] * (S[:, None] - S[None, :])))
+            M = mask * G                                                 # semiseparable matrix
+            for p_ in range(P):
+                d = hd * P + p_
+                xs = x["x"][b, d]
+                ys = M @ (dts * xs) + np.exp(x["a"][hd] * S) * (x["Cm"][b] @ x["h0"][b, hd, p_])
+                ref = (ys + x["Dskip"][hd] * xs) * x["z"][b, d] * _sigmoid(x["z"][b, d])
+                _close(y[b, d], ref, rtol=1e-11, atol=1e-12, what=f"SSD dual form b{b} h{hd} p{p_}")
+            # final state: h_L = exp(a S_L) h0 + sum_s exp(a (S_L - S_s)) Delta_s x_s B_s
+            w = np.exp(x["a"][hd] * (S[-1] - S)) * dts                   # (L,)
+            href = np.exp(x["a"][hd] * S[-1]) * x["h0"][b, hd] + (x["x"][b, hd * P:(hd + 1) * P] * w) @ x["Bm"][b]
+            _close(hl[b, hd], href, rtol=1e-11, atol=1e-12, what=f"SSD dual h_last b{b} h{hd}")
+
+
+def pin_ssd_equals_s6(lib):
+    """SSD is the selective scan with A[d, n] = a[head(d)] for every n, Delta shared by a head's
+    channels and B / C shared by the heads (the S6 oracle is pinned on its own)."""
+    rng = np.random.default_rng(52)
+    Bsz, H, P, L, N = 2, 3, 4, 30, 5
+    x = _ssd_inputs(rng, Bsz, H, P, L, N, h0=True)
+    y, hl = oracle.ssd_scan(x["x"], x["delta"], x["a"], x["Bm"], x["Cm"], Dskip=x["Dskip"], z=x["z"],
+                            delta_bias=x["delta_bias"], h0=x["h0"], return_last_state=True, lib=lib)
+    A = np.repeat(x["a"], P)[:, None] * np.ones((1, N))
+    ys, hs = oracle.selective_scan(x["x"], np.repeat(x["delta"], P, axis=1), A,
+                                   np.transpose(x["Bm"], (0, 2, 1)), np.transpose(x["Cm"], (0, 2, 1)),
+                                   Dskip=np.repeat(x["Dskip"], P), z=x["z"],
+                                   delta_bias=np.repeat(x["delta_bias"], P),
+                                   h0=x["h0"].reshape(Bsz, H * P, N), return_last_state=True)
+    _close(y, ys, rtol=1e-12, atol=1e-12, what="SSD vs S6 y")
+    _close(hl.reshape(Bsz, H * P, N), hs, rtol=1e-12, atol=1e-12, what="SSD vs S6 h_last")
+
+
+def pin_ssd_semiseparable_rank(lib):
+    """The impulse responses of one channel form the matrix M[t, s] (y_t for x = e_s, no gate, no D,
+    Delta_s divided out); every block below the diagonal, M[k:, :k], has rank at most N."""
+    rng = np.random.default_rng(53)
+    L, N = 20, 3
+    delta = rng.standard_normal((1, 1, L))
+    Bm, Cm = rng.standard_normal((1, L, N)), rng.standard_normal((1, L, N))
+    a, bias = np.array([-0.7]), np.array([-1.0])
+    dts = _softplus(delta[0, 0] + bias[0])
+    M = np.zeros((L, L))
+    for s_ in range(L):
+        xin = np.zeros((1, 1, L))
+        xin[0, 0, s_] = 1.0
+        M[:, s_] = oracle.ssd_scan(xin, delta, a, Bm, Cm, delta_bias=bias, lib=lib)[0, 0] / dts[s_]
+    assert np.allclose(np.triu(M, 1), 0.0, atol=0.0), "SSD matrix is not causal"
+    for k in range(N + 1, L - N):
+        sv = np.linalg.svd(M[k:, :k], compute_uv=False)
+        assert sv[N] <= 1e-10 * sv[0], f"block M[{k}:, :{k}] has rank above N: {sv[:N + 2]}"
+
+
+SSD_PINS = [pin_ssd_dual_form, pin_ssd_equals_s6, pin_ssd_semiseparable_rank]
+
+
 COMPLEX_PINS = [pin_complex_zero_imag_is_real, pin_complex_lti_convolution, pin_complex_rotation_impulse,
                 pin_complex_unrolled_sum, pin_complex_conjugate_symmetry]
 
 
-ALL_PINS = CONV_PINS + BWD_PINS + COMPLEX_PINS + [
+ALL_PINS = CONV_PINS + BWD_PINS + COMPLEX_PINS + SSD_PINS + [
     pin_golden_recurrence, pin_golden_gated, pin_lti_equals_convolution, pin_theorem1_gated_rnn,
     pin_unrolled_sum, pin_single_step_closed_form, pin_tree_order_matches_sequential,
     pin_boundary_reset, pin_ignore_window, pin_chunk_invariance, pin_step_matches_scan,

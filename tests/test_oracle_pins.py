@@ -73,6 +73,15 @@ MUTANTS = [
     ("h[n] = h0 ? h0[2 * (c * N + n)] + I * h0[2 * (c * N + n) + 1] : 0.0;",
      "h[n] = h0 ? h0[2 * (c * N + n)] : 0.0;"),
     ("h_last[2 * (c * N + n) + 1] = cimag(h[n]);", "h_last[2 * (c * N + n) + 1] = -cimag(h[n]);"),
+    # the Mamba-2 SSD layer
+    ("h[p * N + n] = abar * h[p * N + n] + dt * Bm[(b * L + t) * N + n] * xt;",
+     "h[p * N + n] = abar * h[p * N + n] + Bm[(b * L + t) * N + n] * xt;"),
+    ("const double abar = exp(dt * a[hd]);", "const double abar = exp(dt * a[0]);"),
+    ("acc += Cm[(b * L + t) * N + n] * h[p * N + n];", "acc += Cm[(b * L + t) * N + n] * h[n];"),
+    ("double v = acc + Dh * xt;", "double v = acc;"),
+    ("h[i] = h0 ? h0[((b * H + hd) * P) * N + i] : 0.0;", "h[i] = 0.0;"),
+    ("h[p * N + n] = abar * h[p * N + n] + dt * Bm[(b * L + t) * N + n] * xt;",
+     "h[p * N + n] = abar * h[p * N + n] + dt * Bm[(b * N + n) * L + t] * xt;"),
 ]
 
 
