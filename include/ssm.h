@@ -1,8 +1,8 @@
 /*
  * ssm.h -- C ABI of the B300 selective state space (S6) library (libssm.so).
  *
- * Four operations, all from the Mamba paper (arXiv 2312.00752) as
- * restated on the pages this library follows:
+ * Five operations, from the Mamba paper (arXiv 2312.00752) and its Mamba-2
+ * successor as restated on the pages this library follows:
  *
  *   ssm_scan_fwd      the selective-scan forward pass.  For every batch b,
  *                     channel d and state n:
@@ -33,6 +33,8 @@
  *                     ("docs.ifdog.com", section "Mamba architecture", step
  *                     3a; step 3b feeds its output to the projections that
  *                     make Delta, B and C and to the scan as u).
+ *   ssm_ssd_fwd       the Mamba-2 state-space-dual layer (scalar A per head,
+ *                     chunked on the tensor cores; see ssm_ssd_args_t).
  *
  * Conventions for every entry point
  *   - All tensor pointers are DEVICE pointers unless stated otherwise; the
@@ -240,6 +242,54 @@ typedef struct ssm_conv_args {
 /* Causal depthwise convolution (+ SiLU) along time (see ssm_conv_args_t). */
 ssm_status_t ssm_causal_conv1d_fwd(const ssm_conv_args_t *args, void *stream);
 
+/*
+ * Arguments of ssm_ssd_fwd: the Mamba-2 state-space-dual (SSD) layer ("Mamba
+ * close reading", alishangtian.com, section on SSD and Mamba-2: A is a scalar
+ * times the identity per head, heads as in multi-head attention, larger
+ * states; "Mamba and state space models", docs.ifdog.com, section "Mamba-2
+ * and structured duality": the layer is multiplication by a semiseparable
+ * matrix (L o C B^T) with a data-dependent decay mask L).  With H heads of P
+ * channels each (channel d = h P + p), per batch b, state n and step t:
+ *   Delta_t  = softplus(delta[b,h,t] + delta_bias[h])   (or the plain sum)
+ *   h_t[p,n] = exp(Delta_t A[h]) h_{t-1}[p,n] + Delta_t B[b,t,n] x[b,d,t]
+ *   y[b,d,t] = (sum_n C[b,t,n] h_t[p,n] + Dskip[h] x[b,d,t]) * silu(z[b,d,t])
+ * B and C are shared by all heads.  Shapes (strides in elements):
+ *   x, z, y      : (batch, nheads * headdim, seqlen)  io_dtype, time stride 1; z nullable
+ *   delta        : (batch, nheads, seqlen)            io_dtype, time stride 1
+ *   Bm, Cm       : (batch, seqlen, dstate)            io_dtype (state index contiguous in the
+ *                                                     fast kernel; any strides otherwise)
+ *   A, Dskip, delta_bias : (nheads,) fp32 contiguous; Dskip and delta_bias nullable
+ *   h0, h_last   : (batch, nheads, headdim, dstate)   fp32, nullable
+ * Limits: 1 <= dstate <= 256.  bf16 I/O with headdim 64, dstate 128, dense
+ * x (rows of seqlen, seqlen a multiple of 8) and dense B / C rows of 128 runs
+ * the chunked tensor-core kernel (tcgen05.mma on 128-step chunks); every other
+ * case runs the recurrence on the CUDA cores.  Outputs must not overlap inputs.
+ */
+#define SSM_SSD_FORCE_GENERIC 0x1   /* flags: run the CUDA-core recurrence */
+typedef struct ssm_ssd_args {
+    int64_t batch, nheads, headdim, seqlen, dstate;   /* B, H, P, L, N */
+    ssm_dtype_t io_dtype;
+    int32_t delta_softplus;
+    const void *x, *delta, *z, *Bm, *Cm;
+    const float *A, *Dskip, *delta_bias;
+    const float *h0;
+    float *h_last;
+    void *y;
+    int64_t stride_x[3], stride_z[3], stride_y[3];    /* (b, d, t) */
+    int64_t stride_delta[3];                          /* (b, h, t) */
+    int64_t stride_B[3], stride_C[3];                 /* (b, t, n) */
+    int64_t stride_h0[4], stride_h_last[4];           /* (b, h, p, n) */
+    int32_t flags;                                    /* SSM_SSD_FORCE_GENERIC or 0 */
+    int32_t reserved0;
+} ssm_ssd_args_t;
+
+/* The Mamba-2 SSD layer (see ssm_ssd_args_t).  Asynchronous on `stream`. */
+ssm_status_t ssm_ssd_fwd(const ssm_ssd_args_t *args, void *stream);
+
+/* 1 if ssm_ssd_fwd takes the tensor-core kernel for these arguments, 0 if
+ * the CUDA-core recurrence, -1 if the arguments are invalid.  Host-only. */
+int ssm_ssd_plan_path(const ssm_ssd_args_t *args);
+
 /* Bytes of device workspace ssm_scan_fwd needs for these arguments (0 for
  * the single-pass paths).  Host-only; validates the arguments first.  The
  * plan it reflects depends on the current device's SM count. */
@@ -314,8 +364,8 @@ int ssm_version(void);
 
 /* sizeof of the argument structs as compiled into the library, so that a
  * binding can check its mirror of them: which = 0 -> ssm_scan_args_t,
- * 1 -> ssm_step_args_t, 2 -> ssm_conv_args_t, 3 -> ssm_scan_bwd_args_t; 0 for
- * any other value. */
+ * 1 -> ssm_step_args_t, 2 -> ssm_conv_args_t, 3 -> ssm_scan_bwd_args_t,
+ * 4 -> ssm_ssd_args_t; 0 for any other value. */
 size_t ssm_abi_sizeof(int which);
 
 #ifdef __cplusplus

@@ -32,7 +32,8 @@ PATH_NAMES = {0: "generic", 1: "tiled", 2: "chunked"}
 EXPORTED_SYMBOLS = ["ssm_scan_workspace_size", "ssm_scan_fwd", "ssm_state_update", "ssm_status_string",
                     "ssm_last_error_detail", "ssm_get_device_status", "ssm_scan_plan_path", "ssm_version",
                     "ssm_abi_sizeof", "ssm_scan_fwd_noalloc", "ssm_causal_conv1d_fwd",
-                    "ssm_scan_bwd_workspace_size", "ssm_scan_bwd", "ssm_probe_sfu"]
+                    "ssm_scan_bwd_workspace_size", "ssm_scan_bwd", "ssm_probe_sfu", "ssm_ssd_fwd",
+                    "ssm_ssd_plan_path"]
 
 _i64 = ctypes.c_int64
 _vp = ctypes.c_void_p
@@ -51,6 +52,19 @@ class ScanArgs(ctypes.Structure):
         ("flags", ctypes.c_int32), ("discretization", ctypes.c_int32), ("chunk_len", _i64),
         ("workspace", _vp), ("workspace_bytes", ctypes.c_size_t),
         ("A_imag", _vp),
+    ]
+
+
+class SsdArgs(ctypes.Structure):
+    """Mirror of ssm_ssd_args_t."""
+    _fields_ = [
+        ("batch", _i64), ("nheads", _i64), ("headdim", _i64), ("seqlen", _i64), ("dstate", _i64),
+        ("io_dtype", ctypes.c_int), ("delta_softplus", ctypes.c_int32),
+        ("x", _vp), ("delta", _vp), ("z", _vp), ("Bm", _vp), ("Cm", _vp),
+        ("A", _vp), ("Dskip", _vp), ("delta_bias", _vp), ("h0", _vp), ("h_last", _vp), ("y", _vp),
+        ("stride_x", _i64 * 3), ("stride_z", _i64 * 3), ("stride_y", _i64 * 3), ("stride_delta", _i64 * 3),
+        ("stride_B", _i64 * 3), ("stride_C", _i64 * 3), ("stride_h0", _i64 * 4), ("stride_h_last", _i64 * 4),
+        ("flags", ctypes.c_int32), ("reserved0", ctypes.c_int32),
     ]
 
 
@@ -138,8 +152,13 @@ def load_library(path: str = LIB_PATH):
         lib.ssm_scan_bwd.restype = ctypes.c_int
         lib.ssm_probe_sfu.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, _vp, _vp]
         lib.ssm_probe_sfu.restype = ctypes.c_int
+        lib.ssm_ssd_fwd.argtypes = [ctypes.POINTER(SsdArgs), _vp]
+        lib.ssm_ssd_fwd.restype = ctypes.c_int
+        lib.ssm_ssd_plan_path.argtypes = [ctypes.POINTER(SsdArgs)]
+        lib.ssm_ssd_plan_path.restype = ctypes.c_int
         if (lib.ssm_abi_sizeof(0) != ctypes.sizeof(ScanArgs) or lib.ssm_abi_sizeof(1) != ctypes.sizeof(StepArgs)
-                or lib.ssm_abi_sizeof(2) != ctypes.sizeof(ConvArgs) or lib.ssm_abi_sizeof(3) != ctypes.sizeof(BwdArgs)):
+                or lib.ssm_abi_sizeof(2) != ctypes.sizeof(ConvArgs) or lib.ssm_abi_sizeof(3) != ctypes.sizeof(BwdArgs)
+                or lib.ssm_abi_sizeof(4) != ctypes.sizeof(SsdArgs)):
             raise ImportError("libssm.so argument structs do not match this binding")
         if path == LIB_PATH:
             _lib = lib
@@ -491,3 +510,59 @@ def ssm_scan_fwd_noalloc(u, delta, A, Bm, Cm, y, Dskip=None, z=None, delta_bias=
                           SSM_SCAN_FORCE_CHUNKED, chunk_len, None, discretization)
     _check(load_library().ssm_scan_fwd_noalloc(ctypes.byref(args), _vp(_stream_handle(stream))))
     return y
+
+
+SSM_SSD_FORCE_GENERIC = 0x1
+
+
+def make_ssd_args(x, delta, A, Bm, Cm, y, Dskip=None, z=None, delta_bias=None, h0=None, h_last=None,
+                  delta_softplus=True, flags=0) -> SsdArgs:
+    """Fill an ssm_ssd_args_t from torch tensors: x, z, y (B, H*P, L); delta (B, H, L); Bm, Cm (B, L, N);
+    A, Dskip, delta_bias (H,); h0, h_last (B, H, P, N)."""
+    Bsz, H, L = delta.shape
+    D = x.shape[1]
+    N = Bm.shape[-1]
+    a = SsdArgs()
+    a.batch, a.nheads, a.headdim, a.seqlen, a.dstate = Bsz, H, D // H, L, N
+    a.io_dtype = _io_dtype(x)
+    a.delta_softplus = 1 if delta_softplus else 0
+    a.x, a.delta, a.z, a.Bm, a.Cm = _ptr(x), _ptr(delta), _ptr(z), _ptr(Bm), _ptr(Cm)
+    a.A, a.Dskip, a.delta_bias, a.h0, a.h_last, a.y = _ptr(A), _ptr(Dskip), _ptr(delta_bias), _ptr(h0), _ptr(h_last), _ptr(y)
+    a.stride_x[:] = _strides(x, 3)
+    a.stride_z[:] = _strides(z, 3)
+    a.stride_y[:] = _strides(y, 3)
+    a.stride_delta[:] = _strides(delta, 3)
+    a.stride_B[:] = _strides(Bm, 3)
+    a.stride_C[:] = _strides(Cm, 3)
+    a.stride_h0[:] = _strides(h0, 4)
+    a.stride_h_last[:] = _strides(h_last, 4)
+    a.flags = int(flags)
+    return a
+
+
+def ssm_ssd_plan_path(args: SsdArgs) -> str:
+    return {1: "tensor_core", 0: "generic"}.get(int(load_library().ssm_ssd_plan_path(ctypes.byref(args))), "invalid")
+
+
+def ssm_ssd_fwd(x, delta, A, Bm, Cm, Dskip=None, z=None, delta_bias=None, h0=None, delta_softplus=True,
+                y=None, return_last_state=False, h_last=None, flags=0, stream=None):
+    """Mamba-2 SSD layer on the GPU: x, z (B, H*P, L); delta (B, H, L); Bm, Cm (B, L, N); A, Dskip,
+    delta_bias (H,) fp32; h0 (B, H, P, N) fp32.  Returns y (B, H*P, L) in the I/O dtype, and h_last
+    (B, H, P, N) fp32 if requested."""
+    torch = _torch()
+    lib = load_library()
+    for name, t in (("x", x), ("delta", delta), ("Bm", Bm), ("Cm", Cm), ("z", z)):
+        if t is not None and not t.is_cuda:
+            raise ValueError(f"{name} must be a CUDA tensor")
+    _f32(A, "A"); _f32(Dskip, "Dskip"); _f32(delta_bias, "delta_bias"); _f32(h0, "h0")
+    A = A.contiguous()
+    Dskip = Dskip.contiguous() if Dskip is not None else None
+    delta_bias = delta_bias.contiguous() if delta_bias is not None else None
+    if y is None:
+        y = torch.empty(x.shape, dtype=x.dtype, device=x.device)
+    Bsz, H, L = delta.shape
+    if return_last_state and h_last is None:
+        h_last = torch.empty((Bsz, H, x.shape[1] // H, Bm.shape[-1]), dtype=torch.float32, device=x.device)
+    args = make_ssd_args(x, delta, A, Bm, Cm, y, Dskip, z, delta_bias, h0, h_last, delta_softplus, flags)
+    _check(lib.ssm_ssd_fwd(ctypes.byref(args), _vp(_stream_handle(stream))))
+    return (y, h_last) if return_last_state else y

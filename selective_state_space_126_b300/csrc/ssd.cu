@@ -1,0 +1,468 @@
+// ssd.cu -- the Mamba-2 state-space-dual (SSD) layer on the fifth-generation tensor cores.
+//
+// What it computes ("Mamba close reading", alishangtian.com, section on SSD and
+// Mamba-2: A is a scalar times the identity per head, heads as in multi-head
+// attention, states 8x larger; "Mamba and state space models", docs.ifdog.com,
+// section "Mamba-2 and structured duality"): per batch b, head h, head channel
+// p (channel d = h P + p), state n and step t,
+//     Delta_t  = softplus(delta[b,h,t] + bias[h]),   abar_t = exp(Delta_t a[h])
+//     h_t[p,n] = abar_t h_{t-1}[p,n] + Delta_t B[b,t,n] x[b,d,t]
+//     y[b,d,t] = (sum_n C[b,t,n] h_t[p,n] + D[h] x[b,d,t]) * silu(z[b,d,t]).
+// The pages' duality: the map x -> y is multiplication by a semiseparable
+// matrix, M = L o (C B^T) with the decay mask L[t,s] = exp(a (S_t - S_s)),
+// S_t = Delta_0 + ... + Delta_t, for s <= t.  Cut the sequence into chunks of
+// Q = 128 steps; within a chunk the masked product is dense, across chunks
+// the state (N x P per head) carries the rest:
+//     G        = C_c B_c^T                                  (Q x Q)
+//     Y_diag   = (L_c o G) diag(Delta) X_c                  (Q x P)
+//     Y_off    = diag(exp(a S_t)) C_c H_in                   (Q x P)
+//     H_chunk  = B_c^T diag(exp(a (S_end - S_s)) Delta_s) X_c  (N x P)
+//     H_out    = exp(a S_end) H_in + H_chunk.
+// The four products are dense contractions and run as tcgen05.mma (bf16
+// operands in shared memory, fp32 accumulators in tensor memory); the decay
+// mask, the scalings, the state recurrence across chunks (fp32, in registers)
+// and the output (D skip, gate) run on the CUDA cores.
+//
+// ssd_chunk_kernel: one CTA of 128 threads per (batch, head) walks its chunks
+// in order, for P = 64 and N = 128 with bf16 I/O.  Thread i owns time row i of
+// the chunk (tensor-memory lane i of G, Y_diag, Y_off) and state row i (lane i
+// of H_chunk, and the fp32 state H[i][0..63] in registers).  Per chunk:
+//   1. TMA: C_c and B_c ((L, N) rows of 128 B, 128B swizzle, two 64-column
+//      boxes each) and X_c ((P, L) rows, two 64-step boxes) -- each already
+//      the K-major operand layout of the MMAs below;
+//   2. Delta, the inclusive prefix sum S (warp shuffles and one shared step),
+//      the weights w_s = exp(a (S_end - S_s)) Delta_s; threads write
+//      X_Delta = Delta_s X (K = s), B~^T = w_s B^T (transposed, K = s) and the
+//      incoming state H_in^T (K = n) in bf16;
+//   3. MMA: G = C B^T, H_chunk = B~^T X, Y_off = C H_in (one commit each);
+//   4. threads read G (tcgen05.ld), apply the causal decay mask
+//      exp(a (S_t - S_s)) on the SFU and write the bf16 scores (K = s);
+//   5. MMA: Y_diag = scores X_Delta;
+//   6. threads update H = exp(a S_end) H + H_chunk and emit
+//      y = (Y_diag + exp(a S_t) Y_off + D x) silu(z), coalesced along t.
+// Other shapes and fp32 I/O take ssd_generic_kernel (one warp per channel, the
+// recurrence itself).
+#include <cstdio>
+#include <cstring>
+
+#include "device_math.cuh"
+#include "scan_common.cuh"
+#include "ssm_internal.h"
+#include "tcgen05.cuh"
+
+namespace ssm {
+namespace {
+
+constexpr int kQ = 128;          // chunk length
+constexpr int kP = 64;           // head dimension of the tensor-core kernel
+constexpr int kN = 128;          // state size of the tensor-core kernel
+constexpr int kSsdThreads = 128;
+
+struct SsdSmem {
+  static constexpr int kC = 0;                 // C chunk: 2 x [128 t][64 n] bf16, swizzled
+  static constexpr int kB = kC + 32768;        // B chunk: 2 x [128 s][64 n]
+  static constexpr int kX = kB + 32768;        // X chunk: 2 x [64 p][64 s]
+  static constexpr int kSP = kX + 16384;       // masked scores: 2 x [128 t][64 s]
+  static constexpr int kXD = kSP + 32768;      // Delta X: 2 x [64 p][64 s]
+  static constexpr int kBT = kXD + 16384;      // weighted B^T: 2 x [128 n][64 s]
+  static constexpr int kSI = kBT + 32768;      // incoming state H_in^T: 2 x [64 p][64 n]
+  static constexpr int kDelta = kSI + 16384;   // float [128]
+  static constexpr int kCum = kDelta + 512;    // float [128]
+  static constexpr int kW = kCum + 512;        // float [128]
+  static constexpr int kWarp = kW + 512;       // float [4] warp totals of the prefix sum
+  static constexpr int kBar = kWarp + 16;      // 4 mbarriers: TMA, G, (H_chunk, Y_off), Y_diag
+  static constexpr int kTaddr = kBar + 32;
+  static constexpr int kBytes = kTaddr + 16;
+  static constexpr int kAlloc = kBytes + 1024;
+};
+
+// tensor-memory columns of the accumulators (lanes = rows)
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kColG = 0, kColYd = 128, kColYo = 192, kColH = 256;
+
+struct SsdMaps {
+  CUtensorMap x, B, C;
+};
+
+__global__ void __launch_bounds__(kSsdThreads, 1)
+    ssd_chunk_kernel(const __grid_constant__ SsdProblem p, const __grid_constant__ SsdMaps tm) {
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  unsigned char* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  using S = SsdSmem;
+  float* sDelta = reinterpret_cast<float*>(smem + S::kDelta);
+  float* sCum = reinterpret_cast<float*>(smem + S::kCum);
+  float* sW = reinterpret_cast<float*>(smem + S::kW);
+  float* sWarp = reinterpret_cast<float*>(smem + S::kWarp);
+  const uint32_t bar_tma = smem_u32(smem + S::kBar), bar_g = bar_tma + 8, bar_ho = bar_tma + 16,
+                 bar_d = bar_tma + 24;
+  uint32_t* taddr_s = reinterpret_cast<uint32_t*>(smem + S::kTaddr);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int64_t bh = blockIdx.x;
+  const int64_t b = bh / p.H, h = bh % p.H;
+  const int nchunks = (int)((p.L + kQ - 1) / kQ);
+  const float a2 = p.a[h] * kLog2e;
+  const float bias = p.bias ? p.bias[h] : 0.f;
+  const float Dh = p.Dskip ? p.Dskip[h] : 0.f;
+
+  if (tid == 0) {
+    for (int i = 0; i < 4; ++i) mbar_init(bar_tma + 8 * i, 1);
+    mbar_init_fence();
+  }
+  if (warp == 0) tmem_alloc(smem_u32(taddr_s), kTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *taddr_s;
+  const uint32_t lane_off = (uint32_t)(32 * warp) << 16;
+
+  // state H[tid][0..63] (state row n = tid, head channels p), fp32 in registers
+  float H[kP];
+#pragma unroll
+  for (int q = 0; q < kP; ++q)
+    H[q] = p.h0 ? p.h0[b * p.sh0[0] + h * p.sh0[1] + q * p.sh0[2] + tid * p.sh0[3]] : 0.f;
+
+  auto issue = [&](int c) {
+    const int t0 = c * kQ;
+    mbar_expect_tx(bar_tma, 2 * 16384 + 2 * 16384 + 2 * 8192);
+    for (int j = 0; j < 2; ++j) {
+      tma_load(smem_u32(smem + S::kC + j * 16384), &tm.C, 64 * j, t0, (int)b, true, bar_tma);
+      tma_load(smem_u32(smem + S::kB + j * 16384), &tm.B, 64 * j, t0, (int)b, true, bar_tma);
+      tma_load(smem_u32(smem + S::kX + j * 8192), &tm.x, t0 + 64 * j, (int)(h * kP), (int)b, true, bar_tma);
+    }
+  };
+  if (tid == 0 && nchunks > 0) issue(0);
+
+  const uint32_t id128 = umma_idesc_bf16(128, 128), id64 = umma_idesc_bf16(128, 64);
+  bool failed = false;
+  bool mma_out = false, mma_d_out = false;   // thread 0: MMAs of the current chunk issued and not yet waited for
+  int c = 0;
+  for (; c < nchunks; ++c) {
+    const uint32_t par = (uint32_t)c & 1u;
+    const int64_t t0 = (int64_t)c * kQ;
+    const int valid = (int)(p.L - t0 < kQ ? p.L - t0 : kQ);   // steps of this chunk inside the sequence
+
+    // ---- 2. Delta, prefix sum S, weights ----
+    float dt = 0.f;
+    if (tid < valid) {
+      const float dv = p.io == SSM_BF16
+                           ? __bfloat162float(static_cast<const __nv_bfloat16*>(p.delta)[b * p.sd[0] + h * p.sd[1] + t0 + tid])
+                           : static_cast<const float*>(p.delta)[b * p.sd[0] + h * p.sd[1] + t0 + tid];
+      dt = delta_of<false>(dv, bias, p.softplus);
+    }
+    float cum = dt;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const float v = __shfl_up_sync(0xffffffffu, cum, o);
+      if (lane >= o) cum += v;
+    }
+    if (lane == 31) sWarp[warp] = cum;
+    // the incoming state as the bf16 operand H_in^T: row p, K = n (this thread's n = tid)
+#pragma unroll
+    for (int q = 0; q < kP; ++q)
+      *reinterpret_cast<__nv_bfloat16*>(smem + S::kSI + (tid >> 6) * 8192 + sw128_offset(q, tid & 63)) =
+          __float2bfloat16_rn(H[q]);
+    __syncthreads();
+    for (int w = 0; w < warp; ++w) cum += sWarp[w];
+    sDelta[tid] = dt;
+    sCum[tid] = cum;
+    __syncthreads();
+    const float cum_end = sCum[kQ - 1];
+    sW[tid] = ex2_approx(a2 * (cum_end - cum)) * dt;
+    const float et = ex2_approx(a2 * cum);   // exp(a S_t)
+
+    // ---- 1. the chunk's tiles ----
+    const bool ok_tma = mbar_wait(bar_tma, par);
+    if (!ok_tma) record_status(p.status, SSM_ERR_TIMEOUT);
+    __syncthreads();   // sW visible
+    if (ok_tma) {
+      // X_Delta[p][s] = Delta_s X[p][s]: thread -> (row p = tid % 64, 64-step block tid / 64)
+      {
+        const int pr = tid & 63, blk = tid >> 6;
+        const unsigned char* src = smem + S::kX + blk * 8192 + pr * 128;
+        unsigned char* dst = smem + S::kXD + blk * 8192 + pr * 128;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const int pos = (j ^ (pr & 7)) << 4;   // logical piece j holds s = 64 blk + 8 j .. + 7
+          float f[8];
+          unpack16(*reinterpret_cast<const uint4*>(src + pos), f);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) f[e] *= sDelta[64 * blk + 8 * j + e];
+          *reinterpret_cast<uint4*>(dst + pos) = pack16(f);
+        }
+      }
+      // B~^T[n][s] = w_s B[s][n]: thread n = tid gathers column n of B
+      {
+        const int n = tid;
+        const unsigned char* src = smem + S::kB + (n >> 6) * 16384;
+#pragma unroll 2
+        for (int j = 0; j < 16; ++j) {   // 8 steps s = 8 j .. 8 j + 7 per 16-byte piece of row n
+          float f[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const int s = 8 * j + e;
+            f[e] = __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(src + sw128_offset(s, n & 63))) * sW[s];
+          }
+          const int sblk = j >> 3, jj = j & 7;
+          *reinterpret_cast<uint4*>(smem + S::kBT + sblk * 16384 + n * 128 + ((jj ^ (n & 7)) << 4)) = pack16(f);
+        }
+      }
+    }
+    fence_async_smem();
+    tc_fence_before();
+    if (__syncthreads_or(!ok_tma)) { failed = true; break; }
+
+    // ---- 3. G = C B^T, H_chunk = B~^T X, Y_off = C H_in ----
+    if (tid == 0) {
+      tc_fence_after();
+      const uint32_t sC = smem_u32(smem + S::kC), sB = smem_u32(smem + S::kB), sX = smem_u32(smem + S::kX);
+      const uint32_t sBT = smem_u32(smem + S::kBT), sSI = smem_u32(smem + S::kSI);
+      for (int k = 0; k < 8; ++k) {
+        const uint32_t o16 = (k >> 2) * 16384 + (k & 3) * 32;
+        umma_bf16(tmem + kColG, umma_desc_sw128(sC + o16), umma_desc_sw128(sB + o16), id128, k > 0);
+      }
+      umma_commit(bar_g);
+      for (int k = 0; k < 8; ++k) {
+        const uint32_t o16 = (k >> 2) * 16384 + (k & 3) * 32, o8 = (k >> 2) * 8192 + (k & 3) * 32;
+        umma_bf16(tmem + kColH, umma_desc_sw128(sBT + o16), umma_desc_sw128(sX + o8), id64, k > 0);
+      }
+      for (int k = 0; k < 8; ++k) {
+        const uint32_t o16 = (k >> 2) * 16384 + (k & 3) * 32, o8 = (k >> 2) * 8192 + (k & 3) * 32;
+        umma_bf16(tmem + kColYo, umma_desc_sw128(sC + o16), umma_desc_sw128(sSI + o8), id64, k > 0);
+      }
+      umma_commit(bar_ho);
+      mma_out = true;
+    }
+
+    // ---- 4. causal decay mask on G -> bf16 scores, row t = tid, K = s ----
+    const bool ok_g = mbar_wait(bar_g, par);
+    if (!ok_g) record_status(p.status, SSM_ERR_TIMEOUT);
+    tc_fence_after();
+    if (__syncthreads_or(!ok_g)) { failed = true; break; }
+#pragma unroll 1
+    for (int s0 = 0; s0 < kQ; s0 += 32) {
+      float g[32];
+      tmem_ld32(tmem + lane_off + kColG + (uint32_t)s0, g);
+#pragma unroll
+      for (int j = 0; j < 32; j += 8) {
+        float f[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const int s = s0 + j + e;
+          f[e] = s <= tid ? g[j + e] * ex2_approx(a2 * (cum - sCum[s])) : 0.f;
+        }
+        const int sblk = (s0 + j) >> 6, piece = ((s0 + j) & 63) >> 3;
+        *reinterpret_cast<uint4*>(smem + S::kSP + sblk * 16384 + tid * 128 + ((piece ^ (tid & 7)) << 4)) = pack16(f);
+      }
+    }
+    fence_async_smem();
+    tc_fence_before();
+    __syncthreads();
+
+    // ---- 5. Y_diag = scores X_Delta ----
+    if (tid == 0) {
+      tc_fence_after();
+      const uint32_t sSP = smem_u32(smem + S::kSP), sXD = smem_u32(smem + S::kXD);
+      for (int k = 0; k < 8; ++k) {
+        const uint32_t o16 = (k >> 2) * 16384 + (k & 3) * 32, o8 = (k >> 2) * 8192 + (k & 3) * 32;
+        umma_bf16(tmem + kColYd, umma_desc_sw128(sSP + o16), umma_desc_sw128(sXD + o8), id64, k > 0);
+      }
+      umma_commit(bar_d);
+      mma_d_out = true;
+    }
+
+    // ---- 6. state update, then the output ----
+    const bool ok_ho = mbar_wait(bar_ho, par);
+    if (!ok_ho) record_status(p.status, SSM_ERR_TIMEOUT);
+    tc_fence_after();
+    if (ok_ho) {
+      const float decay = ex2_approx(a2 * cum_end);
+#pragma unroll
+      for (int q0 = 0; q0 < kP; q0 += 32) {
+        float hc[32];
+        tmem_ld32(tmem + lane_off + kColH + (uint32_t)q0, hc);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) H[q0 + j] = fmaf(decay, H[q0 + j], hc[j]);
+      }
+    }
+    const bool ok_d = mbar_wait(bar_d, par);
+    if (!ok_d) record_status(p.status, SSM_ERR_TIMEOUT);
+    tc_fence_after();
+    if (ok_ho && ok_d) {
+      const int64_t t = t0 + tid;
+      for (int q0 = 0; q0 < kP; q0 += 32) {
+        float yd[32], yo[32];
+        tmem_ld32(tmem + lane_off + kColYd + (uint32_t)q0, yd);
+        tmem_ld32(tmem + lane_off + kColYo + (uint32_t)q0, yo);
+        if (tid < valid) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const int q = q0 + j;
+            const int64_t d = h * kP + q;
+            const float xv = __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(
+                smem + S::kX + (tid >> 6) * 8192 + sw128_offset(q, tid & 63)));
+            float v = fmaf(et, yo[j], yd[j]) + Dh * xv;
+            if (p.z) {
+              const float zv = __bfloat162float(static_cast<const __nv_bfloat16*>(p.z)[b * p.sz[0] + d * p.sz[1] + t]);
+              v *= silu<false>(zv);
+            }
+            static_cast<__nv_bfloat16*>(p.y)[b * p.sy[0] + d * p.sy[1] + t] = __float2bfloat16_rn(v);
+          }
+        }
+      }
+    }
+    tc_fence_before();
+    if (__syncthreads_or(!(ok_ho && ok_d))) { failed = true; break; }
+    mma_out = mma_d_out = false;
+    if (tid == 0 && c + 1 < nchunks) issue(c + 1);
+  }
+
+  if (failed) {
+    // let every copy and MMA this CTA started finish (bounded waits) before its tensor memory is freed
+    if (tid == 0) {
+      const uint32_t par = (uint32_t)c & 1u;
+      mbar_wait(bar_tma, par);          // this chunk's tiles were issued before the loop body started
+      if (mma_out) {
+        mbar_wait(bar_g, par);
+        mbar_wait(bar_ho, par);
+      }
+      if (mma_d_out) mbar_wait(bar_d, par);
+    }
+  } else if (p.h_last) {
+#pragma unroll
+    for (int q = 0; q < kP; ++q) p.h_last[b * p.shl[0] + h * p.shl[1] + q * p.shl[2] + tid * p.shl[3]] = H[q];
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 0) tmem_dealloc(tmem, kTmemCols);
+}
+
+// The recurrence itself, one warp per (batch, channel): lane l keeps states n = l, l + 32, ...;
+// the C contraction is a warp sum.  Any head size, state size up to 256, any strides, fp32 or bf16.
+template <typename IO, int NPL, bool PRECISE>
+__global__ void __launch_bounds__(128) ssd_generic_kernel(const SsdProblem p) {
+  const int64_t wid = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  const int64_t D = p.H * p.P;
+  if (wid >= p.B * D) return;
+  const int64_t b = wid / D, d = wid % D, h = d / p.P, q = d % p.P;
+  const int N = (int)p.N;
+  const float a2 = p.a[h] * kLog2e;
+  const float bias = p.bias ? p.bias[h] : 0.f;
+  const float Dh = p.Dskip ? p.Dskip[h] : 0.f;
+  const IO* x = static_cast<const IO*>(p.x) + b * p.sx[0] + d * p.sx[1];
+  const IO* z = p.z ? static_cast<const IO*>(p.z) + b * p.sz[0] + d * p.sz[1] : nullptr;
+  const IO* dl = static_cast<const IO*>(p.delta) + b * p.sd[0] + h * p.sd[1];
+  const IO* Bm = static_cast<const IO*>(p.Bm) + b * p.sB[0];
+  const IO* Cm = static_cast<const IO*>(p.Cm) + b * p.sC[0];
+  IO* y = static_cast<IO*>(p.y) + b * p.sy[0] + d * p.sy[1];
+  float hs[NPL];
+#pragma unroll
+  for (int j = 0; j < NPL; ++j) {
+    const int n = lane + 32 * j;
+    hs[j] = (n < N && p.h0) ? p.h0[b * p.sh0[0] + h * p.sh0[1] + q * p.sh0[2] + n * p.sh0[3]] : 0.f;
+  }
+  for (int64_t t = 0; t < p.L; ++t) {
+    const float dt = delta_of<PRECISE>(to_f32(dl[t]), bias, p.softplus);
+    const float ab = ex2_approx(dt * a2);
+    const float xv = to_f32(x[t]);
+    const float dx = dt * xv;
+    float acc = 0.f;
+#pragma unroll
+    for (int j = 0; j < NPL; ++j) {
+      const int n = lane + 32 * j;
+      if (n < N) {
+        hs[j] = fmaf(ab, hs[j], dx * to_f32(Bm[t * p.sB[1] + n * p.sB[2]]));
+        acc = fmaf(to_f32(Cm[t * p.sC[1] + n * p.sC[2]]), hs[j], acc);
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+    if (lane == 0) {
+      float v = acc + Dh * xv;
+      if (z) v *= silu<PRECISE>(to_f32(z[t]));
+      y[t] = from_f32<IO>(v);
+    }
+  }
+  if (p.h_last) {
+#pragma unroll
+    for (int j = 0; j < NPL; ++j) {
+      const int n = lane + 32 * j;
+      if (n < N) p.h_last[b * p.shl[0] + h * p.shl[1] + q * p.shl[2] + n * p.shl[3]] = hs[j];
+    }
+  }
+}
+
+template <typename IO, bool PRECISE>
+cudaError_t launch_generic(const SsdProblem& p, cudaStream_t s) {
+  const int64_t warps = p.B * p.H * p.P;
+  const dim3 grid((unsigned)((warps * 32 + 127) / 128));
+  if (p.N <= 32) ssd_generic_kernel<IO, 1, PRECISE><<<grid, 128, 0, s>>>(p);
+  else if (p.N <= 64) ssd_generic_kernel<IO, 2, PRECISE><<<grid, 128, 0, s>>>(p);
+  else if (p.N <= 128) ssd_generic_kernel<IO, 4, PRECISE><<<grid, 128, 0, s>>>(p);
+  else ssd_generic_kernel<IO, 8, PRECISE><<<grid, 128, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
+// Tensor map of a rank-3 bf16 tensor with dims (inner, mid, outer) and byte strides (mid, outer),
+// box (64, box_mid, 1), 128-byte swizzle.
+bool encode_ssd_map(CUtensorMap* map, const void* base, uint64_t inner, uint64_t mid, uint64_t outer,
+                    uint64_t stride_mid_bytes, uint64_t stride_outer_bytes, uint32_t box_mid) {
+  EncodeTiledFn enc = get_encode_tiled();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {inner, mid, outer};
+  cuuint64_t gstr[2] = {stride_mid_bytes, stride_outer_bytes};
+  cuuint32_t box[3] = {64, box_mid, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, gstr, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+bool ssd_tensor_core_eligible(const SsdProblem& p) {
+  if (p.io != SSM_BF16 || p.P != kP || p.N != kN || p.L <= 0) return false;
+  if (p.L % 8 != 0 || p.L > (int64_t)INT32_MAX - kQ || p.B > 65535) return false;
+  const int64_t D = p.H * p.P;
+  // x: (B, D, L) with time stride 1, rows of L, 16-byte aligned; B / C: (B, L, N) dense rows of N
+  auto aligned16 = [](const void* q) { return reinterpret_cast<uintptr_t>(q) % 16 == 0; };
+  if (!aligned16(p.x) || !aligned16(p.Bm) || !aligned16(p.Cm)) return false;
+  if (p.sx[1] != p.L || (p.B > 1 && p.sx[0] != D * p.L)) return false;
+  if (p.sB[2] != 1 || p.sB[1] != kN || (p.B > 1 && p.sB[0] != p.L * kN)) return false;
+  if (p.sC[2] != 1 || p.sC[1] != kN || (p.B > 1 && p.sC[0] != p.L * kN)) return false;
+  return true;
+}
+
+size_t ssd_smem_bytes() { return SsdSmem::kAlloc; }
+
+cudaError_t launch_ssd(const SsdProblem& p, bool tensor_cores, cudaStream_t s) {
+  if (p.B * p.H * p.P == 0) return cudaSuccess;
+  if (!tensor_cores) {
+    if (p.io == SSM_F32) return launch_generic<float, true>(p, s);
+    return launch_generic<__nv_bfloat16, false>(p, s);
+  }
+  SsdMaps tm;
+  std::memset(&tm, 0, sizeof(tm));
+  const int64_t D = p.H * p.P;
+  if (!encode_ssd_map(&tm.x, p.x, (uint64_t)p.L, (uint64_t)D, (uint64_t)p.B, (uint64_t)p.L * 2,
+                      (uint64_t)(D * p.L * 2), 64) ||
+      !encode_ssd_map(&tm.B, p.Bm, kN, (uint64_t)p.L, (uint64_t)p.B, kN * 2, (uint64_t)(p.L * kN * 2), kQ) ||
+      !encode_ssd_map(&tm.C, p.Cm, kN, (uint64_t)p.L, (uint64_t)p.B, kN * 2, (uint64_t)(p.L * kN * 2), kQ))
+    return cudaErrorInvalidValue;
+  static unsigned long long attr_set = 0;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const unsigned long long bit = 1ull << (dev & 63);
+  if (!(__atomic_load_n(&attr_set, __ATOMIC_ACQUIRE) & bit)) {
+    e = cudaFuncSetAttribute(ssd_chunk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SsdSmem::kAlloc);
+    if (e != cudaSuccess) return e;
+    __atomic_fetch_or(&attr_set, bit, __ATOMIC_RELEASE);
+  }
+  ssd_chunk_kernel<<<(unsigned)(p.B * p.H), kSsdThreads, SsdSmem::kAlloc, s>>>(p, tm);
+  return cudaGetLastError();
+}
+
+}  // namespace ssm

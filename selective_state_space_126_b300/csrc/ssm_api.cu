@@ -335,6 +335,7 @@ size_t ssm_abi_sizeof(int which) {
   if (which == 1) return sizeof(ssm_step_args_t);
   if (which == 2) return sizeof(ssm_conv_args_t);
   if (which == 3) return sizeof(ssm_scan_bwd_args_t);
+  if (which == 4) return sizeof(ssm_ssd_args_t);
   return 0;
 }
 
@@ -706,6 +707,128 @@ ssm_status_t ssm_causal_conv1d_fwd(const ssm_conv_args_t* a, void* stream) {
     if (overlaps(o0, o1, i0, i1)) return fail(SSM_ERR_INVALID_ARG, "out overlaps an input");
   }
   cudaError_t e = launch_causal_conv1d(p, device_sm_count(), static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e);
+  return ok();
+}
+
+// ---------------------------------------------------------------------------
+// ssm_ssd_fwd: the Mamba-2 SSD layer
+// ---------------------------------------------------------------------------
+}  // extern "C"
+
+namespace ssm {
+namespace {
+
+ssm_status_t validate_ssd(const ssm_ssd_args_t* a, SsdProblem* p) {
+  if (!a) return fail(SSM_ERR_INVALID_ARG, "args is NULL");
+  if (a->io_dtype != SSM_F32 && a->io_dtype != SSM_BF16) return fail(SSM_ERR_INVALID_ARG, "io_dtype %d", (int)a->io_dtype);
+  if (a->batch < 0 || a->nheads < 0 || a->headdim < 0 || a->seqlen < 0) return fail(SSM_ERR_INVALID_ARG, "negative size");
+  if (a->dstate < 1 || a->dstate > 256) return fail(SSM_ERR_UNSUPPORTED, "dstate %lld outside [1, 256]", (long long)a->dstate);
+  if (a->flags & ~SSM_SSD_FORCE_GENERIC) return fail(SSM_ERR_INVALID_ARG, "flags 0x%x", (unsigned)a->flags);
+  std::memset(p, 0, sizeof(*p));
+  p->B = a->batch; p->H = a->nheads; p->P = a->headdim; p->L = a->seqlen; p->N = a->dstate;
+  p->io = a->io_dtype;
+  p->softplus = a->delta_softplus != 0;
+  p->x = a->x; p->delta = a->delta; p->z = a->z; p->Bm = a->Bm; p->Cm = a->Cm;
+  p->a = a->A; p->Dskip = a->Dskip; p->bias = a->delta_bias; p->h0 = a->h0; p->h_last = a->h_last; p->y = a->y;
+  std::memcpy(p->sx, a->stride_x, sizeof(p->sx));
+  std::memcpy(p->sz, a->stride_z, sizeof(p->sz));
+  std::memcpy(p->sy, a->stride_y, sizeof(p->sy));
+  std::memcpy(p->sd, a->stride_delta, sizeof(p->sd));
+  std::memcpy(p->sB, a->stride_B, sizeof(p->sB));
+  std::memcpy(p->sC, a->stride_C, sizeof(p->sC));
+  std::memcpy(p->sh0, a->stride_h0, sizeof(p->sh0));
+  std::memcpy(p->shl, a->stride_h_last, sizeof(p->shl));
+  if (p->B == 0 || p->H == 0 || p->P == 0) return ok();
+  if (!p->a) return fail(SSM_ERR_INVALID_ARG, "A is NULL");
+  const int es = elem_size(p->io);
+  const int64_t D = p->H * p->P;
+  struct Seq {
+    const char* name;
+    const void* ptr;
+    const int64_t* s;
+    bool required;
+  } seqs[] = {{"x", p->x, p->sx, true}, {"delta", p->delta, p->sd, true}, {"z", p->z, p->sz, false},
+              {"y", p->y, p->sy, true}};
+  for (const Seq& q : seqs) {
+    if (!q.ptr) {
+      if (q.required && p->L > 0) return fail(SSM_ERR_INVALID_ARG, "%s is NULL", q.name);
+      continue;
+    }
+    if (q.s[0] < 0 || q.s[1] < 0) return fail(SSM_ERR_INVALID_ARG, "%s has a negative stride", q.name);
+    if (q.s[2] != 1 && p->L > 1) return fail(SSM_ERR_UNSUPPORTED, "%s time stride must be 1", q.name);
+    if (!aligned(q.ptr, es)) return fail(SSM_ERR_INVALID_ARG, "%s is not %d-byte aligned", q.name, es);
+  }
+  for (const void* q : {p->Bm, p->Cm}) {
+    if (!q && p->L > 0) return fail(SSM_ERR_INVALID_ARG, "Bm or Cm is NULL");
+    if (q && !aligned(q, es)) return fail(SSM_ERR_INVALID_ARG, "Bm or Cm misaligned");
+  }
+  for (int i = 0; i < 3; ++i)
+    if (p->sB[i] < 0 || p->sC[i] < 0) return fail(SSM_ERR_INVALID_ARG, "negative B / C stride");
+  for (int i = 0; i < 4; ++i)
+    if ((p->h0 && p->sh0[i] < 0) || (p->h_last && p->shl[i] < 0)) return fail(SSM_ERR_INVALID_ARG, "negative state stride");
+  for (const float* q : {p->a, p->Dskip, p->bias, p->h0, static_cast<const float*>(p->h_last)})
+    if (q && !aligned(q, 4)) return fail(SSM_ERR_INVALID_ARG, "misaligned fp32 pointer");
+  // outputs one-to-one and disjoint from every input and from each other
+  int64_t ey[3] = {p->B, D, p->L};
+  int64_t sy[3] = {p->sy[0], p->sy[1], 1};
+  int64_t eh[4] = {p->B, p->H, p->P, p->N};
+  if (p->L > 0 && !injective(3, ey, sy)) return fail(SSM_ERR_INVALID_ARG, "y strides overlap");
+  if (p->h_last && !injective(4, eh, p->shl)) return fail(SSM_ERR_INVALID_ARG, "h_last strides overlap");
+  uintptr_t y0 = 0, y1 = 0, hl0 = 0, hl1 = 0;
+  if (p->L > 0) tensor_range(p->y, 3, ey, sy, es, &y0, &y1);
+  if (p->h_last) tensor_range(p->h_last, 4, eh, p->shl, 4, &hl0, &hl1);
+  struct In {
+    const void* ptr;
+    int rank;
+    int64_t ext[4];
+    int64_t str[4];
+    int es;
+  } ins[] = {
+      {p->x, 3, {p->B, D, p->L, 1}, {p->sx[0], p->sx[1], 1, 0}, es},
+      {p->delta, 3, {p->B, p->H, p->L, 1}, {p->sd[0], p->sd[1], 1, 0}, es},
+      {p->z, 3, {p->B, D, p->L, 1}, {p->sz[0], p->sz[1], 1, 0}, es},
+      {p->Bm, 3, {p->B, p->L, p->N, 1}, {p->sB[0], p->sB[1], p->sB[2], 0}, es},
+      {p->Cm, 3, {p->B, p->L, p->N, 1}, {p->sC[0], p->sC[1], p->sC[2], 0}, es},
+      {p->a, 1, {p->H, 1, 1, 1}, {1, 0, 0, 0}, 4},
+      {p->Dskip, 1, {p->H, 1, 1, 1}, {1, 0, 0, 0}, 4},
+      {p->bias, 1, {p->H, 1, 1, 1}, {1, 0, 0, 0}, 4},
+      {p->h0, 4, {p->B, p->H, p->P, p->N}, {p->sh0[0], p->sh0[1], p->sh0[2], p->sh0[3]}, 4},
+  };
+  for (const In& in : ins) {
+    if (!in.ptr) continue;
+    if (in.rank == 3 && p->L == 0 && in.ptr != p->h0) continue;   // empty sequence: nothing is read
+    uintptr_t i0, i1;
+    tensor_range(in.ptr, in.rank, in.ext, in.str, in.es, &i0, &i1);
+    if (p->L > 0 && overlaps(y0, y1, i0, i1)) return fail(SSM_ERR_INVALID_ARG, "y overlaps an input");
+    if (p->h_last && overlaps(hl0, hl1, i0, i1)) return fail(SSM_ERR_INVALID_ARG, "h_last overlaps an input");
+  }
+  if (p->L > 0 && p->h_last && overlaps(y0, y1, hl0, hl1)) return fail(SSM_ERR_INVALID_ARG, "y overlaps h_last");
+  if (p->B * p->H > 2147483647LL) return fail(SSM_ERR_UNSUPPORTED, "too many (batch, head) pairs");
+  return ok();
+}
+
+}  // namespace
+}  // namespace ssm
+
+extern "C" {
+
+int ssm_ssd_plan_path(const ssm_ssd_args_t* args) {
+  SsdProblem p;
+  if (validate_ssd(args, &p) != SSM_OK) return -1;
+  if (p.B == 0 || p.H == 0 || p.P == 0 || p.L == 0) return 0;
+  return (!(args->flags & SSM_SSD_FORCE_GENERIC) && ssd_tensor_core_eligible(p)) ? 1 : 0;
+}
+
+ssm_status_t ssm_ssd_fwd(const ssm_ssd_args_t* args, void* stream) {
+  SsdProblem p;
+  ssm_status_t st = validate_ssd(args, &p);
+  if (st != SSM_OK) return st;
+  if (p.B == 0 || p.H == 0 || p.P == 0) return ok();
+  const bool tc = !(args->flags & SSM_SSD_FORCE_GENERIC) && ssd_tensor_core_eligible(p);
+  if (p.L == 0 && !p.h_last) return ok();
+  p.status = device_status_ptr();
+  cudaError_t e = launch_ssd(p, tc, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e);
   return ok();
 }

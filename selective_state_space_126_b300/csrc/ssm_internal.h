@@ -67,6 +67,19 @@ struct ConvProblem {
   int64_t sx[3], so[3], sw[2], sxh[3];
 };
 
+// Validated Mamba-2 SSD problem, strides in elements.
+struct SsdProblem {
+  int64_t B, H, P, L, N;
+  ssm_dtype_t io;
+  bool softplus;
+  const void *x, *delta, *z, *Bm, *Cm;
+  const float *a, *Dskip, *bias, *h0;
+  float* h_last;
+  void* y;
+  int64_t sx[3], sz[3], sy[3], sd[3], sB[3], sC[3], sh0[4], shl[4];
+  int* status;
+};
+
 enum ScanPath { kPathGeneric = 0, kPathTiled = 1, kPathChunked = 2 };
 
 // Tiled-kernel shape: K threads share one channel's states, NS states per thread.
@@ -93,6 +106,8 @@ cudaError_t launch_scan_tiled(const ScanProblem& p, const ScanPlan& plan, void* 
 cudaError_t launch_state_update(const StepProblem& p, cudaStream_t s);
 cudaError_t launch_causal_conv1d(const ConvProblem& p, int sms, cudaStream_t s);
 cudaError_t launch_scan_bwd(const BwdProblem& p, int sms, cudaStream_t s);
+cudaError_t launch_ssd(const SsdProblem& p, bool tensor_cores, cudaStream_t s);
+bool ssd_tensor_core_eligible(const SsdProblem& p);
 cudaError_t launch_scan_ckpt(const ScanProblem& p, const ScanPlan& plan, float* ckpt, int64_t nseg, cudaStream_t s);
 
 // tile length of the tiled kernel (timesteps)

@@ -169,6 +169,26 @@ def s4d_lin_A(dim: int, dstate: int):
     return np.tile((-0.5 + 1j * np.arange(dstate)).astype(np.complex64), (dim, 1))
 
 
+def ssd_inputs(batch: int, nheads: int, headdim: int, seqlen: int, dstate: int, io_dtype: str = "bf16",
+               seed: int = 0, dt_min: float = 1e-3, dt_max: float = 1e-1) -> dict:
+    """Inputs of the Mamba-2 SSD layer as float32 arrays (values exact in the I/O dtype).
+
+    x, z (B, H*P, L), delta (B, H, L), Bm, Cm (B, L, N) ~ N(0, 1); per head A = -U(1, 16) (the
+    scalar times the identity), Dskip ~ N(0, 1), delta_bias = softplus^-1(Delta0) with Delta0
+    log-uniform in [dt_min, dt_max]."""
+    rng = np.random.default_rng([seed, 7001])
+    r = lambda *shape: round_io(rng.standard_normal(shape, dtype=np.float32), io_dtype)
+    D = nheads * headdim
+    x, z = r(batch, D, seqlen), r(batch, D, seqlen)
+    delta = r(batch, nheads, seqlen)
+    Bm, Cm = r(batch, seqlen, dstate), r(batch, seqlen, dstate)
+    A = (-rng.uniform(1.0, 16.0, nheads)).astype(np.float32)
+    Dskip = rng.standard_normal(nheads, dtype=np.float32)
+    dt0 = np.exp(rng.uniform(np.log(dt_min), np.log(dt_max), nheads))
+    bias = softplus_inverse(dt0).astype(np.float32)
+    return dict(x=x, delta=delta, z=z, Bm=Bm, Cm=Cm, A=A, Dskip=Dskip, delta_bias=bias)
+
+
 def conv_params(dim: int, width: int, seed: int = 0):
     """Conv taps (D, W) and bias (D,) as float32, uniform in +-1/sqrt(W)."""
     bound = 1.0 / np.sqrt(width)

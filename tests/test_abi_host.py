@@ -351,3 +351,54 @@ def test_complex_validation(lib):
     # the backward pass and the no-allocation entry point take a real A
     assert lib.ssm_scan_fwd_noalloc(ctypes.byref(scan_args(L=4096, A_imag=FAKE["ws"])), None) == \
         ssm.SSM_ERR_UNSUPPORTED
+
+
+def ssd_args(B=2, H=3, P=64, L=256, N=128, io=ssm.SSM_BF16, **over):
+    a = ssm.SsdArgs()
+    a.batch, a.nheads, a.headdim, a.seqlen, a.dstate = B, H, P, L, N
+    a.io_dtype = io
+    a.delta_softplus = 1
+    a.x, a.delta, a.z, a.Bm, a.Cm = FAKE["u"], FAKE["delta"], FAKE["z"], FAKE["Bm"], FAKE["Cm"]
+    a.A, a.Dskip, a.delta_bias, a.y = FAKE["A"], FAKE["Dskip"], FAKE["bias"], FAKE["y"]
+    D = H * P
+    for f in ("stride_x", "stride_z", "stride_y"):
+        getattr(a, f)[:] = [D * L, L, 1]
+    a.stride_delta[:] = [H * L, L, 1]
+    a.stride_B[:] = [L * N, N, 1]
+    a.stride_C[:] = [L * N, N, 1]
+    for k, v in over.items():
+        if isinstance(v, list):
+            getattr(a, k)[:] = v
+        else:
+            setattr(a, k, v)
+    return a
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(x=None), ssm.SSM_ERR_INVALID_ARG),
+    (dict(A=None), ssm.SSM_ERR_INVALID_ARG),
+    (dict(Bm=None), ssm.SSM_ERR_INVALID_ARG),
+    (dict(dstate=0), ssm.SSM_ERR_UNSUPPORTED),
+    (dict(dstate=257), ssm.SSM_ERR_UNSUPPORTED),
+    (dict(io_dtype=5), ssm.SSM_ERR_INVALID_ARG),
+    (dict(seqlen=-1), ssm.SSM_ERR_INVALID_ARG),
+    (dict(flags=2), ssm.SSM_ERR_INVALID_ARG),
+    (dict(stride_x=[3 * 64 * 256, 256, 2]), ssm.SSM_ERR_UNSUPPORTED),
+    (dict(stride_y=[0, 256, 1]), ssm.SSM_ERR_INVALID_ARG),            # two batch rows on one output row
+    (dict(y=FAKE["u"] + 1024), ssm.SSM_ERR_INVALID_ARG),               # y overlaps x
+    (dict(h_last=FAKE["A"], stride_h_last=[3 * 64 * 128, 64 * 128, 128, 1]), ssm.SSM_ERR_INVALID_ARG),
+    (dict(x=FAKE["u"] + 1), ssm.SSM_ERR_INVALID_ARG),                  # misaligned
+])
+def test_ssd_validation(lib, over, code):
+    assert lib.ssm_ssd_fwd(ctypes.byref(ssd_args(**over)), None) == code
+
+
+def test_ssd_plan(lib):
+    assert ssm.ssm_ssd_plan_path(ssd_args()) == "tensor_core"
+    assert ssm.ssm_ssd_plan_path(ssd_args(flags=ssm.SSM_SSD_FORCE_GENERIC)) == "generic"
+    assert ssm.ssm_ssd_plan_path(ssd_args(P=32)) == "generic"                  # headdim other than 64
+    assert ssm.ssm_ssd_plan_path(ssd_args(N=64, stride_B=[256 * 64, 64, 1], stride_C=[256 * 64, 64, 1])) == "generic"
+    assert ssm.ssm_ssd_plan_path(ssd_args(io=ssm.SSM_F32)) == "generic"
+    assert ssm.ssm_ssd_plan_path(ssd_args(L=252)) == "generic"                 # rows not 16-byte aligned
+    assert ssm.ssm_ssd_plan_path(ssd_args(stride_B=[128 * 256, 1, 256])) == "generic"   # state not contiguous
+    assert lib.ssm_ssd_fwd(ctypes.byref(ssd_args(B=0)), None) == ssm.SSM_OK
