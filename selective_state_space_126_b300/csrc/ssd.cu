@@ -23,13 +23,16 @@
 // mask, the scalings, the state recurrence across chunks (fp32, in registers)
 // and the output (D skip, gate) run on the CUDA cores.
 //
-// ssd_chunk_kernel: one CTA of 128 threads per (batch, head) walks its chunks
-// in order, for P = 64 and N = 128 with bf16 I/O.  Thread i owns time row i of
-// the chunk (tensor-memory lane i of G, Y_diag, Y_off) and state row i (lane i
-// of H_chunk, and the fp32 state H[i][0..63] in registers).  Per chunk:
+// ssd_chunk_kernel: one CTA of 256 threads per (batch, head) walks its chunks
+// in order, for P = 64 and N = 128 with bf16 I/O.  Threads i and i + 128 own
+// time row i of the chunk (tensor-memory lane i of G, Y_diag, Y_off; each one
+// half of the columns) and state row i (lane i of H_chunk, and half each of
+// the fp32 state H[i][0..63] in registers).  Per chunk:
 //   1. TMA: C_c and B_c ((L, N) rows of 128 B, 128B swizzle, two 64-column
 //      boxes each) and X_c ((P, L) rows, two 64-step boxes) -- each already
-//      the K-major operand layout of the MMAs below;
+//      the K-major operand layout of the MMAs below -- and the gate's z_c.
+//      B_c has its own barrier and the next chunk's B is loaded as soon as
+//      this one's is consumed (after step 4);
 //   2. Delta, the inclusive prefix sum S (warp shuffles and one shared step),
 //      the weights w_s = exp(a (S_end - S_s)) Delta_s; threads write
 //      X_Delta = Delta_s X (K = s), B~^T = w_s B^T (transposed, K = s) and the
@@ -56,7 +59,7 @@ namespace {
 constexpr int kQ = 128;          // chunk length
 constexpr int kP = 64;           // head dimension of the tensor-core kernel
 constexpr int kN = 128;          // state size of the tensor-core kernel
-constexpr int kSsdThreads = 128;
+constexpr int kSsdThreads = 256;
 
 struct SsdSmem {
   static constexpr int kC = 0;                 // C chunk: 2 x [128 t][64 n] bf16, swizzled
@@ -66,12 +69,13 @@ struct SsdSmem {
   static constexpr int kXD = kSP + 32768;      // Delta X: 2 x [64 p][64 s]
   static constexpr int kBT = kXD + 16384;      // weighted B^T: 2 x [128 n][64 s]
   static constexpr int kSI = kBT + 32768;      // incoming state H_in^T: 2 x [64 p][64 n]
-  static constexpr int kDelta = kSI + 16384;   // float [128]
+  static constexpr int kZ = kSI + 16384;       // z chunk: 2 x [64 p][64 t] (the gate)
+  static constexpr int kDelta = kZ + 16384;    // float [128]
   static constexpr int kCum = kDelta + 512;    // float [128]
   static constexpr int kW = kCum + 512;        // float [128]
   static constexpr int kWarp = kW + 512;       // float [4] warp totals of the prefix sum
-  static constexpr int kBar = kWarp + 16;      // 4 mbarriers: TMA, G, (H_chunk, Y_off), Y_diag
-  static constexpr int kTaddr = kBar + 32;
+  static constexpr int kBar = kWarp + 16;      // 5 mbarriers: TMA (C, X, z), TMA (B), G, (H_chunk, Y_off), Y_diag
+  static constexpr int kTaddr = kBar + 40;
   static constexpr int kBytes = kTaddr + 16;
   static constexpr int kAlloc = kBytes + 1024;
 };
@@ -81,7 +85,7 @@ constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColG = 0, kColYd = 128, kColYo = 192, kColH = 256;
 
 struct SsdMaps {
-  CUtensorMap x, B, C;
+  CUtensorMap x, z, B, C;
 };
 
 __global__ void __launch_bounds__(kSsdThreads, 1)
@@ -93,11 +97,14 @@ __global__ void __launch_bounds__(kSsdThreads, 1)
   float* sCum = reinterpret_cast<float*>(smem + S::kCum);
   float* sW = reinterpret_cast<float*>(smem + S::kW);
   float* sWarp = reinterpret_cast<float*>(smem + S::kWarp);
-  const uint32_t bar_tma = smem_u32(smem + S::kBar), bar_g = bar_tma + 8, bar_ho = bar_tma + 16,
-                 bar_d = bar_tma + 24;
+  const uint32_t bar_tma = smem_u32(smem + S::kBar), bar_tmab = bar_tma + 8, bar_g = bar_tma + 16,
+                 bar_ho = bar_tma + 24, bar_d = bar_tma + 32;
   uint32_t* taddr_s = reinterpret_cast<uint32_t*>(smem + S::kTaddr);
 
+  // thread = (row r, half hf): row r is time step r of the chunk and state index r; the half picks
+  // columns [64 hf, 64 hf + 64) of the score row and head channels [32 hf, 32 hf + 32)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int r = tid & (kQ - 1), hf = tid >> 7;
   const int64_t bh = blockIdx.x;
   const int64_t b = bh / p.H, h = bh % p.H;
   const int nchunks = (int)((p.L + kQ - 1) / kQ);
@@ -106,7 +113,7 @@ __global__ void __launch_bounds__(kSsdThreads, 1)
   const float Dh = p.Dskip ? p.Dskip[h] : 0.f;
 
   if (tid == 0) {
-    for (int i = 0; i < 4; ++i) mbar_init(bar_tma + 8 * i, 1);
+    for (int i = 0; i < 5; ++i) mbar_init(bar_tma + 8 * i, 1);
     mbar_init_fence();
   }
   if (warp == 0) tmem_alloc(smem_u32(taddr_s), kTmemCols);
@@ -114,103 +121,124 @@ __global__ void __launch_bounds__(kSsdThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *taddr_s;
-  const uint32_t lane_off = (uint32_t)(32 * warp) << 16;
+  const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;   // this warp's 32 tensor-memory lanes: rows r
 
-  // state H[tid][0..63] (state row n = tid, head channels p), fp32 in registers
-  float H[kP];
+  // state H[r][32 hf .. 32 hf + 31] (state row n = r, head channels p), fp32 in registers
+  constexpr int kHalfP = kP / 2;
+  float H[kHalfP];
 #pragma unroll
-  for (int q = 0; q < kP; ++q)
-    H[q] = p.h0 ? p.h0[b * p.sh0[0] + h * p.sh0[1] + q * p.sh0[2] + tid * p.sh0[3]] : 0.f;
+  for (int j = 0; j < kHalfP; ++j)
+    H[j] = p.h0 ? p.h0[b * p.sh0[0] + h * p.sh0[1] + (kHalfP * hf + j) * p.sh0[2] + r * p.sh0[3]] : 0.f;
 
-  auto issue = [&](int c) {
+  // thread 0 tracks the copies and MMAs in flight (chunk index, or -1) for a bounded drain on failure
+  int cxz_pend = -1, b_pend = -1;
+  bool mma_out = false, mma_d_out = false;
+  auto issue_cxz = [&](int c) {   // C, X and z of chunk c
     const int t0 = c * kQ;
-    mbar_expect_tx(bar_tma, 2 * 16384 + 2 * 16384 + 2 * 8192);
+    mbar_expect_tx(bar_tma, 2 * 16384 + 2 * 8192 + (p.z ? 2 * 8192 : 0));
     for (int j = 0; j < 2; ++j) {
       tma_load(smem_u32(smem + S::kC + j * 16384), &tm.C, 64 * j, t0, (int)b, true, bar_tma);
-      tma_load(smem_u32(smem + S::kB + j * 16384), &tm.B, 64 * j, t0, (int)b, true, bar_tma);
       tma_load(smem_u32(smem + S::kX + j * 8192), &tm.x, t0 + 64 * j, (int)(h * kP), (int)b, true, bar_tma);
+      if (p.z) tma_load(smem_u32(smem + S::kZ + j * 8192), &tm.z, t0 + 64 * j, (int)(h * kP), (int)b, true, bar_tma);
     }
+    cxz_pend = c;
   };
-  if (tid == 0 && nchunks > 0) issue(0);
+  auto issue_b = [&](int c) {     // B of chunk c (its buffer frees up earlier than the others)
+    mbar_expect_tx(bar_tmab, 2 * 16384);
+    for (int j = 0; j < 2; ++j)
+      tma_load(smem_u32(smem + S::kB + j * 16384), &tm.B, 64 * j, c * kQ, (int)b, true, bar_tmab);
+    b_pend = c;
+  };
+  if (tid == 0 && nchunks > 0) {
+    issue_b(0);
+    issue_cxz(0);
+  }
 
   const uint32_t id128 = umma_idesc_bf16(128, 128), id64 = umma_idesc_bf16(128, 64);
+  // raw delta of step t (this row's step of a chunk), loaded one chunk ahead
+  auto load_delta = [&](int64_t t) -> float {
+    if (hf != 0 || t >= p.L) return 0.f;
+    const int64_t o = b * p.sd[0] + h * p.sd[1] + t;
+    return p.io == SSM_BF16 ? __bfloat162float(__ldg(static_cast<const __nv_bfloat16*>(p.delta) + o))
+                            : __ldg(static_cast<const float*>(p.delta) + o);
+  };
+  float dnext = nchunks > 0 ? load_delta(r) : 0.f;
   bool failed = false;
-  bool mma_out = false, mma_d_out = false;   // thread 0: MMAs of the current chunk issued and not yet waited for
   int c = 0;
   for (; c < nchunks; ++c) {
     const uint32_t par = (uint32_t)c & 1u;
     const int64_t t0 = (int64_t)c * kQ;
     const int valid = (int)(p.L - t0 < kQ ? p.L - t0 : kQ);   // steps of this chunk inside the sequence
 
-    // ---- 2. Delta, prefix sum S, weights ----
+    // ---- 2. Delta, prefix sum S (rows, half 0), weights; the incoming state as an operand ----
     float dt = 0.f;
-    if (tid < valid) {
-      const float dv = p.io == SSM_BF16
-                           ? __bfloat162float(static_cast<const __nv_bfloat16*>(p.delta)[b * p.sd[0] + h * p.sd[1] + t0 + tid])
-                           : static_cast<const float*>(p.delta)[b * p.sd[0] + h * p.sd[1] + t0 + tid];
-      dt = delta_of<false>(dv, bias, p.softplus);
-    }
+    if (hf == 0 && r < valid) dt = delta_of<false>(dnext, bias, p.softplus);
+    dnext = load_delta(t0 + kQ + r);   // the next chunk's, in flight during this one
     float cum = dt;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       const float v = __shfl_up_sync(0xffffffffu, cum, o);
       if (lane >= o) cum += v;
     }
-    if (lane == 31) sWarp[warp] = cum;
-    // the incoming state as the bf16 operand H_in^T: row p, K = n (this thread's n = tid)
+    if (hf == 0 && lane == 31) sWarp[warp] = cum;
+    // H_in^T as the bf16 operand: row p, K = n (this thread's n = r, its 32 head channels)
 #pragma unroll
-    for (int q = 0; q < kP; ++q)
-      *reinterpret_cast<__nv_bfloat16*>(smem + S::kSI + (tid >> 6) * 8192 + sw128_offset(q, tid & 63)) =
-          __float2bfloat16_rn(H[q]);
+    for (int j = 0; j < kHalfP; ++j)
+      *reinterpret_cast<__nv_bfloat16*>(smem + S::kSI + (r >> 6) * 8192 + sw128_offset(kHalfP * hf + j, r & 63)) =
+          __float2bfloat16_rn(H[j]);
     __syncthreads();
-    for (int w = 0; w < warp; ++w) cum += sWarp[w];
-    sDelta[tid] = dt;
-    sCum[tid] = cum;
+    if (hf == 0) {
+      for (int w = 0; w < warp; ++w) cum += sWarp[w];
+      sDelta[r] = dt;
+      sCum[r] = cum;
+    }
     __syncthreads();
+    cum = sCum[r];
     const float cum_end = sCum[kQ - 1];
-    sW[tid] = ex2_approx(a2 * (cum_end - cum)) * dt;
-    const float et = ex2_approx(a2 * cum);   // exp(a S_t)
+    if (hf == 0) sW[r] = ex2_approx(a2 * (cum_end - cum)) * sDelta[r];
+    const float et = ex2_approx(a2 * cum);   // exp(a S_t) of row t = r
 
-    // ---- 1. the chunk's tiles ----
-    const bool ok_tma = mbar_wait(bar_tma, par);
-    if (!ok_tma) record_status(p.status, SSM_ERR_TIMEOUT);
+    // ---- 1. B of this chunk; B~^T[n][s] = w_s B[s][n] (thread: n = r, steps [64 hf, 64 hf + 64)) ----
+    const bool ok_b = mbar_wait(bar_tmab, par);
+    if (!ok_b) record_status(p.status, SSM_ERR_TIMEOUT);
+    if (tid == 0 && ok_b) b_pend = -1;
     __syncthreads();   // sW visible
-    if (ok_tma) {
-      // X_Delta[p][s] = Delta_s X[p][s]: thread -> (row p = tid % 64, 64-step block tid / 64)
-      {
-        const int pr = tid & 63, blk = tid >> 6;
-        const unsigned char* src = smem + S::kX + blk * 8192 + pr * 128;
-        unsigned char* dst = smem + S::kXD + blk * 8192 + pr * 128;
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const int pos = (j ^ (pr & 7)) << 4;   // logical piece j holds s = 64 blk + 8 j .. + 7
-          float f[8];
-          unpack16(*reinterpret_cast<const uint4*>(src + pos), f);
-#pragma unroll
-          for (int e = 0; e < 8; ++e) f[e] *= sDelta[64 * blk + 8 * j + e];
-          *reinterpret_cast<uint4*>(dst + pos) = pack16(f);
-        }
-      }
-      // B~^T[n][s] = w_s B[s][n]: thread n = tid gathers column n of B
-      {
-        const int n = tid;
-        const unsigned char* src = smem + S::kB + (n >> 6) * 16384;
+    if (ok_b) {
+      const int n = r;
+      const unsigned char* src = smem + S::kB + (n >> 6) * 16384;
 #pragma unroll 2
-        for (int j = 0; j < 16; ++j) {   // 8 steps s = 8 j .. 8 j + 7 per 16-byte piece of row n
-          float f[8];
+      for (int jj = 0; jj < 8; ++jj) {   // piece jj of step block hf: steps s = 64 hf + 8 jj .. + 7
+        float f[8];
 #pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            const int s = 8 * j + e;
-            f[e] = __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(src + sw128_offset(s, n & 63))) * sW[s];
-          }
-          const int sblk = j >> 3, jj = j & 7;
-          *reinterpret_cast<uint4*>(smem + S::kBT + sblk * 16384 + n * 128 + ((jj ^ (n & 7)) << 4)) = pack16(f);
+        for (int e = 0; e < 8; ++e) {
+          const int sl = 8 * jj + e, sg = 64 * hf + sl;
+          f[e] = __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(src + sw128_offset(sg, n & 63))) * sW[sg];
         }
+        *reinterpret_cast<uint4*>(smem + S::kBT + hf * 16384 + n * 128 + ((jj ^ (n & 7)) << 4)) = pack16(f);
+      }
+    }
+    // ---- C, X, z; X_Delta[p][s] = Delta_s X[p][s] (thread: row p, step block, 4 of the 8 pieces) ----
+    const bool ok_t = ok_b && mbar_wait(bar_tma, par);
+    if (!ok_t) record_status(p.status, SSM_ERR_TIMEOUT);
+    if (tid == 0 && ok_t) cxz_pend = -1;
+    if (ok_t) {
+      const int pr = tid & 63, blk = (tid >> 6) & 1, ph = tid >> 7;
+      const unsigned char* src = smem + S::kX + blk * 8192 + pr * 128;
+      unsigned char* dst = smem + S::kXD + blk * 8192 + pr * 128;
+#pragma unroll
+      for (int jj = 0; jj < 4; ++jj) {
+        const int j = 4 * ph + jj;
+        const int pos = (j ^ (pr & 7)) << 4;   // logical piece j holds s = 64 blk + 8 j .. + 7
+        float f[8];
+        unpack16(*reinterpret_cast<const uint4*>(src + pos), f);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) f[e] *= sDelta[64 * blk + 8 * j + e];
+        *reinterpret_cast<uint4*>(dst + pos) = pack16(f);
       }
     }
     fence_async_smem();
     tc_fence_before();
-    if (__syncthreads_or(!ok_tma)) { failed = true; break; }
+    if (__syncthreads_or(!ok_t)) { failed = true; break; }
 
     // ---- 3. G = C B^T, H_chunk = B~^T X, Y_off = C H_in ----
     if (tid == 0) {
@@ -234,13 +262,15 @@ __global__ void __launch_bounds__(kSsdThreads, 1)
       mma_out = true;
     }
 
-    // ---- 4. causal decay mask on G -> bf16 scores, row t = tid, K = s ----
+    // ---- 4. causal decay mask on G -> bf16 scores (thread: row t = r, steps [64 hf, 64 hf + 64)) ----
     const bool ok_g = mbar_wait(bar_g, par);
     if (!ok_g) record_status(p.status, SSM_ERR_TIMEOUT);
     tc_fence_after();
     if (__syncthreads_or(!ok_g)) { failed = true; break; }
+    // B is consumed (B~^T built, G complete): the next chunk's B can land while this one finishes
+    if (tid == 0 && c + 1 < nchunks) issue_b(c + 1);
 #pragma unroll 1
-    for (int s0 = 0; s0 < kQ; s0 += 32) {
+    for (int s0 = 64 * hf; s0 < 64 * hf + 64; s0 += 32) {
       float g[32];
       tmem_ld32(tmem + lane_off + kColG + (uint32_t)s0, g);
 #pragma unroll
@@ -249,10 +279,10 @@ __global__ void __launch_bounds__(kSsdThreads, 1)
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
           const int s = s0 + j + e;
-          f[e] = s <= tid ? g[j + e] * ex2_approx(a2 * (cum - sCum[s])) : 0.f;
+          f[e] = s <= r ? g[j + e] * ex2_approx(a2 * (cum - sCum[s])) : 0.f;
         }
         const int sblk = (s0 + j) >> 6, piece = ((s0 + j) & 63) >> 3;
-        *reinterpret_cast<uint4*>(smem + S::kSP + sblk * 16384 + tid * 128 + ((piece ^ (tid & 7)) << 4)) = pack16(f);
+        *reinterpret_cast<uint4*>(smem + S::kSP + sblk * 16384 + r * 128 + ((piece ^ (r & 7)) << 4)) = pack16(f);
       }
     }
     fence_async_smem();
@@ -271,57 +301,50 @@ __global__ void __launch_bounds__(kSsdThreads, 1)
       mma_d_out = true;
     }
 
-    // ---- 6. state update, then the output ----
+    // ---- 6. state update (thread: n = r, channels [32 hf, +32)), then the output (t = r, same channels) ----
     const bool ok_ho = mbar_wait(bar_ho, par);
     if (!ok_ho) record_status(p.status, SSM_ERR_TIMEOUT);
     tc_fence_after();
     if (ok_ho) {
       const float decay = ex2_approx(a2 * cum_end);
+      float hc[32];
+      tmem_ld32(tmem + lane_off + kColH + (uint32_t)(kHalfP * hf), hc);
 #pragma unroll
-      for (int q0 = 0; q0 < kP; q0 += 32) {
-        float hc[32];
-        tmem_ld32(tmem + lane_off + kColH + (uint32_t)q0, hc);
-#pragma unroll
-        for (int j = 0; j < 32; ++j) H[q0 + j] = fmaf(decay, H[q0 + j], hc[j]);
-      }
+      for (int j = 0; j < kHalfP; ++j) H[j] = fmaf(decay, H[j], hc[j]);
     }
     const bool ok_d = mbar_wait(bar_d, par);
     if (!ok_d) record_status(p.status, SSM_ERR_TIMEOUT);
     tc_fence_after();
     if (ok_ho && ok_d) {
-      const int64_t t = t0 + tid;
-      for (int q0 = 0; q0 < kP; q0 += 32) {
-        float yd[32], yo[32];
-        tmem_ld32(tmem + lane_off + kColYd + (uint32_t)q0, yd);
-        tmem_ld32(tmem + lane_off + kColYo + (uint32_t)q0, yo);
-        if (tid < valid) {
+      const int64_t t = t0 + r;
+      float yd[32], yo[32];
+      tmem_ld32(tmem + lane_off + kColYd + (uint32_t)(kHalfP * hf), yd);
+      tmem_ld32(tmem + lane_off + kColYo + (uint32_t)(kHalfP * hf), yo);
+      if (r < valid) {
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            const int q = q0 + j;
-            const int64_t d = h * kP + q;
-            const float xv = __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(
-                smem + S::kX + (tid >> 6) * 8192 + sw128_offset(q, tid & 63)));
-            float v = fmaf(et, yo[j], yd[j]) + Dh * xv;
-            if (p.z) {
-              const float zv = __bfloat162float(static_cast<const __nv_bfloat16*>(p.z)[b * p.sz[0] + d * p.sz[1] + t]);
-              v *= silu<false>(zv);
-            }
-            static_cast<__nv_bfloat16*>(p.y)[b * p.sy[0] + d * p.sy[1] + t] = __float2bfloat16_rn(v);
-          }
+        for (int j = 0; j < kHalfP; ++j) {
+          const int q = kHalfP * hf + j;
+          const int64_t d = h * kP + q;
+          const int zx = (r >> 6) * 8192 + sw128_offset(q, r & 63);
+          const float xv = __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(smem + S::kX + zx));
+          float v = fmaf(et, yo[j], yd[j]) + Dh * xv;
+          if (p.z) v *= silu<false>(__bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(smem + S::kZ + zx)));
+          static_cast<__nv_bfloat16*>(p.y)[b * p.sy[0] + d * p.sy[1] + t] = __float2bfloat16_rn(v);
         }
       }
     }
     tc_fence_before();
     if (__syncthreads_or(!(ok_ho && ok_d))) { failed = true; break; }
     mma_out = mma_d_out = false;
-    if (tid == 0 && c + 1 < nchunks) issue(c + 1);
+    if (tid == 0 && c + 1 < nchunks) issue_cxz(c + 1);
   }
 
   if (failed) {
     // let every copy and MMA this CTA started finish (bounded waits) before its tensor memory is freed
     if (tid == 0) {
+      if (b_pend >= 0) mbar_wait(bar_tmab, (uint32_t)b_pend & 1u);
+      if (cxz_pend >= 0) mbar_wait(bar_tma, (uint32_t)cxz_pend & 1u);
       const uint32_t par = (uint32_t)c & 1u;
-      mbar_wait(bar_tma, par);          // this chunk's tiles were issued before the loop body started
       if (mma_out) {
         mbar_wait(bar_g, par);
         mbar_wait(bar_ho, par);
@@ -330,7 +353,8 @@ __global__ void __launch_bounds__(kSsdThreads, 1)
     }
   } else if (p.h_last) {
 #pragma unroll
-    for (int q = 0; q < kP; ++q) p.h_last[b * p.shl[0] + h * p.shl[1] + q * p.shl[2] + tid * p.shl[3]] = H[q];
+    for (int j = 0; j < kHalfP; ++j)
+      p.h_last[b * p.shl[0] + h * p.shl[1] + (kHalfP * hf + j) * p.shl[2] + r * p.shl[3]] = H[j];
   }
   tc_fence_before();
   __syncthreads();
@@ -430,6 +454,7 @@ bool ssd_tensor_core_eligible(const SsdProblem& p) {
   auto aligned16 = [](const void* q) { return reinterpret_cast<uintptr_t>(q) % 16 == 0; };
   if (!aligned16(p.x) || !aligned16(p.Bm) || !aligned16(p.Cm)) return false;
   if (p.sx[1] != p.L || (p.B > 1 && p.sx[0] != D * p.L)) return false;
+  if (p.z && (!aligned16(p.z) || p.sz[1] != p.L || (p.B > 1 && p.sz[0] != D * p.L))) return false;
   if (p.sB[2] != 1 || p.sB[1] != kN || (p.B > 1 && p.sB[0] != p.L * kN)) return false;
   if (p.sC[2] != 1 || p.sC[1] != kN || (p.B > 1 && p.sC[0] != p.L * kN)) return false;
   return true;
@@ -448,6 +473,8 @@ cudaError_t launch_ssd(const SsdProblem& p, bool tensor_cores, cudaStream_t s) {
   const int64_t D = p.H * p.P;
   if (!encode_ssd_map(&tm.x, p.x, (uint64_t)p.L, (uint64_t)D, (uint64_t)p.B, (uint64_t)p.L * 2,
                       (uint64_t)(D * p.L * 2), 64) ||
+      (p.z && !encode_ssd_map(&tm.z, p.z, (uint64_t)p.L, (uint64_t)D, (uint64_t)p.B, (uint64_t)p.L * 2,
+                              (uint64_t)(D * p.L * 2), 64)) ||
       !encode_ssd_map(&tm.B, p.Bm, kN, (uint64_t)p.L, (uint64_t)p.B, kN * 2, (uint64_t)(p.L * kN * 2), kQ) ||
       !encode_ssd_map(&tm.C, p.Cm, kN, (uint64_t)p.L, (uint64_t)p.B, kN * 2, (uint64_t)(p.L * kN * 2), kQ))
     return cudaErrorInvalidValue;
