@@ -58,7 +58,7 @@ def parse():
     ap.add_argument("--only-rows", action="store_true",
                     help="time only the other workloads' rows (one line of JSON; for profiling their kernels)")
     ap.add_argument("--rows", default="all",
-                    help="comma-separated subset of rows: m130, ti, long, decode, conv, bwd, zoh, cplx")
+                    help="comma-separated subset of rows: m130, ti, long, decode, conv, bwd, zoh, cplx, ssd")
     ap.add_argument("--decode-steps", type=int, default=1000, help="decode steps of the decode row")
     return ap.parse_args()
 
@@ -345,6 +345,7 @@ ROW_KEYS = {"cplx": "mamba2.8b_s4dlin_complex_bf16_b4_d5120_l2048_n16",
             "m130": "mamba130m_bf16_b8_d1536_l2048_n16", "ti": "mamba2.8b_ti_bf16_b1_d5120_l2048_n16",
             "long": "long_bf16_b1_d1536_l1048576_n16", "decode": "decode_bf16_b256_d5120_n16_x1000",
             "conv": "conv1d_silu_bf16_b4_d5120_l2048_w4", "bwd": "scan_bwd_mamba2.8b_bf16_b4_d5120_l2048_n16",
+            "ssd": "ssd_mamba2_2.7b_bf16_b4_h80_p64_l2048_n128",
             "zoh": "mamba2.8b_zoh_bf16_b4_d5120_l2048_n16"}
 
 
@@ -469,6 +470,41 @@ def other_rows(lib, ssm, peak, stream, dev, which="all", decode_steps=1000):
                       "hbm_gbs_algorithmic": gbs, "frac": gbs / peak, "algorithmic_bytes": byt,
                       "workspace_bytes": need.value, "l2": "inputs larger than L2"}
         del inp, dy, grads, bws
+        torch.cuda.empty_cache()
+
+    if "ssd" in sel:
+        # the Mamba-2 SSD layer (scalar A per head): 4 x 80 heads x 64 channels, L = 2048, N = 128, bf16
+        name = ROW_KEYS["ssd"]
+        Bsz, H, P, L, N = 4, 80, 64, 2048, 128
+        g = torch.Generator(device=dev)
+        g.manual_seed(5000)
+        rnd = lambda *shape: torch.randn(*shape, generator=g, device=dev).to(torch.bfloat16)
+        x, z, dl = rnd(Bsz, H * P, L), rnd(Bsz, H * P, L), rnd(Bsz, H, L)
+        Bm, Cm = rnd(Bsz, L, N), rnd(Bsz, L, N)
+        small = syn.ssd_inputs(1, H, 1, 8, N, "bf16", seed=5000)     # per-head A, Dskip, delta_bias
+        Ah, Dh, bh = (torch.from_numpy(small[k]).to(dev) for k in ("A", "Dskip", "delta_bias"))
+        ys = torch.empty_like(x)
+        sa = ssm.make_ssd_args(x, dl, Ah, Bm, Cm, ys, Dh, z, bh)
+        path = ssm.ssm_ssd_plan_path(sa)
+
+        def srun():
+            rc = lib.ssm_ssd_fwd(ctypes.byref(sa), sh)
+            if rc != 0:
+                raise RuntimeError(ssm.status_name(rc) + " " + lib.ssm_last_error_detail().decode())
+
+        for _ in range(3):
+            srun()
+        ms = time_launches(srun, 50, stream, None)
+        es = 2
+        byt = (3 * Bsz * H * P * L + Bsz * H * L + 2 * Bsz * L * N) * es + 3 * H * 4
+        chunks = (L + 127) // 128
+        flops = Bsz * H * chunks * 2 * (128 * 128 * N + 3 * 128 * P * 128)   # C B^T, state, inter- and intra-chunk
+        gbs = byt / (ms * 1e-3) / 1e9
+        tfl = flops / (ms * 1e-3) / 1e12
+        rows[name] = {"ms": ms, "value": Bsz * H * P * N * L / (ms * 1e-3), "unit": UNIT, "path": path,
+                      "launches": 1, "hbm_gbs_algorithmic": gbs, "frac": gbs / peak, "algorithmic_bytes": byt,
+                      "tensor_tflops": tfl, "tensor_flops_per_launch": flops, "l2": "inputs larger than L2"}
+        del x, z, dl, Bm, Cm, ys
         torch.cuda.empty_cache()
 
     if "decode" not in sel:

@@ -273,7 +273,10 @@ __global__ void __launch_bounds__(128) state_update_bulk_kernel(const StepProble
 
 // Wide fast path for N = 16: one thread per channel with all 16 states, 128
 // channels per CTA, so that a batch row is one 8 KB state copy plus three
-// 256-byte copies of u, delta, z and two 32-byte copies of B, C.  Thread c
+// 256-byte copies of u, delta, z and two 32-byte copies of B, C.  The new
+// state is written back into the slot and leaves, with the row of y, as two
+// bulk stores (8 KB and 256 bytes), so that HBM sees whole contiguous rows in
+// both directions.  Thread c
 // visits its four 16-byte state pieces in an order rotated by (c / 2) % 4,
 // which spreads a quarter-warp's shared-memory reads over all bank groups; A,
 // B and C are read in the same rotated order, so no piece is ever moved back.
@@ -359,12 +362,16 @@ __global__ void __launch_bounds__(128) state_update_wide_kernel(const StepProble
         const int issued = k >= 1 ? k - 1 + kWideSlots : kWideSlots;   // rows [0, issued) went out
         for (int j = k; j < issued && j < rows; ++j)
           (void)mbar_wait(bar0 + 8 * (j % kWideSlots), (uint32_t)(j / kWideSlots) & 1u);
+        bulk_wait<0>();
       }
       return;
     }
-    // every thread is done with row k-1: its slot takes row k-1+kWideSlots
-    if (c == 0 && k >= 1 && k - 1 + kWideSlots < rows) issue(k - 1 + kWideSlots);
-    const unsigned char* sl = slots[s];
+    // every thread is done with row k-1 and its store has read the slot: the slot takes row k-1+kWideSlots
+    if (c == 0 && k >= 1 && k - 1 + kWideSlots < rows) {
+      bulk_wait_read<0>();
+      issue(k - 1 + kWideSlots);
+    }
+    unsigned char* sl = slots[s];
     const int64_t b = g + (int64_t)k * row_groups;
     const float uv = to_f32(reinterpret_cast<const IO*>(sl + W::kU)[c]);
     const float dv = to_f32(reinterpret_cast<const IO*>(sl + W::kDelta)[c]);
@@ -372,11 +379,11 @@ __global__ void __launch_bounds__(128) state_update_wide_kernel(const StepProble
     const float dt = delta_of<PRECISE>(dv, bias, p.softplus);
     const float2 dt2 = make_float2(dt, dt), du2 = make_float2(dt * uv, dt * uv);
     float2 acc = make_float2(0.f, 0.f);
-    float* st = p.state + b * p.sst[0] + d * 16;
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       const int piece = (j + rot) & 3;
-      const float4 hv = *reinterpret_cast<const float4*>(sl + W::kState + (c * 16 + 4 * piece) * 4);
+      float4* hp = reinterpret_cast<float4*>(sl + W::kState + (c * 16 + 4 * piece) * 4);
+      const float4 hv = *hp;
       float Bv[4], Cv[4];
       load_piece(reinterpret_cast<const IO*>(sl + W::kB) + 4 * piece, Bv);
       load_piece(reinterpret_cast<const IO*>(sl + W::kC) + 4 * piece, Cv);
@@ -387,12 +394,21 @@ __global__ void __launch_bounds__(128) state_update_wide_kernel(const StepProble
       const float2 h1 = __ffma2_rn(a1, make_float2(hv.z, hv.w), __fmul2_rn(du2, make_float2(Bv[2], Bv[3])));
       acc = __ffma2_rn(make_float2(Cv[0], Cv[1]), h0, acc);
       acc = __ffma2_rn(make_float2(Cv[2], Cv[3]), h1, acc);
-      *reinterpret_cast<float4*>(st + 4 * piece) = make_float4(h0.x, h0.y, h1.x, h1.y);
+      *hp = make_float4(h0.x, h0.y, h1.x, h1.y);   // the new state goes back into the slot
     }
     float out = fmaf(Dd, uv, acc.x + acc.y);
     if (has_z) out *= silu<PRECISE>(zv);
-    static_cast<IO*>(p.y)[b * p.sy[0] + d] = from_f32<IO>(out);
+    reinterpret_cast<IO*>(sl + W::kU)[c] = from_f32<IO>(out);   // y over this thread's own u
+    // the slot's state tile and y row leave as two bulk stores once every thread has written them
+    fence_async_smem();
+    __syncthreads();
+    if (c == 0) {
+      bulk_store(p.state + b * p.sst[0] + d0 * 16, smem_u32(sl + W::kState), W::CH * 16 * 4);
+      bulk_store(static_cast<IO*>(p.y) + b * p.sy[0] + d0, smem_u32(sl + W::kU), W::kSeq);
+      bulk_commit();
+    }
   }
+  if (c == 0) bulk_wait<0>();   // the slots outlive their stores
 }
 
 // Whether the fast path takes these arguments (dense rows, 16-byte aligned bulk copies).
