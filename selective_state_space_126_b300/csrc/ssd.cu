@@ -23,11 +23,13 @@
 // mask, the scalings, the state recurrence across chunks (fp32, in registers)
 // and the output (D skip, gate) run on the CUDA cores.
 //
-// ssd_chunk_kernel: one CTA of 256 threads per (batch, head) walks its chunks
-// in order, for P = 64 and N = 128 with bf16 I/O.  Threads i and i + 128 own
-// time row i of the chunk (tensor-memory lane i of G, Y_diag, Y_off; each one
-// half of the columns) and state row i (lane i of H_chunk, and half each of
-// the fp32 state H[i][0..63] in registers).  Per chunk:
+// ssd_chunk_kernel: one CTA of 512 threads per (batch, head) walks its chunks
+// in order, for P = 64 and N = 128 with bf16 I/O.  Threads i, i + 128, i + 256
+// and i + 384 own time row i of the chunk (tensor-memory lane i of G, Y_diag,
+// Y_off; each one quarter of the columns) and state row i (lane i of H_chunk,
+// and a quarter each of the fp32 state H[i][0..63] in registers).  The phases
+// between the MMAs are thread work with little parallelism inside a thread, so
+// four warps per scheduler (rather than two) hide their latencies.  Per chunk:
 //   1. TMA: C_c and B_c ((L, N) rows of 128 B, 128B swizzle, two 64-column
 //      boxes each) and X_c ((P, L) rows, two 64-step boxes) -- each already
 //      the K-major operand layout of the MMAs below -- and the gate's z_c.
@@ -59,7 +61,11 @@ namespace {
 constexpr int kQ = 128;          // chunk length
 constexpr int kP = 64;           // head dimension of the tensor-core kernel
 constexpr int kN = 128;          // state size of the tensor-core kernel
-constexpr int kSsdThreads = 256;
+constexpr int kSsdThreads = 512;
+constexpr int kCQ = kSsdThreads / kQ;  // threads per chunk row (column quarters)
+constexpr int kPQ = kP / kCQ;          // head channels per thread (state update, output)
+constexpr int kSQ = kQ / kCQ;          // steps per thread (weighted B^T, scores)
+static_assert(kSQ % 32 == 0 && kPQ % 16 == 0, "thread split");
 
 struct SsdSmem {
   static constexpr int kC = 0;                 // C chunk: 2 x [128 t][64 n] bf16, swizzled
@@ -101,10 +107,11 @@ __global__ void __launch_bounds__(kSsdThreads, 1)
                  bar_ho = bar_tma + 24, bar_d = bar_tma + 32;
   uint32_t* taddr_s = reinterpret_cast<uint32_t*>(smem + S::kTaddr);
 
-  // thread = (row r, half hf): row r is time step r of the chunk and state index r; the half picks
-  // columns [64 hf, 64 hf + 64) of the score row and head channels [32 hf, 32 hf + 32)
+  // thread = (row r, quarter cq): row r is time step r of the chunk and state index r; the quarter
+  // picks steps [kSQ cq, kSQ cq + kSQ) of the score row and head channels [kPQ cq, kPQ cq + kPQ);
+  // warp w reaches tensor-memory lanes 32 (w % 4) .. + 31, which are its rows
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int r = tid & (kQ - 1), hf = tid >> 7;
+  const int r = tid & (kQ - 1), cq = tid / kQ;
   const int64_t bh = blockIdx.x;
   const int64_t b = bh / p.H, h = bh % p.H;
   const int nchunks = (int)((p.L + kQ - 1) / kQ);
@@ -123,12 +130,11 @@ __global__ void __launch_bounds__(kSsdThreads, 1)
   const uint32_t tmem = *taddr_s;
   const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;   // this warp's 32 tensor-memory lanes: rows r
 
-  // state H[r][32 hf .. 32 hf + 31] (state row n = r, head channels p), fp32 in registers
-  constexpr int kHalfP = kP / 2;
-  float H[kHalfP];
+  // state H[r][kPQ cq .. kPQ cq + kPQ - 1] (state row n = r, head channels p), fp32 in registers
+  float H[kPQ];
 #pragma unroll
-  for (int j = 0; j < kHalfP; ++j)
-    H[j] = p.h0 ? p.h0[b * p.sh0[0] + h * p.sh0[1] + (kHalfP * hf + j) * p.sh0[2] + r * p.sh0[3]] : 0.f;
+  for (int j = 0; j < kPQ; ++j)
+    H[j] = p.h0 ? p.h0[b * p.sh0[0] + h * p.sh0[1] + (kPQ * cq + j) * p.sh0[2] + r * p.sh0[3]] : 0.f;
 
   // thread 0 tracks the copies and MMAs in flight (chunk index, or -1) for a bounded drain on failure
   int cxz_pend = -1, b_pend = -1;
@@ -157,7 +163,7 @@ __global__ void __launch_bounds__(kSsdThreads, 1)
   const uint32_t id128 = umma_idesc_bf16(128, 128), id64 = umma_idesc_bf16(128, 64);
   // raw delta of step t (this row's step of a chunk), loaded one chunk ahead
   auto load_delta = [&](int64_t t) -> float {
-    if (hf != 0 || t >= p.L) return 0.f;
+    if (cq != 0 || t >= p.L) return 0.f;
     const int64_t o = b * p.sd[0] + h * p.sd[1] + t;
     return p.io == SSM_BF16 ? __bfloat162float(__ldg(static_cast<const __nv_bfloat16*>(p.delta) + o))
                             : __ldg(static_cast<const float*>(p.delta) + o);
@@ -172,7 +178,7 @@ __global__ void __launch_bounds__(kSsdThreads, 1)
 
     // ---- 2. Delta, prefix sum S (rows, half 0), weights; the incoming state as an operand ----
     float dt = 0.f;
-    if (hf == 0 && r < valid) dt = delta_of<false>(dnext, bias, p.softplus);
+    if (cq == 0 && r < valid) dt = delta_of<false>(dnext, bias, p.softplus);
     dnext = load_delta(t0 + kQ + r);   // the next chunk's, in flight during this one
     float cum = dt;
 #pragma unroll
@@ -180,14 +186,14 @@ __global__ void __launch_bounds__(kSsdThreads, 1)
       const float v = __shfl_up_sync(0xffffffffu, cum, o);
       if (lane >= o) cum += v;
     }
-    if (hf == 0 && lane == 31) sWarp[warp] = cum;
+    if (cq == 0 && lane == 31) sWarp[warp] = cum;
     // H_in^T as the bf16 operand: row p, K = n (this thread's n = r, its 32 head channels)
 #pragma unroll
-    for (int j = 0; j < kHalfP; ++j)
-      *reinterpret_cast<__nv_bfloat16*>(smem + S::kSI + (r >> 6) * 8192 + sw128_offset(kHalfP * hf + j, r & 63)) =
+    for (int j = 0; j < kPQ; ++j)
+      *reinterpret_cast<__nv_bfloat16*>(smem + S::kSI + (r >> 6) * 8192 + sw128_offset(kPQ * cq + j, r & 63)) =
           __float2bfloat16_rn(H[j]);
     __syncthreads();
-    if (hf == 0) {
+    if (cq == 0) {
       for (int w = 0; w < warp; ++w) cum += sWarp[w];
       sDelta[r] = dt;
       sCum[r] = cum;
@@ -195,10 +201,10 @@ __global__ void __launch_bounds__(kSsdThreads, 1)
     __syncthreads();
     cum = sCum[r];
     const float cum_end = sCum[kQ - 1];
-    if (hf == 0) sW[r] = ex2_approx(a2 * (cum_end - cum)) * sDelta[r];
+    if (cq == 0) sW[r] = ex2_approx(a2 * (cum_end - cum)) * sDelta[r];
     const float et = ex2_approx(a2 * cum);   // exp(a S_t) of row t = r
 
-    // ---- 1. B of this chunk; B~^T[n][s] = w_s B[s][n] (thread: n = r, steps [64 hf, 64 hf + 64)) ----
+    // ---- 1. B of this chunk; B~^T[n][s] = w_s B[s][n] (thread: n = r, steps [kSQ cq, kSQ cq + kSQ)) ----
     const bool ok_b = mbar_wait(bar_tmab, par);
     if (!ok_b) record_status(p.status, SSM_ERR_TIMEOUT);
     if (tid == 0 && ok_b) b_pend = -1;
@@ -207,27 +213,29 @@ __global__ void __launch_bounds__(kSsdThreads, 1)
       const int n = r;
       const unsigned char* src = smem + S::kB + (n >> 6) * 16384;
 #pragma unroll 2
-      for (int jj = 0; jj < 8; ++jj) {   // piece jj of step block hf: steps s = 64 hf + 8 jj .. + 7
+      for (int jj = 0; jj < kSQ / 8; ++jj) {   // steps s = kSQ cq + 8 jj .. + 7
+        const int s8 = kSQ * cq + 8 * jj;
         float f[8];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const int sl = 8 * jj + e, sg = 64 * hf + sl;
-          f[e] = __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(src + sw128_offset(sg, n & 63))) * sW[sg];
-        }
-        *reinterpret_cast<uint4*>(smem + S::kBT + hf * 16384 + n * 128 + ((jj ^ (n & 7)) << 4)) = pack16(f);
+        for (int e = 0; e < 8; ++e)
+          f[e] = __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(src + sw128_offset(s8 + e, n & 63))) *
+                 sW[s8 + e];
+        *reinterpret_cast<uint4*>(smem + S::kBT + (s8 >> 6) * 16384 + n * 128 + ((((s8 & 63) >> 3) ^ (n & 7)) << 4)) =
+            pack16(f);
       }
     }
-    // ---- C, X, z; X_Delta[p][s] = Delta_s X[p][s] (thread: row p, step block, 4 of the 8 pieces) ----
+    // ---- C, X, z; X_Delta[p][s] = Delta_s X[p][s] (thread: row p, step block, 8 / kCQ of the 8 pieces) ----
     const bool ok_t = ok_b && mbar_wait(bar_tma, par);
     if (!ok_t) record_status(p.status, SSM_ERR_TIMEOUT);
     if (tid == 0 && ok_t) cxz_pend = -1;
     if (ok_t) {
       const int pr = tid & 63, blk = (tid >> 6) & 1, ph = tid >> 7;
+      constexpr int kXP = 8 / kCQ;
       const unsigned char* src = smem + S::kX + blk * 8192 + pr * 128;
       unsigned char* dst = smem + S::kXD + blk * 8192 + pr * 128;
 #pragma unroll
-      for (int jj = 0; jj < 4; ++jj) {
-        const int j = 4 * ph + jj;
+      for (int jj = 0; jj < kXP; ++jj) {
+        const int j = kXP * ph + jj;
         const int pos = (j ^ (pr & 7)) << 4;   // logical piece j holds s = 64 blk + 8 j .. + 7
         float f[8];
         unpack16(*reinterpret_cast<const uint4*>(src + pos), f);
@@ -262,7 +270,7 @@ __global__ void __launch_bounds__(kSsdThreads, 1)
       mma_out = true;
     }
 
-    // ---- 4. causal decay mask on G -> bf16 scores (thread: row t = r, steps [64 hf, 64 hf + 64)) ----
+    // ---- 4. causal decay mask on G -> bf16 scores (thread: row t = r, steps [kSQ cq, kSQ cq + kSQ)) ----
     const bool ok_g = mbar_wait(bar_g, par);
     if (!ok_g) record_status(p.status, SSM_ERR_TIMEOUT);
     tc_fence_after();
@@ -270,7 +278,7 @@ __global__ void __launch_bounds__(kSsdThreads, 1)
     // B is consumed (B~^T built, G complete): the next chunk's B can land while this one finishes
     if (tid == 0 && c + 1 < nchunks) issue_b(c + 1);
 #pragma unroll 1
-    for (int s0 = 64 * hf; s0 < 64 * hf + 64; s0 += 32) {
+    for (int s0 = kSQ * cq; s0 < kSQ * cq + kSQ; s0 += 32) {
       float g[32];
       tmem_ld32(tmem + lane_off + kColG + (uint32_t)s0, g);
 #pragma unroll
@@ -301,34 +309,34 @@ __global__ void __launch_bounds__(kSsdThreads, 1)
       mma_d_out = true;
     }
 
-    // ---- 6. state update (thread: n = r, channels [32 hf, +32)), then the output (t = r, same channels) ----
+    // ---- 6. state update (thread: n = r, channels [kPQ cq, +kPQ)), then the output (t = r, same channels) ----
     const bool ok_ho = mbar_wait(bar_ho, par);
     if (!ok_ho) record_status(p.status, SSM_ERR_TIMEOUT);
     tc_fence_after();
     if (ok_ho) {
       const float decay = ex2_approx(a2 * cum_end);
-      float hc[32];
-      tmem_ld32(tmem + lane_off + kColH + (uint32_t)(kHalfP * hf), hc);
+      float hc[kPQ];
+      tmem_ld(tmem + lane_off + kColH + (uint32_t)(kPQ * cq), hc);
 #pragma unroll
-      for (int j = 0; j < kHalfP; ++j) H[j] = fmaf(decay, H[j], hc[j]);
+      for (int j = 0; j < kPQ; ++j) H[j] = fmaf(decay, H[j], hc[j]);
     }
     const bool ok_d = mbar_wait(bar_d, par);
     if (!ok_d) record_status(p.status, SSM_ERR_TIMEOUT);
     tc_fence_after();
     if (ok_ho && ok_d) {
       const int64_t t = t0 + r;
-      float yd[32], yo[32];
-      tmem_ld32(tmem + lane_off + kColYd + (uint32_t)(kHalfP * hf), yd);
-      tmem_ld32(tmem + lane_off + kColYo + (uint32_t)(kHalfP * hf), yo);
+      float yd[kPQ], yo[kPQ];
+      tmem_ld(tmem + lane_off + kColYd + (uint32_t)(kPQ * cq), yd);
+      tmem_ld(tmem + lane_off + kColYo + (uint32_t)(kPQ * cq), yo);
       if (r < valid) {
 #pragma unroll
-        for (int j = 0; j < kHalfP; ++j) {
-          const int q = kHalfP * hf + j;
+        for (int j = 0; j < kPQ; ++j) {
+          const int q = kPQ * cq + j;
           const int64_t d = h * kP + q;
           const int zx = (r >> 6) * 8192 + sw128_offset(q, r & 63);
           const float xv = __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(smem + S::kX + zx));
           float v = fmaf(et, yo[j], yd[j]) + Dh * xv;
-          if (p.z) v *= silu<false>(__bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(smem + S::kZ + zx)));
+          if (p.z) v *= silu_tanh(__bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(smem + S::kZ + zx)));
           static_cast<__nv_bfloat16*>(p.y)[b * p.sy[0] + d * p.sy[1] + t] = __float2bfloat16_rn(v);
         }
       }
@@ -353,8 +361,8 @@ __global__ void __launch_bounds__(kSsdThreads, 1)
     }
   } else if (p.h_last) {
 #pragma unroll
-    for (int j = 0; j < kHalfP; ++j)
-      p.h_last[b * p.shl[0] + h * p.shl[1] + (kHalfP * hf + j) * p.shl[2] + r * p.shl[3]] = H[j];
+    for (int j = 0; j < kPQ; ++j)
+      p.h_last[b * p.shl[0] + h * p.shl[1] + (kPQ * cq + j) * p.shl[2] + r * p.shl[3]] = H[j];
   }
   tc_fence_before();
   __syncthreads();
