@@ -66,6 +66,10 @@ constexpr int kCQ = kSsdThreads / kQ;  // threads per chunk row (column quarters
 constexpr int kPQ = kP / kCQ;          // head channels per thread (state update, output)
 constexpr int kSQ = kQ / kCQ;          // steps per thread (weighted B^T, scores)
 static_assert(kSQ % 32 == 0 && kPQ % 16 == 0, "thread split");
+// The thread that issues the TMA loads and the MMAs: lane 0 of the warp for rows 0..31 and the last
+// quarter of the steps, whose block of the causal score matrix is all zero, so that the time it
+// spends issuing MMAs does not hold back the score phase.
+constexpr int kIssuer = (kCQ - 1) * kQ;
 
 struct SsdSmem {
   static constexpr int kC = 0;                 // C chunk: 2 x [128 t][64 n] bf16, swizzled
@@ -89,6 +93,30 @@ struct SsdSmem {
 // tensor-memory columns of the accumulators (lanes = rows)
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColG = 0, kColYd = 128, kColYo = 192, kColH = 256;
+
+// Four 8 x 8 bf16 matrices from shared memory, transposed on the way (lane l gives the address of
+// row l % 8 of matrix l / 8); register m of lane l holds elements (2 (l % 4), l / 4) and
+// (2 (l % 4) + 1, l / 4) of matrix m, the first in the low half.
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t (&v)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3])
+               : "r"(addr));
+}
+
+// Four 8 x 8 bf16 matrices to shared memory (lane l gives the address of row l % 8 of matrix l / 8);
+// register m of lane l holds elements (l / 4, 2 (l % 4)) and (l / 4, 2 (l % 4) + 1) of matrix m.
+__device__ __forceinline__ void stsm_x4(uint32_t addr, const uint32_t (&v)[4]) {
+  asm volatile("stmatrix.sync.aligned.m8n8.x4.shared.b16 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v[0]), "r"(v[1]),
+               "r"(v[2]), "r"(v[3])
+               : "memory");
+}
+
+// (lo, hi) bf16 pair times (w.x, w.y) in fp32, rounded back to a bf16 pair.
+__device__ __forceinline__ uint32_t scale_bf16x2(uint32_t v, float2 w) {
+  const float lo = __uint_as_float(v << 16) * w.x, hi = __uint_as_float(v & 0xffff0000u) * w.y;
+  const __nv_bfloat162 r = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&r);
+}
 
 struct SsdMaps {
   CUtensorMap x, z, B, C;
@@ -136,9 +164,11 @@ __global__ void __launch_bounds__(kSsdThreads, 1)
   for (int j = 0; j < kPQ; ++j)
     H[j] = p.h0 ? p.h0[b * p.sh0[0] + h * p.sh0[1] + (kPQ * cq + j) * p.sh0[2] + r * p.sh0[3]] : 0.f;
 
-  // thread 0 tracks the copies and MMAs in flight (chunk index, or -1) for a bounded drain on failure
+  // the issuing thread tracks the copies (chunk index, or -1) and MMA groups in flight for a bounded
+  // drain on failure
+  const bool issuer = tid == kIssuer;
   int cxz_pend = -1, b_pend = -1;
-  bool mma_out = false, mma_d_out = false;
+  bool g_out = false, ho_out = false, d_out = false;
   auto issue_cxz = [&](int c) {   // C, X and z of chunk c
     const int t0 = c * kQ;
     mbar_expect_tx(bar_tma, 2 * 16384 + 2 * 8192 + (p.z ? 2 * 8192 : 0));
@@ -155,7 +185,7 @@ __global__ void __launch_bounds__(kSsdThreads, 1)
       tma_load(smem_u32(smem + S::kB + j * 16384), &tm.B, 64 * j, c * kQ, (int)b, true, bar_tmab);
     b_pend = c;
   };
-  if (tid == 0 && nchunks > 0) {
+  if (issuer && nchunks > 0) {
     issue_b(0);
     issue_cxz(0);
   }
@@ -207,27 +237,32 @@ __global__ void __launch_bounds__(kSsdThreads, 1)
     // ---- 1. B of this chunk; B~^T[n][s] = w_s B[s][n] (thread: n = r, steps [kSQ cq, kSQ cq + kSQ)) ----
     const bool ok_b = mbar_wait(bar_tmab, par);
     if (!ok_b) record_status(p.status, SSM_ERR_TIMEOUT);
-    if (tid == 0 && ok_b) b_pend = -1;
+    if (issuer && ok_b) b_pend = -1;
     __syncthreads();   // sW visible
-    if (ok_b) {
-      const int n = r;
-      const unsigned char* src = smem + S::kB + (n >> 6) * 16384;
-#pragma unroll 2
-      for (int jj = 0; jj < kSQ / 8; ++jj) {   // steps s = kSQ cq + 8 jj .. + 7
-        const int s8 = kSQ * cq + 8 * jj;
-        float f[8];
+    // warp w transposes steps [32 (w % 4), +32) x states [32 (w / 4), +32) in 8 x 8 blocks: lane l
+    // addresses row l % 8 of block l / 8 (one 16-byte row piece each), and after the transposing
+    // load holds, for each of the four step blocks m, the pair of steps 32 (w % 4) + 8 m + 2 (l % 4)
+    // + {0, 1} of state n0 + l / 4; the weights of those steps are the same for every state block
+    if (__all_sync(0xffffffffu, ok_b)) {
+      const int s0 = 32 * (warp & 3), nb0 = 32 * (warp >> 2), mi = lane >> 3, ri = lane & 7;
+      float2 wv[4];
 #pragma unroll
-        for (int e = 0; e < 8; ++e)
-          f[e] = __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(src + sw128_offset(s8 + e, n & 63))) *
-                 sW[s8 + e];
-        *reinterpret_cast<uint4*>(smem + S::kBT + (s8 >> 6) * 16384 + n * 128 + ((((s8 & 63) >> 3) ^ (n & 7)) << 4)) =
-            pack16(f);
+      for (int m = 0; m < 4; ++m) wv[m] = *reinterpret_cast<const float2*>(sW + s0 + 8 * m + 2 * (lane & 3));
+#pragma unroll
+      for (int nb = 0; nb < 4; ++nb) {
+        const int n0 = nb0 + 8 * nb;
+        uint32_t v[4];
+        ldsm_x4_trans(smem_u32(smem + S::kB + (n0 >> 6) * 16384 + sw128_offset(s0 + 8 * mi + ri, n0 & 63)), v);
+#pragma unroll
+        for (int m = 0; m < 4; ++m) v[m] = scale_bf16x2(v[m], wv[m]);
+        const int n = n0 + ri, sb = s0 + 8 * mi;
+        stsm_x4(smem_u32(smem + S::kBT + (sb >> 6) * 16384 + n * 128 + ((((sb & 63) >> 3) ^ (n & 7)) << 4)), v);
       }
     }
     // ---- C, X, z; X_Delta[p][s] = Delta_s X[p][s] (thread: row p, step block, 8 / kCQ of the 8 pieces) ----
     const bool ok_t = ok_b && mbar_wait(bar_tma, par);
     if (!ok_t) record_status(p.status, SSM_ERR_TIMEOUT);
-    if (tid == 0 && ok_t) cxz_pend = -1;
+    if (issuer && ok_t) cxz_pend = -1;
     if (ok_t) {
       const int pr = tid & 63, blk = (tid >> 6) & 1, ph = tid >> 7;
       constexpr int kXP = 8 / kCQ;
@@ -248,16 +283,29 @@ __global__ void __launch_bounds__(kSsdThreads, 1)
     tc_fence_before();
     if (__syncthreads_or(!ok_t)) { failed = true; break; }
 
-    // ---- 3. G = C B^T, H_chunk = B~^T X, Y_off = C H_in ----
-    if (tid == 0) {
+    // ---- 3. G = C B^T (H_chunk and Y_off follow once G is complete) ----
+    const uint32_t sC = smem_u32(smem + S::kC);
+    if (issuer) {
       tc_fence_after();
-      const uint32_t sC = smem_u32(smem + S::kC), sB = smem_u32(smem + S::kB), sX = smem_u32(smem + S::kX);
-      const uint32_t sBT = smem_u32(smem + S::kBT), sSI = smem_u32(smem + S::kSI);
+      const uint32_t sB = smem_u32(smem + S::kB);
       for (int k = 0; k < 8; ++k) {
         const uint32_t o16 = (k >> 2) * 16384 + (k & 3) * 32;
         umma_bf16(tmem + kColG, umma_desc_sw128(sC + o16), umma_desc_sw128(sB + o16), id128, k > 0);
       }
       umma_commit(bar_g);
+      g_out = true;
+    }
+
+    // ---- 4. causal decay mask on G -> bf16 scores (thread: row t = r, steps [kSQ cq, kSQ cq + kSQ)) ----
+    const bool ok_g = mbar_wait(bar_g, par);
+    if (!ok_g) record_status(p.status, SSM_ERR_TIMEOUT);
+    tc_fence_after();
+    if (__syncthreads_or(!ok_g)) { failed = true; break; }
+    // H_chunk = B~^T X and Y_off = C H_in run on the tensor cores while the threads build the scores;
+    // B is consumed (B~^T built, G complete), so the next chunk's B can land meanwhile
+    if (issuer) {
+      g_out = false;
+      const uint32_t sX = smem_u32(smem + S::kX), sBT = smem_u32(smem + S::kBT), sSI = smem_u32(smem + S::kSI);
       for (int k = 0; k < 8; ++k) {
         const uint32_t o16 = (k >> 2) * 16384 + (k & 3) * 32, o8 = (k >> 2) * 8192 + (k & 3) * 32;
         umma_bf16(tmem + kColH, umma_desc_sw128(sBT + o16), umma_desc_sw128(sX + o8), id64, k > 0);
@@ -267,18 +315,20 @@ __global__ void __launch_bounds__(kSsdThreads, 1)
         umma_bf16(tmem + kColYo, umma_desc_sw128(sC + o16), umma_desc_sw128(sSI + o8), id64, k > 0);
       }
       umma_commit(bar_ho);
-      mma_out = true;
+      ho_out = true;
+      if (c + 1 < nchunks) issue_b(c + 1);
     }
-
-    // ---- 4. causal decay mask on G -> bf16 scores (thread: row t = r, steps [kSQ cq, kSQ cq + kSQ)) ----
-    const bool ok_g = mbar_wait(bar_g, par);
-    if (!ok_g) record_status(p.status, SSM_ERR_TIMEOUT);
-    tc_fence_after();
-    if (__syncthreads_or(!ok_g)) { failed = true; break; }
-    // B is consumed (B~^T built, G complete): the next chunk's B can land while this one finishes
-    if (tid == 0 && c + 1 < nchunks) issue_b(c + 1);
 #pragma unroll 1
     for (int s0 = kSQ * cq; s0 < kSQ * cq + kSQ; s0 += 32) {
+      if (s0 > 32 * (warp & 3) + 31) {   // above the diagonal for every row of this warp: zeros
+#pragma unroll
+        for (int j = 0; j < 32; j += 8) {
+          const int sblk = (s0 + j) >> 6, piece = ((s0 + j) & 63) >> 3;
+          *reinterpret_cast<uint4*>(smem + S::kSP + sblk * 16384 + r * 128 + ((piece ^ (r & 7)) << 4)) =
+              make_uint4(0u, 0u, 0u, 0u);
+        }
+        continue;
+      }
       float g[32];
       tmem_ld32(tmem + lane_off + kColG + (uint32_t)s0, g);
 #pragma unroll
@@ -298,7 +348,7 @@ __global__ void __launch_bounds__(kSsdThreads, 1)
     __syncthreads();
 
     // ---- 5. Y_diag = scores X_Delta ----
-    if (tid == 0) {
+    if (issuer) {
       tc_fence_after();
       const uint32_t sSP = smem_u32(smem + S::kSP), sXD = smem_u32(smem + S::kXD);
       for (int k = 0; k < 8; ++k) {
@@ -306,7 +356,7 @@ __global__ void __launch_bounds__(kSsdThreads, 1)
         umma_bf16(tmem + kColYd, umma_desc_sw128(sSP + o16), umma_desc_sw128(sXD + o8), id64, k > 0);
       }
       umma_commit(bar_d);
-      mma_d_out = true;
+      d_out = true;
     }
 
     // ---- 6. state update (thread: n = r, channels [kPQ cq, +kPQ)), then the output (t = r, same channels) ----
@@ -343,21 +393,19 @@ __global__ void __launch_bounds__(kSsdThreads, 1)
     }
     tc_fence_before();
     if (__syncthreads_or(!(ok_ho && ok_d))) { failed = true; break; }
-    mma_out = mma_d_out = false;
-    if (tid == 0 && c + 1 < nchunks) issue_cxz(c + 1);
+    ho_out = d_out = false;
+    if (issuer && c + 1 < nchunks) issue_cxz(c + 1);
   }
 
   if (failed) {
     // let every copy and MMA this CTA started finish (bounded waits) before its tensor memory is freed
-    if (tid == 0) {
+    if (issuer) {
       if (b_pend >= 0) mbar_wait(bar_tmab, (uint32_t)b_pend & 1u);
       if (cxz_pend >= 0) mbar_wait(bar_tma, (uint32_t)cxz_pend & 1u);
       const uint32_t par = (uint32_t)c & 1u;
-      if (mma_out) {
-        mbar_wait(bar_g, par);
-        mbar_wait(bar_ho, par);
-      }
-      if (mma_d_out) mbar_wait(bar_d, par);
+      if (g_out) mbar_wait(bar_g, par);
+      if (ho_out) mbar_wait(bar_ho, par);
+      if (d_out) mbar_wait(bar_d, par);
     }
   } else if (p.h_last) {
 #pragma unroll
