@@ -34,15 +34,19 @@
 //      boxes each) and X_c ((P, L) rows, two 64-step boxes) -- each already
 //      the K-major operand layout of the MMAs below -- and the gate's z_c.
 //      B_c has its own barrier and the next chunk's B is loaded as soon as
-//      this one's is consumed (after step 4);
+//      this one's is consumed (after G);
 //   2. Delta, the inclusive prefix sum S (warp shuffles and one shared step),
-//      the weights w_s = exp(a (S_end - S_s)) Delta_s; threads write
-//      X_Delta = Delta_s X (K = s), B~^T = w_s B^T (transposed, K = s) and the
-//      incoming state H_in^T (K = n) in bf16;
-//   3. MMA: G = C B^T, H_chunk = B~^T X, Y_off = C H_in (one commit each);
-//   4. threads read G (tcgen05.ld), apply the causal decay mask
-//      exp(a (S_t - S_s)) on the SFU and write the bf16 scores (K = s);
-//   5. MMA: Y_diag = scores X_Delta;
+//      the weights w_s = exp(a (S_end - S_s)) Delta_s and the column terms
+//      a S_s log2(e) - log2(Delta_s) of the scores; threads write the incoming
+//      state H_in^T (K = n) in bf16;
+//   3. MMA: G = C B^T, issued as soon as C and B are in, runs while the
+//      threads write B~^T = w_s B^T (K = s) with 8 x 8 transposing loads and
+//      stores (ldmatrix.trans / stmatrix); then H_chunk = B~^T X and
+//      Y_off = C H_in are queued behind it (one commit each);
+//   4. threads read G (tcgen05.ld), apply the causal decay mask and the step
+//      factor, exp(a (S_t - S_s)) Delta_s, on the SFU and write the bf16
+//      scores (K = s); blocks above the diagonal are written as zeros;
+//   5. MMA: Y_diag = scores X;
 //   6. threads update H = exp(a S_end) H + H_chunk and emit
 //      y = (Y_diag + exp(a S_t) Y_off + D x) silu(z), coalesced along t.
 // Other shapes and fp32 I/O take ssd_generic_kernel (one warp per channel, the
@@ -76,14 +80,14 @@ struct SsdSmem {
   static constexpr int kB = kC + 32768;        // B chunk: 2 x [128 s][64 n]
   static constexpr int kX = kB + 32768;        // X chunk: 2 x [64 p][64 s]
   static constexpr int kSP = kX + 16384;       // masked scores: 2 x [128 t][64 s]
-  static constexpr int kXD = kSP + 32768;      // Delta X: 2 x [64 p][64 s]
-  static constexpr int kBT = kXD + 16384;      // weighted B^T: 2 x [128 n][64 s]
+  static constexpr int kBT = kSP + 32768;      // weighted B^T: 2 x [128 n][64 s]
   static constexpr int kSI = kBT + 32768;      // incoming state H_in^T: 2 x [64 p][64 n]
   static constexpr int kZ = kSI + 16384;       // z chunk: 2 x [64 p][64 t] (the gate)
   static constexpr int kDelta = kZ + 16384;    // float [128]
   static constexpr int kCum = kDelta + 512;    // float [128]
   static constexpr int kW = kCum + 512;        // float [128]
-  static constexpr int kWarp = kW + 512;       // float [4] warp totals of the prefix sum
+  static constexpr int kAS = kW + 512;         // float [128]: a S_s log2(e), less log2(Delta_s) under softplus
+  static constexpr int kWarp = kAS + 512;      // float [4] warp totals of the prefix sum
   static constexpr int kBar = kWarp + 16;      // 5 mbarriers: TMA (C, X, z), TMA (B), G, (H_chunk, Y_off), Y_diag
   static constexpr int kTaddr = kBar + 40;
   static constexpr int kBytes = kTaddr + 16;
@@ -130,6 +134,7 @@ __global__ void __launch_bounds__(kSsdThreads, 1)
   float* sDelta = reinterpret_cast<float*>(smem + S::kDelta);
   float* sCum = reinterpret_cast<float*>(smem + S::kCum);
   float* sW = reinterpret_cast<float*>(smem + S::kW);
+  float* sAS = reinterpret_cast<float*>(smem + S::kAS);
   float* sWarp = reinterpret_cast<float*>(smem + S::kWarp);
   const uint32_t bar_tma = smem_u32(smem + S::kBar), bar_tmab = bar_tma + 8, bar_g = bar_tma + 16,
                  bar_ho = bar_tma + 24, bar_d = bar_tma + 32;
@@ -231,7 +236,11 @@ __global__ void __launch_bounds__(kSsdThreads, 1)
     __syncthreads();
     cum = sCum[r];
     const float cum_end = sCum[kQ - 1];
-    if (cq == 0) sW[r] = ex2_approx(a2 * (cum_end - cum)) * sDelta[r];
+    if (cq == 0) {
+      sW[r] = ex2_approx(a2 * (cum_end - cum)) * sDelta[r];
+      // the score's column factor Delta_s enters the exponent when it is positive (softplus)
+      sAS[r] = p.softplus ? a2 * cum - __log2f(sDelta[r]) : a2 * cum;
+    }
     const float et = ex2_approx(a2 * cum);   // exp(a S_t) of row t = r
 
     // ---- 1. B of this chunk; B~^T[n][s] = w_s B[s][n] (thread: n = r, steps [kSQ cq, kSQ cq + kSQ)) ----
@@ -239,6 +248,18 @@ __global__ void __launch_bounds__(kSsdThreads, 1)
     if (!ok_b) record_status(p.status, SSM_ERR_TIMEOUT);
     if (issuer && ok_b) b_pend = -1;
     __syncthreads();   // sW visible
+    // ---- 3. G = C B^T needs only the two TMA tiles: it runs while the threads build B~^T ----
+    const uint32_t sC = smem_u32(smem + S::kC);
+    if (issuer && ok_b && mbar_wait(bar_tma, par)) {
+      tc_fence_after();
+      const uint32_t sB = smem_u32(smem + S::kB);
+      for (int k = 0; k < 8; ++k) {
+        const uint32_t o16 = (k >> 2) * 16384 + (k & 3) * 32;
+        umma_bf16(tmem + kColG, umma_desc_sw128(sC + o16), umma_desc_sw128(sB + o16), id128, k > 0);
+      }
+      umma_commit(bar_g);
+      g_out = true;
+    }
     // warp w transposes steps [32 (w % 4), +32) x states [32 (w / 4), +32) in 8 x 8 blocks: lane l
     // addresses row l % 8 of block l / 8 (one 16-byte row piece each), and after the transposing
     // load holds, for each of the four step blocks m, the pair of steps 32 (w % 4) + 8 m + 2 (l % 4)
@@ -259,52 +280,25 @@ __global__ void __launch_bounds__(kSsdThreads, 1)
         stsm_x4(smem_u32(smem + S::kBT + (sb >> 6) * 16384 + n * 128 + ((((sb & 63) >> 3) ^ (n & 7)) << 4)), v);
       }
     }
-    // ---- C, X, z; X_Delta[p][s] = Delta_s X[p][s] (thread: row p, step block, 8 / kCQ of the 8 pieces) ----
+    // ---- C, X and z of this chunk ----
     const bool ok_t = ok_b && mbar_wait(bar_tma, par);
     if (!ok_t) record_status(p.status, SSM_ERR_TIMEOUT);
     if (issuer && ok_t) cxz_pend = -1;
-    if (ok_t) {
-      const int pr = tid & 63, blk = (tid >> 6) & 1, ph = tid >> 7;
-      constexpr int kXP = 8 / kCQ;
-      const unsigned char* src = smem + S::kX + blk * 8192 + pr * 128;
-      unsigned char* dst = smem + S::kXD + blk * 8192 + pr * 128;
-#pragma unroll
-      for (int jj = 0; jj < kXP; ++jj) {
-        const int j = kXP * ph + jj;
-        const int pos = (j ^ (pr & 7)) << 4;   // logical piece j holds s = 64 blk + 8 j .. + 7
-        float f[8];
-        unpack16(*reinterpret_cast<const uint4*>(src + pos), f);
-#pragma unroll
-        for (int e = 0; e < 8; ++e) f[e] *= sDelta[64 * blk + 8 * j + e];
-        *reinterpret_cast<uint4*>(dst + pos) = pack16(f);
-      }
-    }
     fence_async_smem();
     tc_fence_before();
     if (__syncthreads_or(!ok_t)) { failed = true; break; }
-
-    // ---- 3. G = C B^T (H_chunk and Y_off follow once G is complete) ----
-    const uint32_t sC = smem_u32(smem + S::kC);
-    if (issuer) {
-      tc_fence_after();
-      const uint32_t sB = smem_u32(smem + S::kB);
-      for (int k = 0; k < 8; ++k) {
-        const uint32_t o16 = (k >> 2) * 16384 + (k & 3) * 32;
-        umma_bf16(tmem + kColG, umma_desc_sw128(sC + o16), umma_desc_sw128(sB + o16), id128, k > 0);
-      }
-      umma_commit(bar_g);
-      g_out = true;
-    }
 
     // ---- 4. causal decay mask on G -> bf16 scores (thread: row t = r, steps [kSQ cq, kSQ cq + kSQ)) ----
     const bool ok_g = mbar_wait(bar_g, par);
     if (!ok_g) record_status(p.status, SSM_ERR_TIMEOUT);
     tc_fence_after();
     if (__syncthreads_or(!ok_g)) { failed = true; break; }
-    // H_chunk = B~^T X and Y_off = C H_in run on the tensor cores while the threads build the scores;
-    // B is consumed (B~^T built, G complete), so the next chunk's B can land meanwhile
+    // H_chunk = B~^T X and Y_off = C H_in (operands written by the threads) run on the tensor cores
+    // while the threads build the scores; B is consumed (B~^T built, G complete), so the next
+    // chunk's B can land meanwhile
     if (issuer) {
       g_out = false;
+      tc_fence_after();
       const uint32_t sX = smem_u32(smem + S::kX), sBT = smem_u32(smem + S::kBT), sSI = smem_u32(smem + S::kSI);
       for (int k = 0; k < 8; ++k) {
         const uint32_t o16 = (k >> 2) * 16384 + (k & 3) * 32, o8 = (k >> 2) * 8192 + (k & 3) * 32;
@@ -331,13 +325,23 @@ __global__ void __launch_bounds__(kSsdThreads, 1)
       }
       float g[32];
       tmem_ld32(tmem + lane_off + kColG + (uint32_t)s0, g);
+      const float ac = a2 * cum;
 #pragma unroll
       for (int j = 0; j < 32; j += 8) {
         float f[8];
+        // scores[t][s] = exp(a (S_t - S_s)) Delta_s G[t][s] for s <= t
+        if (p.softplus) {
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const int s = s0 + j + e;
-          f[e] = s <= r ? g[j + e] * ex2_approx(a2 * (cum - sCum[s])) : 0.f;
+          for (int e = 0; e < 8; ++e) {
+            const int s = s0 + j + e;
+            f[e] = s <= r ? g[j + e] * ex2_approx(ac - sAS[s]) : 0.f;
+          }
+        } else {
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const int s = s0 + j + e;
+            f[e] = s <= r ? g[j + e] * ex2_approx(ac - sAS[s]) * sDelta[s] : 0.f;
+          }
         }
         const int sblk = (s0 + j) >> 6, piece = ((s0 + j) & 63) >> 3;
         *reinterpret_cast<uint4*>(smem + S::kSP + sblk * 16384 + r * 128 + ((piece ^ (r & 7)) << 4)) = pack16(f);
@@ -347,13 +351,13 @@ __global__ void __launch_bounds__(kSsdThreads, 1)
     tc_fence_before();
     __syncthreads();
 
-    // ---- 5. Y_diag = scores X_Delta ----
+    // ---- 5. Y_diag = scores X ----
     if (issuer) {
       tc_fence_after();
-      const uint32_t sSP = smem_u32(smem + S::kSP), sXD = smem_u32(smem + S::kXD);
+      const uint32_t sSP = smem_u32(smem + S::kSP), sX = smem_u32(smem + S::kX);
       for (int k = 0; k < 8; ++k) {
         const uint32_t o16 = (k >> 2) * 16384 + (k & 3) * 32, o8 = (k >> 2) * 8192 + (k & 3) * 32;
-        umma_bf16(tmem + kColYd, umma_desc_sw128(sSP + o16), umma_desc_sw128(sXD + o8), id64, k > 0);
+        umma_bf16(tmem + kColYd, umma_desc_sw128(sSP + o16), umma_desc_sw128(sX + o8), id64, k > 0);
       }
       umma_commit(bar_d);
       d_out = true;
