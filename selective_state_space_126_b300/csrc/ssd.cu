@@ -32,9 +32,10 @@
 // four warps per scheduler (rather than two) hide their latencies.  Per chunk:
 //   1. TMA: C_c and B_c ((L, N) rows of 128 B, 128B swizzle, two 64-column
 //      boxes each) and X_c ((P, L) rows, two 64-step boxes) -- each already
-//      the K-major operand layout of the MMAs below -- and the gate's z_c.
-//      B_c has its own barrier and the next chunk's B is loaded as soon as
-//      this one's is consumed (after G);
+//      the K-major operand layout of the MMAs below -- and the gate's z_c,
+//      on three barriers: the next chunk's B is loaded as soon as this one's
+//      is consumed (after G), its C and X once every MMA of this chunk is
+//      complete (they are read only by the MMAs), its z after the output;
 //   2. Delta, the inclusive prefix sum S (warp shuffles and one shared step),
 //      the weights w_s = exp(a (S_end - S_s)) Delta_s and the column terms
 //      a S_s log2(e) - log2(Delta_s) of the scores; threads write the incoming
@@ -45,10 +46,11 @@
 //      Y_off = C H_in are queued behind it (one commit each);
 //   4. threads read G (tcgen05.ld), apply the causal decay mask and the step
 //      factor, exp(a (S_t - S_s)) Delta_s, on the SFU and write the bf16
-//      scores (K = s); blocks above the diagonal are written as zeros;
+//      scores (K = s); blocks above the diagonal are written as zeros, and D
+//      is added on the diagonal so that Y_diag carries the skip term D x_t;
 //   5. MMA: Y_diag = scores X;
 //   6. threads update H = exp(a S_end) H + H_chunk and emit
-//      y = (Y_diag + exp(a S_t) Y_off + D x) silu(z), coalesced along t.
+//      y = (Y_diag + exp(a S_t) Y_off) silu(z), coalesced along t.
 // Other shapes and fp32 I/O take ssd_generic_kernel (one warp per channel, the
 // recurrence itself).
 #include <cstdio>
@@ -88,8 +90,8 @@ struct SsdSmem {
   static constexpr int kW = kCum + 512;        // float [128]
   static constexpr int kAS = kW + 512;         // float [128]: a S_s log2(e), less log2(Delta_s) under softplus
   static constexpr int kWarp = kAS + 512;      // float [4] warp totals of the prefix sum
-  static constexpr int kBar = kWarp + 16;      // 5 mbarriers: TMA (C, X, z), TMA (B), G, (H_chunk, Y_off), Y_diag
-  static constexpr int kTaddr = kBar + 40;
+  static constexpr int kBar = kWarp + 16;      // 6 mbarriers: TMA (C, X), TMA (B), G, (H_chunk, Y_off), Y_diag, TMA (z)
+  static constexpr int kTaddr = kBar + 48;
   static constexpr int kBytes = kTaddr + 16;
   static constexpr int kAlloc = kBytes + 1024;
 };
@@ -137,7 +139,7 @@ __global__ void __launch_bounds__(kSsdThreads, 1)
   float* sAS = reinterpret_cast<float*>(smem + S::kAS);
   float* sWarp = reinterpret_cast<float*>(smem + S::kWarp);
   const uint32_t bar_tma = smem_u32(smem + S::kBar), bar_tmab = bar_tma + 8, bar_g = bar_tma + 16,
-                 bar_ho = bar_tma + 24, bar_d = bar_tma + 32;
+                 bar_ho = bar_tma + 24, bar_d = bar_tma + 32, bar_tmaz = bar_tma + 40;
   uint32_t* taddr_s = reinterpret_cast<uint32_t*>(smem + S::kTaddr);
 
   // thread = (row r, quarter cq): row r is time step r of the chunk and state index r; the quarter
@@ -153,7 +155,7 @@ __global__ void __launch_bounds__(kSsdThreads, 1)
   const float Dh = p.Dskip ? p.Dskip[h] : 0.f;
 
   if (tid == 0) {
-    for (int i = 0; i < 5; ++i) mbar_init(bar_tma + 8 * i, 1);
+    for (int i = 0; i < 6; ++i) mbar_init(bar_tma + 8 * i, 1);
     mbar_init_fence();
   }
   if (warp == 0) tmem_alloc(smem_u32(taddr_s), kTmemCols);
@@ -172,17 +174,26 @@ __global__ void __launch_bounds__(kSsdThreads, 1)
   // the issuing thread tracks the copies (chunk index, or -1) and MMA groups in flight for a bounded
   // drain on failure
   const bool issuer = tid == kIssuer;
-  int cxz_pend = -1, b_pend = -1;
+  int cx_pend = -1, z_pend = -1, b_pend = -1;
   bool g_out = false, ho_out = false, d_out = false;
-  auto issue_cxz = [&](int c) {   // C, X and z of chunk c
+  // C and X of chunk c: read only by the MMAs, so the next chunk's can land as soon as Y_diag (the
+  // last MMA to read them) is complete
+  auto issue_cx = [&](int c) {
     const int t0 = c * kQ;
-    mbar_expect_tx(bar_tma, 2 * 16384 + 2 * 8192 + (p.z ? 2 * 8192 : 0));
+    mbar_expect_tx(bar_tma, 2 * 16384 + 2 * 8192);
     for (int j = 0; j < 2; ++j) {
       tma_load(smem_u32(smem + S::kC + j * 16384), &tm.C, 64 * j, t0, (int)b, true, bar_tma);
       tma_load(smem_u32(smem + S::kX + j * 8192), &tm.x, t0 + 64 * j, (int)(h * kP), (int)b, true, bar_tma);
-      if (p.z) tma_load(smem_u32(smem + S::kZ + j * 8192), &tm.z, t0 + 64 * j, (int)(h * kP), (int)b, true, bar_tma);
     }
-    cxz_pend = c;
+    cx_pend = c;
+  };
+  // z of chunk c: read by the threads in the output phase, so the next chunk's lands after it
+  auto issue_z = [&](int c) {
+    if (!p.z) return;
+    mbar_expect_tx(bar_tmaz, 2 * 8192);
+    for (int j = 0; j < 2; ++j)
+      tma_load(smem_u32(smem + S::kZ + j * 8192), &tm.z, c * kQ + 64 * j, (int)(h * kP), (int)b, true, bar_tmaz);
+    z_pend = c;
   };
   auto issue_b = [&](int c) {     // B of chunk c (its buffer frees up earlier than the others)
     mbar_expect_tx(bar_tmab, 2 * 16384);
@@ -192,18 +203,19 @@ __global__ void __launch_bounds__(kSsdThreads, 1)
   };
   if (issuer && nchunks > 0) {
     issue_b(0);
-    issue_cxz(0);
+    issue_cx(0);
+    issue_z(0);
   }
 
   const uint32_t id128 = umma_idesc_bf16(128, 128), id64 = umma_idesc_bf16(128, 64);
-  // raw delta of step t (this row's step of a chunk), loaded one chunk ahead
-  auto load_delta = [&](int64_t t) -> float {
-    if (cq != 0 || t >= p.L) return 0.f;
-    const int64_t o = b * p.sd[0] + h * p.sd[1] + t;
-    return p.io == SSM_BF16 ? __bfloat162float(__ldg(static_cast<const __nv_bfloat16*>(p.delta) + o))
-                            : __ldg(static_cast<const float*>(p.delta) + o);
+  // raw delta of step t (this row's step of a chunk; bf16 bits, this kernel's I/O type), loaded one
+  // chunk ahead and widened only where it is used, so that no instruction of the issuing chunk waits
+  // for the load
+  auto load_delta = [&](int64_t t) -> unsigned short {
+    if (cq != 0 || t >= p.L) return 0;
+    return __ldg(static_cast<const unsigned short*>(p.delta) + b * p.sd[0] + h * p.sd[1] + t);
   };
-  float dnext = nchunks > 0 ? load_delta(r) : 0.f;
+  unsigned short dnext = nchunks > 0 ? load_delta(r) : 0;
   bool failed = false;
   int c = 0;
   for (; c < nchunks; ++c) {
@@ -213,7 +225,7 @@ __global__ void __launch_bounds__(kSsdThreads, 1)
 
     // ---- 2. Delta, prefix sum S (rows, half 0), weights; the incoming state as an operand ----
     float dt = 0.f;
-    if (cq == 0 && r < valid) dt = delta_of<false>(dnext, bias, p.softplus);
+    if (cq == 0 && r < valid) dt = delta_of<false>(__uint_as_float((uint32_t)dnext << 16), bias, p.softplus);
     dnext = load_delta(t0 + kQ + r);   // the next chunk's, in flight during this one
     float cum = dt;
 #pragma unroll
@@ -283,7 +295,7 @@ __global__ void __launch_bounds__(kSsdThreads, 1)
     // ---- C, X and z of this chunk ----
     const bool ok_t = ok_b && mbar_wait(bar_tma, par);
     if (!ok_t) record_status(p.status, SSM_ERR_TIMEOUT);
-    if (issuer && ok_t) cxz_pend = -1;
+    if (issuer && ok_t) cx_pend = -1;
     fence_async_smem();
     tc_fence_before();
     if (__syncthreads_or(!ok_t)) { failed = true; break; }
@@ -346,6 +358,11 @@ __global__ void __launch_bounds__(kSsdThreads, 1)
         const int sblk = (s0 + j) >> 6, piece = ((s0 + j) & 63) >> 3;
         *reinterpret_cast<uint4*>(smem + S::kSP + sblk * 16384 + r * 128 + ((piece ^ (r & 7)) << 4)) = pack16(f);
       }
+      if (s0 == (r & ~31)) {   // the diagonal block: D x_t enters Y_diag through scores[t][t]
+        __nv_bfloat16* dg =
+            reinterpret_cast<__nv_bfloat16*>(smem + S::kSP + (r >> 6) * 16384 + sw128_offset(r, r & 63));
+        *dg = __float2bfloat16_rn(__bfloat162float(*dg) + Dh);
+      }
     }
     fence_async_smem();
     tc_fence_before();
@@ -377,7 +394,12 @@ __global__ void __launch_bounds__(kSsdThreads, 1)
     const bool ok_d = mbar_wait(bar_d, par);
     if (!ok_d) record_status(p.status, SSM_ERR_TIMEOUT);
     tc_fence_after();
-    if (ok_ho && ok_d) {
+    // every MMA of this chunk is complete: C and X of the next chunk can land now
+    if (issuer && ok_ho && ok_d && c + 1 < nchunks) issue_cx(c + 1);
+    const bool ok_z = !p.z || mbar_wait(bar_tmaz, par);
+    if (!ok_z) record_status(p.status, SSM_ERR_TIMEOUT);
+    if (issuer && p.z && ok_z) z_pend = -1;
+    if (ok_ho && ok_d && ok_z) {
       const int64_t t = t0 + r;
       float yd[kPQ], yo[kPQ];
       tmem_ld(tmem + lane_off + kColYd + (uint32_t)(kPQ * cq), yd);
@@ -388,24 +410,24 @@ __global__ void __launch_bounds__(kSsdThreads, 1)
           const int q = kPQ * cq + j;
           const int64_t d = h * kP + q;
           const int zx = (r >> 6) * 8192 + sw128_offset(q, r & 63);
-          const float xv = __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(smem + S::kX + zx));
-          float v = fmaf(et, yo[j], yd[j]) + Dh * xv;
+          float v = fmaf(et, yo[j], yd[j]);
           if (p.z) v *= silu_tanh(__bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(smem + S::kZ + zx)));
           static_cast<__nv_bfloat16*>(p.y)[b * p.sy[0] + d * p.sy[1] + t] = __float2bfloat16_rn(v);
         }
       }
     }
     tc_fence_before();
-    if (__syncthreads_or(!(ok_ho && ok_d))) { failed = true; break; }
+    if (__syncthreads_or(!(ok_ho && ok_d && ok_z))) { failed = true; break; }
     ho_out = d_out = false;
-    if (issuer && c + 1 < nchunks) issue_cxz(c + 1);
+    if (issuer && c + 1 < nchunks) issue_z(c + 1);
   }
 
   if (failed) {
     // let every copy and MMA this CTA started finish (bounded waits) before its tensor memory is freed
     if (issuer) {
       if (b_pend >= 0) mbar_wait(bar_tmab, (uint32_t)b_pend & 1u);
-      if (cxz_pend >= 0) mbar_wait(bar_tma, (uint32_t)cxz_pend & 1u);
+      if (cx_pend >= 0) mbar_wait(bar_tma, (uint32_t)cx_pend & 1u);
+      if (z_pend >= 0) mbar_wait(bar_tmaz, (uint32_t)z_pend & 1u);
       const uint32_t par = (uint32_t)c & 1u;
       if (g_out) mbar_wait(bar_g, par);
       if (ho_out) mbar_wait(bar_ho, par);
