@@ -88,7 +88,7 @@ struct SsdSmem {
   static constexpr int kDelta = kZ + 16384;    // float [128]
   static constexpr int kCum = kDelta + 512;    // float [128]
   static constexpr int kW = kCum + 512;        // float [128]
-  static constexpr int kAS = kW + 512;         // float [128]: a S_s log2(e), less log2(Delta_s) under softplus
+  static constexpr int kAS = kW + 512;         // float [128]: -a S_s log2(e), plus log2(Delta_s) under softplus
   static constexpr int kWarp = kAS + 512;      // float [4] warp totals of the prefix sum
   static constexpr int kBar = kWarp + 16;      // 6 mbarriers: TMA (C, X), TMA (B), G, (H_chunk, Y_off), Y_diag, TMA (z)
   static constexpr int kTaddr = kBar + 48;
@@ -251,7 +251,7 @@ __global__ void __launch_bounds__(kSsdThreads, 1)
     if (cq == 0) {
       sW[r] = ex2_approx(a2 * (cum_end - cum)) * sDelta[r];
       // the score's column factor Delta_s enters the exponent when it is positive (softplus)
-      sAS[r] = p.softplus ? a2 * cum - __log2f(sDelta[r]) : a2 * cum;
+      sAS[r] = p.softplus ? __log2f(sDelta[r]) - a2 * cum : -a2 * cum;
     }
     const float et = ex2_approx(a2 * cum);   // exp(a S_t) of row t = r
 
@@ -337,28 +337,31 @@ __global__ void __launch_bounds__(kSsdThreads, 1)
       }
       float g[32];
       tmem_ld32(tmem + lane_off + kColG + (uint32_t)s0, g);
-      const float ac = a2 * cum;
+      // scores[t][s] = exp(a (S_t - S_s)) Delta_s G[t][s] for s <= t, two columns per packed operation;
+      // only the diagonal block has entries above the diagonal to clear
+      const float2 ac2 = make_float2(a2 * cum, a2 * cum);
+      const bool diag = s0 == (r & ~31);
 #pragma unroll
       for (int j = 0; j < 32; j += 8) {
         float f[8];
-        // scores[t][s] = exp(a (S_t - S_s)) Delta_s G[t][s] for s <= t
-        if (p.softplus) {
 #pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            const int s = s0 + j + e;
-            f[e] = s <= r ? g[j + e] * ex2_approx(ac - sAS[s]) : 0.f;
-          }
-        } else {
+        for (int e = 0; e < 8; e += 2) {
+          const int s = s0 + j + e;
+          const float2 x = __fadd2_rn(ac2, *reinterpret_cast<const float2*>(sAS + s));
+          float2 v = __fmul2_rn(make_float2(g[j + e], g[j + e + 1]), make_float2(ex2_approx(x.x), ex2_approx(x.y)));
+          if (!p.softplus) v = __fmul2_rn(v, *reinterpret_cast<const float2*>(sDelta + s));
+          f[e] = v.x;
+          f[e + 1] = v.y;
+        }
+        if (diag) {
 #pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            const int s = s0 + j + e;
-            f[e] = s <= r ? g[j + e] * ex2_approx(ac - sAS[s]) * sDelta[s] : 0.f;
-          }
+          for (int e = 0; e < 8; ++e)
+            if (s0 + j + e > r) f[e] = 0.f;
         }
         const int sblk = (s0 + j) >> 6, piece = ((s0 + j) & 63) >> 3;
         *reinterpret_cast<uint4*>(smem + S::kSP + sblk * 16384 + r * 128 + ((piece ^ (r & 7)) << 4)) = pack16(f);
       }
-      if (s0 == (r & ~31)) {   // the diagonal block: D x_t enters Y_diag through scores[t][t]
+      if (diag) {   // D x_t enters Y_diag through scores[t][t]
         __nv_bfloat16* dg =
             reinterpret_cast<__nv_bfloat16*>(smem + S::kSP + (r >> 6) * 16384 + sw128_offset(r, r & 63));
         *dg = __float2bfloat16_rn(__bfloat162float(*dg) + Dh);
