@@ -72,7 +72,8 @@ def _bind(lib):
     lib.oracle_state_update.argtypes = [i64, i64, i64, dp] + [dp] * 8 + [
         ctypes.c_int, ctypes.c_int, dp]
     lib.oracle_selective_scan_bwd.restype = ctypes.c_int
-    lib.oracle_selective_scan_bwd.argtypes = [i64, i64, i64, i64] + [dp] * 9 + [ctypes.c_int] + [dp] * 11
+    lib.oracle_selective_scan_bwd.argtypes = [i64, i64, i64, i64] + [dp] * 9 + [ctypes.c_int] + [dp] * 11 + \
+        [ctypes.c_int]
     lib.oracle_causal_conv1d.restype = ctypes.c_int
     lib.oracle_causal_conv1d.argtypes = [i64, i64, i64, i64] + [dp] * 4 + [ctypes.c_int, dp]
     lib.oracle_selective_scan_complex.restype = ctypes.c_int
@@ -255,9 +256,9 @@ def causal_conv1d(x, w, bias=None, x_hist=None, silu=True, lib=None):
 
 
 def selective_scan_bwd(u, delta, A, Bm, Cm, dy, Dskip=None, z=None, delta_bias=None, h0=None,
-                       delta_softplus=True, dh_last=None, lib=None):
-    """fp64 gradients of the (Euler) selective scan for an upstream gradient dy (B, D, L) of y and,
-    optionally, dh_last (B, D, N) of the final state.
+                       delta_softplus=True, dh_last=None, disc=DISC_EULER, lib=None):
+    """fp64 gradients of the selective scan (Euler or exact-ZOH input term, ``disc``) for an upstream
+    gradient dy (B, D, L) of y and, optionally, dh_last (B, D, N) of the final state.
 
     Returns a dict with du, ddelta (B, D, L); dz (B, D, L) if z is given; dBm, dCm shaped like the
     given Bm, Cm (a leading batch of 1 gets the sum over the batch); dA (D, N); dDskip (D,) if Dskip is
@@ -288,7 +289,7 @@ def selective_scan_bwd(u, delta, A, Bm, Cm, dy, Dskip=None, z=None, delta_bias=N
                                        int(bool(delta_softplus)), _ptr(dy), _ptr(dh_last),
                                        _ptr(out["du"]), _ptr(out["ddelta"]), _ptr(out["dz"]), _ptr(out["dBm"]),
                                        _ptr(out["dCm"]), _ptr(out["dA"]), _ptr(out["dDskip"]),
-                                       _ptr(out["ddelta_bias"]), _ptr(out["dh0"]))
+                                       _ptr(out["ddelta_bias"]), _ptr(out["dh0"]), int(disc))
     if rc != 0:
         raise RuntimeError("oracle_selective_scan_bwd failed")
     if bc_shared:

@@ -455,7 +455,25 @@ int oracle_causal_conv1d(int64_t B, int64_t D, int64_t L, int64_t W, const doubl
 }
 
 /*
- * Reverse-mode derivative of the scan above (Euler input term), for training
+ * d/dA of the exact-ZOH input coefficient g = (exp(Delta A) - 1) / A:
+ *   dg/dA = (Delta e^{Delta A} A - (e^{Delta A} - 1)) / A^2 = Delta^2 psi(Delta A),
+ *   psi(x) = (x e^x - (e^x - 1)) / x^2 = sum_{k>=1} k x^{k-1} / (k+1)!  (psi(0) = 1/2).
+ * The closed form cancels for small |x|, so below |x| = 1e-3 the series is summed
+ * (the dropped terms are below 1e-13 relative there).
+ */
+static double zoh_coef_dA(double dt, double a_cont) {
+    const double x = dt * a_cont;
+    double psi;
+    if (fabs(x) < 1e-3) {
+        psi = 0.5 + x / 3.0 + x * x / 8.0 + x * x * x / 30.0;
+    } else {
+        psi = (x * exp(x) - expm1(x)) / (x * x);
+    }
+    return dt * dt * psi;
+}
+
+/*
+ * Reverse-mode derivative of the scan above (Euler or exact-ZOH input term), for training
  * with recomputation ("gitcode", section 3.3.2: the backward pass recomputes
  * the intermediate states instead of storing them; the oracle, being slow and
  * plain, simply keeps every state of one channel).  Given the upstream
@@ -463,7 +481,9 @@ int oracle_causal_conv1d(int64_t B, int64_t D, int64_t L, int64_t W, const doubl
  * gradient of every input.  Written out from the chain rule on
  *   Delta_t = softplus(s_t), s_t = delta_t + bias       dDelta/ds = sigmoid(s_t)
  *   a_t[n]  = exp(Delta_t A[n])                          da/dDelta = a A, da/dA = a Delta
- *   h_t[n]  = a_t[n] h_{t-1}[n] + Delta_t B_t[n] u_t
+ *   h_t[n]  = a_t[n] h_{t-1}[n] + g_t[n] B_t[n] u_t
+ *   g = Delta (Euler: dg/dDelta = 1, dg/dA = 0) or g = (a - 1) / A (exact ZOH,
+ *   "docs.ifdog.com", section "Discretisation": dg/dDelta = a, dg/dA = Delta^2 psi)
  *   p_t     = sum_n C_t[n] h_t[n] + D u_t,   y_t = p_t silu(z_t)
  *   silu'(z) = sigmoid(z) (1 + z (1 - sigmoid(z)))
  * with the adjoint lambda_t[n] = dL/dh_t[n] = (dy_t silu(z_t)) C_t[n]
@@ -480,10 +500,12 @@ int oracle_selective_scan_bwd(int64_t B, int64_t D, int64_t L, int64_t N,
                               const double *h0, int delta_softplus,
                               const double *dy, const double *dh_last,
                               double *du, double *ddelta, double *dz, double *dBm, double *dCm,
-                              double *dA, double *dDskip, double *ddelta_bias, double *dh0) {
+                              double *dA, double *dDskip, double *ddelta_bias, double *dh0, int disc) {
     if (B < 0 || D < 0 || L < 0 || N < 0) return -1;
     if (!u || !delta || !Bm || !Cm || !A || !dy || !du || !ddelta || !dBm || !dCm || !dA || !ddelta_bias)
         return -1;
+    if (disc != ORACLE_DISC_EULER && disc != ORACLE_DISC_ZOH) return -1;
+    const int zoh = disc == ORACLE_DISC_ZOH;
     if (z && !dz) return -1;
     if (Dskip && !dDskip) return -1;
     memset(dBm, 0, sizeof(double) * (size_t)(B * N * L));
@@ -510,7 +532,7 @@ int oracle_selective_scan_bwd(int64_t B, int64_t D, int64_t L, int64_t N,
                 dts[t] = discretisation_step(dl[t], bias, delta_softplus);
                 double acc = 0.0;
                 for (int64_t n = 0; n < N; ++n) {
-                    double hn = exp(dts[t] * Ad[n]) * hs[t * N + n] + dts[t] * Bb[n * L + t] * uc[t];
+                    double hn = exp(dts[t] * Ad[n]) * hs[t * N + n] + input_term(dts[t], Ad[n], Bb[n * L + t], uc[t], disc);
                     hs[(t + 1) * N + n] = hn;
                     acc += Cb[n * L + t] * hn;
                 }
@@ -532,11 +554,16 @@ int oracle_selective_scan_bwd(int64_t B, int64_t D, int64_t L, int64_t N,
                     const double lt = lam[n] + yt * Cb[n * L + t];   /* lambda_t */
                     const double at = exp(dts[t] * Ad[n]);   /* Abar_t[n] */
                     const double hprev = hs[t * N + n];
+                    const double bu = Bb[n * L + t] * uc[t];
+                    /* the input coefficient g and its partial derivatives */
+                    const double g = zoh ? (Ad[n] == 0.0 ? dts[t] : expm1(dts[t] * Ad[n]) / Ad[n]) : dts[t];
+                    const double dg_dDelta = zoh ? at : 1.0;
+                    const double dg_dA = zoh ? zoh_coef_dA(dts[t], Ad[n]) : 0.0;
                     dCm[b * N * L + n * L + t] += yt * hs[(t + 1) * N + n];
-                    dA[d * N + n] += lt * hprev * at * dts[t];
-                    dDelta += lt * (hprev * at * Ad[n] + Bb[n * L + t] * uc[t]);
-                    dBm[b * N * L + n * L + t] += lt * dts[t] * uc[t];
-                    du_acc += lt * dts[t] * Bb[n * L + t];
+                    dA[d * N + n] += lt * (hprev * at * dts[t] + bu * dg_dA);
+                    dDelta += lt * (hprev * at * Ad[n] + bu * dg_dDelta);
+                    dBm[b * N * L + n * L + t] += lt * g * uc[t];
+                    du_acc += lt * g * Bb[n * L + t];
                     lam[n] = lt * at;                               /* carried to step t-1 */
                 }
                 du[c * L + t] = du_acc;

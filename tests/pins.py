@@ -314,8 +314,9 @@ def pin_zoh_to_euler_small_delta(lib):
 # scalar objective sum(dy * y) + sum(dh_last * h_last), element by element.
 # ---------------------------------------------------------------------------
 
-def _fd_check_bwd(lib, gate, dskip, bias, softplus, h0, dh_last, bc_shared=False, seed=21):
+def _fd_check_bwd(lib, gate, dskip, bias, softplus, h0, dh_last, bc_shared=False, seed=21, disc=None):
     rng = np.random.default_rng(seed)
+    disc = oracle.DISC_EULER if disc is None else disc
     Bsz, D, L, N = 2, 3, 7, 4
     p = dict(u=rng.standard_normal((Bsz, D, L)), delta=rng.standard_normal((Bsz, D, L)) * 0.7,
              z=rng.standard_normal((Bsz, D, L)) if gate else None,
@@ -324,13 +325,18 @@ def _fd_check_bwd(lib, gate, dskip, bias, softplus, h0, dh_last, bc_shared=False
              A=-rng.uniform(0.3, 2.0, (D, N)), Dskip=rng.standard_normal(D) if dskip else None,
              delta_bias=rng.standard_normal(D) * 0.5 if bias else None,
              h0=rng.standard_normal((Bsz, D, N)) if h0 else None)
+    if disc == oracle.DISC_ZOH:
+        # one state with A = 0 and one with |A| = 1e-4: the exact-ZOH coefficient's A-derivative
+        # takes its small-|Delta A| series there
+        p["A"][:, 1] = 0.0
+        p["A"][:, 2] = rng.choice([-1e-4, 1e-4], D)
     dy = rng.standard_normal((Bsz, D, L))
     dhl = rng.standard_normal((Bsz, D, N)) if dh_last else None
 
     def objective(q):
         y, hl = oracle.selective_scan(q["u"], q["delta"], q["A"], q["Bm"], q["Cm"], Dskip=q["Dskip"], z=q["z"],
                                       delta_bias=q["delta_bias"], h0=q["h0"], delta_softplus=softplus,
-                                      return_last_state=True, nthreads=1, lib=lib)
+                                      disc=disc, return_last_state=True, nthreads=1, lib=lib)
         v = float(np.sum(dy * y))
         if dhl is not None:
             v += float(np.sum(dhl * hl))
@@ -338,7 +344,7 @@ def _fd_check_bwd(lib, gate, dskip, bias, softplus, h0, dh_last, bc_shared=False
 
     g = oracle.selective_scan_bwd(p["u"], p["delta"], p["A"], p["Bm"], p["Cm"], dy, Dskip=p["Dskip"], z=p["z"],
                                   delta_bias=p["delta_bias"], h0=p["h0"], delta_softplus=softplus, dh_last=dhl,
-                                  lib=lib)
+                                  disc=disc, lib=lib)
     names = {"u": "du", "delta": "ddelta", "z": "dz", "Bm": "dBm", "Cm": "dCm", "A": "dA", "Dskip": "dDskip",
              "delta_bias": "ddelta_bias", "h0": "dh0"}
     for key, gname in names.items():
@@ -375,7 +381,20 @@ def pin_bwd_finite_differences_shared_bc(lib):
                   seed=23)
 
 
-BWD_PINS = [pin_bwd_finite_differences_full, pin_bwd_finite_differences_bare, pin_bwd_finite_differences_shared_bc]
+def pin_bwd_finite_differences_zoh(lib):
+    """Exact-ZOH input term, every option on; includes states with A = 0 and |A| = 1e-4."""
+    _fd_check_bwd(lib, gate=True, dskip=True, bias=True, softplus=True, h0=True, dh_last=True, seed=24,
+                  disc=oracle.DISC_ZOH)
+
+
+def pin_bwd_finite_differences_zoh_bare(lib):
+    """Exact-ZOH input term, every option off."""
+    _fd_check_bwd(lib, gate=False, dskip=False, bias=False, softplus=False, h0=False, dh_last=False, seed=25,
+                  disc=oracle.DISC_ZOH)
+
+
+BWD_PINS = [pin_bwd_finite_differences_full, pin_bwd_finite_differences_bare, pin_bwd_finite_differences_shared_bc,
+            pin_bwd_finite_differences_zoh, pin_bwd_finite_differences_zoh_bare]
 
 
 # ---------------------------------------------------------------------------

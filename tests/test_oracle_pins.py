@@ -56,14 +56,21 @@ MUTANTS = [
     ("out[row * L + t] = use_silu ? v * sigmoid(v) : v;", "out[row * L + t] = use_silu ? sigmoid(v) : v;"),
     # the backward pass
     ("lam[n] = lt * at;", "lam[n] = lt;"),
-    ("dDelta += lt * (hprev * at * Ad[n] + Bb[n * L + t] * uc[t]);", "dDelta += lt * hprev * at * Ad[n];"),
+    ("dDelta += lt * (hprev * at * Ad[n] + bu * dg_dDelta);", "dDelta += lt * hprev * at * Ad[n];"),
     ("dz[c * L + t] = dyc[t] * pre[t] * sg * (1.0 + zc[t] * (1.0 - sg));", "dz[c * L + t] = dyc[t] * pre[t] * sg;"),
-    ("dA[d * N + n] += lt * hprev * at * dts[t];", "dA[d * N + n] += lt * hprev * at;"),
+    ("dA[d * N + n] += lt * (hprev * at * dts[t] + bu * dg_dA);", "dA[d * N + n] += lt * (hprev * at + bu * dg_dA);"),
     ("if (dDskip) dDskip[d] += yt * uc[t];", "if (dDskip) dDskip[d] += dyc[t] * uc[t];"),
     ("dCm[b * N * L + n * L + t] += yt * hs[(t + 1) * N + n];", "dCm[b * N * L + n * L + t] += yt * hs[t * N + n];"),
     ("const double dd = delta_softplus ? dDelta * sigmoid(dl[t] + bias) : dDelta;",
      "const double dd = dDelta;"),
-    ("du_acc += lt * dts[t] * Bb[n * L + t];", "du_acc += lt * Bb[n * L + t];"),
+    ("du_acc += lt * g * Bb[n * L + t];", "du_acc += lt * Bb[n * L + t];"),
+    # the backward pass with the exact-ZOH input term
+    ("const double dg_dDelta = zoh ? at : 1.0;", "const double dg_dDelta = 1.0;"),
+    ("const double dg_dA = zoh ? zoh_coef_dA(dts[t], Ad[n]) : 0.0;", "const double dg_dA = 0.0;"),
+    ("psi = 0.5 + x / 3.0 + x * x / 8.0 + x * x * x / 30.0;", "psi = 0.5 + x / 2.0 + x * x / 8.0 + x * x * x / 30.0;"),
+    ("psi = (x * exp(x) - expm1(x)) / (x * x);", "psi = (x * exp(x) - expm1(x)) / x;"),
+    ("const double g = zoh ? (Ad[n] == 0.0 ? dts[t] : expm1(dts[t] * Ad[n]) / Ad[n]) : dts[t];",
+     "const double g = dts[t];"),
     # the complex (S4D-Lin) scan
     ("double v = creal(acc) + Dd * ut;", "double v = cimag(acc) + Dd * ut;"),
     ("const double complex abar = cexp(dt * a);", "const double complex abar = cexp(dt * conj(a));"),
