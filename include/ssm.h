@@ -184,8 +184,12 @@ typedef struct ssm_step_args {
  *   dh0           : (batch, dim, dstate)   fp32, nullable
  * dA, dB, dC, dDskip and ddelta_bias are sums over the batch (and time, and
  * for dB/dC over the channels): the call overwrites them (zeroes, then adds
- * with atomics, so the order of the fp32 sums is not fixed).  Limits:
- * 1 <= dstate <= 16; the gradient outputs must not overlap each other or any
+ * with atomics, so the order of the fp32 sums is not fixed).  Both input
+ * terms of fwd.discretization are differentiated: Euler (g = Delta) and the
+ * exact zero-order hold (g = (exp(Delta A) - 1) / A, whose derivatives are
+ * dg/dDelta = exp(Delta A) and dg/dA = Delta^2 psi(Delta A) with
+ * psi(x) = (x e^x - (e^x - 1)) / x^2).  Limits: 1 <= dstate <= 16; a real A
+ * (fwd.A_imag NULL); the gradient outputs must not overlap each other or any
  * input.
  */
 #define SSM_BWD_SEGMENT 8

@@ -399,9 +399,9 @@ def make_bwd_args(fwd: ScanArgs, dy, grads: dict, dh_last=None) -> BwdArgs:
 
 
 def ssm_scan_bwd(u, delta, A, Bm, Cm, dy, Dskip=None, z=None, delta_bias=None, h0=None, delta_softplus=True,
-                 dh_last=None, return_dh0=True, workspace=None, stream=None):
-    """Gradients of ssm_scan_fwd for an upstream gradient ``dy`` (B, D, L) of y (and ``dh_last``
-    (B, D, N) fp32 of the final state, optional).
+                 dh_last=None, return_dh0=True, workspace=None, stream=None, discretization=SSM_DISC_EULER):
+    """Gradients of ssm_scan_fwd (Euler or exact-ZOH input term, ``discretization``) for an upstream
+    gradient ``dy`` (B, D, L) of y (and ``dh_last`` (B, D, N) fp32 of the final state, optional).
 
     Returns a dict: du, ddelta (and dz if z is given) in the I/O dtype, (B, D, L); dA (D, N); dB, dC
     fp32 shaped like Bm, Cm ((N, L) when they are shared across the batch); dDskip (D,) if Dskip is
@@ -434,7 +434,8 @@ def ssm_scan_bwd(u, delta, A, Bm, Cm, dy, Dskip=None, z=None, delta_bias=None, h
         g["ddelta_bias"] = torch.empty(D, dtype=torch.float32, device=dev)
     if return_dh0:
         g["dh0"] = torch.empty((Bsz, D, N), dtype=torch.float32, device=dev)
-    fwd = make_scan_args(u, delta, A, Bm, Cm, None, Dskip, z, delta_bias, h0, None, delta_softplus)
+    fwd = make_scan_args(u, delta, A, Bm, Cm, None, Dskip, z, delta_bias, h0, None, delta_softplus,
+                         discretization=discretization)
     args = make_bwd_args(fwd, dy, g, dh_last)
     need = ctypes.c_size_t(0)
     _check(lib.ssm_scan_bwd_workspace_size(ctypes.byref(args), ctypes.byref(need)))

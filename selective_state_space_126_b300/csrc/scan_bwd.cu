@@ -3,7 +3,11 @@
 // What it computes: the reverse-mode derivative of the forward recurrence
 // (see scan_tiled.cu) through the chain rule,
 //   Delta_t = softplus(s_t), s_t = delta_t + bias      dDelta/ds = sigmoid(s_t)
-//   Abar_t[n] = exp(Delta_t A[n]),  h_t = Abar_t h_{t-1} + Delta_t B_t u_t
+//   Abar_t[n] = exp(Delta_t A[n]),  h_t = Abar_t h_{t-1} + g_t B_t u_t
+// with the input coefficient g = Delta (Euler) or the exact zero-order hold
+// g = (Abar - 1) / A ("Mamba and state space models", docs.ifdog.com, section
+// "Discretisation"), whose partial derivatives are dg/dDelta = Abar and
+// dg/dA = Delta^2 psi(Delta A), psi(x) = (x e^x - (e^x - 1)) / x^2,
 //   p_t = sum_n C_t[n] h_t[n] + D u_t,  y_t = p_t silu(z_t)
 // with the adjoint lambda_t[n] = dL/dh_t[n] = (dy_t silu(z_t)) C_t[n]
 // + Abar_{t+1}[n] lambda_{t+1}[n], run backwards in time.  As in section 3.3.2
@@ -42,6 +46,28 @@ namespace ssm {
 namespace {
 
 constexpr int SEG = SSM_BWD_SEGMENT;   // steps per checkpoint
+
+// Delta^2 psi(x) for x = Delta A and a = e^x: the A-derivative of the exact-ZOH coefficient.
+// psi(x) = sum_{k>=1} k x^(k-1) / (k+1)! = 1/2 + x/3 + x^2/8 + x^3/30 + x^4/144 + x^5/840 + x^6/5760 + ...
+// is summed below |x| = 1/4 (the next term is below 3e-9 relative there), where the closed form
+// cancels; above it the closed form loses at most a few bits of the fp32 mantissa.
+template <bool PRECISE>
+__device__ __forceinline__ float zoh_dg_dA(float dt, float x, float a) {
+  float psi;
+  if (fabsf(x) < 0.25f) {
+    psi = 1.7361111111111111e-04f;                 // 1/5760
+    psi = fmaf(psi, x, 1.1904761904761905e-03f);   // 1/840
+    psi = fmaf(psi, x, 6.9444444444444444e-03f);   // 1/144
+    psi = fmaf(psi, x, 3.3333333333333333e-02f);   // 1/30
+    psi = fmaf(psi, x, 0.125f);                    // 1/8
+    psi = fmaf(psi, x, 3.3333333333333333e-01f);   // 1/3
+    psi = fmaf(psi, x, 0.5f);
+  } else {
+    const float num = fmaf(x, a, 1.f - a);
+    psi = PRECISE ? num / (x * x) : __fdividef(num, x * x);
+  }
+  return dt * dt * psi;
+}
 
 template <bool PRECISE>
 __device__ __forceinline__ float sigmoid_f(float v) {
@@ -141,7 +167,7 @@ __device__ __forceinline__ float2 f2(float v) { return make_float2(v, v); }
 // (lanes c and c + 16), each lane holding 8 of the channel's states as four
 // f32x2 pairs.  Sums over the states (the C contraction, dDelta, du) take one
 // shuffle between the two lanes of a channel.
-template <typename IO, bool PRECISE>
+template <typename IO, bool PRECISE, bool ZOH>
 __global__ void __launch_bounds__(32) scan_bwd_kernel(const BwdProblem p) {
   constexpr int CHW = 16;                            // channels per warp
   __shared__ float4 hist[(SEG + 1) * 2 * 32];        // [row][half of the lane's 8 states][lane]
@@ -158,7 +184,7 @@ __global__ void __launch_bounds__(32) scan_bwd_kernel(const BwdProblem p) {
   const int64_t L = f.L;
   const int64_t c = b * f.D + (valid ? d : 0);
 
-  float2 A2[4], h[4];
+  float2 A2[4], h[4], Ai[4];   // Ai: 1 / A, for the exact-ZOH coefficient
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
     float av[2], hv[2];
@@ -169,6 +195,8 @@ __global__ void __launch_bounds__(32) scan_bwd_kernel(const BwdProblem p) {
       hv[e] = (valid && n < N && f.h0) ? f.h0[b * f.sh0[0] + d * f.sh0[1] + n * f.sh0[2]] : 0.f;
     }
     A2[q] = make_float2(av[0], av[1]);
+    // infinite at A = 0, where the coefficient takes its series
+    Ai[q] = ZOH ? make_float2(kLog2e / av[0], kLog2e / av[1]) : make_float2(0.f, 0.f);
     h[q] = make_float2(hv[0], hv[1]);
   }
   const float bias = (valid && f.bias) ? f.bias[d] : 0.f;
@@ -202,6 +230,19 @@ __global__ void __launch_bounds__(32) scan_bwd_kernel(const BwdProblem p) {
     const float2 x = __fmul2_rn(f2(dt), A2[q]);
     return make_float2(ex2_approx(x.x), ex2_approx(x.y));
   };
+  // Delta A (natural base) of a pair of states
+  auto dtA = [&](float dt, int q) { return __fmul2_rn(__fmul2_rn(f2(dt), A2[q]), f2(kLn2)); };
+  // the exact-ZOH input coefficient g of a pair of states, as the forward kernels compute it
+  auto zoh_g = [&](float dt, int q, float2 a) {
+    const float2 x = dtA(dt, q);
+    if (PRECISE) return make_float2(zoh_coef<true>(dt, x.x, a.x, Ai[q].x), zoh_coef<true>(dt, x.y, a.y, Ai[q].y));
+    return zoh_coef2_fast(f2(dt), x, a, Ai[q]);
+  };
+  // the input term of a pair of states: Delta u B (Euler) or g u B (exact ZOH)
+  auto input = [&](float dt, float uv, int q, float2 a, float2 bq) {
+    if constexpr (ZOH) return __fmul2_rn(__fmul2_rn(zoh_g(dt, q, a), f2(uv)), bq);
+    return __fmul2_rn(f2(dt * uv), bq);
+  };
 
   // ---- forward sweep: the checkpoints, unless the tiled forward kernel wrote them ----
   for (int64_t seg = 0; p.sweep && seg < p.nseg; ++seg) {
@@ -215,9 +256,12 @@ __global__ void __launch_bounds__(32) scan_bwd_kernel(const BwdProblem p) {
     for (int t = 0; t < SEG; ++t) {
       if (t0 + t >= L) break;
       const float dt = valid ? delta_of<PRECISE>(ld<IO>(f.delta, odl + t0 + t), bias, f.softplus) : 0.f;
-      const float du = valid ? dt * ld<IO>(f.u, ou + t0 + t) : 0.f;
+      const float uv = valid ? ld<IO>(f.u, ou + t0 + t) : 0.f;
 #pragma unroll
-      for (int q = 0; q < 4; ++q) h[q] = __ffma2_rn(abar(dt, q), h[q], __fmul2_rn(f2(du), bpair(t, q)));
+      for (int q = 0; q < 4; ++q) {
+        const float2 a = abar(dt, q);
+        h[q] = __ffma2_rn(a, h[q], input(dt, uv, q, a, bpair(t, q)));
+      }
     }
   }
 
@@ -266,12 +310,21 @@ __global__ void __launch_bounds__(32) scan_bwd_kernel(const BwdProblem p) {
       const float s = valid ? ss[t] + bias : 0.f;
       ss[t] = s;
       const float dt = valid ? (f.softplus ? softplus<PRECISE>(s) : s) : 0.f;
-      const float du = dt * uv;
       float2 acc = make_float2(0.f, 0.f);
+      if constexpr (ZOH) {
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        h[q] = __ffma2_rn(abar(dt, q), h[q], __fmul2_rn(f2(du), bpair(t, q)));
-        acc = __ffma2_rn(cpair(t, q), h[q], acc);
+        for (int q = 0; q < 4; ++q) {
+          const float2 a = abar(dt, q);
+          h[q] = __ffma2_rn(a, h[q], input(dt, uv, q, a, bpair(t, q)));
+          acc = __ffma2_rn(cpair(t, q), h[q], acc);
+        }
+      } else {
+        const float du = dt * uv;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          h[q] = __ffma2_rn(abar(dt, q), h[q], __fmul2_rn(f2(du), bpair(t, q)));
+          acc = __ffma2_rn(cpair(t, q), h[q], acc);
+        }
       }
       hist[((t + 1) * 2) * 32 + lane] = make_float4(h[0].x, h[0].y, h[1].x, h[1].y);
       hist[((t + 1) * 2 + 1) * 32 + lane] = make_float4(h[2].x, h[2].y, h[3].x, h[3].y);
@@ -304,27 +357,58 @@ __global__ void __launch_bounds__(32) scan_bwd_kernel(const BwdProblem p) {
                             make_float2(hp1.z, hp1.w)};
       const float2 ht[4] = {make_float2(ht0.x, ht0.y), make_float2(ht0.z, ht0.w), make_float2(ht1.x, ht1.y),
                             make_float2(ht1.z, ht1.w)};
-      float2 sq = make_float2(0.f, 0.f), sb = make_float2(0.f, 0.f), vb[4], vc[4];
+      float2 vb[4], vc[4];
+      float sqs, sbs, sgs = 0.f;
+      if constexpr (ZOH) {
+        // sq: sum_n lambda h_{t-1} Abar A log2(e); sb: sum_n Abar lambda B (dg/dDelta = Abar);
+        // sg: sum_n lambda g B
+        float2 sq = make_float2(0.f, 0.f), sb = make_float2(0.f, 0.f), sg = make_float2(0.f, 0.f);
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const float2 l = __ffma2_rn(f2(yt), cpair(t, q), lam[q]);   // lambda_t
-        const float2 a = abar(dt, q);
-        const float2 qv = __fmul2_rn(__fmul2_rn(l, hp[q]), a);
-        dA[q] = __ffma2_rn(qv, f2(dt), dA[q]);
-        sq = __ffma2_rn(qv, A2[q], sq);
-        sb = __ffma2_rn(l, bpair(t, q), sb);
-        vb[q] = __fmul2_rn(l, f2(du));
-        vc[q] = __fmul2_rn(f2(yt), ht[q]);
-        lam[q] = __fmul2_rn(l, a);
+        for (int q = 0; q < 4; ++q) {
+          const float2 l = __ffma2_rn(f2(yt), cpair(t, q), lam[q]);   // lambda_t
+          const float2 a = abar(dt, q);
+          const float2 qv = __fmul2_rn(__fmul2_rn(l, hp[q]), a);
+          const float2 ln = __fmul2_rn(l, a);                         // lambda carried to step t - 1
+          const float2 x = dtA(dt, q);
+          const float2 g = zoh_g(dt, q, a);
+          const float2 w = make_float2(zoh_dg_dA<PRECISE>(dt, x.x, a.x), zoh_dg_dA<PRECISE>(dt, x.y, a.y));
+          const float2 lb = __fmul2_rn(l, bpair(t, q));
+          dA[q] = __ffma2_rn(qv, f2(dt), __ffma2_rn(__fmul2_rn(lb, f2(uv)), w, dA[q]));
+          sq = __ffma2_rn(qv, A2[q], sq);
+          sb = __ffma2_rn(ln, bpair(t, q), sb);
+          sg = __ffma2_rn(lb, g, sg);
+          vb[q] = __fmul2_rn(__fmul2_rn(l, g), f2(uv));
+          vc[q] = __fmul2_rn(f2(yt), ht[q]);
+          lam[q] = ln;
+        }
+        sqs = sq.x + sq.y;
+        sbs = sb.x + sb.y;
+        sgs = sg.x + sg.y;
+        sgs += __shfl_xor_sync(0xffffffffu, sgs, 16);
+      } else {
+        float2 sq = make_float2(0.f, 0.f), sb = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const float2 l = __ffma2_rn(f2(yt), cpair(t, q), lam[q]);   // lambda_t
+          const float2 a = abar(dt, q);
+          const float2 qv = __fmul2_rn(__fmul2_rn(l, hp[q]), a);
+          dA[q] = __ffma2_rn(qv, f2(dt), dA[q]);
+          sq = __ffma2_rn(qv, A2[q], sq);
+          sb = __ffma2_rn(l, bpair(t, q), sb);
+          vb[q] = __fmul2_rn(l, f2(du));
+          vc[q] = __fmul2_rn(f2(yt), ht[q]);
+          lam[q] = __fmul2_rn(l, a);
+        }
+        sqs = sq.x + sq.y;
+        sbs = sb.x + sb.y;
       }
       ht0 = hp0;
       ht1 = hp1;
-      float sqs = sq.x + sq.y, sbs = sb.x + sb.y;
       sqs += __shfl_xor_sync(0xffffffffu, sqs, 16);
       sbs += __shfl_xor_sync(0xffffffffu, sbs, 16);
       if (valid && lead) {
         const float dDelta = fmaf(sqs, kLn2, sbs * uv);
-        duo[t] = fmaf(sbs, dt, yt * Dd);
+        duo[t] = ZOH ? sgs + yt * Dd : fmaf(sbs, dt, yt * Dd);
         const float dd = f.softplus ? dDelta * sigmoid_f<PRECISE>(ss[t]) : dDelta;
         ddo[t] = dd;
         dbias += dd;
@@ -407,7 +491,8 @@ cudaError_t launch_typed(const BwdProblem& p, int sms, cudaStream_t s) {
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const dim3 grid((unsigned)((p.f.D + 15) / 16), (unsigned)p.f.B);
-  scan_bwd_kernel<IO, PRECISE><<<grid, 32, 0, s>>>(p);
+  if (p.f.zoh) scan_bwd_kernel<IO, PRECISE, true><<<grid, 32, 0, s>>>(p);
+  else scan_bwd_kernel<IO, PRECISE, false><<<grid, 32, 0, s>>>(p);
   return cudaGetLastError();
 }
 

@@ -513,14 +513,14 @@ cudaError_t launch_shape(const ScanProblem& p, const ScanPlan& plan, ScanKernelP
   return launch_one<IO, K, NS, MODE_OUTPUT, PRECISE, ZOH>(tp, tm, grid, s);
 }
 
-template <typename IO, bool PRECISE>
+template <typename IO, bool PRECISE, bool ZOH>
 cudaError_t launch_ckpt_typed(const ScanPlan& plan, const ScanKernelParams& tp, const ScanMaps& tm,
                               const ScanProblem& p, cudaStream_t s) {
   const dim3 grid((unsigned)((p.D + CH - 1) / CH), 1, (unsigned)p.B);
   const int K = plan.shape.K, NS = plan.shape.NS;
-  if (K == 1 && NS == 16) return launch_one<IO, 1, 16, MODE_CKPT, PRECISE, false>(tp, tm, grid, s);
-  if (K == 2 && NS == 8) return launch_one<IO, 2, 8, MODE_CKPT, PRECISE, false>(tp, tm, grid, s);
-  if (K == 4 && NS == 4) return launch_one<IO, 4, 4, MODE_CKPT, PRECISE, false>(tp, tm, grid, s);
+  if (K == 1 && NS == 16) return launch_one<IO, 1, 16, MODE_CKPT, PRECISE, ZOH>(tp, tm, grid, s);
+  if (K == 2 && NS == 8) return launch_one<IO, 2, 8, MODE_CKPT, PRECISE, ZOH>(tp, tm, grid, s);
+  if (K == 4 && NS == 4) return launch_one<IO, 4, 4, MODE_CKPT, PRECISE, ZOH>(tp, tm, grid, s);
   return cudaErrorInvalidValue;
 }
 
@@ -574,8 +574,11 @@ cudaError_t launch_scan_ckpt(const ScanProblem& p, const ScanPlan& plan, float* 
   if (!make_scan_kernel_args(p, plan, nullptr, 16, T, &tp, &tm)) return cudaErrorInvalidValue;
   tp.ckpt = ckpt;
   tp.nseg = nseg;
-  if (p.io == SSM_F32) return launch_ckpt_typed<float, true>(plan, tp, tm, p, s);
-  return launch_ckpt_typed<__nv_bfloat16, false>(plan, tp, tm, p, s);
+  if (p.io == SSM_F32)
+    return p.zoh ? launch_ckpt_typed<float, true, true>(plan, tp, tm, p, s)
+                 : launch_ckpt_typed<float, true, false>(plan, tp, tm, p, s);
+  return p.zoh ? launch_ckpt_typed<__nv_bfloat16, false, true>(plan, tp, tm, p, s)
+               : launch_ckpt_typed<__nv_bfloat16, false, false>(plan, tp, tm, p, s);
 }
 
 size_t tiled_smem_bytes(ssm_dtype_t io, int K, int NS) {

@@ -488,7 +488,6 @@ ssm_status_t validate_bwd(const ssm_scan_bwd_args_t* a, BwdProblem* p) {
   if (st != SSM_OK) return st;
   const ScanProblem& f = p->f;
   if (f.N > 16) return fail(SSM_ERR_UNSUPPORTED, "the backward pass takes dstate <= 16");
-  if (f.zoh) return fail(SSM_ERR_UNSUPPORTED, "the backward pass takes the Euler discretisation");
   if (f.cplx) return fail(SSM_ERR_UNSUPPORTED, "the backward pass takes a real A");
   p->dy = a->dy; p->dhl = a->dh_last;
   p->du = a->du; p->ddelta = a->ddelta; p->dz = a->dz;

@@ -318,10 +318,17 @@ def test_discretization_validation(lib):
     assert lib.ssm_scan_workspace_size(ctypes.byref(scan_args(discretization=ssm.SSM_DISC_ZOH)), ctypes.byref(n)) == 0
 
 
-def test_bwd_rejects_zoh(lib):
+def test_bwd_takes_zoh_and_rejects_complex_a(lib):
+    # the exact-ZOH input term is differentiated: same workspace (the checkpoints) as Euler
     a = bwd_args()
     a.fwd.discretization = ssm.SSM_DISC_ZOH
-    assert bwd_ws(a)[0] == ssm.SSM_ERR_UNSUPPORTED
+    rc, n = bwd_ws(a)
+    assert rc == ssm.SSM_OK and n == bwd_ws(bwd_args())[1] > 0
+    a.fwd.discretization = 2
+    assert bwd_ws(a)[0] == ssm.SSM_ERR_INVALID_ARG
+    c = bwd_args()
+    c.fwd.A_imag = FAKE["ws"]
+    assert bwd_ws(c)[0] == ssm.SSM_ERR_UNSUPPORTED
 
 
 def test_step_discretization_validation(lib):

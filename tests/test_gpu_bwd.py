@@ -39,15 +39,15 @@ def make_inputs(B, D, L, N, io, seed, gate=True, dskip=True, bias=True, h0=False
                 dy=r(B, D, L), dh_last=rng.standard_normal((B, D, N)).astype(np.float32) if dhl else None)
 
 
-def run_and_compare(p, io, softplus=True, what=""):
+def run_and_compare(p, io, softplus=True, what="", zoh=False):
     dev = {k: to_dev(v, io if k in ("u", "delta", "z", "Bm", "Cm", "dy") else None) for k, v in p.items()}
     g = ssm.ssm_scan_bwd(dev["u"], dev["delta"], dev["A"], dev["Bm"], dev["Cm"], dev["dy"], Dskip=dev["Dskip"],
                          z=dev["z"], delta_bias=dev["delta_bias"], h0=dev["h0"], delta_softplus=softplus,
-                         dh_last=dev["dh_last"])
+                         dh_last=dev["dh_last"], discretization=ssm.SSM_DISC_ZOH if zoh else ssm.SSM_DISC_EULER)
     torch.cuda.synchronize()
     ref = oracle.selective_scan_bwd(p["u"], p["delta"], p["A"], p["Bm"], p["Cm"], p["dy"], Dskip=p["Dskip"],
                                     z=p["z"], delta_bias=p["delta_bias"], h0=p["h0"], delta_softplus=softplus,
-                                    dh_last=p["dh_last"])
+                                    dh_last=p["dh_last"], disc=oracle.DISC_ZOH if zoh else oracle.DISC_EULER)
     for k, v in g.items():
         r = ref[{"dB": "dBm", "dC": "dCm"}.get(k, k)]   # the oracle names them after its Bm, Cm
         got = host(v).reshape(r.shape)
@@ -147,3 +147,53 @@ def test_bwd_checkpoint_paths_agree(io, monkeypatch):
         assert torch.equal(tiled[k], sweep[k]), k
     for k in ("dA", "dB", "dC", "dDskip", "ddelta_bias"):
         assert rel_l2(host(tiled[k]), host(sweep[k])) <= 1e-6, k
+
+
+# ---- the exact zero-order-hold input term (g = (exp(Delta A) - 1) / A) ----
+
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+@pytest.mark.parametrize("shape", [(1, 1, 1, 1), (2, 5, 7, 4), (2, 33, 40, 16), (3, 40, 100, 13)])
+def test_bwd_zoh_shapes(io, shape):
+    B, D, L, N = shape
+    p = make_inputs(B, D, L, N, io, seed=sum(shape) + 50, h0=True, dhl=True)
+    run_and_compare(p, io, what=f"zoh {shape}", zoh=True)
+
+
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+@pytest.mark.parametrize("opts", [dict(gate=False, dskip=False, bias=False), dict(shared_bc=True, dhl=True)])
+def test_bwd_zoh_options(io, opts):
+    p = make_inputs(2, 48, 67, 16, io, seed=len(opts) * 7 + 51, **opts)
+    run_and_compare(p, io, what=f"zoh {opts}", zoh=True)
+
+
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+def test_bwd_zoh_small_and_zero_A(io):
+    """States with A = 0 and |A| down to 1e-4, and small Delta: the coefficient and its A-derivative take
+    their series branches (|Delta A| below 1/64 and 1/4) there."""
+    p = make_inputs(2, 40, 60, 16, io, seed=57, h0=True, dhl=True)
+    p["A"][:, 0] = 0.0
+    p["A"][:, 1] = -1e-4
+    p["A"][:, 2] = -3e-2
+    p["delta"][0] = syn.round_io(np.full_like(p["delta"][0], -6.0), io)   # Delta ~ 2.5e-3 in batch row 0
+    run_and_compare(p, io, what="zoh small A", zoh=True)
+
+
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+def test_bwd_zoh_checkpoint_paths_agree(io, monkeypatch):
+    """With the exact-ZOH term too, the tiled forward kernel's checkpoints equal the backward kernel's own
+    forward sweep: du, ddelta, dz and dh0 match bit for bit."""
+    p = make_inputs(2, 64, 256, 16, io, seed=58, h0=True, dhl=True)
+    dev = {k: to_dev(v, io if k in ("u", "delta", "z", "Bm", "Cm", "dy") else None) for k, v in p.items()}
+
+    def run():
+        g = ssm.ssm_scan_bwd(dev["u"], dev["delta"], dev["A"], dev["Bm"], dev["Cm"], dev["dy"], Dskip=dev["Dskip"],
+                             z=dev["z"], delta_bias=dev["delta_bias"], h0=dev["h0"], dh_last=dev["dh_last"],
+                             discretization=ssm.SSM_DISC_ZOH)
+        torch.cuda.synchronize()
+        return {k: v.clone() for k, v in g.items()}
+
+    tiled = run()
+    monkeypatch.setenv("SSM_BWD_SWEEP", "1")
+    sweep = run()
+    for k in ("du", "ddelta", "dz", "dh0"):
+        assert torch.equal(tiled[k], sweep[k]), f"zoh {k} differs between the checkpoint paths"
