@@ -58,7 +58,7 @@ def parse():
     ap.add_argument("--only-rows", action="store_true",
                     help="time only the other workloads' rows (one line of JSON; for profiling their kernels)")
     ap.add_argument("--rows", default="all",
-                    help="comma-separated subset of rows: m130, ti, long, decode, conv, bwd, zoh, cplx, ssd")
+                    help="comma-separated subset of rows: m130, ti, long, decode, conv, bwd, bwdzoh, zoh, cplx, ssd")
     ap.add_argument("--decode-steps", type=int, default=1000, help="decode steps of the decode row")
     return ap.parse_args()
 
@@ -346,6 +346,7 @@ ROW_KEYS = {"cplx": "mamba2.8b_s4dlin_complex_bf16_b4_d5120_l2048_n16",
             "long": "long_bf16_b1_d1536_l1048576_n16", "decode": "decode_bf16_b256_d5120_n16_x1000",
             "conv": "conv1d_silu_bf16_b4_d5120_l2048_w4", "bwd": "scan_bwd_mamba2.8b_bf16_b4_d5120_l2048_n16",
             "ssd": "ssd_mamba2_2.7b_bf16_b4_h80_p64_l2048_n128",
+            "bwdzoh": "scan_bwd_zoh_mamba2.8b_bf16_b4_d5120_l2048_n16",
             "zoh": "mamba2.8b_zoh_bf16_b4_d5120_l2048_n16"}
 
 
@@ -433,9 +434,11 @@ def other_rows(lib, ssm, peak, stream, dev, which="all", decode_steps=1000):
         del x, xo, wt, cb
         torch.cuda.empty_cache()
 
-    if "bwd" in sel:
+    for bkey, bdisc in (("bwd", ssm.SSM_DISC_EULER), ("bwdzoh", ssm.SSM_DISC_ZOH)):
+        if bkey not in sel:
+            continue
         # the backward pass (all gradients, states recomputed) on the 2.8B-shaped layer
-        name = ROW_KEYS["bwd"]
+        name = ROW_KEYS[bkey]
         cfg = syn.M2P8
         inp = random_device_inputs(cfg, 0, dev)
         dy = torch.randn(inp["u"].shape, generator=torch.Generator(device=dev).manual_seed(4000), device=dev).to(
@@ -446,7 +449,7 @@ def other_rows(lib, ssm, peak, stream, dev, which="all", decode_steps=1000):
                      dC=torch.empty(Bsz, N, L, device=dev), dDskip=torch.empty(D, device=dev),
                      ddelta_bias=torch.empty(D, device=dev), dh0=torch.empty(Bsz, D, N, device=dev))
         fa = ssm.make_scan_args(inp["u"], inp["delta"], inp["A"], inp["Bm"], inp["Cm"], None, inp["Dskip"], inp["z"],
-                                inp["delta_bias"])
+                                inp["delta_bias"], discretization=bdisc)
         ba = ssm.make_bwd_args(fa, dy, grads)
         need = ctypes.c_size_t(0)
         if lib.ssm_scan_bwd_workspace_size(ctypes.byref(ba), ctypes.byref(need)) != 0:

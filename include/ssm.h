@@ -188,7 +188,7 @@ typedef struct ssm_step_args {
  * terms of fwd.discretization are differentiated: Euler (g = Delta) and the
  * exact zero-order hold (g = (exp(Delta A) - 1) / A, whose derivatives are
  * dg/dDelta = exp(Delta A) and dg/dA = Delta^2 psi(Delta A) with
- * psi(x) = (x e^x - (e^x - 1)) / x^2).  Limits: 1 <= dstate <= 16; a real A
+ * psi(x) = (x e^x - (e^x - 1)) / x^2).  Limits: 1 <= dstate <= 64; a real A
  * (fwd.A_imag NULL); the gradient outputs must not overlap each other or any
  * input.
  */
@@ -205,7 +205,8 @@ typedef struct ssm_scan_bwd_args {
 } ssm_scan_bwd_args_t;
 
 /* Bytes of device workspace ssm_scan_bwd needs (the state checkpoints:
- * batch * dim * ceil(seqlen / SSM_BWD_SEGMENT) * 16 floats).  Host-only. */
+ * batch * dim * ceil(seqlen / SSM_BWD_SEGMENT) * NP floats, NP = 16, 32 or 64
+ * for dstate up to 16, 32 or 64).  Host-only. */
 ssm_status_t ssm_scan_bwd_workspace_size(const ssm_scan_bwd_args_t *args, size_t *bytes);
 
 /* Gradients of the selective scan (see ssm_scan_bwd_args_t). */

@@ -163,19 +163,22 @@ __device__ __forceinline__ void store_seg(void* base, int64_t off, const float (
 
 __device__ __forceinline__ float2 f2(float v) { return make_float2(v, v); }
 
-// One warp per CTA: 16 channels of one batch row, two lanes per channel
-// (lanes c and c + 16), each lane holding 8 of the channel's states as four
-// f32x2 pairs.  Sums over the states (the C contraction, dDelta, du) take one
-// shuffle between the two lanes of a channel.
-template <typename IO, bool PRECISE, bool ZOH>
+// One warp per CTA: 32 / LPC channels of one batch row, LPC lanes per channel
+// (lanes c, c + 32 / LPC, ...), each lane holding 8 of the channel's states as
+// four f32x2 pairs (LPC = 2, 4, 8 for N up to 16, 32, 64).  Sums over the
+// states (the C contraction, dDelta, du) take log2(LPC) shuffles between the
+// lanes of a channel.
+template <typename IO, bool PRECISE, bool ZOH, int LPC>
 __global__ void __launch_bounds__(32) scan_bwd_kernel(const BwdProblem p) {
-  constexpr int CHW = 16;                            // channels per warp
+  constexpr int CHW = 32 / LPC;                      // channels per warp
+  constexpr int NP = 8 * LPC;                        // states per channel, padded
+  constexpr int NCOL = 2 * NP / 32;                  // dB / dC columns each lane sums
   __shared__ float4 hist[(SEG + 1) * 2 * 32];        // [row][half of the lane's 8 states][lane]
-  __shared__ __align__(16) float bcs[SEG][32];       // [t][B_t[0..15] | C_t[0..15]]
-  __shared__ __align__(16) float red[CHW][36];       // [channel][dB_t[0..15] | dC_t[0..15]]
+  __shared__ __align__(16) float bcs[SEG][2 * NP];   // [t][B_t[0..NP) | C_t[0..NP)]
+  __shared__ __align__(16) float red[CHW][2 * NP + 4];   // [channel][dB_t[0..NP) | dC_t[0..NP)]
   const ScanProblem& f = p.f;
   const int lane = threadIdx.x;
-  const int ch = lane & 15, g = lane >> 4;           // channel within the warp, half of its states
+  const int ch = lane % CHW, g = lane / CHW;         // channel within the warp, group of 8 of its states
   const int64_t b = blockIdx.y;
   const int64_t d = (int64_t)blockIdx.x * CHW + ch;
   const bool valid = d < f.D;
@@ -203,29 +206,41 @@ __global__ void __launch_bounds__(32) scan_bwd_kernel(const BwdProblem p) {
   const float Dd = (valid && f.Dskip) ? f.Dskip[d] : 0.f;
   const int64_t ou = b * f.su[0] + d * f.su[1], odl = b * f.sd[0] + d * f.sd[1], oz = b * f.sz[0] + d * f.sz[1];
   const int64_t ody = b * p.sdy[0] + d * p.sdy[1];
-  // this lane's half of each 16-float checkpoint record
-  float4* ck = reinterpret_cast<float4*>(p.ckpt + c * p.nseg * 16 + g * 8);
+  // this lane's 8 floats of each NP-float checkpoint record
+  float4* ck = reinterpret_cast<float4*>(p.ckpt + c * p.nseg * NP + g * 8);
+  constexpr int CKQ = NP / 4;                        // float4 pieces per checkpoint record
+  // the sum of a per-lane value over the LPC lanes of this lane's channel
+  auto channel_sum = [](float v) {
+#pragma unroll
+    for (int o = CHW; o < 32; o <<= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+  };
 
+  // rows j < NP of the staging block are B's, the others C's; lane l stages rows l, l + 32, ...
   auto stage_bc = [&](int64_t seg) {
     __syncwarp();
-    const int n = lane & 15;
-    const void* base = lane < 16 ? f.Bm : f.Cm;
-    const int64_t* sb = lane < 16 ? f.sB : f.sC;
     const int64_t t0 = seg * SEG;
     const int steps = L - t0 < SEG ? (int)(L - t0) : SEG;
-    float v[SEG];
-    if (n < N) {
-      load_seg<IO>(base, b * sb[0] + n * sb[1] + t0, p.vecbc && steps == SEG, steps, v);
-    } else {
 #pragma unroll
-      for (int t = 0; t < SEG; ++t) v[t] = 0.f;
+    for (int k = 0; k < NCOL; ++k) {
+      const int row = lane + 32 * k;
+      const int n = row % NP;
+      const void* base = row < NP ? f.Bm : f.Cm;
+      const int64_t* sb = row < NP ? f.sB : f.sC;
+      float v[SEG];
+      if (n < N) {
+        load_seg<IO>(base, b * sb[0] + n * sb[1] + t0, p.vecbc && steps == SEG, steps, v);
+      } else {
+#pragma unroll
+        for (int t = 0; t < SEG; ++t) v[t] = 0.f;
+      }
+#pragma unroll
+      for (int t = 0; t < SEG; ++t) bcs[t][row] = v[t];
     }
-#pragma unroll
-    for (int t = 0; t < SEG; ++t) bcs[t][lane] = v[t];
     __syncwarp();
   };
   auto bpair = [&](int t, int q) { return *reinterpret_cast<const float2*>(&bcs[t][g * 8 + 2 * q]); };
-  auto cpair = [&](int t, int q) { return *reinterpret_cast<const float2*>(&bcs[t][16 + g * 8 + 2 * q]); };
+  auto cpair = [&](int t, int q) { return *reinterpret_cast<const float2*>(&bcs[t][NP + g * 8 + 2 * q]); };
   auto abar = [&](float dt, int q) {
     const float2 x = __fmul2_rn(f2(dt), A2[q]);
     return make_float2(ex2_approx(x.x), ex2_approx(x.y));
@@ -248,8 +263,8 @@ __global__ void __launch_bounds__(32) scan_bwd_kernel(const BwdProblem p) {
   for (int64_t seg = 0; p.sweep && seg < p.nseg; ++seg) {
     stage_bc(seg);
     if (valid) {
-      ck[seg * 4] = make_float4(h[0].x, h[0].y, h[1].x, h[1].y);
-      ck[seg * 4 + 1] = make_float4(h[2].x, h[2].y, h[3].x, h[3].y);
+      ck[seg * CKQ] = make_float4(h[0].x, h[0].y, h[1].x, h[1].y);
+      ck[seg * CKQ + 1] = make_float4(h[2].x, h[2].y, h[3].x, h[3].y);
     }
     const int64_t t0 = seg * SEG;
 #pragma unroll
@@ -284,7 +299,7 @@ __global__ void __launch_bounds__(32) scan_bwd_kernel(const BwdProblem p) {
     const int64_t t0 = seg * SEG;
     const int steps = L - t0 < SEG ? (int)(L - t0) : SEG;
     if (valid) {
-      const float4 v0 = ck[seg * 4], v1 = ck[seg * 4 + 1];
+      const float4 v0 = ck[seg * CKQ], v1 = ck[seg * CKQ + 1];
       h[0] = make_float2(v0.x, v0.y); h[1] = make_float2(v0.z, v0.w);
       h[2] = make_float2(v1.x, v1.y); h[3] = make_float2(v1.z, v1.w);
     }
@@ -300,7 +315,7 @@ __global__ void __launch_bounds__(32) scan_bwd_kernel(const BwdProblem p) {
       if (f.z) load_seg<IO>(f.z, oz + t0, vec, steps, zs);
     }
     float dts[SEG], yts[SEG];
-    float dzo[SEG], duo[SEG], ddo[SEG], sums[SEG];   // the segment's outputs, written once it is done
+    float dzo[SEG], duo[SEG], ddo[SEG], sums[NCOL][SEG];   // the segment's outputs, written once it is done
     // recompute the segment's states from its checkpoint
 #pragma unroll
     for (int t = 0; t < SEG; ++t) {
@@ -328,8 +343,7 @@ __global__ void __launch_bounds__(32) scan_bwd_kernel(const BwdProblem p) {
       }
       hist[((t + 1) * 2) * 32 + lane] = make_float4(h[0].x, h[0].y, h[1].x, h[1].y);
       hist[((t + 1) * 2 + 1) * 32 + lane] = make_float4(h[2].x, h[2].y, h[3].x, h[3].y);
-      float part = acc.x + acc.y;
-      part += __shfl_xor_sync(0xffffffffu, part, 16);   // the other half of the channel's states
+      const float part = channel_sum(acc.x + acc.y);   // over all the channel's states
       const float dyv = valid ? dys[t] : 0.f;
       float yt = dyv;
       if (f.z) {
@@ -383,8 +397,7 @@ __global__ void __launch_bounds__(32) scan_bwd_kernel(const BwdProblem p) {
         }
         sqs = sq.x + sq.y;
         sbs = sb.x + sb.y;
-        sgs = sg.x + sg.y;
-        sgs += __shfl_xor_sync(0xffffffffu, sgs, 16);
+        sgs = channel_sum(sg.x + sg.y);
       } else {
         float2 sq = make_float2(0.f, 0.f), sb = make_float2(0.f, 0.f);
 #pragma unroll
@@ -404,8 +417,8 @@ __global__ void __launch_bounds__(32) scan_bwd_kernel(const BwdProblem p) {
       }
       ht0 = hp0;
       ht1 = hp1;
-      sqs += __shfl_xor_sync(0xffffffffu, sqs, 16);
-      sbs += __shfl_xor_sync(0xffffffffu, sbs, 16);
+      sqs = channel_sum(sqs);
+      sbs = channel_sum(sbs);
       if (valid && lead) {
         const float dDelta = fmaf(sqs, kLn2, sbs * uv);
         duo[t] = ZOH ? sgs + yt * Dd : fmaf(sbs, dt, yt * Dd);
@@ -417,19 +430,22 @@ __global__ void __launch_bounds__(32) scan_bwd_kernel(const BwdProblem p) {
       // channel sums of dB_t[n] and dC_t[n]: transpose through shared memory
       *reinterpret_cast<float4*>(&red[ch][g * 8]) = make_float4(vb[0].x, vb[0].y, vb[1].x, vb[1].y);
       *reinterpret_cast<float4*>(&red[ch][g * 8 + 4]) = make_float4(vb[2].x, vb[2].y, vb[3].x, vb[3].y);
-      *reinterpret_cast<float4*>(&red[ch][16 + g * 8]) = make_float4(vc[0].x, vc[0].y, vc[1].x, vc[1].y);
-      *reinterpret_cast<float4*>(&red[ch][16 + g * 8 + 4]) = make_float4(vc[2].x, vc[2].y, vc[3].x, vc[3].y);
+      *reinterpret_cast<float4*>(&red[ch][NP + g * 8]) = make_float4(vc[0].x, vc[0].y, vc[1].x, vc[1].y);
+      *reinterpret_cast<float4*>(&red[ch][NP + g * 8 + 4]) = make_float4(vc[2].x, vc[2].y, vc[3].x, vc[3].y);
       __syncwarp();
-      float sum = 0.f;
 #pragma unroll
-      for (int r = 0; r < CHW; ++r) sum += red[r][lane];
+      for (int k = 0; k < NCOL; ++k) {   // lane l sums columns l, l + 32, ...
+        float sum = 0.f;
+#pragma unroll
+        for (int r = 0; r < CHW; ++r) sum += red[r][lane + 32 * k];
+        sums[k][t] = sum;
+      }
       __syncwarp();
-      sums[t] = sum;
       (void)tg;
     }
     // the segment's outputs: per-step values of this channel (lead lane) and the channel sums of
-    // dB / dC (lane j: row j % 16 of dB for j < 16, of dC otherwise), as 16-byte pieces when the
-    // rows allow it
+    // dB / dC (column j: row j of dB for j < NP, row j - NP of dC otherwise), as 16-byte pieces when
+    // the rows allow it
     if (valid && lead) {
       const int64_t odu = b * p.sdu[0] + d * p.sdu[1] + t0, odd = b * p.sdd[0] + d * p.sdd[1] + t0;
       const int64_t odz = b * p.sdz[0] + d * p.sdz[1] + t0;
@@ -447,19 +463,21 @@ __global__ void __launch_bounds__(32) scan_bwd_kernel(const BwdProblem p) {
         }
       }
     }
-    {
-      const int n = lane & 15;
+#pragma unroll
+    for (int k = 0; k < NCOL; ++k) {
+      const int col = lane + 32 * k;
+      const int n = col % NP;
       if (n < N) {
-        float* dst = lane < 16 ? p.dB + b * p.sdB[0] + n * p.sdB[1] : p.dC + b * p.sdC[0] + n * p.sdC[1];
-        const int64_t st2 = lane < 16 ? p.sdB[2] : p.sdC[2];
+        float* dst = col < NP ? p.dB + b * p.sdB[0] + n * p.sdB[1] : p.dC + b * p.sdC[0] + n * p.sdC[1];
+        const int64_t st2 = col < NP ? p.sdB[2] : p.sdC[2];
         if (p.vecdbc && steps == SEG) {
-          atomicAdd(reinterpret_cast<float4*>(dst + t0), make_float4(sums[0], sums[1], sums[2], sums[3]));
-          atomicAdd(reinterpret_cast<float4*>(dst + t0 + 4), make_float4(sums[4], sums[5], sums[6], sums[7]));
+          atomicAdd(reinterpret_cast<float4*>(dst + t0), make_float4(sums[k][0], sums[k][1], sums[k][2], sums[k][3]));
+          atomicAdd(reinterpret_cast<float4*>(dst + t0 + 4), make_float4(sums[k][4], sums[k][5], sums[k][6], sums[k][7]));
         } else {
 #pragma unroll
           for (int t = 0; t < SEG; ++t) {
             if (t >= steps) break;
-            atomicAdd(dst + (t0 + t) * st2, sums[t]);
+            atomicAdd(dst + (t0 + t) * st2, sums[k][t]);
           }
         }
       }
@@ -490,9 +508,19 @@ cudaError_t launch_typed(const BwdProblem& p, int sms, cudaStream_t s) {
   bwd_zero_kernel<<<zb, 256, 0, s>>>(p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  const dim3 grid((unsigned)((p.f.D + 15) / 16), (unsigned)p.f.B);
-  if (p.f.zoh) scan_bwd_kernel<IO, PRECISE, true><<<grid, 32, 0, s>>>(p);
-  else scan_bwd_kernel<IO, PRECISE, false><<<grid, 32, 0, s>>>(p);
+  // lanes per channel by the state size: 2 (N <= 16, 16 channels per warp), 4 (N <= 32), 8 (N <= 64)
+  const int lpc = bwd_lanes_per_channel(p.f.N);
+  const int chw = 32 / lpc;
+  const dim3 grid((unsigned)((p.f.D + chw - 1) / chw), (unsigned)p.f.B);
+#define SSM_BWD_LAUNCH(L)                                                   \
+  if (lpc == L) {                                                           \
+    if (p.f.zoh) scan_bwd_kernel<IO, PRECISE, true, L><<<grid, 32, 0, s>>>(p); \
+    else scan_bwd_kernel<IO, PRECISE, false, L><<<grid, 32, 0, s>>>(p);        \
+  }
+  SSM_BWD_LAUNCH(2)
+  SSM_BWD_LAUNCH(4)
+  SSM_BWD_LAUNCH(8)
+#undef SSM_BWD_LAUNCH
   return cudaGetLastError();
 }
 

@@ -487,7 +487,7 @@ ssm_status_t validate_bwd(const ssm_scan_bwd_args_t* a, BwdProblem* p) {
   ssm_status_t st = validate_scan(&fa, &p->f);
   if (st != SSM_OK) return st;
   const ScanProblem& f = p->f;
-  if (f.N > 16) return fail(SSM_ERR_UNSUPPORTED, "the backward pass takes dstate <= 16");
+  if (f.N > 64) return fail(SSM_ERR_UNSUPPORTED, "the backward pass takes dstate <= 64");
   if (f.cplx) return fail(SSM_ERR_UNSUPPORTED, "the backward pass takes a real A");
   p->dy = a->dy; p->dhl = a->dh_last;
   p->du = a->du; p->ddelta = a->ddelta; p->dz = a->dz;
@@ -581,7 +581,7 @@ ssm_status_t validate_bwd(const ssm_scan_bwd_args_t* a, BwdProblem* p) {
 }
 
 size_t bwd_workspace_bytes(const BwdProblem& p) {
-  return (size_t)(p.f.B * p.f.D * p.nseg) * 16 * sizeof(float);
+  return (size_t)(p.f.B * p.f.D * p.nseg) * (size_t)(8 * bwd_lanes_per_channel(p.f.N)) * sizeof(float);
 }
 
 }  // namespace

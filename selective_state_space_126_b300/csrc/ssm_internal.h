@@ -47,7 +47,7 @@ struct BwdProblem {
   int64_t sdy[3], sdu[3], sdd[3], sdz[3], sdB[3], sdC[3], sdhl[3], sdh0[3];
   int64_t bc_rows;     // rows of dB / dC: 1 when B / C are shared across the batch
   int64_t nseg;        // checkpoints per channel
-  float* ckpt;         // [B][D][nseg][16] fp32
+  float* ckpt;         // [B][D][nseg][8 * bwd_lanes_per_channel(N)] fp32
   int sweep;           // 1: the backward kernel writes the checkpoints itself; 0: they are already there
   int vec;             // u, delta, z, dy rows start on 16-byte boundaries (128-bit segment loads)
   int vecbc;           // the same for the rows of B and C
@@ -106,6 +106,8 @@ cudaError_t launch_scan_tiled(const ScanProblem& p, const ScanPlan& plan, void* 
 cudaError_t launch_state_update(const StepProblem& p, cudaStream_t s);
 cudaError_t launch_causal_conv1d(const ConvProblem& p, int sms, cudaStream_t s);
 cudaError_t launch_scan_bwd(const BwdProblem& p, int sms, cudaStream_t s);
+// lanes of the backward kernel per channel (8 states each) and so the checkpoint record length / 8
+inline int bwd_lanes_per_channel(int64_t N) { return N <= 16 ? 2 : N <= 32 ? 4 : 8; }
 cudaError_t launch_ssd(const SsdProblem& p, bool tensor_cores, cudaStream_t s);
 bool ssd_tensor_core_eligible(const SsdProblem& p);
 cudaError_t launch_scan_ckpt(const ScanProblem& p, const ScanPlan& plan, float* ckpt, int64_t nseg, cudaStream_t s);

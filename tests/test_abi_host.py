@@ -303,12 +303,22 @@ def test_bwd_validation(lib, over, code):
     assert bwd_ws(bwd_args(**over))[0] == code
 
 
-def test_bwd_rejects_large_dstate(lib):
-    a = bwd_args(N=32)
-    a.stride_dB[:] = [32 * 256, 256, 1]
-    a.stride_dC[:] = [32 * 256, 256, 1]
-    a.stride_dh0[:] = [64 * 32, 32, 1]
-    assert bwd_ws(a)[0] == ssm.SSM_ERR_UNSUPPORTED
+def test_bwd_state_sizes(lib):
+    # dstate up to 64: the checkpoint record is 16, 32 or 64 floats (8 states per lane, 2 / 4 / 8 lanes);
+    # beyond 64 the call is refused
+    def args(N):
+        a = bwd_args(B=2, D=64, L=256, N=N)
+        a.stride_dB[:] = [N * 256, 256, 1]
+        a.stride_dC[:] = [N * 256, 256, 1]
+        a.stride_dh0[:] = [64 * N, N, 1]
+        a.fwd.stride_B[:] = [N * 256, 256, 1]
+        a.fwd.stride_C[:] = [N * 256, 256, 1]
+        a.fwd.stride_A[:] = [N, 1]
+        return a
+    for N, rec in ((5, 16), (16, 16), (17, 32), (32, 32), (33, 64), (64, 64)):
+        rc, n = bwd_ws(args(N))
+        assert rc == ssm.SSM_OK and n == 2 * 64 * 32 * rec * 4, (N, rc, n)
+    assert bwd_ws(args(65))[0] == ssm.SSM_ERR_UNSUPPORTED
 
 
 def test_discretization_validation(lib):

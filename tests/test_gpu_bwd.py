@@ -197,3 +197,19 @@ def test_bwd_zoh_checkpoint_paths_agree(io, monkeypatch):
     sweep = run()
     for k in ("du", "ddelta", "dz", "dh0"):
         assert torch.equal(tiled[k], sweep[k]), f"zoh {k} differs between the checkpoint paths"
+
+
+# ---- state sizes above 16: 4 or 8 lanes per channel, checkpoints from the backward kernel's own sweep ----
+
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+@pytest.mark.parametrize("shape", [(2, 20, 50, 32), (2, 17, 24, 24), (1, 9, 33, 64), (2, 8, 40, 48)])
+@pytest.mark.parametrize("zoh", [False, True])
+def test_bwd_large_dstate(io, shape, zoh):
+    B, D, L, N = shape
+    p = make_inputs(B, D, L, N, io, seed=sum(shape) + 70 + zoh, h0=True, dhl=True)
+    run_and_compare(p, io, what=f"N={N} zoh={zoh} {shape}", zoh=zoh)
+
+
+def test_bwd_large_dstate_shared_bc_and_options():
+    p = make_inputs(3, 24, 41, 40, "bf16", seed=77, gate=False, dskip=False, shared_bc=True, dhl=True)
+    run_and_compare(p, "bf16", what="N=40 shared B/C, no gate, no D")
