@@ -47,26 +47,24 @@ namespace {
 
 constexpr int SEG = SSM_BWD_SEGMENT;   // steps per checkpoint
 
-// Delta^2 psi(x) for x = Delta A and a = e^x: the A-derivative of the exact-ZOH coefficient.
-// psi(x) = sum_{k>=1} k x^(k-1) / (k+1)! = 1/2 + x/3 + x^2/8 + x^3/30 + x^4/144 + x^5/840 + x^6/5760 + ...
-// is summed below |x| = 1/4 (the next term is below 3e-9 relative there), where the closed form
-// cancels; above it the closed form loses at most a few bits of the fp32 mantissa.
-template <bool PRECISE>
-__device__ __forceinline__ float zoh_dg_dA(float dt, float x, float a) {
-  float psi;
-  if (fabsf(x) < 0.25f) {
-    psi = 1.7361111111111111e-04f;                 // 1/5760
-    psi = fmaf(psi, x, 1.1904761904761905e-03f);   // 1/840
-    psi = fmaf(psi, x, 6.9444444444444444e-03f);   // 1/144
-    psi = fmaf(psi, x, 3.3333333333333333e-02f);   // 1/30
-    psi = fmaf(psi, x, 0.125f);                    // 1/8
-    psi = fmaf(psi, x, 3.3333333333333333e-01f);   // 1/3
-    psi = fmaf(psi, x, 0.5f);
-  } else {
-    const float num = fmaf(x, a, 1.f - a);
-    psi = PRECISE ? num / (x * x) : __fdividef(num, x * x);
-  }
-  return dt * dt * psi;
+// The A-derivative of the exact-ZOH coefficient g = (e^x - 1) / A (x = Delta A, a = e^x) for a pair of
+// states: dg/dA = (Delta a - g) / A.  That difference cancels for small |x|, so below |x| = 1/4 it is
+// Delta^2 psi(x), psi(x) = sum_{k>=1} k x^(k-1) / (k+1)! = 1/2 + x/3 + x^2/8 + x^3/30 + x^4/144
+// + x^5/840 + x^6/5760 + ... (the next term is below 3e-9 relative there); above it the difference
+// keeps all but a few bits.  Both forms are evaluated on packed f32x2 operations and selected per
+// state, so the lanes of a warp do not diverge.
+__device__ __forceinline__ float2 zoh_dg_dA2(float dt, float2 x, float2 a, float2 g, float2 inv_a) {
+  const float2 d2 = make_float2(dt, dt);
+  float2 psi = __ffma2_rn(x, make_float2(1.7361111111111111e-04f, 1.7361111111111111e-04f),   // 1/5760
+                          make_float2(1.1904761904761905e-03f, 1.1904761904761905e-03f));      // 1/840
+  psi = __ffma2_rn(psi, x, make_float2(6.9444444444444444e-03f, 6.9444444444444444e-03f));     // 1/144
+  psi = __ffma2_rn(psi, x, make_float2(3.3333333333333333e-02f, 3.3333333333333333e-02f));     // 1/30
+  psi = __ffma2_rn(psi, x, make_float2(0.125f, 0.125f));                                       // 1/8
+  psi = __ffma2_rn(psi, x, make_float2(3.3333333333333333e-01f, 3.3333333333333333e-01f));     // 1/3
+  psi = __ffma2_rn(psi, x, make_float2(0.5f, 0.5f));
+  const float2 small = __fmul2_rn(__fmul2_rn(d2, d2), psi);
+  const float2 large = __fmul2_rn(__ffma2_rn(d2, a, make_float2(-g.x, -g.y)), inv_a);
+  return make_float2(fabsf(x.x) < 0.25f ? small.x : large.x, fabsf(x.y) < 0.25f ? small.y : large.y);
 }
 
 template <bool PRECISE>
@@ -385,7 +383,7 @@ __global__ void __launch_bounds__(32) scan_bwd_kernel(const BwdProblem p) {
           const float2 ln = __fmul2_rn(l, a);                         // lambda carried to step t - 1
           const float2 x = dtA(dt, q);
           const float2 g = zoh_g(dt, q, a);
-          const float2 w = make_float2(zoh_dg_dA<PRECISE>(dt, x.x, a.x), zoh_dg_dA<PRECISE>(dt, x.y, a.y));
+          const float2 w = zoh_dg_dA2(dt, x, a, g, Ai[q]);
           const float2 lb = __fmul2_rn(l, bpair(t, q));
           dA[q] = __ffma2_rn(qv, f2(dt), __ffma2_rn(__fmul2_rn(lb, f2(uv)), w, dA[q]));
           sq = __ffma2_rn(qv, A2[q], sq);
