@@ -89,6 +89,11 @@ typedef enum {
 #define SSM_SCAN_FORCE_GENERIC 0x1   /* use the stride-general kernel */
 #define SSM_SCAN_FORCE_TILED   0x2   /* use the tiled single-pass kernel (error if impossible) */
 #define SSM_SCAN_FORCE_CHUNKED 0x4   /* use the three-pass chunked kernel (error if impossible) */
+/* use the warp-shuffle associative scan: lanes over 32 consecutive steps,
+ * five combine rounds per tile, one warp per channel (Euler input term, real
+ * A, dstate <= 16, any strides; SSM_ERR_UNSUPPORTED otherwise).  Never chosen
+ * automatically: it does several times the arithmetic per state update. */
+#define SSM_SCAN_FORCE_WARPSCAN 0x8
 
 /*
  * Arguments of ssm_scan_fwd.  Shapes (with strides in elements, time stride 1):

@@ -15,7 +15,8 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 ROOT = os.path.dirname(HERE)
 LIB = os.path.join(HERE, "libssm.so")
-SOURCES = ["ssm_api.cu", "scan_generic.cu", "scan_tiled.cu", "state_update.cu", "conv1d.cu", "scan_bwd.cu", "probe.cu", "ssd.cu"]
+SOURCES = ["ssm_api.cu", "scan_generic.cu", "scan_tiled.cu", "scan_warp.cu", "state_update.cu", "conv1d.cu", "scan_bwd.cu",
+           "probe.cu", "ssd.cu"]
 HEADERS = ["device_math.cuh", "async_copy.cuh", "scan_common.cuh", "ssm_internal.h", "tcgen05.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",

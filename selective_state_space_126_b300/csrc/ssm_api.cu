@@ -229,6 +229,14 @@ ssm_status_t plan_scan(const ssm_scan_args_t* a, const ScanProblem& p, ScanPlan*
     plan->path = kPathGeneric;
     return ok();
   }
+  if (flags & SSM_SCAN_FORCE_WARPSCAN) {
+    if (flags & (SSM_SCAN_FORCE_TILED | SSM_SCAN_FORCE_CHUNKED))
+      return fail(SSM_ERR_INVALID_ARG, "SSM_SCAN_FORCE_WARPSCAN excludes the other paths");
+    if (p.zoh || p.cplx || p.N > 16)
+      return fail(SSM_ERR_UNSUPPORTED, "the warp-shuffle scan takes the Euler term, a real A and dstate <= 16");
+    plan->path = kPathWarpScan;
+    return ok();
+  }
   if (!eligible) {
     if (flags & (SSM_SCAN_FORCE_TILED | SSM_SCAN_FORCE_CHUNKED))
       return fail(SSM_ERR_UNSUPPORTED, "layout not eligible for the tiled kernels (alignment / strides / seqlen)");
@@ -388,6 +396,8 @@ ssm_status_t ssm_scan_fwd(const ssm_scan_args_t* args, void* stream) {
   cudaError_t e;
   if (plan.path == kPathGeneric) {
     e = launch_scan_generic(p, s);
+  } else if (plan.path == kPathWarpScan) {
+    e = launch_scan_warp(p, s);
   } else {
     if (plan.workspace_bytes > 0) {
       if (!args->workspace) return fail(SSM_ERR_WORKSPACE, "workspace of %zu bytes required", plan.workspace_bytes);

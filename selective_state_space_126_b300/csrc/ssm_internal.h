@@ -80,7 +80,7 @@ struct SsdProblem {
   int* status;
 };
 
-enum ScanPath { kPathGeneric = 0, kPathTiled = 1, kPathChunked = 2 };
+enum ScanPath { kPathGeneric = 0, kPathTiled = 1, kPathChunked = 2, kPathWarpScan = 3 };
 
 // Tiled-kernel shape: K threads share one channel's states, NS states per thread.
 struct TiledShape {
@@ -102,6 +102,7 @@ int* device_status_ptr();
 
 // launchers (return a cudaError_t from the launch)
 cudaError_t launch_scan_generic(const ScanProblem& p, cudaStream_t s);
+cudaError_t launch_scan_warp(const ScanProblem& p, cudaStream_t s);
 cudaError_t launch_scan_tiled(const ScanProblem& p, const ScanPlan& plan, void* workspace, cudaStream_t s);
 cudaError_t launch_state_update(const StepProblem& p, cudaStream_t s);
 cudaError_t launch_causal_conv1d(const ConvProblem& p, int sms, cudaStream_t s);

@@ -168,6 +168,8 @@ def test_step_empty_is_noop(lib):
     (dict(B=4, D=1536, L=2048), "tiled"),            # 192 CTAs: the single pass measured faster
     (dict(B=1, D=5120, L=1024), "tiled"),            # too short to chunk
     (dict(B=4, D=1536, L=8192), "chunked"),          # long and under two CTAs per SM
+    (dict(L=255, flags=ssm.SSM_SCAN_FORCE_WARPSCAN), "warpscan"),   # any layout: plain strided loads
+    (dict(B=1, D=5120, L=2048, flags=ssm.SSM_SCAN_FORCE_WARPSCAN), "warpscan"),
 ])
 def test_plan(lib, kw, path):
     # the planner's cut-offs are in CTAs per SM; these expected paths hold for 148 SMs (B300, and
@@ -183,6 +185,20 @@ def test_plan(lib, kw, path):
     assert ssm.ssm_scan_plan_path(a) == path
     ws = ssm.ssm_scan_workspace_size(a)
     assert (ws > 0) == (path == "chunked")
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(N=17), ssm.SSM_ERR_UNSUPPORTED),                                   # more than 16 states
+    (dict(discretization=ssm.SSM_DISC_ZOH), ssm.SSM_ERR_UNSUPPORTED),        # Euler input term only
+    (dict(A_imag=FAKE["ws"]), ssm.SSM_ERR_UNSUPPORTED),                      # real A only
+    (dict(extra=ssm.SSM_SCAN_FORCE_TILED), ssm.SSM_ERR_INVALID_ARG),         # one forced path at a time
+    (dict(extra=ssm.SSM_SCAN_FORCE_CHUNKED), ssm.SSM_ERR_INVALID_ARG),
+])
+def test_warpscan_limits(lib, kw, code):
+    kw = dict(kw)
+    extra = kw.pop("extra", 0)
+    a = scan_args(flags=ssm.SSM_SCAN_FORCE_WARPSCAN | extra, **kw)
+    assert call_scan(a) == code, lib.ssm_last_error_detail()
 
 
 def test_force_tiled_on_ragged_is_unsupported(lib):

@@ -17,7 +17,7 @@ from gpu_util import (assert_close, device_inputs, host, oracle_channels, rel_l2
 pytestmark = pytest.mark.gpu
 
 FLAGS = {"auto": 0, "generic": ssm.SSM_SCAN_FORCE_GENERIC, "tiled": ssm.SSM_SCAN_FORCE_TILED,
-         "chunked": ssm.SSM_SCAN_FORCE_CHUNKED}
+         "chunked": ssm.SSM_SCAN_FORCE_CHUNKED, "warpscan": ssm.SSM_SCAN_FORCE_WARPSCAN}
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -143,6 +143,56 @@ def test_padded_row_strides():
                          Dskip=to_dev(case["Dskip"]), z=dev["z"], delta_bias=to_dev(case["delta_bias"]))
     yr, _ = oracle_case(case)
     assert_close("f32", host(y), yr, "strided")
+
+
+# ---------------------------------------------------------------------------
+# the warp-shuffle associative scan (lanes over time), forced by its flag
+# ---------------------------------------------------------------------------
+
+WARP_SHAPES = [(1, 1, 1, 16), (1, 3, 7, 4), (2, 5, 31, 16), (1, 37, 255, 16), (2, 33, 256, 16),
+               (1, 100, 1000, 13), (1, 17, 4097, 16), (2, 40, 512, 1), (3, 7, 40, 5)]
+
+
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+@pytest.mark.parametrize("shape", WARP_SHAPES, ids=lambda s: "x".join(map(str, s)))
+def test_warpscan_shapes(io, shape):
+    """Ragged L (partial last tile of 32 lanes), tiny D, N < 16, with h0: against the oracle."""
+    B, D, L, N = shape
+    case = rand_case(B, D, L, N, io, seed=B * 1000 + D + L + N, h0=True)
+    yr, hr = oracle_case(case)
+    y, hl = gpu_scan(case, io, "warpscan")
+    assert_close(io, y, yr, f"y warpscan {shape}")
+    assert_close(io, hl, hr, f"h_last warpscan {shape}")
+
+
+@pytest.mark.parametrize("opt", ["no_gate", "no_dskip", "no_bias", "no_h0", "shared_bc", "softplus_off", "bare"])
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+def test_warpscan_options(io, opt):
+    kw = dict(gate=opt not in ("no_gate", "bare"), dskip=opt not in ("no_dskip", "bare"),
+              bias=opt not in ("no_bias", "bare"), h0=opt not in ("no_h0", "bare"), shared_bc=opt == "shared_bc")
+    case = rand_case(3, 70, 320, 16, io, seed=7, **kw)
+    softplus = opt != "softplus_off"
+    if not softplus:
+        case["delta"] = syn.round_io(np.abs(case["delta"]) * 0.05, io)
+        case["delta_bias"] = None
+    yr, hr = oracle_case(case, softplus)
+    y, hl = gpu_scan(case, io, "warpscan", softplus=softplus)
+    assert_close(io, y, yr, f"y {opt} warpscan")
+    assert_close(io, hl, hr, f"h_last {opt} warpscan")
+
+
+def test_warpscan_workload_sampled():
+    """The batch-1 2.8B-shaped time-invariant layer (5120 channels) on the warp-shuffle scan, sampled."""
+    cfg = syn.M2P8_TI
+    inp = device_inputs(cfg)
+    y, hl = ssm.ssm_scan_fwd(inp["u"], inp["delta"], inp["A"], inp["Bm"], inp["Cm"], Dskip=inp["Dskip"],
+                             z=inp["z"], delta_bias=inp["delta_bias"], return_last_state=True,
+                             flags=ssm.SSM_SCAN_FORCE_WARPSCAN)
+    torch.cuda.synchronize()
+    chans = sample_channels(cfg, k=32)
+    yr, hr = oracle_channels(cfg, chans)
+    assert_close("bf16", np.stack([host(y[b, d]) for b, d in chans]), yr, "ti warpscan")
+    assert_close("bf16", np.stack([host(hl[b, d]) for b, d in chans]), hr, "ti warpscan h_last")
 
 
 def test_chunked_equals_single_pass_medium():
