@@ -121,7 +121,7 @@ def job_value(updates_per_rank: int, world: int, ms_per_step: float) -> float:
 
 def ssm_launches(lib, ssm, args) -> int:
     """Kernel launches one ssm_scan_fwd makes for these arguments."""
-    return {"tiled": 1, "chunked": 3, "generic": 1}[ssm.ssm_scan_plan_path(args)]
+    return {"tiled": 1, "split": 2, "chunked": 3, "generic": 1, "warpscan": 1}[ssm.ssm_scan_plan_path(args)]
 
 
 def measured_peaks():
@@ -399,7 +399,7 @@ def other_rows(lib, ssm, peak, stream, dev, which="all", decode_steps=1000):
         ms = time_launches(run, n, stream, flush if algo < (256 << 20) else None)
         gbs = algo / (ms * 1e-3) / 1e9
         rows[name] = {"ms": ms, "value": cfg.updates / (ms * 1e-3), "unit": UNIT, "path": path,
-                      "launches": {"tiled": 1, "chunked": 3, "generic": 1}[path],
+                      "launches": {"tiled": 1, "split": 2, "chunked": 3, "generic": 1}[path],
                       "hbm_gbs_algorithmic": gbs, "frac": gbs / peak, "algorithmic_bytes": algo,
                       "l2": "flushed between launches" if algo < (256 << 20) else "inputs larger than L2"}
         del inp, y, ws
@@ -778,7 +778,8 @@ def main():
     # ---- roofline of the scan kernel ----
     peak, peak_kind = measured_peaks()
     algo = algorithmic_bytes(cfg)
-    kernel_ms = launch_ms / launches_per_step if path != "tiled" else launch_ms
+    # the split single pass's two launches run side by side: their union is the scan kernel's time
+    kernel_ms = launch_ms / launches_per_step if path not in ("tiled", "split") else launch_ms
     achieved = algo / (launch_ms * 1e-3) / 1e9
     traffic = None
     if os.path.exists(TRAFFIC_FILE):

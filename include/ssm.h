@@ -366,7 +366,11 @@ ssm_status_t ssm_scan_fwd_noalloc(const ssm_scan_args_t *args, void *stream);
 ssm_status_t ssm_probe_sfu(int op, int blocks, int iters, float *sink, void *stream);
 
 /* Kernel path ssm_scan_fwd would take for these arguments:
- * 0 = generic, 1 = tiled single pass, 2 = chunked three-pass; -1 on error. */
+ * 0 = generic, 1 = tiled single pass, 2 = chunked three-pass, 3 = warp-shuffle
+ * scan (SSM_SCAN_FORCE_WARPSCAN), 4 = tiled single pass split over two launches
+ * (bf16 grids of more than 4 and at most 5 32-channel blocks per SM: 4 per SM
+ * on two-warp CTAs, the rest on four-warp CTAs that run beside them); -1 on
+ * error. */
 int ssm_scan_plan_path(const ssm_scan_args_t *args);
 
 /* Library ABI version: (major << 16) | minor. */

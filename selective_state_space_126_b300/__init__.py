@@ -26,7 +26,7 @@ SSM_OK, SSM_ERR_INVALID_ARG, SSM_ERR_UNSUPPORTED, SSM_ERR_CUDA, SSM_ERR_TIMEOUT,
 SSM_F32, SSM_BF16 = 0, 1
 SSM_SCAN_FORCE_GENERIC, SSM_SCAN_FORCE_TILED, SSM_SCAN_FORCE_CHUNKED, SSM_SCAN_FORCE_WARPSCAN = 0x1, 0x2, 0x4, 0x8
 SSM_DISC_EULER, SSM_DISC_ZOH = 0, 1
-PATH_NAMES = {0: "generic", 1: "tiled", 2: "chunked", 3: "warpscan"}
+PATH_NAMES = {0: "generic", 1: "tiled", 2: "chunked", 3: "warpscan", 4: "split"}
 
 # every symbol include/ssm.h declares
 EXPORTED_SYMBOLS = ["ssm_scan_workspace_size", "ssm_scan_fwd", "ssm_state_update", "ssm_status_string",

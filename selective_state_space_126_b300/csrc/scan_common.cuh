@@ -40,6 +40,10 @@ struct ScanKernelParams {
   int* status;
   float* ckpt;      // MODE_CKPT: [B][D][nseg][16], the state before every segment
   int64_t nseg;
+  // split single pass (see ssm_api.cu): with nblk > 0, CTA j runs unit u = unit0 + j, batch row
+  // u / nblk and channels 32 (u % nblk) ..; else the grid gives (channel block, chunk, batch)
+  int64_t unit0, nblk;
+  int pdl;          // 1: let the next launch start at once; 2: before exiting, wait for the launch before
 };
 
 struct ScanMaps {

@@ -129,9 +129,12 @@ __global__ void __launch_bounds__(32 * K, min_blocks(K, NS))
   const int warp = tid >> 5, lane = tid & 31;
   const int g = warp;                            // state group of this warp
   const int c = lane;                            // channel within the CTA
-  const int64_t b = blockIdx.z;
+  // split single pass: the first launch lets the second start at once (it reads nothing the first writes)
+  if (p.pdl == 1) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  const int64_t unit = p.unit0 + blockIdx.x;
+  const int64_t b = p.nblk > 0 ? unit / p.nblk : (int64_t)blockIdx.z;
   const int chunk = blockIdx.y;
-  const int64_t d0 = (int64_t)blockIdx.x * CH;
+  const int64_t d0 = p.nblk > 0 ? (unit % p.nblk) * CH : (int64_t)blockIdx.x * CH;
   const int64_t d = d0 + c;
   const bool valid = d < p.D;
   const int N = p.N;
@@ -476,6 +479,9 @@ __global__ void __launch_bounds__(32 * K, min_blocks(K, NS))
       if (g == 0) p.rec_s[r] = dsum;
     }
   }
+  // split single pass, second launch: finish only after the first launch has (so that whatever the
+  // stream runs next sees both)
+  if (p.pdl == 2) asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 template <typename IO, int K, int NS, int MODE, bool PRECISE, bool ZOH, bool CPLX = false>
@@ -491,6 +497,21 @@ cudaError_t launch_one(const ScanKernelParams& tp, const ScanMaps& tm, dim3 grid
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::kAlloc);
     if (e != cudaSuccess) return e;
     __atomic_fetch_or(&attr_set, bit, __ATOMIC_RELEASE);
+  }
+  if (tp.pdl == 2) {
+    // may start while the launch before runs (programmatic dependent launch); it waits for that
+    // launch to finish before exiting
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(32 * K);
+    cfg.dynamicSmemBytes = S::kAlloc;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, tp, tm);
   }
   kern<<<grid, 32 * K, S::kAlloc, s>>>(tp, tm);
   return cudaGetLastError();
@@ -540,6 +561,19 @@ template <typename IO, bool PRECISE, bool ZOH>
 cudaError_t launch_typed(const ScanProblem& p, const ScanPlan& plan, ScanKernelParams& tp, const ScanMaps& tm,
                          cudaStream_t s) {
   const int K = plan.shape.K, NS = plan.shape.NS;
+  if (plan.split_home > 0) {
+    // split single pass: the home units on two-warp CTAs, then the extra units on four-warp CTAs
+    // (4 states per thread) that run beside them
+    if (K != 2 || NS != 8 || plan.nchunks != 1) return cudaErrorInvalidValue;
+    tp.nblk = (p.D + CH - 1) / CH;
+    tp.unit0 = 0;
+    tp.pdl = 1;
+    cudaError_t e = launch_one<IO, 2, 8, MODE_OUTPUT, PRECISE, ZOH>(tp, tm, dim3((unsigned)plan.split_home), s);
+    if (e != cudaSuccess) return e;
+    tp.unit0 = plan.split_home;
+    tp.pdl = 2;
+    return launch_one<IO, 4, 4, MODE_OUTPUT, PRECISE, ZOH>(tp, tm, dim3((unsigned)plan.split_extra), s);
+  }
   if (K == 1 && NS == 16) return launch_shape<IO, 1, 16, PRECISE, ZOH>(p, plan, tp, tm, s);
   if (K == 2 && NS == 8) return launch_shape<IO, 2, 8, PRECISE, ZOH>(p, plan, tp, tm, s);
   if (K == 4 && NS == 4) return launch_shape<IO, 4, 4, PRECISE, ZOH>(p, plan, tp, tm, s);

@@ -219,6 +219,28 @@ TiledShape pick_shape(const ScanProblem& p, int64_t ctas, int sms) {
   return TiledShape{2, 8, 32};
 }
 
+// Split single pass.  An SM's four schedulers each issue for their own warps,
+// and a one-wave grid of the two-warp (K = 2) CTAs takes as long as the
+// schedulers holding the most warps: on B300, 592 CTAs of a 4 x D x 2048 scan
+// (4 per SM, 2 warps per scheduler) took 193 us for D = 4736, while 640 and
+// 740 CTAs (4 x 5120 and 4 x 5920 channels: 3 warps on some schedulers) both
+// took 253 us.  So when the grid has more than 4 and at most 5 CTAs per SM,
+// the first 4 per SM ("home" units of a batch row and 32 channels) run as one
+// launch and the rest ("extra" units, at most one per SM) as a second launch
+// of the four-warp CTA (4 states per thread), which starts while the first
+// runs (programmatic dependent launch) and fits beside its 4 CTAs: each extra
+// unit adds one quarter-unit warp to a scheduler instead of a third half-unit
+// one.  SSM_SCAN_KERNEL=k2 keeps the single launch.
+void plan_split(const ScanProblem& p, int sms, ScanPlan* plan) {
+  const char* env = getenv("SSM_SCAN_KERNEL");
+  if (env) return;
+  if (p.io != SSM_BF16 || p.cplx || p.zoh || p.N > 16 || plan->shape.K != 2 || plan->shape.NS != 8) return;
+  const int64_t units = p.B * ((p.D + 31) / 32), home = 4 * (int64_t)sms;
+  if (units <= home || units > home + sms) return;
+  plan->split_home = (int)home;
+  plan->split_extra = (int)(units - home);
+}
+
 ssm_status_t plan_scan(const ssm_scan_args_t* a, const ScanProblem& p, ScanPlan* plan) {
   std::memset(plan, 0, sizeof(*plan));
   plan->nchunks = 1;
@@ -292,6 +314,7 @@ ssm_status_t plan_scan(const ssm_scan_args_t* a, const ScanProblem& p, ScanPlan*
     }
   }
   plan->path = kPathTiled;
+  plan_split(p, sms, plan);
   return ok();
 }
 
@@ -381,6 +404,7 @@ int ssm_scan_plan_path(const ssm_scan_args_t* args) {
   if (p.B == 0 || p.D == 0) return 0;
   ScanPlan plan;
   if (plan_scan(args, p, &plan) != SSM_OK) return -1;
+  if (plan.path == kPathTiled && plan.split_home > 0) return 4;   // the single pass in two launches
   return (int)plan.path;
 }
 

@@ -95,6 +95,7 @@ struct ScanPlan {
   int64_t chunk_len;      // chunked path: timesteps per chunk (multiple of the tile)
   int64_t nchunks;
   size_t workspace_bytes;
+  int split_home, split_extra;   // split single pass: units of the two-warp launch / of the four-warp one
 };
 
 // device status word of the current device (bounded-wait timeouts)

@@ -163,7 +163,8 @@ def test_step_empty_is_noop(lib):
     (dict(L=256, flags=ssm.SSM_SCAN_FORCE_GENERIC), "generic"),
     (dict(L=4096, flags=ssm.SSM_SCAN_FORCE_CHUNKED, chunk_len=1024), "chunked"),
     (dict(B=1, D=1536, L=1 << 20), "chunked"),       # long sequence, few channels
-    (dict(B=4, D=5120, L=2048), "tiled"),
+    (dict(B=4, D=5120, L=2048), "split"),            # 640 CTAs: 592 (4 per SM) + 48 four-warp CTAs
+    (dict(B=4, D=5120, L=2048, io=ssm.SSM_F32), "tiled"),   # the split is a bf16 form
     (dict(B=1, D=5120, L=2048), "chunked"),          # 160 CTAs: about one per SM
     (dict(B=4, D=1536, L=2048), "tiled"),            # 192 CTAs: the single pass measured faster
     (dict(B=1, D=5120, L=1024), "tiled"),            # too short to chunk
@@ -182,6 +183,13 @@ def test_plan(lib, kw, path):
     chunk_len = kw.pop("chunk_len", 0)
     B, D, L = kw.get("B", 2), kw.get("D", 64), kw["L"]
     a = scan_args(B=B, D=D, L=L, io=kw.get("io", ssm.SSM_BF16), flags=flags, chunk_len=chunk_len)
+    if path == "split":
+        import os
+        os.environ["SSM_SCAN_KERNEL"] = "k2"        # the single launch on request
+        try:
+            assert ssm.ssm_scan_plan_path(a) == "tiled"
+        finally:
+            del os.environ["SSM_SCAN_KERNEL"]
     assert ssm.ssm_scan_plan_path(a) == path
     ws = ssm.ssm_scan_workspace_size(a)
     assert (ws > 0) == (path == "chunked")

@@ -146,6 +146,51 @@ def test_padded_row_strides():
 
 
 # ---------------------------------------------------------------------------
+# the split single pass: bf16 grids of more than 4 and at most 5 two-warp CTAs
+# per SM run 4 per SM as one launch and the remaining units as a second launch
+# of four-warp CTAs beside them (on 148 SMs: 593 to 740 units of 32 channels)
+# ---------------------------------------------------------------------------
+
+SPLIT_CASES = [(4, 4790, 256, 16), (5, 3800, 512, 13), (4, 5120, 64, 16)]
+
+
+@pytest.mark.parametrize("shape", SPLIT_CASES, ids=lambda s: "x".join(map(str, s)))
+def test_split_single_pass(shape, monkeypatch):
+    """A ragged last channel block among the second launch's units (4790 channels), N < 16 (the general
+    stage forms), h0 and h_last: against the oracle, and against the single launch (the second launch
+    sums 4 state groups per channel instead of 2, so the two agree to fp32 rounding)."""
+    if torch.cuda.get_device_properties(0).multi_processor_count != 148:
+        pytest.skip("the cases are sized for 148 SMs")
+    B, D, L, N = shape
+    case = rand_case(B, D, L, N, "bf16", seed=B + D + L + N, h0=True)
+    yr, hr = oracle_case(case)
+    y, hl = gpu_scan(case, "bf16", "auto")
+    assert_close("bf16", y, yr, f"y split {shape}")
+    assert_close("bf16", hl, hr, f"h_last split {shape}")
+    monkeypatch.setenv("SSM_SCAN_KERNEL", "k2")
+    y2, h2 = gpu_scan(case, "bf16", "auto")
+    assert rel_l2(y, y2) < 1e-3 and rel_l2(hl, h2) < 1e-5
+    # batch row 0 is all units of the first launch (the two-warp CTAs): the single launch's bits
+    assert np.array_equal(y[0], y2[0])
+
+
+@pytest.mark.parametrize("opt", ["no_gate", "no_dskip", "shared_bc", "softplus_off"])
+def test_split_options(opt):
+    if torch.cuda.get_device_properties(0).multi_processor_count != 148:
+        pytest.skip("the case is sized for 148 SMs")
+    case = rand_case(4, 4790, 256, 16, "bf16", seed=3, gate=opt != "no_gate", dskip=opt != "no_dskip",
+                     h0=True, shared_bc=opt == "shared_bc")
+    softplus = opt != "softplus_off"
+    if not softplus:
+        case["delta"] = syn.round_io(np.abs(case["delta"]) * 0.05, "bf16")
+        case["delta_bias"] = None
+    y, hl = gpu_scan(case, "bf16", "auto", softplus=softplus)
+    yr, hr = oracle_case(case, softplus)
+    assert_close("bf16", y, yr, f"y split {opt}")
+    assert_close("bf16", hl, hr, f"h_last split {opt}")
+
+
+# ---------------------------------------------------------------------------
 # the warp-shuffle associative scan (lanes over time), forced by its flag
 # ---------------------------------------------------------------------------
 

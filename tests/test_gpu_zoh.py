@@ -60,6 +60,18 @@ def test_zoh_scan(io, shape, flags):
     assert_close(io, host(hl), hr, f"h_last {shape}")
 
 
+def test_zoh_split_single_pass():
+    """The split single pass (600 units of 32 channels on 148 SMs: 592 on two-warp CTAs, 8 on four-warp CTAs
+    launched beside them) with the exact-ZOH term, against the oracle."""
+    if torch.cuda.get_device_properties(0).multi_processor_count != 148:
+        pytest.skip("the case is sized for 148 SMs")
+    p = scan_inputs(4, 4790, 256, 16, "bf16", seed=21, zero_a=True)
+    y, hl = run_scan(p, "bf16")
+    yr, hr = oracle_scan(p)
+    assert_close("bf16", host(y), yr, "y split")
+    assert_close("bf16", host(hl), hr, "h_last split")
+
+
 @pytest.mark.parametrize("io", ["f32", "bf16"])
 def test_zoh_chunked(io):
     p = scan_inputs(2, 64, 1024, 16, io, seed=3)
