@@ -469,7 +469,11 @@ def other_rows(lib, ssm, peak, stream, dev, which="all", decode_steps=1000):
         es = inp["u"].element_size()
         byt = 7 * Bsz * D * L * es + 2 * Bsz * N * L * es + 2 * Bsz * N * L * 4 + (D * N + 2 * D) * 4
         gbs = byt / (ms * 1e-3) / 1e9
-        rows[name] = {"ms": ms, "value": cfg.updates / (ms * 1e-3), "unit": UNIT, "launches": 3,
+        # checkpoint pass (two launches when it takes the split single pass), zeroing, backward kernel
+        ckpt_launches = 2 if ssm.ssm_scan_plan_path(ssm.make_scan_args(
+            inp["u"], inp["delta"], inp["A"], inp["Bm"], inp["Cm"], dy, inp["Dskip"], inp["z"], inp["delta_bias"],
+            discretization=bdisc, flags=ssm.SSM_SCAN_FORCE_TILED)) == "split" else 1
+        rows[name] = {"ms": ms, "value": cfg.updates / (ms * 1e-3), "unit": UNIT, "launches": 2 + ckpt_launches,
                       "hbm_gbs_algorithmic": gbs, "frac": gbs / peak, "algorithmic_bytes": byt,
                       "workspace_bytes": need.value, "l2": "inputs larger than L2"}
         del inp, dy, grads, bws

@@ -535,10 +535,23 @@ cudaError_t launch_shape(const ScanProblem& p, const ScanPlan& plan, ScanKernelP
 }
 
 template <typename IO, bool PRECISE, bool ZOH>
-cudaError_t launch_ckpt_typed(const ScanPlan& plan, const ScanKernelParams& tp, const ScanMaps& tm,
+cudaError_t launch_ckpt_typed(const ScanPlan& plan, ScanKernelParams& tp, const ScanMaps& tm,
                               const ScanProblem& p, cudaStream_t s) {
   const dim3 grid((unsigned)((p.D + CH - 1) / CH), 1, (unsigned)p.B);
   const int K = plan.shape.K, NS = plan.shape.NS;
+  if (plan.split_home > 0) {
+    // the split single pass of launch_typed: the checkpoints are the same per-(channel, state)
+    // recurrences whichever CTA shape runs them
+    if (K != 2 || NS != 8) return cudaErrorInvalidValue;
+    tp.nblk = (p.D + CH - 1) / CH;
+    tp.unit0 = 0;
+    tp.pdl = 1;
+    cudaError_t e = launch_one<IO, 2, 8, MODE_CKPT, PRECISE, ZOH>(tp, tm, dim3((unsigned)plan.split_home), s);
+    if (e != cudaSuccess) return e;
+    tp.unit0 = plan.split_home;
+    tp.pdl = 2;
+    return launch_one<IO, 4, 4, MODE_CKPT, PRECISE, ZOH>(tp, tm, dim3((unsigned)plan.split_extra), s);
+  }
   if (K == 1 && NS == 16) return launch_one<IO, 1, 16, MODE_CKPT, PRECISE, ZOH>(tp, tm, grid, s);
   if (K == 2 && NS == 8) return launch_one<IO, 2, 8, MODE_CKPT, PRECISE, ZOH>(tp, tm, grid, s);
   if (K == 4 && NS == 4) return launch_one<IO, 4, 4, MODE_CKPT, PRECISE, ZOH>(tp, tm, grid, s);
