@@ -165,6 +165,10 @@ def test_step_empty_is_noop(lib):
     (dict(B=1, D=1536, L=1 << 20), "chunked"),       # long sequence, few channels
     (dict(B=4, D=5120, L=2048), "split"),            # 640 CTAs: 592 (4 per SM) + 48 four-warp CTAs
     (dict(B=4, D=5120, L=2048, io=ssm.SSM_F32), "tiled"),   # the split is a bf16 form
+    (dict(B=4, D=5120, L=2048, disc=ssm.SSM_DISC_ZOH), "tiled"),   # ZOH keeps one launch (measured faster)
+    (dict(B=4, D=5920, L=2048), "split"),            # 740 CTAs: 148 four-warp CTAs, one per SM
+    (dict(B=4, D=5952, L=2048), "tiled"),            # 744 CTAs: more than 5 per SM, two waves anyway
+    (dict(B=4, D=4736, L=2048), "tiled"),            # 592 CTAs: 4 per SM already
     (dict(B=1, D=5120, L=2048), "chunked"),          # 160 CTAs: about one per SM
     (dict(B=4, D=1536, L=2048), "tiled"),            # 192 CTAs: the single pass measured faster
     (dict(B=1, D=5120, L=1024), "tiled"),            # too short to chunk
@@ -182,7 +186,8 @@ def test_plan(lib, kw, path):
     flags = kw.pop("flags", 0)
     chunk_len = kw.pop("chunk_len", 0)
     B, D, L = kw.get("B", 2), kw.get("D", 64), kw["L"]
-    a = scan_args(B=B, D=D, L=L, io=kw.get("io", ssm.SSM_BF16), flags=flags, chunk_len=chunk_len)
+    a = scan_args(B=B, D=D, L=L, io=kw.get("io", ssm.SSM_BF16), flags=flags, chunk_len=chunk_len,
+                  discretization=kw.get("disc", ssm.SSM_DISC_EULER))
     if path == "split":
         import os
         os.environ["SSM_SCAN_KERNEL"] = "k2"        # the single launch on request
