@@ -560,9 +560,20 @@ cudaError_t launch_ckpt_typed(const ScanPlan& plan, ScanKernelParams& tp, const 
 
 // complex A: single pass only (the planner never chunks it), Euler input term
 template <typename IO, bool PRECISE>
-cudaError_t launch_complex(const ScanProblem& p, const ScanPlan& plan, const ScanKernelParams& tp, const ScanMaps& tm,
+cudaError_t launch_complex(const ScanProblem& p, const ScanPlan& plan, ScanKernelParams& tp, const ScanMaps& tm,
                            cudaStream_t s) {
   if (plan.nchunks != 1) return cudaErrorInvalidValue;
+  if (plan.split_home > 0) {   // the split single pass of launch_typed
+    if (plan.shape.K != 2 || plan.shape.NS != 8) return cudaErrorInvalidValue;
+    tp.nblk = (p.D + CH - 1) / CH;
+    tp.unit0 = 0;
+    tp.pdl = 1;
+    cudaError_t e = launch_one<IO, 2, 8, MODE_OUTPUT, PRECISE, false, true>(tp, tm, dim3((unsigned)plan.split_home), s);
+    if (e != cudaSuccess) return e;
+    tp.unit0 = plan.split_home;
+    tp.pdl = 2;
+    return launch_one<IO, 4, 4, MODE_OUTPUT, PRECISE, false, true>(tp, tm, dim3((unsigned)plan.split_extra), s);
+  }
   const dim3 grid((unsigned)((p.D + CH - 1) / CH), 1, (unsigned)p.B);
   const int K = plan.shape.K, NS = plan.shape.NS;
   if (K == 2 && NS == 8) return launch_one<IO, 2, 8, MODE_OUTPUT, PRECISE, false, true>(tp, tm, grid, s);

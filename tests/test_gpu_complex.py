@@ -82,6 +82,30 @@ def test_complex_path_choice():
     assert ssm.ssm_scan_workspace_size(a) == 0
 
 
+def test_complex_split_single_pass(monkeypatch):
+    """600 units of 32 channels on 148 SMs: the split single pass (592 on two-warp CTAs, 8 on four-warp CTAs
+    beside them) with a complex A and h0, against the oracle and the single launch."""
+    if torch.cuda.get_device_properties(0).multi_processor_count != 148:
+        pytest.skip("the case is sized for 148 SMs")
+    p = complex_inputs(4, 4790, 128, 16, "bf16", seed=11)
+    d = {k: to_dev(v, "bf16" if k in ("u", "delta", "z", "Bm", "Cm") else None)
+         for k, v in p.items() if k not in ("A", "h0")}
+    A = torch.from_numpy(p["A"]).cuda()
+    y = torch.empty_like(d["u"])
+    a = ssm.make_scan_args(d["u"], d["delta"], A.real.contiguous(), d["Bm"], d["Cm"], y, d["Dskip"], d["z"],
+                           d["delta_bias"], A_imag=A.imag.contiguous())
+    assert ssm.ssm_scan_plan_path(a) == "split"
+    y, hl = run_scan(p, "bf16")
+    yr, hr = oracle_scan(p)
+    assert_close("bf16", host(y), yr, "y split")
+    got = hl.cpu().numpy()
+    assert_close("bf16", np.stack([got.real, got.imag]).astype(np.float64), np.stack([hr.real, hr.imag]),
+                 "h_last split")
+    monkeypatch.setenv("SSM_SCAN_KERNEL", "k2")
+    y2, h2 = run_scan(p, "bf16")
+    assert torch.equal(y[0], y2[0])          # batch row 0: all units of the first launch
+
+
 def test_complex_without_gate_and_state():
     p = complex_inputs(2, 64, 256, 16, "f32", seed=5, gate=False)
     d = {k: to_dev(v) for k, v in p.items() if k not in ("A", "h0") and v is not None}
