@@ -517,6 +517,23 @@ cudaError_t launch_one(const ScanKernelParams& tp, const ScanMaps& tm, dim3 grid
   return cudaGetLastError();
 }
 
+// The split single pass (planned by ssm_api.cu): the first split_home units on two-warp CTAs, then the
+// other units on four-warp CTAs (4 states per thread) that start while the first launch runs and
+// finish after it.
+template <typename IO, int MODE, bool PRECISE, bool ZOH, bool CPLX>
+cudaError_t launch_split(const ScanProblem& p, const ScanPlan& plan, ScanKernelParams& tp, const ScanMaps& tm,
+                         cudaStream_t s) {
+  if (plan.shape.K != 2 || plan.shape.NS != 8 || plan.nchunks != 1) return cudaErrorInvalidValue;
+  tp.nblk = (p.D + CH - 1) / CH;
+  tp.unit0 = 0;
+  tp.pdl = 1;
+  cudaError_t e = launch_one<IO, 2, 8, MODE, PRECISE, ZOH, CPLX>(tp, tm, dim3((unsigned)plan.split_home), s);
+  if (e != cudaSuccess) return e;
+  tp.unit0 = plan.split_home;
+  tp.pdl = 2;
+  return launch_one<IO, 4, 4, MODE, PRECISE, ZOH, CPLX>(tp, tm, dim3((unsigned)plan.split_extra), s);
+}
+
 template <typename IO, int K, int NS, bool PRECISE, bool ZOH>
 cudaError_t launch_shape(const ScanProblem& p, const ScanPlan& plan, ScanKernelParams& tp, const ScanMaps& tm,
                          cudaStream_t s) {
@@ -539,19 +556,8 @@ cudaError_t launch_ckpt_typed(const ScanPlan& plan, ScanKernelParams& tp, const 
                               const ScanProblem& p, cudaStream_t s) {
   const dim3 grid((unsigned)((p.D + CH - 1) / CH), 1, (unsigned)p.B);
   const int K = plan.shape.K, NS = plan.shape.NS;
-  if (plan.split_home > 0) {
-    // the split single pass of launch_typed: the checkpoints are the same per-(channel, state)
-    // recurrences whichever CTA shape runs them
-    if (K != 2 || NS != 8) return cudaErrorInvalidValue;
-    tp.nblk = (p.D + CH - 1) / CH;
-    tp.unit0 = 0;
-    tp.pdl = 1;
-    cudaError_t e = launch_one<IO, 2, 8, MODE_CKPT, PRECISE, ZOH>(tp, tm, dim3((unsigned)plan.split_home), s);
-    if (e != cudaSuccess) return e;
-    tp.unit0 = plan.split_home;
-    tp.pdl = 2;
-    return launch_one<IO, 4, 4, MODE_CKPT, PRECISE, ZOH>(tp, tm, dim3((unsigned)plan.split_extra), s);
-  }
+  // the checkpoints are the same per-(channel, state) recurrences whichever CTA shape runs them
+  if (plan.split_home > 0) return launch_split<IO, MODE_CKPT, PRECISE, ZOH, false>(p, plan, tp, tm, s);
   if (K == 1 && NS == 16) return launch_one<IO, 1, 16, MODE_CKPT, PRECISE, ZOH>(tp, tm, grid, s);
   if (K == 2 && NS == 8) return launch_one<IO, 2, 8, MODE_CKPT, PRECISE, ZOH>(tp, tm, grid, s);
   if (K == 4 && NS == 4) return launch_one<IO, 4, 4, MODE_CKPT, PRECISE, ZOH>(tp, tm, grid, s);
@@ -563,17 +569,7 @@ template <typename IO, bool PRECISE>
 cudaError_t launch_complex(const ScanProblem& p, const ScanPlan& plan, ScanKernelParams& tp, const ScanMaps& tm,
                            cudaStream_t s) {
   if (plan.nchunks != 1) return cudaErrorInvalidValue;
-  if (plan.split_home > 0) {   // the split single pass of launch_typed
-    if (plan.shape.K != 2 || plan.shape.NS != 8) return cudaErrorInvalidValue;
-    tp.nblk = (p.D + CH - 1) / CH;
-    tp.unit0 = 0;
-    tp.pdl = 1;
-    cudaError_t e = launch_one<IO, 2, 8, MODE_OUTPUT, PRECISE, false, true>(tp, tm, dim3((unsigned)plan.split_home), s);
-    if (e != cudaSuccess) return e;
-    tp.unit0 = plan.split_home;
-    tp.pdl = 2;
-    return launch_one<IO, 4, 4, MODE_OUTPUT, PRECISE, false, true>(tp, tm, dim3((unsigned)plan.split_extra), s);
-  }
+  if (plan.split_home > 0) return launch_split<IO, MODE_OUTPUT, PRECISE, false, true>(p, plan, tp, tm, s);
   const dim3 grid((unsigned)((p.D + CH - 1) / CH), 1, (unsigned)p.B);
   const int K = plan.shape.K, NS = plan.shape.NS;
   if (K == 2 && NS == 8) return launch_one<IO, 2, 8, MODE_OUTPUT, PRECISE, false, true>(tp, tm, grid, s);
@@ -585,19 +581,7 @@ template <typename IO, bool PRECISE, bool ZOH>
 cudaError_t launch_typed(const ScanProblem& p, const ScanPlan& plan, ScanKernelParams& tp, const ScanMaps& tm,
                          cudaStream_t s) {
   const int K = plan.shape.K, NS = plan.shape.NS;
-  if (plan.split_home > 0) {
-    // split single pass: the home units on two-warp CTAs, then the extra units on four-warp CTAs
-    // (4 states per thread) that run beside them
-    if (K != 2 || NS != 8 || plan.nchunks != 1) return cudaErrorInvalidValue;
-    tp.nblk = (p.D + CH - 1) / CH;
-    tp.unit0 = 0;
-    tp.pdl = 1;
-    cudaError_t e = launch_one<IO, 2, 8, MODE_OUTPUT, PRECISE, ZOH>(tp, tm, dim3((unsigned)plan.split_home), s);
-    if (e != cudaSuccess) return e;
-    tp.unit0 = plan.split_home;
-    tp.pdl = 2;
-    return launch_one<IO, 4, 4, MODE_OUTPUT, PRECISE, ZOH>(tp, tm, dim3((unsigned)plan.split_extra), s);
-  }
+  if (plan.split_home > 0) return launch_split<IO, MODE_OUTPUT, PRECISE, ZOH, false>(p, plan, tp, tm, s);
   if (K == 1 && NS == 16) return launch_shape<IO, 1, 16, PRECISE, ZOH>(p, plan, tp, tm, s);
   if (K == 2 && NS == 8) return launch_shape<IO, 2, 8, PRECISE, ZOH>(p, plan, tp, tm, s);
   if (K == 4 && NS == 4) return launch_shape<IO, 4, 4, PRECISE, ZOH>(p, plan, tp, tm, s);
