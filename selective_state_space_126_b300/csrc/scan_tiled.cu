@@ -566,10 +566,9 @@ cudaError_t launch_ckpt_typed(const ScanPlan& plan, ScanKernelParams& tp, const 
 
 // complex A: single pass only (the planner never chunks it), Euler input term
 template <typename IO, bool PRECISE>
-cudaError_t launch_complex(const ScanProblem& p, const ScanPlan& plan, ScanKernelParams& tp, const ScanMaps& tm,
+cudaError_t launch_complex(const ScanProblem& p, const ScanPlan& plan, const ScanKernelParams& tp, const ScanMaps& tm,
                            cudaStream_t s) {
-  if (plan.nchunks != 1) return cudaErrorInvalidValue;
-  if (plan.split_home > 0) return launch_split<IO, MODE_OUTPUT, PRECISE, false, true>(p, plan, tp, tm, s);
+  if (plan.nchunks != 1 || plan.split_home > 0) return cudaErrorInvalidValue;
   const dim3 grid((unsigned)((p.D + CH - 1) / CH), 1, (unsigned)p.B);
   const int K = plan.shape.K, NS = plan.shape.NS;
   if (K == 2 && NS == 8) return launch_one<IO, 2, 8, MODE_OUTPUT, PRECISE, false, true>(tp, tm, grid, s);

@@ -216,6 +216,11 @@ TiledShape pick_shape(const ScanProblem& p, int64_t ctas, int sms) {
     if (!strcmp(env, "k4")) return TiledShape{4, 4, 32};
   }
   if (ctas <= 4 * (int64_t)sms) return TiledShape{4, 4, 32};
+  // the exact-ZOH and complex-A variants do several times the arithmetic per state, in longer dependent
+  // chains, and gain more from warps than from states per thread: on B300 (4 x 5120 x 2048, bf16) the
+  // ZOH scan took 407 us with 4 threads per channel against 503 us with 2, the complex scan 709 us
+  // against 970 us (753 us split over two launches)
+  if (p.zoh || p.cplx) return TiledShape{4, 4, 32};
   return TiledShape{2, 8, 32};
 }
 
@@ -230,14 +235,13 @@ TiledShape pick_shape(const ScanProblem& p, int64_t ctas, int sms) {
 // of the four-warp CTA (4 states per thread), which starts while the first
 // runs (programmatic dependent launch) and fits beside its 4 CTAs: each extra
 // unit adds one quarter-unit warp to a scheduler instead of a third half-unit
-// one.  Taken for the Euler term with a real or complex A (252.8 -> 223.5 us
-// and 949 -> 752 us on 4 x 5120 x 2048); with the exact-ZOH term the split
-// measured slower (518 against 502 us).  SSM_SCAN_KERNEL=k2 keeps the single
-// launch.
+// one.  Taken for the Euler term with a real A (252.8 -> 223.5 us on
+// 4 x 5120 x 2048); the exact-ZOH and complex-A variants run the four-warp
+// CTA instead (pick_shape).  SSM_SCAN_KERNEL=k2 keeps the single launch.
 void plan_split(const ScanProblem& p, int sms, ScanPlan* plan) {
   const char* env = getenv("SSM_SCAN_KERNEL");
   if (env) return;
-  if (p.io != SSM_BF16 || p.zoh || p.N > 16 || plan->shape.K != 2 || plan->shape.NS != 8) return;
+  if (p.io != SSM_BF16 || p.zoh || p.cplx || p.N > 16 || plan->shape.K != 2 || plan->shape.NS != 8) return;
   const int64_t units = p.B * ((p.D + 31) / 32), home = 4 * (int64_t)sms;
   if (units <= home || units > home + sms) return;
   plan->split_home = (int)home;
@@ -279,7 +283,6 @@ ssm_status_t plan_scan(const ssm_scan_args_t* a, const ScanProblem& p, ScanPlan*
     plan->path = kPathTiled;
     plan->shape = pick_shape(p, p.B * ((p.D + 31) / 32), device_sm_count());
     if (plan->shape.K == 1) plan->shape = TiledShape{2, 8, 32};   // the complex variant exists for K = 2 and 4
-    plan_split(p, device_sm_count(), plan);   // 4 x 5120 x 2048, complex: 949 -> 752 us
     return ok();
   }
   const int sms = device_sm_count();

@@ -169,7 +169,7 @@ def test_step_empty_is_noop(lib):
     (dict(B=4, D=5920, L=2048), "split"),            # 740 CTAs: 148 four-warp CTAs, one per SM
     (dict(B=4, D=5952, L=2048), "tiled"),            # 744 CTAs: more than 5 per SM, two waves anyway
     (dict(B=4, D=4736, L=2048), "tiled"),            # 592 CTAs: 4 per SM already
-    (dict(B=4, D=5120, L=2048, cplx=True), "split"),  # complex A: the split too
+    (dict(B=4, D=5120, L=2048, cplx=True), "tiled"),  # complex A: four-warp CTAs, one launch
     (dict(B=1, D=5120, L=2048), "chunked"),          # 160 CTAs: about one per SM
     (dict(B=4, D=1536, L=2048), "tiled"),            # 192 CTAs: the single pass measured faster
     (dict(B=1, D=5120, L=1024), "tiled"),            # too short to chunk

@@ -82,9 +82,10 @@ def test_complex_path_choice():
     assert ssm.ssm_scan_workspace_size(a) == 0
 
 
-def test_complex_split_single_pass(monkeypatch):
-    """600 units of 32 channels on 148 SMs: the split single pass (592 on two-warp CTAs, 8 on four-warp CTAs
-    beside them) with a complex A and h0, against the oracle and the single launch."""
+def test_complex_full_grid_shapes(monkeypatch):
+    """600 units of 32 channels (more than 4 per SM on 148 SMs) with a complex A and h0: the planner's
+    four-warp CTAs in one launch, the two-warp CTAs, and the two-warp CTAs split over two launches, each
+    against the oracle."""
     if torch.cuda.get_device_properties(0).multi_processor_count != 148:
         pytest.skip("the case is sized for 148 SMs")
     p = complex_inputs(4, 4790, 128, 16, "bf16", seed=11)
@@ -94,16 +95,16 @@ def test_complex_split_single_pass(monkeypatch):
     y = torch.empty_like(d["u"])
     a = ssm.make_scan_args(d["u"], d["delta"], A.real.contiguous(), d["Bm"], d["Cm"], y, d["Dskip"], d["z"],
                            d["delta_bias"], A_imag=A.imag.contiguous())
-    assert ssm.ssm_scan_plan_path(a) == "split"
-    y, hl = run_scan(p, "bf16")
     yr, hr = oracle_scan(p)
-    assert_close("bf16", host(y), yr, "y split")
-    got = hl.cpu().numpy()
-    assert_close("bf16", np.stack([got.real, got.imag]).astype(np.float64), np.stack([hr.real, hr.imag]),
-                 "h_last split")
-    monkeypatch.setenv("SSM_SCAN_KERNEL", "k2")
-    y2, h2 = run_scan(p, "bf16")
-    assert torch.equal(y[0], y2[0])          # batch row 0: all units of the first launch
+    for env, path in ((None, "tiled"), ("k2", "tiled")):
+        if env:
+            monkeypatch.setenv("SSM_SCAN_KERNEL", env)
+        assert ssm.ssm_scan_plan_path(a) == path
+        y, hl = run_scan(p, "bf16")
+        assert_close("bf16", host(y), yr, f"y {env}")
+        got = hl.cpu().numpy()
+        assert_close("bf16", np.stack([got.real, got.imag]).astype(np.float64), np.stack([hr.real, hr.imag]),
+                     f"h_last {env}")
 
 
 def test_complex_without_gate_and_state():
