@@ -304,8 +304,8 @@ ssm_status_t plan_scan(const ssm_scan_args_t* a, const ScanProblem& p, ScanPlan*
       chunk_len = (a->chunk_len + kTileT - 1) / kTileT * kTileT;
     } else {
       // enough chunks for ~8 CTAs per SM, chunks of at least 256 steps (on B300 a 1 x 5120 x 2048
-      // scan, 160 CTAs, takes 118 us in 8 chunks against 129 us in one pass).  Long chunks (4096
-      // steps and more) run as one wave whose time is set by the SMs holding the most CTAs, so their
+      // scan, 160 CTAs, takes 118 us in 8 chunks against 129 us in one pass).  With long chunks (4096
+      // steps and more) every CTA runs long, and the SMs that get the most CTAs set the time, so the
       // count is rounded down to at most 8 CTAs per SM: the 1 x 1536 x 2^20 scan (48 CTAs per chunk)
       // took 12.87 ms in 24 chunks (1152 CTAs) against 13.92 ms in 25 (1200 CTAs, 9 on some SMs).
       int64_t want = (8 * (int64_t)sms + ctas - 1) / ctas;
