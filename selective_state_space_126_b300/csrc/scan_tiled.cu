@@ -50,6 +50,16 @@
 // MODE_CKPT serves the backward pass: one pass from h0 that writes the state
 // before every SSM_BWD_SEGMENT-th step to a checkpoint array and emits nothing
 // else.
+//
+// The split single pass (launch_split): a one-wave grid of more than 4 and at
+// most 5 two-warp CTAs per SM would put a third warp on some of an SM's four
+// schedulers and take as long as 5 CTAs everywhere.  So the first 4 per SM run
+// as one launch and the rest as a second launch of the four-warp CTA, which
+// fits beside them.  Both take their unit (batch row, 32-channel block) from
+// a linear index (unit0 + blockIdx.x); the first executes
+// griddepcontrol.launch_dependents on entry so that the second, a programmatic
+// dependent launch, starts at once, and the second executes
+// griddepcontrol.wait before exiting, so that the stream's next work sees both.
 #include <cstdio>
 #include <cstring>
 #include <type_traits>
