@@ -174,6 +174,47 @@ def test_split_single_pass(shape, monkeypatch):
     assert np.array_equal(y[0], y2[0])
 
 
+def test_split_in_cuda_graph():
+    """The split single pass's two launches (the second a programmatic dependent launch) captured in a CUDA
+    graph and replayed: the same bits as the eager call, on fresh inputs copied into the captured buffers."""
+    if torch.cuda.get_device_properties(0).multi_processor_count != 148:
+        pytest.skip("the case is sized for 148 SMs")
+    case = rand_case(4, 4790, 256, 16, "bf16", seed=17)
+    dev = {k: (to_dev(v, "bf16") if k in ("u", "delta", "z", "Bm", "Cm") else to_dev(v)) for k, v in case.items()}
+    y = torch.empty_like(dev["u"])
+    args = ssm.make_scan_args(dev["u"], dev["delta"], dev["A"], dev["Bm"], dev["Cm"], y, dev["Dskip"], dev["z"],
+                              dev["delta_bias"])
+    assert ssm.ssm_scan_plan_path(args) == "split"
+
+    def call():
+        ssm.ssm_scan_fwd(dev["u"], dev["delta"], dev["A"], dev["Bm"], dev["Cm"], Dskip=dev["Dskip"], z=dev["z"],
+                         delta_bias=dev["delta_bias"], y=y)
+
+    call()                                   # eager (also sets the kernels' attributes before capture)
+    torch.cuda.synchronize()
+    eager = y.clone()
+    stream = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        call()                               # warm the side stream
+        stream.synchronize()
+        y.zero_()
+        with torch.cuda.graph(g, stream=stream):
+            call()
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(y, eager)
+    case2 = rand_case(4, 4790, 256, 16, "bf16", seed=18)
+    for k in ("u", "delta", "z"):
+        dev[k].copy_(to_dev(case2[k], "bf16"))
+    g.replay()
+    torch.cuda.synchronize()
+    replayed = y.clone()
+    call()
+    torch.cuda.synchronize()
+    assert torch.equal(replayed, y)
+
+
 @pytest.mark.parametrize("opt", ["no_gate", "no_dskip", "shared_bc", "softplus_off"])
 def test_split_options(opt):
     if torch.cuda.get_device_properties(0).multi_processor_count != 148:
